@@ -1,0 +1,241 @@
+"""Seeded synthetic inputs for the LoRA MoE expert layer.
+
+This module only draws random inputs: it holds none of the layer's arithmetic
+(no adapter mapping, no bucketing, no projections), so that both the CUDA path
+and the CPU oracle can be fed from it without sharing any of the method.
+
+Distributions (the same for every workload):
+  * x ~ N(0, 1);  W_gate_up ~ N(0, 1/H);  W_down ~ N(0, 1/I)
+  * LoRA A, B ~ N(0, 0.02^2) on the first r_l rank rows/columns of slot l and
+    exactly zero in the rank padding up to R ([num_loras, num_experts, rank, dim]
+    stacks as in the adapter memory pool).  With ``lora_std="fan_in"`` they are
+    N(0, 1/fan_in) instead, which makes the LoRA delta O(1).
+  * router logits ~ N(0, 1) (plus a fixed per-expert bias where stated),
+    softmax, top-k (sorted), renormalised to sum 1.  topk_ids int32,
+    topk_weights float32.
+  * x, W, A, B are stored as bf16.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerConfig:
+    name: str
+    hidden: int            # H
+    intermediate: int      # I (per expert)
+    num_experts: int       # E
+    topk: int              # K
+    num_loras: int         # L
+    max_rank: int          # R
+    block_size: int        # align block size
+    num_tokens: int        # T
+    description: str
+
+
+CONFIGS = {
+    "tiny": LayerConfig(
+        "tiny", 256, 512, 8, 2, 4, 16, 16, 64,
+        "hidden 256, intermediate 512, 8 experts top-2, 4 slots ranks [0,8,16,8] alpha 16, "
+        "64 tokens in segments [10,22,7,25] with adapters [1,-1,2,3]"),
+    "qwen_moe_prefill": LayerConfig(
+        "qwen_moe_prefill", 2048, 768, 128, 8, 8, 64, 16, 4096,
+        "Qwen-MoE-like prefill: hidden 2048, intermediate 768, 128 experts top-8, 8 slots ranks "
+        "{8,16,32,64} alpha=2r, 4096 tokens in 16 segments (lens U{64..512} rescaled), one adapter -1"),
+    "decode": LayerConfig(
+        "decode", 2048, 768, 128, 8, 32, 32, 16, 256,
+        "decode: hidden 2048, intermediate 768, 128 experts top-8, 32 slots ranks {0,8,16,32} "
+        "alpha=2r, 256 requests x 1 token, adapters uniform with 10% -1"),
+    "deepseek_v3_prefill": LayerConfig(
+        "deepseek_v3_prefill", 7168, 2048, 256, 8, 4, 64, 16, 8192,
+        "DeepSeek-V3-like prefill: hidden 7168, intermediate 2048, 256 experts top-8, 4 slots ranks "
+        "{16,32,64,64} alpha=2r, 8192 tokens in 8 segments of 1024, router bias N(0,0.5)"),
+    "metadata_stress": LayerConfig(
+        "metadata_stress", 0, 0, 256, 8, 64, 64, 64, 1048576,
+        "metadata stress: 1,048,576 tokens in 4096 segments (geometric lens, mean 256), 64 slots "
+        "ranks uniform {0,8,16,32,64}, top-8 of 256 experts, block size 64"),
+}
+
+
+@dataclasses.dataclass
+class Batch:
+    """Per-batch request structure and routing (inputs of batch_info and align)."""
+    seg_lens: torch.Tensor        # int32 [bs]
+    seg_indptr: torch.Tensor      # int32 [bs+1]
+    weight_indices: torch.Tensor  # int32 [bs]
+    lora_ranks: torch.Tensor      # int32 [L]
+    scalings: torch.Tensor        # float32 [L]  alpha_l / r_l (0 for rank 0)
+    topk_ids: torch.Tensor        # int32 [T, K]
+    topk_weights: torch.Tensor    # float32 [T, K]
+
+
+@dataclasses.dataclass
+class LayerWeights:
+    w_gate_up: torch.Tensor    # bf16 [E, 2I, H]  (gate rows, then up rows)
+    w_down: torch.Tensor       # bf16 [E, H, I]
+    lora_a_gu: torch.Tensor    # bf16 [L, E, 2, R, H]
+    lora_b_gu: torch.Tensor    # bf16 [L, E, 2, I, R]
+    lora_a_down: torch.Tensor  # bf16 [L, E, R, I]
+    lora_b_down: torch.Tensor  # bf16 [L, E, H, R]
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _rescale_lengths(raw: torch.Tensor, total: int) -> torch.Tensor:
+    """Scale positive lengths to sum exactly `total`: floor, remainder to the largest."""
+    raw = raw.double()
+    scaled = torch.floor(raw * total / raw.sum()).long().clamp_min(1)
+    diff = total - int(scaled.sum())
+    scaled[int(torch.argmax(scaled))] += diff
+    assert int(scaled.sum()) == total and int(scaled.min()) >= 1
+    return scaled.int()
+
+
+def _indptr(seg_lens: torch.Tensor) -> torch.Tensor:
+    out = torch.zeros(seg_lens.numel() + 1, dtype=torch.int64)
+    out[1:] = torch.cumsum(seg_lens.long(), 0)
+    return out.int()
+
+
+def route(num_tokens: int, num_experts: int, topk: int, g: torch.Generator, device,
+          expert_bias_std: float = 0.0, chunk: int = 1 << 16):
+    """Softmax top-k routing from N(0,1) logits (+ optional fixed per-expert bias)."""
+    bias = None
+    if expert_bias_std > 0:
+        bias = torch.randn(num_experts, generator=g, device=device) * expert_bias_std
+    ids = torch.empty(num_tokens, topk, dtype=torch.int32, device=device)
+    wts = torch.empty(num_tokens, topk, dtype=torch.float32, device=device)
+    for t0 in range(0, num_tokens, chunk):
+        t1 = min(num_tokens, t0 + chunk)
+        logits = torch.randn(t1 - t0, num_experts, generator=g, device=device)
+        if bias is not None:
+            logits += bias
+        probs = torch.softmax(logits, dim=-1)
+        w, i = torch.topk(probs, topk, dim=-1, sorted=True)
+        w = w / w.sum(dim=-1, keepdim=True)
+        ids[t0:t1] = i.int()
+        wts[t0:t1] = w.float()
+    return ids, wts
+
+
+def _ranks_and_scalings(cfg: LayerConfig, g: torch.Generator):
+    L = cfg.num_loras
+    if cfg.name == "tiny":
+        ranks = [0, 8, 16, 8]
+        scal = [0.0 if r == 0 else 16.0 / r for r in ranks]
+    elif cfg.name == "qwen_moe_prefill":
+        ranks = [[8, 16, 32, 64][l % 4] for l in range(L)]
+        scal = [2.0] * L
+    elif cfg.name == "decode":
+        ranks = [[0, 8, 16, 32][l % 4] for l in range(L)]
+        scal = [0.0 if r == 0 else 2.0 for r in ranks]
+    elif cfg.name == "deepseek_v3_prefill":
+        ranks = [16, 32, 64, 64]
+        scal = [2.0] * L
+    elif cfg.name == "metadata_stress":
+        choices = torch.tensor([0, 8, 16, 32, 64])
+        ranks = choices[torch.randint(0, 5, (L,), generator=g)].tolist()
+        scal = [0.0 if r == 0 else 2.0 for r in ranks]
+    else:
+        raise KeyError(cfg.name)
+    return torch.tensor(ranks, dtype=torch.int32), torch.tensor(scal, dtype=torch.float32)
+
+
+def _segments(cfg: LayerConfig, g: torch.Generator):
+    """Request segment lengths and adapter ids (CPU generator, small)."""
+    T, L = cfg.num_tokens, cfg.num_loras
+    if cfg.name == "tiny":
+        lens = torch.tensor([10, 22, 7, 25], dtype=torch.int32)
+        adapters = torch.tensor([1, -1, 2, 3], dtype=torch.int32)
+    elif cfg.name == "qwen_moe_prefill":
+        raw = torch.randint(64, 513, (16,), generator=g)
+        lens = _rescale_lengths(raw, T)
+        adapters = torch.randint(0, L, (16,), generator=g).int()
+        adapters[int(torch.randint(0, 16, (1,), generator=g))] = -1
+    elif cfg.name == "decode":
+        lens = torch.ones(256, dtype=torch.int32)
+        adapters = torch.randint(0, L, (256,), generator=g).int()
+        none = torch.rand(256, generator=g) < 0.1
+        adapters[none] = -1
+    elif cfg.name == "deepseek_v3_prefill":
+        lens = torch.full((8,), 1024, dtype=torch.int32)
+        adapters = torch.randint(0, L, (8,), generator=g).int()
+    elif cfg.name == "metadata_stress":
+        u = torch.rand(4096, generator=g, dtype=torch.float64).clamp_min(1e-12)
+        p = 1.0 / 256.0
+        geo = torch.floor(torch.log(u) / math.log1p(-p)) + 1  # geometric on {1,2,...}, mean 256
+        lens = _rescale_lengths(geo, T)
+        adapters = torch.randint(0, L, (4096,), generator=g).int()
+    else:
+        raise KeyError(cfg.name)
+    return lens, adapters
+
+
+def make_batch(cfg: LayerConfig, device="cpu", seed: int = 0) -> Batch:
+    """Request segments, adapter ids, ranks/scalings and routing for one batch."""
+    gc = _gen("cpu", seed)
+    lens, adapters = _segments(cfg, gc)
+    ranks, scal = _ranks_and_scalings(cfg, gc)
+    gd = _gen(device, seed + 1)
+    bias = 0.5 if cfg.name in ("deepseek_v3_prefill",) else 0.0
+    ids, wts = route(cfg.num_tokens, cfg.num_experts, cfg.topk, gd, device, expert_bias_std=bias)
+    return Batch(lens.to(device), _indptr(lens).to(device), adapters.to(device),
+                 ranks.to(device), scal.to(device), ids, wts)
+
+
+def make_weights(cfg: LayerConfig, ranks: torch.Tensor, device="cpu", seed: int = 0,
+                 lora_std: Optional[str] = None) -> LayerWeights:
+    """Expert weights and zero-padded LoRA stacks, bf16."""
+    E, H, I, L, R = cfg.num_experts, cfg.hidden, cfg.intermediate, cfg.num_loras, cfg.max_rank
+    g = _gen(device, seed + 2)
+    bf = torch.bfloat16
+
+    def randn(shape, std):
+        return torch.randn(shape, generator=g, device=device, dtype=bf).mul_(std)
+
+    w_gate_up = torch.empty(E, 2 * I, H, dtype=bf, device=device)
+    w_down = torch.empty(E, H, I, dtype=bf, device=device)
+    for e in range(E):  # per expert keeps temporaries small at large sizes
+        w_gate_up[e] = randn((2 * I, H), 1.0 / math.sqrt(H))
+        w_down[e] = randn((H, I), 1.0 / math.sqrt(I))
+    a_gu = torch.zeros(L, E, 2, R, H, dtype=bf, device=device)
+    b_gu = torch.zeros(L, E, 2, I, R, dtype=bf, device=device)
+    a_d = torch.zeros(L, E, R, I, dtype=bf, device=device)
+    b_d = torch.zeros(L, E, H, R, dtype=bf, device=device)
+    ranks_l = [int(r) for r in ranks.tolist()]
+    for l in range(L):
+        r = ranks_l[l]
+        if r == 0:
+            continue
+        if lora_std == "fan_in":
+            sa_gu, sb_gu, sa_d, sb_d = 1 / math.sqrt(H), 1 / math.sqrt(r), 1 / math.sqrt(I), 1 / math.sqrt(r)
+        else:
+            sa_gu = sb_gu = sa_d = sb_d = 0.02
+        a_gu[l, :, :, :r, :] = randn((E, 2, r, H), sa_gu)
+        b_gu[l, :, :, :, :r] = randn((E, 2, I, r), sb_gu)
+        a_d[l, :, :r, :] = randn((E, r, I), sa_d)
+        b_d[l, :, :, :r] = randn((E, H, r), sb_d)
+    return LayerWeights(w_gate_up, w_down, a_gu, b_gu, a_d, b_d)
+
+
+def make_x(cfg: LayerConfig, device="cpu", seed: int = 0) -> torch.Tensor:
+    g = _gen(device, seed + 3)
+    return torch.randn(cfg.num_tokens, cfg.hidden, generator=g, device=device,
+                       dtype=torch.bfloat16)
+
+
+def custom_config(name: str = "custom", **kw) -> LayerConfig:
+    """A LayerConfig with explicit sizes (tests of ragged and edge shapes)."""
+    base = dict(hidden=256, intermediate=512, num_experts=8, topk=2, num_loras=4, max_rank=16,
+                block_size=16, num_tokens=64, description="custom")
+    base.update(kw)
+    return LayerConfig(name=name, **base)

@@ -1,0 +1,190 @@
+"""CPU oracle for the multi-adapter LoRA MoE expert layer (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` legs are the only callers.
+The CUDA library never imports, links or loads anything here, and this module
+imports nothing from the CUDA package.
+
+The arithmetic lives in ``moe_lora_oracle.c`` (plain C, fp64 accumulation);
+this module only compiles it with gcc on first use and marshals numpy arrays.
+bf16 tensors are passed as their uint16 bit patterns (widened exactly in C);
+float64 arrays are accepted for the same operands so that tests can feed values
+that bf16 cannot hold (the dense-materialised W + s*B*A check).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_lora_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD_DIR, "libmoe_lora_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+INVALID = -1
+UNDERCOVERED = -2
+INDEX = -3
+CAPACITY = -4
+NOMEM = -7
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP) into oracle/_build; return the path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-std=c11", "-Wall", "-shared", "-fPIC",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            vp = ctypes.c_void_p
+            i32, i64 = ctypes.c_int32, ctypes.c_int64
+            lib.oracle_batch_info.restype = ctypes.c_int
+            lib.oracle_batch_info.argtypes = [i32p, i32p, i32p, i32, i32, i32, i32, i32p, i32p]
+            lib.oracle_align_capacity.restype = i64
+            lib.oracle_align_capacity.argtypes = [i32, i32, i32, i32, i32]
+            lib.oracle_align.restype = ctypes.c_int
+            lib.oracle_align.argtypes = [i32p, i32p, i32, i32, i32, i32, i32,
+                                         i32p, i32p, i32p, i32p, i64]
+            lib.oracle_forward.restype = ctypes.c_int
+            lib.oracle_forward.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
+                                           vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                           i64, i64, i64, i64, i64, i64, i64,
+                                           vp, i64, vp, ctypes.c_int]
+            lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def batch_info(seg_indptr, weight_indices, lora_ranks, num_tokens: int, max_len: int = 0):
+    """Returns (status, token_lora_mapping[num_tokens], adapter_enabled[num_loras])."""
+    seg_indptr, weight_indices, lora_ranks = _i32(seg_indptr), _i32(weight_indices), _i32(lora_ranks)
+    bs = weight_indices.shape[0]
+    if seg_indptr.shape[0] != bs + 1:
+        return INVALID, None, None
+    mapping = np.zeros(max(num_tokens, 0), dtype=np.int32)
+    enabled = np.zeros(lora_ranks.shape[0], dtype=np.int32)
+    st = _load().oracle_batch_info(_p32(seg_indptr), _p32(weight_indices), _p32(lora_ranks),
+                                   bs, lora_ranks.shape[0], num_tokens, max_len,
+                                   _p32(mapping), _p32(enabled))
+    return int(st), mapping, enabled
+
+
+def align_capacity(num_tokens: int, topk: int, num_experts: int, num_loras: int,
+                   block_size: int) -> int:
+    return int(_load().oracle_align_capacity(num_tokens, topk, num_experts, num_loras, block_size))
+
+
+def align(topk_ids, token_lora_mapping, num_experts: int, num_loras: int, block_size: int):
+    """Returns (status, sorted_token_ids[npad], block_expert_ids[npad/bs],
+    block_lora_ids[npad/bs], npad); arrays are trimmed to the valid prefix."""
+    topk_ids = _i32(topk_ids)
+    if topk_ids.ndim != 2:
+        return INVALID, None, None, None, 0
+    T, K = topk_ids.shape
+    mapping = _i32(token_lora_mapping)
+    cap = align_capacity(T, K, num_experts, num_loras, block_size)
+    if cap < 0:
+        return INVALID, None, None, None, 0
+    sorted_ids = np.zeros(max(cap, 1), dtype=np.int32)
+    nblk = max(cap // block_size, 1)
+    bexp = np.zeros(nblk, dtype=np.int32)
+    blora = np.zeros(nblk, dtype=np.int32)
+    npad = np.zeros(1, dtype=np.int32)
+    st = _load().oracle_align(_p32(topk_ids), _p32(mapping), T, K, num_experts, num_loras,
+                              block_size, _p32(sorted_ids), _p32(bexp), _p32(blora),
+                              _p32(npad), cap)
+    n = int(npad[0])
+    if st != OK:
+        return int(st), None, None, None, 0
+    return int(st), sorted_ids[:n].copy(), bexp[: n // block_size].copy(), \
+        blora[: n // block_size].copy(), n
+
+
+def _operand(a):
+    """(pointer, dtype code, keep-alive array) for a bf16-bits or float64 operand."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16 or a.dtype == np.int16:
+        a = np.ascontiguousarray(a.view(np.uint16))
+        return a.ctypes.data, 0, a
+    if a.dtype == np.float64:
+        a = np.ascontiguousarray(a)
+        return a.ctypes.data, 1, a
+    raise TypeError(f"oracle operands are bf16 bit patterns (uint16) or float64, got {a.dtype}")
+
+
+def forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+            w_gate_up, w_down, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
+            tokens=None, threads: int = 0):
+    """Returns (status, y) with y float64 [len(tokens) or T, H].
+
+    Shapes: x [T,H]; topk_ids/topk_weights [T,K]; mapping [T]; ranks/scalings [L];
+    w_gate_up [E,2I,H]; w_down [E,H,I]; lora_a_gu [L,E,2,R,H]; lora_b_gu [L,E,2,I,R];
+    lora_a_down [L,E,R,I]; lora_b_down [L,E,H,R].  Weight operands must all share
+    one dtype (bf16 bits or float64).
+    """
+    x_np = np.asarray(x)
+    T, H = x_np.shape
+    topk_ids = _i32(topk_ids)
+    K = topk_ids.shape[1]
+    topk_weights = np.ascontiguousarray(np.asarray(topk_weights, dtype=np.float32))
+    mapping = _i32(token_lora_mapping)
+    lora_ranks = _i32(lora_ranks)
+    scalings = np.ascontiguousarray(np.asarray(scalings, dtype=np.float32))
+    E, I2, H2 = np.asarray(w_gate_up).shape
+    I = I2 // 2
+    L, _, _, R, _ = np.asarray(lora_a_gu).shape
+    assert H2 == H and np.asarray(w_down).shape == (E, H, I)
+    assert np.asarray(lora_b_gu).shape == (L, E, 2, I, R)
+    assert np.asarray(lora_a_down).shape == (L, E, R, I)
+    assert np.asarray(lora_b_down).shape == (L, E, H, R)
+    xp, xdt, xk = _operand(x_np)
+    ops = [_operand(a) for a in (w_gate_up, w_down, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down)]
+    wdt = ops[0][1]
+    if any(o[1] != wdt for o in ops):
+        raise TypeError("weight operands must share one dtype")
+    if tokens is None:
+        tok = None
+        n_out = T
+        tok_ptr = None
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        n_out = tok.shape[0]
+        tok_ptr = tok.ctypes.data
+    y = np.zeros((n_out, H), dtype=np.float64)
+    st = _load().oracle_forward(
+        xp, xdt, topk_ids.ctypes.data, topk_weights.ctypes.data, mapping.ctypes.data,
+        lora_ranks.ctypes.data, scalings.ctypes.data,
+        ops[0][0], ops[1][0], ops[2][0], ops[3][0], ops[4][0], ops[5][0], wdt,
+        T, K, E, H, I, L, R, tok_ptr, n_out, y.ctypes.data, int(threads))
+    del xk, tok
+    return int(st), y

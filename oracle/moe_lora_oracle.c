@@ -1,0 +1,348 @@
+/*
+ * moe_lora_oracle.c -- plain, slow, obviously-correct CPU oracle for the
+ * multi-adapter LoRA mixture-of-experts expert layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library under lora_moe_expert_info_gb300/csrc.
+ *
+ * Sources (web pages summarising sglang pull requests):
+ *   [PR14105] "LoRA on MoE expert layers" page, section 实现拆解 (implementation
+ *             breakdown): the layer formula
+ *               y = (W_down + a/r B_d A_d)[SiLU((W_gate + a/r B_g A_g)x)
+ *                                          (.) ((W_up + a/r B_u A_u)x)],
+ *             the align kernel that orders tokens by LoRA adapter and expert
+ *             id, and the 4-D adapter stack [num_loras, num_experts, rank, dim].
+ *   [PR24160] "shared MoE LoRA batch info" page, sections 实现拆解 and
+ *             关键源码片段 (MoELoRABatchInfo dataclass; test_moe_lora_info.py):
+ *             token_lora_mapping = repeat_interleave(weight_indices, seg_lens),
+ *             adapter_enabled = scatter of (rank > 0) at weight_indices, -1 means
+ *             "no adapter", and the "under-covers tokens" launch check.
+ *
+ * Precision: every floating-point sum is accumulated in double.  bf16 inputs
+ * are widened exactly (a bf16 value is the top 16 bits of a float).
+ *
+ * Readings taken where the pages are silent (each also listed in the design
+ * notes):
+ *   - weight_indices == -1 copies -1 into the mapping and never touches
+ *     adapter_enabled; slots no request uses are 0.
+ *   - align key order is expert-major, adapter-minor, with "no adapter" (-1)
+ *     first inside each expert; ties keep ascending pair index p = t*K + k.
+ *     Every non-empty bucket is padded to a multiple of block_size with the
+ *     sentinel P = T*K.
+ *   - the top-k weight multiplies the whole expert output, LoRA delta
+ *     included; an adapter contributes iff its id is >= 0 and its rank > 0;
+ *     only the first rank columns/rows of the zero-padded stacks are read.
+ *
+ * Parity pins (see tests/test_oracle_*.py): the worked mapping example of
+ * [PR24160]; torch.repeat_interleave on random segments; brute-force sorted()
+ * for align; a dense SwiGLU MLP via torch for one expert; dense-materialised
+ * W + s*B*A against the factored form; base identity for B = 0, adapter -1
+ * and rank 0; linearity and permutation invariances of the top-k combine.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_INVALID (-1)
+#define ORC_UNDERCOVERED (-2)
+#define ORC_INDEX (-3)
+#define ORC_CAPACITY (-4)
+#define ORC_NOMEM (-7)
+
+/* ------------------------------------------------------------------------ */
+/* batch info  ([PR24160] 实现拆解 items 1-3; 关键源码片段: dataclass fields and  */
+/* the expected-value rules of test_compute_moe_lora_info_expands_segments)  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * seg_indptr[bs+1], weight_indices[bs], lora_ranks[num_loras]
+ *   -> token_lora_mapping[num_tokens], adapter_enabled[num_loras].
+ * max_len > 0 is the launch hint of the page's kernel: a launch of bs segments
+ * of at most max_len tokens each under-covers the batch when
+ * bs * max_len < num_tokens or some segment is longer than max_len.
+ */
+int oracle_batch_info(const int32_t* seg_indptr, const int32_t* weight_indices,
+                      const int32_t* lora_ranks, int32_t bs, int32_t num_loras,
+                      int32_t num_tokens, int32_t max_len,
+                      int32_t* token_lora_mapping, int32_t* adapter_enabled) {
+  if (bs < 0 || num_loras < 0 || num_tokens < 0 || max_len < 0) return ORC_INVALID;
+  if (seg_indptr[0] != 0 || seg_indptr[bs] != num_tokens) return ORC_INVALID;
+  for (int32_t i = 0; i < bs; ++i)
+    if (seg_indptr[i + 1] < seg_indptr[i]) return ORC_INVALID;
+  if (max_len > 0) {
+    if ((int64_t)bs * (int64_t)max_len < (int64_t)num_tokens) return ORC_UNDERCOVERED;
+    for (int32_t i = 0; i < bs; ++i)
+      if (seg_indptr[i + 1] - seg_indptr[i] > max_len) return ORC_UNDERCOVERED;
+  }
+  for (int32_t i = 0; i < bs; ++i)
+    if (weight_indices[i] < -1 || weight_indices[i] >= num_loras) return ORC_INDEX;
+
+  /* token_lora_mapping: request i's adapter repeated over its segment. */
+  for (int32_t i = 0; i < bs; ++i)
+    for (int32_t t = seg_indptr[i]; t < seg_indptr[i + 1]; ++t)
+      token_lora_mapping[t] = weight_indices[i];
+
+  /* adapter_enabled: zeros, then 1 at each used slot whose rank is > 0. */
+  for (int32_t l = 0; l < num_loras; ++l) adapter_enabled[l] = 0;
+  for (int32_t i = 0; i < bs; ++i) {
+    int32_t l = weight_indices[i];
+    if (l >= 0) adapter_enabled[l] = (lora_ranks[l] > 0) ? 1 : 0;
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* (lora, expert) align  ([PR14105] 实现拆解: the align kernel sorts tokens by  */
+/* LoRA adapter and expert id; block_size padding as in the page's name)     */
+/* ------------------------------------------------------------------------ */
+
+/* Upper bound on the padded length: every non-empty bucket adds < block_size. */
+int64_t oracle_align_capacity(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                              int32_t num_loras, int32_t block_size) {
+  if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_loras < 0 || block_size < 1)
+    return -1;
+  int64_t P = (int64_t)num_tokens * topk;
+  int64_t NB = (int64_t)num_experts * (num_loras + 1);
+  int64_t buckets = P < NB ? P : NB;
+  int64_t n = P + buckets * (block_size - 1);
+  return (n + block_size - 1) / block_size * block_size;
+}
+
+/*
+ * topk_ids[T*K] (expert of pair p = t*K + k), token_lora_mapping[T]
+ *   -> sorted_token_ids[capacity] (pair ids; pad slots hold P),
+ *      block_expert_ids[capacity/block_size], block_lora_ids[...],
+ *      *num_tokens_post_pad.
+ * A stable counting sort on key = e*(L+1) + (lora+1).
+ */
+int oracle_align(const int32_t* topk_ids, const int32_t* token_lora_mapping,
+                 int32_t num_tokens, int32_t topk, int32_t num_experts, int32_t num_loras,
+                 int32_t block_size, int32_t* sorted_token_ids, int32_t* block_expert_ids,
+                 int32_t* block_lora_ids, int32_t* num_tokens_post_pad, int64_t capacity) {
+  if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_loras < 0 || block_size < 1)
+    return ORC_INVALID;
+  const int64_t P = (int64_t)num_tokens * topk;
+  if (P >= INT32_MAX) return ORC_INVALID;
+  const int64_t C = (int64_t)num_loras + 1;      /* adapter classes per expert */
+  const int64_t NB = (int64_t)num_experts * C;   /* buckets                    */
+
+  int64_t* count = (int64_t*)calloc((size_t)NB, sizeof(int64_t));
+  int64_t* start = (int64_t*)calloc((size_t)NB, sizeof(int64_t));
+  int64_t* cursor = (int64_t*)calloc((size_t)NB, sizeof(int64_t));
+  if (!count || !start || !cursor) {
+    free(count); free(start); free(cursor);
+    return ORC_NOMEM;
+  }
+
+  /* 1. count pairs per bucket, rejecting ids outside their ranges */
+  for (int64_t p = 0; p < P; ++p) {
+    int32_t e = topk_ids[p];
+    int32_t l = token_lora_mapping[p / topk];
+    if (e < 0 || e >= num_experts || l < -1 || l >= num_loras) {
+      free(count); free(start); free(cursor);
+      return ORC_INDEX;
+    }
+    count[(int64_t)e * C + (l + 1)] += 1;
+  }
+
+  /* 2. bucket starts: exclusive running sum of counts rounded up to block_size */
+  int64_t total = 0;
+  for (int64_t b = 0; b < NB; ++b) {
+    start[b] = total;
+    total += (count[b] + block_size - 1) / block_size * block_size;
+  }
+  if (total > capacity) {
+    free(count); free(start); free(cursor);
+    return ORC_CAPACITY;
+  }
+
+  /* 3. place pairs in increasing p: stable within a bucket */
+  for (int64_t b = 0; b < NB; ++b) cursor[b] = start[b];
+  for (int64_t p = 0; p < P; ++p) {
+    int64_t b = (int64_t)topk_ids[p] * C + (token_lora_mapping[p / topk] + 1);
+    sorted_token_ids[cursor[b]] = (int32_t)p;
+    cursor[b] += 1;
+  }
+
+  /* 4. pad each bucket's tail with the sentinel P; label its blocks */
+  for (int64_t b = 0; b < NB; ++b) {
+    int64_t padded = (count[b] + block_size - 1) / block_size * block_size;
+    for (int64_t j = count[b]; j < padded; ++j) sorted_token_ids[start[b] + j] = (int32_t)P;
+    for (int64_t blk = start[b] / block_size; blk < (start[b] + padded) / block_size; ++blk) {
+      block_expert_ids[blk] = (int32_t)(b / C);
+      block_lora_ids[blk] = (int32_t)(b % C) - 1;
+    }
+  }
+  *num_tokens_post_pad = (int32_t)total;
+
+  free(count); free(start); free(cursor);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* forward  ([PR14105] 实现拆解: FusedMoEWithLoRA formula; top-k weighted sum  */
+/* over the selected experts; 4-D stacks [num_loras, num_experts, rank, dim]) */
+/* ------------------------------------------------------------------------ */
+
+/* dtype 0: bf16 bit patterns (uint16); dtype 1: IEEE double. */
+static double ld(const void* base, int dtype, int64_t idx) {
+  if (dtype == 0) {
+    uint32_t u = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+  }
+  return ((const double*)base)[idx];
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * Layouts (row-major):
+ *   x           [T, H]
+ *   topk_ids    [T, K] int32, topk_weights [T, K] float
+ *   mapping     [T] int32 in [-1, L);  lora_ranks [L] int32; scalings [L] float
+ *   w_gate_up   [E, 2I, H]   rows 0..I-1 gate, I..2I-1 up
+ *   w_down      [E, H, I]
+ *   lora_a_gu   [L, E, 2, R, H]   index 0 = gate, 1 = up
+ *   lora_b_gu   [L, E, 2, I, R]
+ *   lora_a_down [L, E, R, I]
+ *   lora_b_down [L, E, H, R]
+ *   y           [n_out, H] double, row j for token tokens[j] (or j if tokens == NULL)
+ */
+int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
+                   const float* topk_weights, const int32_t* token_lora_mapping,
+                   const int32_t* lora_ranks, const float* scalings,
+                   const void* w_gate_up, const void* w_down, const void* lora_a_gu,
+                   const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                   int w_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                   int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                   int num_threads) {
+  if (T < 0 || K < 1 || E < 1 || H < 1 || I < 1 || L < 0 || R < 0 || n_out < 0)
+    return ORC_INVALID;
+  for (int64_t l = 0; l < L; ++l)
+    if (lora_ranks[l] < 0 || lora_ranks[l] > R) return ORC_INVALID;
+  for (int64_t j = 0; j < n_out; ++j) {
+    int64_t t = tokens ? tokens[j] : j;
+    if (t < 0 || t >= T) return ORC_INVALID;
+    if (token_lora_mapping[t] < -1 || token_lora_mapping[t] >= L) return ORC_INDEX;
+    for (int64_t k = 0; k < K; ++k)
+      if (topk_ids[t * K + k] < 0 || topk_ids[t * K + k] >= E) return ORC_INDEX;
+  }
+  int status = ORC_OK;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+
+#pragma omp parallel
+  {
+    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    double* zg = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+    double* zu = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+    double* zd = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
+    const int ok = xv && a && zg && zu && zd;
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_out; ++j) {
+      if (!ok) {
+#pragma omp atomic write
+        status = ORC_NOMEM;
+        continue;
+      }
+      {
+        const int64_t t = tokens ? tokens[j] : j;
+        double* yrow = y + j * H;
+        for (int64_t h = 0; h < H; ++h) yrow[h] = 0.0;
+        for (int64_t h = 0; h < H; ++h) xv[h] = ld(x, x_dtype, t * H + h);
+
+        const int32_t l = token_lora_mapping[t];
+        const int used = (l >= 0) && (lora_ranks[l] > 0);
+        const int64_t r = used ? lora_ranks[l] : 0;
+        const double s = used ? (double)scalings[l] : 0.0;
+
+        for (int64_t k = 0; k < K; ++k) {
+          const int64_t e = topk_ids[t * K + k];
+          const double w = (double)topk_weights[t * K + k];
+
+          /* LoRA shrink for gate and up: z = A x (first r rows only) */
+          for (int64_t q = 0; q < r; ++q) {
+            const int64_t ag = (((l * E + e) * 2 + 0) * R + q) * H;
+            const int64_t au = (((l * E + e) * 2 + 1) * R + q) * H;
+            double sg = 0.0, su = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+              sg += ld(lora_a_gu, w_dtype, ag + h) * xv[h];
+              su += ld(lora_a_gu, w_dtype, au + h) * xv[h];
+            }
+            zg[q] = sg;
+            zu[q] = su;
+          }
+
+          /* gate and up projections, each with its own LoRA delta; SiLU(g) * u */
+          for (int64_t i = 0; i < I; ++i) {
+            const int64_t wg = (e * 2 * I + i) * H;
+            const int64_t wu = (e * 2 * I + I + i) * H;
+            double g = 0.0, u = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+              g += ld(w_gate_up, w_dtype, wg + h) * xv[h];
+              u += ld(w_gate_up, w_dtype, wu + h) * xv[h];
+            }
+            if (r > 0) {
+              const int64_t bg = (((l * E + e) * 2 + 0) * I + i) * R;
+              const int64_t bu = (((l * E + e) * 2 + 1) * I + i) * R;
+              double dg = 0.0, du = 0.0;
+              for (int64_t q = 0; q < r; ++q) {
+                dg += ld(lora_b_gu, w_dtype, bg + q) * zg[q];
+                du += ld(lora_b_gu, w_dtype, bu + q) * zu[q];
+              }
+              g += s * dg;
+              u += s * du;
+            }
+            a[i] = silu(g) * u;
+          }
+
+          /* LoRA shrink for down: zd = A_d a */
+          for (int64_t q = 0; q < r; ++q) {
+            const int64_t ad = ((l * E + e) * R + q) * I;
+            double sd = 0.0;
+            for (int64_t i = 0; i < I; ++i) sd += ld(lora_a_down, w_dtype, ad + i) * a[i];
+            zd[q] = sd;
+          }
+
+          /* down projection with its LoRA delta, weighted into y */
+          for (int64_t h = 0; h < H; ++h) {
+            const int64_t wd = (e * H + h) * I;
+            double d = 0.0;
+            for (int64_t i = 0; i < I; ++i) d += ld(w_down, w_dtype, wd + i) * a[i];
+            if (r > 0) {
+              const int64_t bd = ((l * E + e) * H + h) * R;
+              double dd = 0.0;
+              for (int64_t q = 0; q < r; ++q) dd += ld(lora_b_down, w_dtype, bd + q) * zd[q];
+              d += s * dd;
+            }
+            yrow[h] += w * d;
+          }
+        }
+      }
+    }
+    free(xv); free(a); free(zg); free(zu); free(zd);
+  }
+  return status;
+}
+
+/* Threads the OpenMP runtime would use (reported beside the CPU timing). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
