@@ -1,0 +1,173 @@
+/*
+ * moe_lora.h -- C ABI of the GB300 (sm_103a) multi-adapter LoRA MoE expert layer.
+ *
+ * The layer (sglang PR #14105 page, "LoRA on MoE expert layers", section
+ * 实现拆解, FusedMoEWithLoRA formula), per token t with adapter l = mapping[t]:
+ *
+ *   y_t = sum_k w[t,k] * (W_down,e + s_l B_d A_d) [ SiLU((W_gate,e + s_l B_g A_g) x_t)
+ *                                                   (.) ((W_up,e + s_l B_u A_u) x_t) ]
+ *
+ * with e = topk_ids[t,k], s_l = alpha_l / r_l, and the adapter used iff l >= 0
+ * and r_l > 0.  The per-batch adapter metadata follows the sglang PR #24160
+ * page ("shared MoE LoRA batch info", sections 实现拆解 and 关键源码片段:
+ * MoELoRABatchInfo and test_moe_lora_info.py).
+ *
+ * Conventions for every call:
+ *   - Array pointers are DEVICE memory owned by the caller unless a comment
+ *     says otherwise.  The library never allocates device memory: scratch is the
+ *     caller's `workspace` of at least the size the matching *_workspace_bytes()
+ *     query returns, 256-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void*.  Every call only enqueues work
+ *     on it and never synchronises the device or the stream.
+ *   - The return value is a host-detected status (MLR_OK or a negative
+ *     MLR_ERR_*).  On an error return nothing was enqueued.
+ *   - `d_status` (nullable, device int32) receives device-detected errors as
+ *     OR-ed MLR_STATUS_* bits; the library never clears it (the caller zeroes it).
+ *     Kernels never trap: on bad input they set a bit, skip the offending
+ *     element and keep every write inside the caller's buffers.
+ *   - bf16 operands are passed as their 16-bit patterns (mlr_bf16).
+ *   - All int32 ids; pair index p = t*topk + k for token t and slot k.
+ */
+#ifndef MOE_LORA_H_
+#define MOE_LORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host return codes */
+#define MLR_OK 0
+#define MLR_ERR_INVALID (-1)      /* bad scalar argument or null pointer          */
+#define MLR_ERR_UNDERCOVERED (-2) /* bs * max_len < num_tokens ("under-covers")   */
+#define MLR_ERR_INDEX (-3)        /* an id outside its range (host-visible cases)  */
+#define MLR_ERR_CAPACITY (-4)     /* output capacity or workspace too small        */
+#define MLR_ERR_CUDA (-5)         /* a CUDA launch or driver call failed           */
+#define MLR_ERR_TIMEOUT (-6)      /* reserved: device wait timed out (see status)  */
+#define MLR_ERR_UNSUPPORTED (-8)  /* shape outside what the kernels implement      */
+
+/* device status bits, OR-ed into *d_status */
+#define MLR_STATUS_BAD_INDPTR 0x01   /* seg_indptr not 0..num_tokens non-decreasing    */
+#define MLR_STATUS_UNDERCOVERED 0x02 /* a segment is longer than max_len               */
+#define MLR_STATUS_INDEX 0x04        /* adapter or expert id out of range (skipped)     */
+#define MLR_STATUS_CAPACITY 0x08     /* padded length exceeded capacity (truncated)     */
+#define MLR_STATUS_TIMEOUT 0x10      /* a pipeline wait gave up; results are invalid    */
+#define MLR_STATUS_RANK 0x20         /* lora_ranks[l] outside [0, max_rank]             */
+
+typedef uint16_t mlr_bf16; /* bfloat16 bit pattern */
+
+/* Library version string (static storage). */
+const char* moe_lora_version(void);
+
+/* Human-readable text for an MLR_OK / MLR_ERR_* code (static storage). */
+const char* moe_lora_status_string(int code);
+
+/*
+ * moe_lora_batch_info -- once per batch, expand request segments into the
+ * per-token adapter map and the per-slot enabled mask.
+ * Source: sglang PR #24160 page, 实现拆解 items 1-3 (MoELoRABatchInfo fields,
+ * _compute_moe_lora_info computed once per batch) and 关键源码片段
+ * (test_compute_moe_lora_info_expands_segments / ..._rejects_undercovered_launch).
+ *
+ *   seg_indptr[bs+1]      request segment offsets, 0 = seg_indptr[0] <= ... <= seg_indptr[bs] = num_tokens
+ *   weight_indices[bs]    adapter slot of each request, in [-1, num_loras); -1 = no adapter
+ *   lora_ranks[num_loras] rank of each slot (0 = slot holds no adapter)
+ *   max_len               0: no hint.  > 0: the longest segment the caller promises;
+ *                         bs * max_len < num_tokens returns MLR_ERR_UNDERCOVERED (host),
+ *                         a longer segment sets MLR_STATUS_UNDERCOVERED (device)
+ *   token_lora_mapping    out [>= num_tokens]: weight_indices of the token's request.
+ *                         Entries at and beyond num_tokens are never written.
+ *   adapter_enabled       out [num_loras]: 1 iff some request uses the slot and its rank
+ *                         is > 0, else 0 (every entry written; -1 requests are skipped)
+ * Limits: 0 <= bs, num_tokens < 2^31; 0 <= num_loras <= 65536.
+ */
+int moe_lora_batch_info(const int32_t* seg_indptr, const int32_t* weight_indices,
+                        const int32_t* lora_ranks, int32_t bs, int32_t num_loras,
+                        int32_t num_tokens, int32_t max_len, int32_t* token_lora_mapping,
+                        int32_t* adapter_enabled, int32_t* d_status, void* stream);
+
+/*
+ * moe_lora_align_capacity -- length the sorted_token_ids buffer must have:
+ * roundup(P + min(P, E*(L+1)) * (block_size-1), block_size) with P = num_tokens*topk.
+ * The block arrays need capacity / block_size entries.  Returns -1 on bad sizes.
+ */
+int64_t moe_lora_align_capacity(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                int32_t num_loras, int32_t block_size);
+
+/* Scratch bytes moe_lora_align needs for these sizes (0 on bad sizes). */
+size_t moe_lora_align_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                      int32_t num_loras, int32_t block_size);
+
+/*
+ * moe_lora_align -- per layer, bucket the (token, slot) pairs by (expert, adapter).
+ * Source: sglang PR #14105 page, 实现拆解 (moe_lora_align_block_size: sorts tokens by
+ * LoRA adapter and expert id; padded to block_size).
+ *
+ * Order: key(p) = e*(L+1) + (lora(t)+1) with e = topk_ids[p], lora(t) =
+ * token_lora_mapping[t] in [-1, L): expert-major, "no adapter" first inside an
+ * expert, then adapters by id; inside a bucket pairs keep ascending p (stable).
+ * Each non-empty bucket is padded to a multiple of block_size with the sentinel P.
+ *
+ *   topk_ids[T*K], token_lora_mapping[T]        inputs
+ *   sorted_token_ids[capacity]                  out: pair ids, pads = P; valid prefix
+ *                                               [0, *num_tokens_post_pad)
+ *   block_expert_ids, block_lora_ids[capacity/block_size]
+ *                                               out: expert and adapter (-1 = none) of
+ *                                               each block of the valid prefix
+ *   num_tokens_post_pad[1]                      out (device)
+ * Ids out of range set MLR_STATUS_INDEX and the pair is dropped; a padded length
+ * above capacity sets MLR_STATUS_CAPACITY and writes stop at capacity.
+ * Limits: T*K < 2^31, E*(L+1) <= 40960, 1 <= block_size <= 4096.
+ */
+int moe_lora_align(const int32_t* topk_ids, const int32_t* token_lora_mapping,
+                   int32_t num_tokens, int32_t topk, int32_t num_experts, int32_t num_loras,
+                   int32_t block_size, int32_t* sorted_token_ids, int32_t* block_expert_ids,
+                   int32_t* block_lora_ids, int32_t* num_tokens_post_pad, int64_t capacity,
+                   void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
+
+/* Scratch bytes fused_moe_lora_forward needs for these sizes (0 on bad sizes). */
+size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                      int32_t hidden, int32_t intermediate, int32_t num_loras,
+                                      int32_t max_rank);
+
+/*
+ * fused_moe_lora_forward -- the LoRA MoE expert layer (formula at the top).
+ * Source: sglang PR #14105 page, 实现拆解 (FusedMoEWithLoRA: LoRA after gate_up and
+ * before down; align kernel; fused LoRA A/B kernel; 4-D stacks
+ * [num_loras, num_experts, rank, dim]); the top-k weighted sum over experts.
+ *
+ *   x             bf16 [T, H]
+ *   topk_ids      int32 [T, K] in [0, E);  topk_weights float [T, K]
+ *   token_lora_mapping int32 [T] in [-1, L) (from moe_lora_batch_info)
+ *   lora_ranks    int32 [L] in [0, R];  scalings float [L] = alpha_l / r_l
+ *   w_gate_up     bf16 [E, 2I, H]   rows 0..I-1 gate, rows I..2I-1 up
+ *   w_down        bf16 [E, H, I]
+ *   lora_a_gu     bf16 [L, E, 2, R, H]   [.., 0, ..] gate, [.., 1, ..] up
+ *   lora_b_gu     bf16 [L, E, 2, I, R]
+ *   lora_a_down   bf16 [L, E, R, I]
+ *   lora_b_down   bf16 [L, E, H, R]
+ *   y             bf16 [T, H] out
+ * Stacks hold slot l's factors in the first r_l rank rows/columns; the rank
+ * padding must be finite (the adapter pool keeps it zero).  Accumulation is
+ * fp32; the gate/up activation and the LoRA intermediates are rounded to bf16.
+ * Runs the align internally (block 16).  Requirements: H, I, R multiples of 8,
+ * H, I >= 64, R <= 256, every base pointer 16-byte aligned.
+ * The top-k combine uses fp32 atomics, so y may differ in the last bits between runs.
+ */
+int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                           const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                           const float* scalings, const mlr_bf16* w_gate_up,
+                           const mlr_bf16* w_down, const mlr_bf16* lora_a_gu,
+                           const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                           const mlr_bf16* lora_b_down, int32_t num_tokens, int32_t topk,
+                           int32_t num_experts, int32_t hidden, int32_t intermediate,
+                           int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
+                           size_t ws_bytes, int32_t* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H_ */

@@ -1,0 +1,355 @@
+// align.cu -- moe_lora_align: bucket (token, slot) pairs by (expert, adapter),
+// stable, each bucket padded to block_size (sglang PR #14105 page, 实现拆解:
+// moe_lora_align_block_size "sorts tokens by LoRA adapter and expert id").
+//
+// key(p) = e * (L+1) + (lora + 1); NB = E * (L+1) buckets.  Pairs are split
+// into G contiguous chunks of up to 32768 pairs.  Four launches:
+//   1. count    : per chunk, a shared-memory histogram over NB buckets
+//                 -> cnt[g][b]
+//   2. colscan  : per bucket, exclusive prefix over chunks (in place) and the
+//                 bucket total
+//   3. bktscan  : one block, exclusive scan of the padded totals -> bucket
+//                 starts and num_tokens_post_pad
+//   4. scatter  : per chunk, stable local ranks and the final placement
+//                 (plus the pad sentinels and the per-block expert/adapter ids)
+// Stability inside a chunk: pairs are visited in rounds of 1024 consecutive
+// indices separated by barriers, so a bucket's slots follow round order; the
+// few same-round neighbours of a pair are re-ranked by index when it is placed.
+#include "mlr_align.cuh"
+
+namespace mlr {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kMaxItems = 32;                         // pairs per thread per chunk
+constexpr int kMaxChunk = kThreads * kMaxItems;       // 32768 (fits uint16 indices)
+constexpr int kColThreads = 256;
+
+__device__ __forceinline__ int pair_key(const int32_t* __restrict__ topk_ids,
+                                        const int32_t* __restrict__ mapping, int64_t p, int topk,
+                                        int E, int C, int L, int& bad) {
+  const int e = __ldg(topk_ids + p);
+  const int l = __ldg(mapping + p / topk);
+  if (e < 0 || e >= E || l < -1 || l >= L) {
+    bad |= MLR_STATUS_INDEX;
+    return -1;
+  }
+  return e * C + (l + 1);
+}
+
+// Block-wide exclusive scan of s[0..n) in place; s[n] receives the total.
+__device__ void block_exclusive_scan(uint32_t* s, int n) {
+  __shared__ uint32_t warp_tot[32];
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
+  uint32_t local = 0;
+  for (int b = b0; b < b1; ++b) local += s[b];
+  // inclusive warp scan of the per-thread sums
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    uint32_t w = lane < nw ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    if (lane < nw) warp_tot[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  uint32_t run = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0u);
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = s[b];
+    s[b] = run;
+    run += c;
+  }
+  if (threadIdx.x == blockDim.x - 1) s[n] = run;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads)
+align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
+                   int64_t P, int topk, int E, int L, int chunk, uint32_t* __restrict__ cnt,
+                   int32_t* d_status) {
+  extern __shared__ uint32_t hist[];
+  const int C = L + 1, NB = E * C;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0u;
+  __syncthreads();
+  const int64_t p0 = (int64_t)blockIdx.x * chunk;
+  const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
+  int bad = 0;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int key = pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
+    if (key >= 0) atomicAdd(&hist[key], 1u);
+  }
+  if (bad) set_status(d_status, bad);
+  __syncthreads();
+  uint32_t* row = cnt + (int64_t)blockIdx.x * NB;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) row[b] = hist[b];
+}
+
+__global__ void __launch_bounds__(kColThreads)
+align_colscan_kernel(uint32_t* __restrict__ cnt, int G, int NB, uint32_t* __restrict__ btotal) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= NB) return;
+  uint32_t run = 0;
+  int g = 0;
+  for (; g + 4 <= G; g += 4) {
+    uint32_t c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = cnt[(int64_t)(g + q) * NB + b];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      cnt[(int64_t)(g + q) * NB + b] = run;
+      run += c[q];
+    }
+  }
+  for (; g < G; ++g) {
+    const uint32_t c = cnt[(int64_t)g * NB + b];
+    cnt[(int64_t)g * NB + b] = run;
+    run += c;
+  }
+  btotal[b] = run;
+}
+
+__global__ void __launch_bounds__(kThreads)
+align_bucketscan_kernel(const uint32_t* __restrict__ btotal, int NB, int block_size,
+                        uint32_t* __restrict__ bstart, int32_t* __restrict__ num_post_pad,
+                        int64_t capacity, int32_t* d_status) {
+  // bstart[0..NB] holds padded totals, then is scanned in place.
+  for (int b = threadIdx.x; b < NB; b += blockDim.x)
+    bstart[b] = (btotal[b] + block_size - 1) / block_size * block_size;
+  __syncthreads();
+  // per-thread contiguous ranges read global memory; fine for one block
+  __shared__ uint32_t warp_tot[32];
+  const int per = (NB + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
+  uint32_t local = 0;
+  for (int b = b0; b < b1; ++b) local += bstart[b];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    uint32_t w = lane < nw ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    if (lane < nw) warp_tot[lane] = w;
+  }
+  __syncthreads();
+  uint32_t run = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0u);
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = bstart[b];
+    bstart[b] = run;
+    run += c;
+  }
+  if (threadIdx.x == blockDim.x - 1) {
+    bstart[NB] = run;
+    *num_post_pad = (int32_t)run;
+    if ((int64_t)run > capacity) set_status(d_status, MLR_STATUS_CAPACITY);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
+                     int64_t P, int topk, int E, int L, int chunk, int block_size,
+                     const uint32_t* __restrict__ cnt, const uint32_t* __restrict__ btotal,
+                     const uint32_t* __restrict__ bstart, int32_t* __restrict__ sorted_ids,
+                     int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
+                     int64_t capacity) {
+  extern __shared__ uint32_t smem[];
+  const int C = L + 1, NB = E * C;
+  uint32_t* off = smem;                                             // [NB + 1]
+  uint16_t* stage = reinterpret_cast<uint16_t*>(smem + NB + 1);     // [chunk]
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) off[b] = 0u;
+  __syncthreads();
+
+  const int64_t p0 = (int64_t)blockIdx.x * chunk;
+  const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
+  const int rounds = (n + kThreads - 1) / kThreads;
+  // (key << 16) | slot per pair; key < 40960 and slot < 32768 both fit 16 bits
+  uint32_t ks[kMaxItems];
+  int bad = 0;
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it) {
+    if (it < rounds) {
+      const int j = it * kThreads + threadIdx.x;
+      ks[it] = 0xFFFFFFFFu;
+      if (j < n) {
+        const int key = pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
+        if (key >= 0) ks[it] = ((uint32_t)key << 16) | atomicAdd(&off[key], 1u);
+      }
+      __syncthreads();  // rounds are ordered: a bucket's slots follow round order
+    }
+  }
+  block_exclusive_scan(off, NB);
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it)
+    if (it < rounds && ks[it] != 0xFFFFFFFFu)
+      stage[off[ks[it] >> 16] + (ks[it] & 0xFFFFu)] = (uint16_t)(it * kThreads + threadIdx.x);
+  __syncthreads();
+
+  const uint32_t* crow = cnt + (int64_t)blockIdx.x * NB;
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it) {
+    if (it < rounds && ks[it] != 0xFFFFFFFFu) {
+      const int k = (int)(ks[it] >> 16);
+      const uint32_t j = it * kThreads + threadIdx.x;
+      const int lo = (int)off[k], hi = (int)off[k + 1];
+      const int pos = lo + (int)(ks[it] & 0xFFFFu);
+      // same-round neighbours form one contiguous run around pos
+      int less = 0, m = pos - 1;
+      while (m >= lo && (stage[m] >> 10) == (uint32_t)it) {
+        less += stage[m] < j;
+        --m;
+      }
+      const int round_start = m + 1;
+      for (m = pos + 1; m < hi && (stage[m] >> 10) == (uint32_t)it; ++m) less += stage[m] < j;
+      const int64_t dst = (int64_t)bstart[k] + crow[k] + (round_start - lo) + less;
+      if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + j);
+    }
+  }
+
+  // pad sentinels and per-block labels: buckets are shared out over all threads
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t cap_blocks = capacity / block_size;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < NB; b += nthreads) {
+    const int64_t s = bstart[b], e = bstart[b + 1];
+    if (s == e) continue;
+    for (int64_t q = s + btotal[b]; q < e && q < capacity; ++q) sorted_ids[q] = (int32_t)P;
+    const int expert = (int)(b / C), lora = (int)(b % C) - 1;
+    for (int64_t blk = s / block_size; blk < e / block_size && blk < cap_blocks; ++blk) {
+      block_expert[blk] = expert;
+      block_lora[blk] = lora;
+    }
+  }
+}
+
+}  // namespace
+
+AlignPlan align_plan(int32_t num_tokens, int32_t topk, int32_t num_experts, int32_t num_loras,
+                     int32_t block_size) {
+  AlignPlan pl{};
+  pl.ok = false;
+  if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_loras < 0 || block_size < 1 ||
+      block_size > kMaxAlignBlock)
+    return pl;
+  pl.P = (int64_t)num_tokens * topk;
+  const int64_t NB = (int64_t)num_experts * (num_loras + 1);
+  if (pl.P >= INT32_MAX || NB > kMaxAlignBuckets) return pl;
+  pl.NB = (int)NB;
+  int64_t chunk = round_up(ceil_div(pl.P, 148), kThreads);
+  chunk = chunk < kThreads ? kThreads : (chunk > kMaxChunk ? kMaxChunk : chunk);
+  pl.chunk = (int)chunk;
+  pl.G = (int)ceil_div(pl.P, chunk);
+  const int64_t buckets = pl.P < NB ? pl.P : NB;
+  pl.capacity = round_up(pl.P + buckets * (block_size - 1), block_size);
+  if (pl.capacity >= INT32_MAX) return pl;
+  pl.cnt_off = 0;
+  pl.btotal_off = round_up((int64_t)pl.G * NB * 4, 256);
+  pl.bstart_off = pl.btotal_off + round_up(NB * 4, 256);
+  pl.ws_bytes = pl.bstart_off + round_up((NB + 1) * 4, 256);
+  pl.ok = true;
+  return pl;
+}
+
+size_t align_smem_count(const AlignPlan& pl) { return (size_t)pl.NB * 4; }
+size_t align_smem_scatter(const AlignPlan& pl) {
+  return (size_t)(pl.NB + 1) * 4 + round_up((int64_t)pl.chunk * 2, 16);
+}
+
+int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk,
+                 int E, int L, int block_size, int32_t* sorted_ids, int32_t* block_expert,
+                 int32_t* block_lora, int32_t* num_post_pad, int64_t capacity, void* workspace,
+                 int32_t* d_status, cudaStream_t stream) {
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.cnt_off);
+  uint32_t* btotal = reinterpret_cast<uint32_t*>(ws + pl.btotal_off);
+  uint32_t* bstart = reinterpret_cast<uint32_t*>(ws + pl.bstart_off);
+  const size_t sm_count = align_smem_count(pl), sm_scatter = align_smem_scatter(pl);
+  if (sm_scatter > 48 * 1024) {
+    if (cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_scatter) != cudaSuccess)
+      return MLR_ERR_CUDA;
+  }
+  if (sm_count > 48 * 1024) {
+    if (cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm_count) != cudaSuccess)
+      return MLR_ERR_CUDA;
+  }
+  if (pl.G > 0) {
+    align_count_kernel<<<pl.G, kThreads, sm_count, stream>>>(topk_ids, mapping, pl.P, topk, E, L,
+                                                             pl.chunk, cnt, d_status);
+    MLR_CHECK_LAUNCH();
+  }
+  align_colscan_kernel<<<(int)ceil_div(pl.NB, kColThreads), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB,
+                                                                                     btotal);
+  MLR_CHECK_LAUNCH();
+  align_bucketscan_kernel<<<1, kThreads, 0, stream>>>(btotal, pl.NB, block_size, bstart, num_post_pad,
+                                                      capacity, d_status);
+  MLR_CHECK_LAUNCH();
+  if (pl.G > 0) {
+    align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(
+        topk_ids, mapping, pl.P, topk, E, L, pl.chunk, block_size, cnt, btotal, bstart, sorted_ids,
+        block_expert, block_lora, capacity);
+    MLR_CHECK_LAUNCH();
+  }
+  return MLR_OK;
+}
+
+}  // namespace mlr
+
+extern "C" int64_t moe_lora_align_capacity(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                           int32_t num_loras, int32_t block_size) {
+  const mlr::AlignPlan pl = mlr::align_plan(num_tokens, topk, num_experts, num_loras, block_size);
+  return pl.ok ? pl.capacity : -1;
+}
+
+extern "C" size_t moe_lora_align_workspace_bytes(int32_t num_tokens, int32_t topk,
+                                                 int32_t num_experts, int32_t num_loras,
+                                                 int32_t block_size) {
+  const mlr::AlignPlan pl = mlr::align_plan(num_tokens, topk, num_experts, num_loras, block_size);
+  return pl.ok ? (size_t)pl.ws_bytes : 0;
+}
+
+extern "C" int moe_lora_align(const int32_t* topk_ids, const int32_t* token_lora_mapping,
+                              int32_t num_tokens, int32_t topk, int32_t num_experts,
+                              int32_t num_loras, int32_t block_size, int32_t* sorted_token_ids,
+                              int32_t* block_expert_ids, int32_t* block_lora_ids,
+                              int32_t* num_tokens_post_pad, int64_t capacity, void* workspace,
+                              size_t ws_bytes, int32_t* d_status, void* stream) {
+  using namespace mlr;
+  const AlignPlan pl = align_plan(num_tokens, topk, num_experts, num_loras, block_size);
+  if (!pl.ok) {
+    if (num_tokens < 0 || topk < 1 || num_experts < 1 || num_loras < 0 || block_size < 1)
+      return MLR_ERR_INVALID;
+    return MLR_ERR_UNSUPPORTED;
+  }
+  if (num_tokens_post_pad == nullptr || capacity < 0) return MLR_ERR_INVALID;
+  if (pl.P > 0 && (topk_ids == nullptr || token_lora_mapping == nullptr)) return MLR_ERR_INVALID;
+  if (capacity > 0 && (sorted_token_ids == nullptr || block_expert_ids == nullptr ||
+                       block_lora_ids == nullptr))
+    return MLR_ERR_INVALID;
+  if (workspace == nullptr || ws_bytes < (size_t)pl.ws_bytes) return MLR_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLR_ERR_INVALID;
+  return align_launch(pl, topk_ids, token_lora_mapping, topk, num_experts, num_loras, block_size,
+                      sorted_token_ids, block_expert_ids, block_lora_ids, num_tokens_post_pad,
+                      capacity, workspace, d_status, static_cast<cudaStream_t>(stream));
+}

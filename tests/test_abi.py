@@ -1,0 +1,90 @@
+"""The C-ABI library builds, loads and exports every function include/*.h declares.
+
+CPU only: nothing here launches a kernel.  The host-side argument checks that
+return before any CUDA call are exercised with never-dereferenced pointers.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import lora_moe_expert_info_gb300 as mlr
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return mlr.library()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("moe_lora_batch_info", "moe_lora_align", "fused_moe_lora_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_library_is_the_in_tree_build(lib):
+    assert os.path.realpath(lib._name).startswith(os.path.realpath(ROOT))
+    assert lib.moe_lora_version().decode().startswith("moe_lora")
+
+
+@pytest.mark.parametrize("T,K,E,L,bs", [(64, 2, 8, 4, 16), (4096, 8, 128, 8, 16), (0, 8, 4, 4, 16),
+                                        (1, 1, 100, 100, 16), (1048576, 8, 256, 64, 64)])
+def test_align_capacity_matches_oracle_bound(lib, T, K, E, L, bs):
+    assert mlr.moe_lora_align_capacity(T, K, E, L, bs) == oracle.align_capacity(T, K, E, L, bs)
+    assert mlr.moe_lora_align_workspace_bytes(T, K, E, L, bs) > 0
+
+
+def test_align_rejects_bad_sizes(lib):
+    assert mlr.moe_lora_align_capacity(-1, 2, 8, 4, 16) == -1
+    assert mlr.moe_lora_align_capacity(4, 0, 8, 4, 16) == -1
+    assert mlr.moe_lora_align_workspace_bytes(4, 2, 0, 4, 16) == 0
+    assert mlr.moe_lora_align_capacity(4, 2, 1024, 64, 16) == -1   # E*(L+1) above the limit
+
+
+def test_batch_info_host_checks(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the call returns before any launch
+    f = lib.moe_lora_batch_info
+    assert f(fake, fake, fake, -1, 4, 8, 0, fake, fake, None, None) == mlr.MLR_ERR_INVALID
+    assert f(None, fake, fake, 1, 4, 8, 0, fake, fake, None, None) == mlr.MLR_ERR_INVALID
+    # the page's under-covered launch: bs=1, max_len=1, 300 tokens
+    assert f(fake, fake, fake, 1, 1, 300, 1, fake, fake, None, None) == mlr.MLR_ERR_UNDERCOVERED
+    assert f(fake, fake, fake, 1, 70000, 8, 0, fake, fake, None, None) == mlr.MLR_ERR_UNSUPPORTED
+
+
+def test_align_host_checks(lib):
+    fake = ctypes.c_void_p(0x1000)
+    f = lib.moe_lora_align
+    ws = mlr.moe_lora_align_workspace_bytes(64, 2, 8, 4, 16)
+    cap = mlr.moe_lora_align_capacity(64, 2, 8, 4, 16)
+    assert f(fake, fake, 64, 2, 8, 4, 0, fake, fake, fake, fake, cap, fake, ws, None, None) \
+        == mlr.MLR_ERR_INVALID
+    assert f(fake, fake, 64, 2, 8, 4, 16, fake, fake, fake, fake, cap, fake, ws - 1, None, None) \
+        == mlr.MLR_ERR_CAPACITY
+    assert f(fake, fake, 64, 2, 8, 4, 16, fake, fake, fake, None, cap, fake, ws, None, None) \
+        == mlr.MLR_ERR_INVALID
+
+
+def test_status_strings(lib):
+    assert b"under-covers" in lib.moe_lora_status_string(mlr.MLR_ERR_UNDERCOVERED)
+    assert lib.moe_lora_status_string(0) == b"ok"
