@@ -166,6 +166,26 @@ int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const flo
                            int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
                            size_t ws_bytes, int32_t* d_status, void* stream);
 
+/*
+ * Observability.  The pages describe no tracing; these calls exist so that a
+ * caller can attribute the forward's GPU time to its stages without a profiler.
+ *
+ * moe_lora_profile_begin(max_calls): the next max_calls (<= 4096) forward calls
+ *   record a CUDA event on their stream between consecutive stages.  Returns
+ *   MLR_ERR_CUDA if the events cannot be created.
+ * moe_lora_profile_end(stage_ms, max_stages, n_stages, n_calls): blocks until the
+ *   recorded events complete, writes the summed milliseconds of each stage over
+ *   the recorded calls into stage_ms[0..min(max_stages, *n_stages)), the number of
+ *   recorded calls into *n_calls (host pointers), and stops recording.
+ * moe_lora_profile_stage_name(i): "align", "plan", "shrink_gate_up", "gate_up",
+ *   "shrink_down", "down", "convert" (static storage; NULL past the last stage).
+ * moe_lora_launch_count(): kernels this library has launched in this process.
+ */
+int moe_lora_profile_begin(int32_t max_calls);
+int moe_lora_profile_end(double* stage_ms, int32_t max_stages, int32_t* n_stages, int32_t* n_calls);
+const char* moe_lora_profile_stage_name(int32_t stage);
+uint64_t moe_lora_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,15 @@ def library() -> ctypes.CDLL:
             lib.moe_lora_align.restype = ctypes.c_int
             lib.moe_lora_align.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, i64,
                                            vp, sz, vp, vp]
+            lib.moe_lora_profile_begin.restype = ctypes.c_int
+            lib.moe_lora_profile_begin.argtypes = [i32]
+            lib.moe_lora_profile_end.restype = ctypes.c_int
+            lib.moe_lora_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), i32,
+                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            lib.moe_lora_profile_stage_name.restype = ctypes.c_char_p
+            lib.moe_lora_profile_stage_name.argtypes = [i32]
+            lib.moe_lora_launch_count.restype = ctypes.c_uint64
+            lib.moe_lora_launch_count.argtypes = []
             if hasattr(lib, "fused_moe_lora_forward"):
                 lib.fused_moe_lora_workspace_bytes.restype = sz
                 lib.fused_moe_lora_workspace_bytes.argtypes = [i32] * 7

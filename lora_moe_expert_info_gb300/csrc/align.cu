@@ -16,6 +16,7 @@
 // indices separated by barriers, so a bucket's slots follow round order; the
 // few same-round neighbours of a pair are re-ranked by index when it is placed.
 #include "mlr_align.cuh"
+#include "mlr_profile.cuh"
 
 namespace mlr {
 namespace {
@@ -298,18 +299,22 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
     align_count_kernel<<<pl.G, kThreads, sm_count, stream>>>(topk_ids, mapping, pl.P, topk, E, L,
                                                              pl.chunk, cnt, d_status);
     MLR_CHECK_LAUNCH();
+    note_launch();
   }
   align_colscan_kernel<<<(int)ceil_div(pl.NB, kColThreads), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB,
                                                                                      btotal);
   MLR_CHECK_LAUNCH();
+  note_launch();
   align_bucketscan_kernel<<<1, kThreads, 0, stream>>>(btotal, pl.NB, block_size, bstart, num_post_pad,
                                                       capacity, d_status);
   MLR_CHECK_LAUNCH();
+  note_launch();
   if (pl.G > 0) {
     align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(
         topk_ids, mapping, pl.P, topk, E, L, pl.chunk, block_size, cnt, btotal, bstart, sorted_ids,
         block_expert, block_lora, capacity);
     MLR_CHECK_LAUNCH();
+    note_launch();
   }
   return MLR_OK;
 }

@@ -8,7 +8,7 @@
 // every thread resolves 4 consecutive tokens there (one 16-byte store).  The
 // last block validates seg_indptr, the max_len hint and the adapter ids, and
 // writes all num_loras entries of adapter_enabled from a shared bit set.
-#include "mlr_common.cuh"
+#include "mlr_profile.cuh"
 
 namespace mlr {
 namespace {
@@ -135,5 +135,6 @@ extern "C" int moe_lora_batch_info(const int32_t* seg_indptr, const int32_t* wei
       seg_indptr, weight_indices, lora_ranks, bs, num_loras, num_tokens, max_len,
       token_lora_mapping, adapter_enabled, d_status, vec_ok);
   MLR_CHECK_LAUNCH();
+  note_launch();
   return MLR_OK;
 }

@@ -1,0 +1,15 @@
+// mlr_profile.cuh -- launch counting and optional per-stage event recording.
+#pragma once
+#include "mlr_common.cuh"
+
+namespace mlr {
+
+constexpr int kProfStages = 7;  // align, plan, shrink_gu, gate_up, shrink_d, down, convert
+
+void note_launch(int n = 1);
+// Per forward call: returns a slot (>= 0) while recording is on, else -1.
+int prof_call_begin(cudaStream_t stream);
+// Records the boundary after `stage` (0-based) for the call slot.
+void prof_mark(int slot, int stage, cudaStream_t stream);
+
+}  // namespace mlr

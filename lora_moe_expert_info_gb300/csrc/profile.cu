@@ -1,0 +1,80 @@
+// profile.cu -- launch counter and per-stage CUDA-event timing of the forward.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "mlr_profile.cuh"
+
+namespace mlr {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+bool g_on = false;
+int g_max_calls = 0, g_calls = 0;
+std::vector<cudaEvent_t> g_events;  // [max_calls][kProfStages + 1]
+
+const char* kStageNames[kProfStages] = {"align", "plan", "shrink_gate_up", "gate_up",
+                                        "shrink_down", "down", "convert"};
+
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int prof_call_begin(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_on || g_calls >= g_max_calls) return -1;
+  const int slot = g_calls++;
+  cudaEventRecord(g_events[(size_t)slot * (kProfStages + 1)], stream);
+  return slot;
+}
+
+void prof_mark(int slot, int stage, cudaStream_t stream) {
+  if (slot < 0) return;
+  cudaEventRecord(g_events[(size_t)slot * (kProfStages + 1) + stage + 1], stream);
+}
+
+}  // namespace mlr
+
+extern "C" int moe_lora_profile_begin(int32_t max_calls) {
+  using namespace mlr;
+  if (max_calls < 1 || max_calls > 4096) return MLR_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const size_t need = (size_t)max_calls * (kProfStages + 1);
+  while (g_events.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return MLR_ERR_CUDA;
+    g_events.push_back(e);
+  }
+  g_max_calls = max_calls;
+  g_calls = 0;
+  g_on = true;
+  return MLR_OK;
+}
+
+extern "C" int moe_lora_profile_end(double* stage_ms, int32_t max_stages, int32_t* n_stages,
+                                    int32_t* n_calls) {
+  using namespace mlr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_on = false;
+  if (n_stages) *n_stages = kProfStages;
+  if (n_calls) *n_calls = g_calls;
+  if (stage_ms == nullptr) return MLR_OK;
+  for (int s = 0; s < max_stages && s < kProfStages; ++s) stage_ms[s] = 0.0;
+  for (int c = 0; c < g_calls; ++c) {
+    cudaEvent_t* ev = &g_events[(size_t)c * (kProfStages + 1)];
+    if (cudaEventSynchronize(ev[kProfStages]) != cudaSuccess) return MLR_ERR_CUDA;
+    for (int s = 0; s < max_stages && s < kProfStages; ++s) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[s], ev[s + 1]) != cudaSuccess) return MLR_ERR_CUDA;
+      stage_ms[s] += ms;
+    }
+  }
+  return MLR_OK;
+}
+
+extern "C" const char* moe_lora_profile_stage_name(int32_t stage) {
+  return (stage >= 0 && stage < mlr::kProfStages) ? mlr::kStageNames[stage] : nullptr;
+}
+
+extern "C" uint64_t moe_lora_launch_count(void) { return mlr::g_launches.load(); }

@@ -1,0 +1,186 @@
+"""GPU parity of fused_moe_lora_forward against the oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation): |y - y_ref| <= 2e-2 + 2e-2*|y_ref|
+elementwise, y_ref from the fp64 oracle.  Small cases compare every output;
+the two prefill workloads compare a seeded sample of tokens (every output row
+depends only on its own token, so the oracle computes the sample directly).
+A second family checks the LoRA delta itself, y - y_base, with adapters large
+enough (A, B ~ N(0, 1/fan_in), scaling 0.5) that a dropped or misplaced LoRA
+term exceeds the tolerance by an order of magnitude while every intermediate
+stays O(1).  (With scaling 2 the outputs reach |y| ~ 30 and bf16 rounding of the
+O(10) intermediates alone exceeds the absolute part of the tolerance on outputs
+that cancel to ~0; the tolerance is stated for the workloads' distributions.)
+"""
+import numpy as np
+import pytest
+import torch
+
+import lora_moe_expert_info_gb300 as mlr
+import oracle
+from lora_moe_expert_info_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+ATOL = RTOL = 2e-2
+WKEYS = ("w_gate_up", "w_down", "lora_a_gu", "lora_b_gu", "lora_a_down", "lora_b_down")
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def within(y, yref):
+    err = np.abs(y - yref) - (ATOL + RTOL * np.abs(yref))
+    return float(err.max()) if err.size else -1.0
+
+
+class Case:
+    """Inputs on the GPU plus the host copies the oracle reads."""
+
+    def __init__(self, cfg, batch, weights, x, dev, scal_factor=1.0):
+        self.cfg, self.dev = cfg, dev
+        self.b = batch
+        self.scal = (batch.scalings * scal_factor).contiguous()
+        self.w = weights
+        self.x = x
+        st, mp, _ = oracle.batch_info(batch.seg_indptr.cpu().numpy(), batch.weight_indices.cpu().numpy(),
+                                      batch.lora_ranks.cpu().numpy(), cfg.num_tokens)
+        assert st == 0
+        self.mapping = mp
+
+    def gpu(self, mapping=None, **over):
+        m = self.mapping if mapping is None else mapping
+        args = dict(x=self.x, topk_ids=self.b.topk_ids, topk_weights=self.b.topk_weights,
+                    token_lora_mapping=torch.from_numpy(np.ascontiguousarray(m)).to(self.dev),
+                    lora_ranks=self.b.lora_ranks, scalings=self.scal)
+        args.update({k: getattr(self.w, k) for k in WKEYS})
+        args.update(over)
+        return mlr.fused_moe_lora_forward(**args).float().cpu().numpy()
+
+    def ref(self, tokens=None, mapping=None):
+        m = self.mapping if mapping is None else mapping
+        st, y = oracle.forward(bits(self.x), self.b.topk_ids.cpu().numpy(),
+                               self.b.topk_weights.cpu().numpy(), m, self.b.lora_ranks.cpu().numpy(),
+                               self.scal.cpu().numpy(), *[bits(getattr(self.w, k)) for k in WKEYS],
+                               tokens=tokens)
+        assert st == 0
+        return y
+
+
+def workload_case(name, dev, lora_std=None, seed=0):
+    cfg = workloads.CONFIGS[name]
+    b = workloads.make_batch(cfg, device=dev, seed=seed)
+    w = workloads.make_weights(cfg, b.lora_ranks, device=dev, seed=seed, lora_std=lora_std)
+    x = workloads.make_x(cfg, device=dev, seed=seed)
+    return Case(cfg, b, w, x, dev, scal_factor=0.25 if lora_std == "fan_in" else 1.0)
+
+
+def custom_case(dev, T, K, E, H, I, L, R, ranks, seg_lens, adapters, seed=0, lora_std=None,
+                expert_bias=0.0):
+    cfg = workloads.custom_config(hidden=H, intermediate=I, num_experts=E, topk=K, num_loras=L,
+                                  max_rank=R, num_tokens=T)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    lens = torch.tensor(seg_lens, dtype=torch.int32)
+    ip = torch.zeros(len(seg_lens) + 1, dtype=torch.int32)
+    ip[1:] = torch.cumsum(lens, 0)
+    ranks_t = torch.tensor(ranks, dtype=torch.int32)
+    s_fan = 0.5 if lora_std == "fan_in" else None
+    scal = torch.tensor([0.0 if r == 0 else (s_fan or 2.0 * 8 / r) for r in ranks], dtype=torch.float32)
+    ids, wts = workloads.route(T, E, K, torch.Generator(device=dev).manual_seed(seed + 1), dev,
+                               expert_bias_std=expert_bias)
+    b = workloads.Batch(lens.to(dev), ip.to(dev), torch.tensor(adapters, dtype=torch.int32).to(dev),
+                        ranks_t.to(dev), scal.to(dev), ids, wts)
+    w = workloads.make_weights(cfg, ranks_t, device=dev, seed=seed, lora_std=lora_std)
+    x = torch.randn(T, H, generator=torch.Generator(device=dev).manual_seed(seed + 3), device=dev,
+                    dtype=torch.bfloat16)
+    return Case(cfg, b, w, x, dev)
+
+
+def test_tiny_all_tokens(cuda_device):
+    c = workload_case("tiny", cuda_device)
+    assert within(c.gpu(), c.ref()) <= 0
+
+
+def test_tiny_lora_delta_sensitivity(cuda_device):
+    # A, B ~ N(0, 1/fan_in): the adapter delta is O(1), so its parity is meaningful.
+    c = workload_case("tiny", cuda_device, lora_std="fan_in")
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5  # the delta dwarfs the tolerance
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_ragged_shapes(cuda_device, seed):
+    # H, I not multiples of 64/128, ranks not multiples of 8, R16 > R, skewed routing
+    c = custom_case(cuda_device, T=203, K=3, E=5, H=200, I=136, L=4, R=24, ranks=[12, 0, 24, 5],
+                    seg_lens=[17, 60, 1, 90, 35], adapters=[0, 3, -1, 2, 1], seed=seed,
+                    lora_std="fan_in", expert_bias=1.0)
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
+def test_single_expert_top1(cuda_device):
+    c = custom_case(cuda_device, T=40, K=1, E=1, H=128, I=128, L=2, R=16, ranks=[16, 8],
+                    seg_lens=[25, 15], adapters=[1, 0], lora_std="fan_in")
+    assert within(c.gpu(), c.ref()) <= 0
+
+
+def test_no_loras(cuda_device):
+    c = custom_case(cuda_device, T=70, K=2, E=6, H=192, I=256, L=0, R=0, ranks=[],
+                    seg_lens=[70], adapters=[-1])
+    assert within(c.gpu(), c.ref()) <= 0
+
+
+def test_all_ranks_zero_equals_base(cuda_device):
+    c = custom_case(cuda_device, T=64, K=2, E=4, H=128, I=128, L=3, R=16, ranks=[0, 0, 0],
+                    seg_lens=[30, 34], adapters=[0, 2], lora_std="fan_in")
+    y = c.gpu()
+    y0 = c.gpu(mapping=np.full_like(c.mapping, -1))
+    assert within(y, c.ref()) <= 0
+    assert np.array_equal(y, y0)
+
+
+def test_many_tiles_per_expert(cuda_device):
+    # one hot expert: > 256 rows in one expert, many buckets per tile
+    c = custom_case(cuda_device, T=900, K=2, E=3, H=128, I=192, L=6, R=32,
+                    ranks=[8, 16, 32, 0, 24, 8], seg_lens=[100, 200, 50, 300, 150, 100],
+                    adapters=[0, 1, 2, 3, 4, 5], lora_std="fan_in", expert_bias=3.0)
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
+def test_repeated_calls_identical_metadata(cuda_device):
+    c = workload_case("tiny", cuda_device)
+    y1, y2 = c.gpu(), c.gpu()
+    assert within(y1, c.ref()) <= 0 and within(y2, c.ref()) <= 0
+
+
+def test_decode_all_tokens(cuda_device):
+    c = workload_case("decode", cuda_device)
+    assert within(c.gpu(), c.ref()) <= 0
+
+
+def test_qwen_prefill_sampled(cuda_device):
+    c = workload_case("qwen_moe_prefill", cuda_device)
+    y = c.gpu()
+    toks = np.sort(np.random.default_rng(0).choice(c.cfg.num_tokens, 96, replace=False))
+    toks = np.concatenate([[0, c.cfg.num_tokens - 1], toks])
+    assert within(y[toks], c.ref(tokens=toks)) <= 0
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.slow
+def test_deepseek_prefill_sampled(cuda_device):
+    c = workload_case("deepseek_v3_prefill", cuda_device)
+    y = c.gpu()
+    toks = np.sort(np.random.default_rng(1).choice(c.cfg.num_tokens, 24, replace=False))
+    toks = np.concatenate([[0, c.cfg.num_tokens - 1], toks])
+    assert within(y[toks], c.ref(tokens=toks)) <= 0
+    assert np.isfinite(y).all()
