@@ -127,6 +127,33 @@ int moe_lora_align(const int32_t* topk_ids, const int32_t* token_lora_mapping,
                    int32_t* block_lora_ids, int32_t* num_tokens_post_pad, int64_t capacity,
                    void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
 
+/*
+ * moe_lora_align_noalloc -- moe_lora_align for callers that cannot allocate
+ * device memory (an engine that owns all GPU memory through its own pools and
+ * forbids later allocations, a latency-critical path where cudaMalloc/cudaFree
+ * may synchronise the device, a layer given no allocator).  The pages have no
+ * counterpart: this is an addition of this library.
+ *
+ * Same arguments, results and device status bits as moe_lora_align, minus the
+ * workspace.  The scratch is one fixed 4 MiB array inside the library's device
+ * image (held on every GPU that loads the library until the process exits);
+ * sizes whose align scratch exceeds it (moe_lora_align_workspace_bytes(...) >
+ * 4 MiB, e.g. 1,048,576 tokens x top-8 over 256 experts x 65 adapter classes)
+ * return MLR_ERR_CAPACITY before anything is enqueued -- use moe_lora_align with
+ * a workspace there.  The call allocates nothing.
+ * The first call on a device looks up the array's address on that device (the
+ * current device, which must be the stream's); make that first call before
+ * any stream capture.  All calls share the one array, so calls whose work may
+ * overlap on the GPU (different streams, or different host threads) race and
+ * corrupt each other's results; calls ordered on one stream are safe, and no
+ * clearing is needed between them.
+ */
+int moe_lora_align_noalloc(const int32_t* topk_ids, const int32_t* token_lora_mapping,
+                           int32_t num_tokens, int32_t topk, int32_t num_experts, int32_t num_loras,
+                           int32_t block_size, int32_t* sorted_token_ids, int32_t* block_expert_ids,
+                           int32_t* block_lora_ids, int32_t* num_tokens_post_pad, int64_t capacity,
+                           int32_t* d_status, void* stream);
+
 /* Scratch bytes fused_moe_lora_forward needs for these sizes (0 on bad sizes). */
 size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t num_experts,
                                       int32_t hidden, int32_t intermediate, int32_t num_loras,
