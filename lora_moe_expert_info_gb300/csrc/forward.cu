@@ -6,22 +6,35 @@
 //
 // Launch sequence (one stream, no host synchronisation):
 //   align (block 16)  -> pairs sorted into (expert, adapter) buckets
-//   plan              -> tiles: <= 256 consecutive sorted rows of one expert
-//                        (base GEMMs) or of one (expert, adapter) bucket (shrinks)
+//   plan              -> tiles of <= 256 consecutive sorted rows of one expert
+//                        (with the adapter buckets they meet) for the base GEMMs,
+//                        and of one (expert, adapter) bucket for the shrinks
+//   gather_x          x_sorted[row] = x[token of the row's pair] (zeros on pads)
 //   shrink_gu         z_gu[row] = s_l * A_gu[l,e] x_t          (gate and up)
 //   gate_up           h[row]    = SiLU(W_g x + B_g z_g) * (W_u x + B_u z_u)
 //   shrink_d          z_d[row]  = s_l * A_d[l,e] h[row]
 //   down              y_acc[t] += w * (W_d h + B_d z_d)
 //   convert           y = bf16(y_acc)
-// Every GEMM is "swap-AB" on the 5th-generation tensor cores: the weight rows
-// are the MMA's M = 128 (A operand), the tile's sorted pair rows are N <= 256
-// (B operand), K runs over the hidden / intermediate dimension in 64-wide
-// blocks.  Operands are staged in shared memory by TMA (weights, h, LoRA
-// factors) or by cp.async gathers (token rows of x), the fp32 accumulator lives
-// in TMEM.  Because a tile's rows are sorted by adapter, each adapter owns a
-// contiguous column range of the accumulator: the LoRA expand is issued as
-// extra MMAs on that column range (N = the bucket's rows) into the same TMEM
-// accumulator as the base GEMM, before one epilogue reads it.
+//
+// The four GEMMs share one persistent, warp-specialised kernel on the 5th
+// generation tensor cores.  One CTA per SM walks a static share of the work
+// items (tile x 128-row weight block).  Every GEMM is "swap-AB": weight rows are
+// the MMA's M = 128 (A operand), the tile's sorted pair rows are N <= 256 (B
+// operand), K advances in 64-wide blocks through a ring of shared-memory stages
+// that keeps streaming across item boundaries:
+//   warp 0     producer (lane 0): TMA for weights, LoRA factors and the
+//              contiguous row tiles of x_sorted / h / z.  No thread waits for a
+//              copy, so every stage of the ring can be in flight.  (Gathering
+//              token rows inside the GEMM, 128 bytes per row and K block, moved
+//              too few bytes per request; one copy into sorted order first lets
+//              every operand load be a large tiled box.)
+//   warp 4     TMEM allocation and the single-thread MMA issue (tcgen05.mma)
+//   warps 5-8  epilogue: TMEM -> registers -> global, overlapping the next
+//              item's main loop (double-buffered accumulators where TMEM allows)
+// Because a tile's rows are sorted by adapter, each adapter owns a contiguous
+// column range of the accumulator: the LoRA expand is issued as extra MMAs on
+// that range (N = the bucket's rows) into the same TMEM accumulator as the base
+// GEMM, before the epilogue reads it.
 #include <cudaTypedefs.h>
 
 #include "mlr_align.cuh"
@@ -32,33 +45,40 @@ namespace {
 
 constexpr int kBlock = 16;        // internal align block = MMA N granularity
 constexpr int kTileRows = 256;    // max sorted rows per tile (MMA N)
-constexpr int kMaxBuckets = 20;   // adapter buckets meeting one tile (each >= 16 rows)
-constexpr int kMaxExpand = 160;   // expand steps per tile
-constexpr int kThreads = 160;     // warps 0-3: producers + epilogue; warp 4: MMA issuer
+constexpr int kMaxBuckets = 16;   // adapter buckets meeting one tile (each >= 16 rows)
+constexpr int kEpiWarp0 = 5;
+constexpr int kThreads = 288;     // 9 warps (warps 1-3 idle)
+constexpr int kGatherThreads = 256;
 constexpr int kPlanThreads = 1024;
+constexpr int kEpiBytes = 16 * (128 + 4) * 4;  // one 16-row fp32 staging chunk
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 
 template <int KIND> struct Cfg;
-template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kTmemCols = 256; static constexpr bool kGather = true; };
-template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kTmemCols = 512; static constexpr bool kGather = true; };
-template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kTmemCols = 256; static constexpr bool kGather = false; };
-template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kTmemCols = 256; static constexpr bool kGather = false; };
+template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
+template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512; };
+template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
+template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
 
 struct Maps {
   CUtensorMap m0, m1, m2, m3;
 };
 
+// Base tile: head {e, row0, nrows, nb} followed by nb buckets {j0, nj, l, r16}.
+struct TileRec {
+  int4 head;
+  int4 bk[kMaxBuckets];
+};
+
 struct Params {
-  int T, K, E, H, I, L, R, R16, C, mtiles;
+  int T, K, E, H, I, L, R, R16, C, nblk;
   int64_t P;
-  const uint16_t* x;
   const float* topk_weights;
   const int32_t* lora_ranks;
   const float* scalings;
   const int32_t* sorted_ids;
-  const uint32_t* bstart;  // [E*C + 1] padded bucket starts
-  const int4* tiles;       // base: {e, row0, nrows, 0}; shrink: {e, l, row0, nrows}
+  const TileRec* base_tiles;
+  const int4* shrink_tiles;  // {e, l, row0, nrows}
   const int32_t* n_tiles;
   uint16_t* zgu;  // [cap, 2*R16]
   uint16_t* h;    // [cap, I]
@@ -70,49 +90,62 @@ struct Params {
 struct __align__(16) Ctl {
   uint64_t full[4];
   uint64_t empty[4];
-  uint64_t accum;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
   uint32_t tmem;
   int abort;
-  int nb, nexp;
-  int bj0[kMaxBuckets], bnj[kMaxBuckets], bl[kMaxBuckets], br16[kMaxBuckets];
-  int estep[kMaxExpand];  // bucket << 8 | g << 4 | kg
+  int epi_go;
   int tok[kTileRows];
   float w[kTileRows];
 };
 
 template <int KIND>
 constexpr int smem_bytes() {
-  return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + (int)sizeof(Ctl) + 1024;
+  return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + kEpiBytes + (int)sizeof(Ctl) + 1024;
 }
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
-// Adapter buckets (with a usable LoRA) meeting rows [row0, row0+nrows) of expert e.
-__device__ void tile_buckets(const Params& p, int e, int row0, int nrows, int ngates, Ctl& c) {
-  const int lo = e * p.C, hi = (e + 1) * p.C;
-  int a = lo, b = hi - 1;  // first bucket whose end passes row0
-  while (a < b) {
-    const int mid = (a + b) >> 1;
-    if ((int)p.bstart[mid + 1] > row0) b = mid; else a = mid + 1;
+// One work item: tile rows, weight block, adapter.
+struct Item {
+  int e, l, row0, nrows, nb, mb;
+  const TileRec* rec;
+};
+
+template <int KIND>
+__device__ __forceinline__ Item load_item(const Params& p, int item) {
+  Item it;
+  const int tile = item / p.nblk;
+  it.mb = item % p.nblk;
+  if (KIND == kShrinkGU || KIND == kShrinkD) {
+    const int4 t = p.shrink_tiles[tile];
+    it.e = t.x; it.l = t.y; it.row0 = t.z; it.nrows = t.w; it.nb = 0; it.rec = nullptr;
+  } else {
+    it.rec = p.base_tiles + tile;
+    const int4 h = it.rec->head;
+    it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w;
   }
-  int nb = 0, ne = 0;
-  for (int q = a; q < hi && (int)p.bstart[q] < row0 + nrows; ++q) {
-    const int l = q - lo - 1;
-    if (l < 0) continue;
-    const int r = p.lora_ranks[l];
-    if (r < 0 || r > p.R) { set_status(p.status, MLR_STATUS_RANK); continue; }
-    if (r == 0) continue;
-    const int s0 = max((int)p.bstart[q], row0), s1 = min((int)p.bstart[q + 1], row0 + nrows);
-    if (s1 <= s0 || nb >= kMaxBuckets) continue;
-    const int r16 = (r + 15) & ~15;
-    c.bj0[nb] = s0 - row0; c.bnj[nb] = s1 - s0; c.bl[nb] = l; c.br16[nb] = r16;
-    for (int g = 0; g < ngates; ++g)
-      for (int kg = 0; kg * 64 < r16; ++kg)
-        if (ne < kMaxExpand) c.estep[ne++] = (nb << 8) | (g << 4) | kg;
-    ++nb;
+  return it;
+}
+
+// Expand steps of a base item: per bucket, per gate (2 for gate_up), per 64 ranks.
+__device__ __forceinline__ int expand_steps(const Item& it, int ngates) {
+  int n = 0;
+  for (int b = 0; b < it.nb; ++b) n += ngates * ((it.rec->bk[b].w + 63) >> 6);
+  return n;
+}
+// Decodes expand step k of an item into (bucket, gate, rank group).
+__device__ __forceinline__ void expand_decode(const Item& it, int ngates, int k, int& bi, int& g, int& kg) {
+  for (bi = 0; bi < it.nb; ++bi) {
+    const int per = (it.rec->bk[bi].w + 63) >> 6;
+    if (k < ngates * per) {
+      g = k / per;
+      kg = k % per;
+      return;
+    }
+    k -= ngates * per;
   }
-  c.nb = nb;
-  c.nexp = ne;
+  bi = 0; g = 0; kg = 0;
 }
 
 template <int KIND>
@@ -122,248 +155,272 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
   constexpr bool kShrink = (KIND == kShrinkGU || KIND == kShrinkD);
+  constexpr int kGates = (KIND == kGateUp) ? 2 : 1;
 
-  // ---- which tile / which M block ----
-  const int nblk = kShrink ? p.mtiles : (KIND == kGateUp ? (int)ceil_div(p.I, 128) : (int)ceil_div(p.H, 128));
-  const int tile = blockIdx.x / nblk, mb = blockIdx.x % nblk;
-  if (tile >= *p.n_tiles) return;
-  const int4 td = p.tiles[tile];
-  const int e = td.x;
-  const int l_shr = kShrink ? td.y : -1;
-  const int row0 = kShrink ? td.z : td.y;
-  const int nrows = kShrink ? td.w : td.z;
+  const int n_items = *p.n_tiles * p.nblk;
+  if ((int)blockIdx.x >= n_items) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl& c = *reinterpret_cast<Ctl*>(smem + S * SB);
+  uint8_t* epi = smem + S * SB;
+  Ctl& c = *reinterpret_cast<Ctl*>(epi + kEpiBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  int r_shr = 0, r16_shr = 0;
-  float s_shr = 0.f;
-  if (kShrink) {
-    r_shr = p.lora_ranks[l_shr];
-    r16_shr = (r_shr + 15) & ~15;
-    s_shr = p.scalings[l_shr];
-  }
   const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, 64);
 
-  // ---- setup ----
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&c.full[s], CF::kGather ? 129 : 1);
+      mbar_init(&c.full[s], 1);
       mbar_init(&c.empty[s], 1);
     }
-    mbar_init(&c.accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.acc_full[b], 1);
+      mbar_init(&c.acc_empty[b], 128);
+    }
     c.abort = 0;
-    c.nb = 0;
-    c.nexp = 0;
-    if (KIND == kGateUp || KIND == kDown) tile_buckets(p, e, row0, nrows, KIND == kGateUp ? 2 : 1, c);
     fence_mbar_init();
   }
-  if (CF::kGather || KIND == kDown) {
-    for (int n = tid; n < kTileRows; n += kThreads) {
-      const int pr = (n < nrows) ? p.sorted_ids[row0 + n] : (int)p.P;
-      const bool real = pr >= 0 && pr < p.P;
-      c.tok[n] = real ? pr / p.K : -1;
-      if (KIND == kDown) c.w[n] = real ? p.topk_weights[pr] : 0.f;
-    }
-  }
   if (warp == 4) {
-    tmem_alloc(&c.tmem, CF::kTmemCols);
+    tmem_alloc(&c.tmem, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem;
-  const int nsteps = kShrink ? nk : nk + c.nexp;
   volatile int* abort = &c.abort;
 
-  if (warp < 4) {
-    // =============================== producer ===============================
-    if (CF::kGather || tid == 0) {
-      int s = 0;
-      for (; s < nsteps; ++s) {
-        const int st = s % S, round = s / S;
+  if (warp == 0) {
+    // ================================ producer =================================
+    int gs = 0;  // global step counter of this CTA (ring position)
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const Item it = load_item<KIND>(p, item);
+      const int nsteps = nk + (kShrink ? 0 : expand_steps(it, kGates));
+      for (int s = 0; s < nsteps; ++s, ++gs) {
+        const int st = gs % S, round = gs / S;
         uint8_t* sbuf = smem + st * SB;
-        if (!mbar_wait(&c.empty[st], (round & 1) ^ 1, abort)) break;
+        const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         const bool main_step = s < nk;
-        if (tid == 0) {
+        // row tiles of x_sorted / h are loaded as 64-row boxes
+        const int rbox = (int)ceil_div(it.nrows, 64);
+        if (lane == 0) {
           if (main_step) {
             const int kb = s;
-            if (KIND == kShrinkGU || KIND == kShrinkD) {
-              // LoRA A rows packed into M: gate (or the only) rows then up rows, 8-row groups
+            if (kShrink) {
+              // LoRA A rows packed into M in 8-row groups: gate rows then up rows
+              const int r = p.lora_ranks[it.l];
+              const int r8 = (r + 7) & ~7, r16 = (r + 15) & ~15;
               int ngr = 0;
-              const int r8 = (r_shr + 7) & ~7;
               for (int grp = 0; grp < 16; ++grp) {
-                const int m0 = 128 * mb + grp * 8;
-                const int g = (KIND == kShrinkGU && m0 >= r16_shr) ? 1 : 0;
-                const int q0 = m0 - g * r16_shr;
+                const int m0 = 128 * it.mb + grp * 8;
+                const int g = (KIND == kShrinkGU && m0 >= r16) ? 1 : 0;
+                const int q0 = m0 - g * r16;
                 if (q0 < r8 && (KIND == kShrinkGU || g == 0)) ++ngr;
               }
-              mbar_arrive_expect_tx(&c.full[st], ngr * 1024 + (KIND == kShrinkD ? 32768 : 0));
+              mbar_arrive_expect_tx(&c.full[st], ngr * 1024 + rbox * 8192);
               for (int grp = 0; grp < 16; ++grp) {
-                const int m0 = 128 * mb + grp * 8;
-                const int g = (KIND == kShrinkGU && m0 >= r16_shr) ? 1 : 0;
-                const int q0 = m0 - g * r16_shr;
+                const int m0 = 128 * it.mb + grp * 8;
+                const int g = (KIND == kShrinkGU && m0 >= r16) ? 1 : 0;
+                const int q0 = m0 - g * r16;
                 if (!(q0 < r8 && (KIND == kShrinkGU || g == 0))) continue;
-                const int row = KIND == kShrinkGU ? ((l_shr * p.E + e) * 2 + g) * p.R + q0
-                                                  : (l_shr * p.E + e) * p.R + q0;
+                const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q0
+                                                  : (it.l * p.E + it.e) * p.R + q0;
                 tma_load_2d(sbuf + grp * 1024, &maps.m0, &c.full[st], kb * 64, row);
               }
-              if (KIND == kShrinkD) tma_load_2d(sbuf + 16384, &maps.m1, &c.full[st], kb * 64, row0);
+              // B operand: rows of x_sorted (gate_up shrink) or h (down shrink)
+              for (int q = 0; q < rbox; ++q)
+                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m1, &c.full[st], kb * 64, it.row0 + q * 64);
             } else if (KIND == kGateUp) {
-              mbar_arrive_expect_tx(&c.full[st], 32768);
-              const int i0 = mb * 128;
-              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, e * 2 * p.I + i0);
-              tma_load_2d(sbuf + 16384, &maps.m0, &c.full[st], kb * 64, e * 2 * p.I + p.I + i0);
+              mbar_arrive_expect_tx(&c.full[st], 32768 + rbox * 8192);
+              const int i0 = it.mb * 128;
+              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, it.e * 2 * p.I + i0);
+              tma_load_2d(sbuf + 16384, &maps.m0, &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+              for (int q = 0; q < rbox; ++q)
+                tma_load_2d(sbuf + 32768 + q * 8192, &maps.m3, &c.full[st], kb * 64, it.row0 + q * 64);
             } else {  // kDown
-              mbar_arrive_expect_tx(&c.full[st], 16384 + 32768);
-              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, e * p.H + mb * 128);
-              tma_load_2d(sbuf + 16384, &maps.m1, &c.full[st], kb * 64, row0);
+              mbar_arrive_expect_tx(&c.full[st], 16384 + rbox * 8192);
+              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
+              for (int q = 0; q < rbox; ++q)
+                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m1, &c.full[st], kb * 64, it.row0 + q * 64);
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
-            const int es = c.estep[s - nk];
-            const int bi = es >> 8, g = (es >> 4) & 15, kg = es & 15;
-            const int l = c.bl[bi];
-            const int nch = min(8, (c.br16[bi] - kg * 64) / 8);
-            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + 4096));
-            const int m0 = mb * 128;
-            const int brow = KIND == kGateUp ? ((l * p.E + e) * 2 + g) * p.I + m0 : (l * p.E + e) * p.H + m0;
+            int bi, g, kg;
+            expand_decode(it, kGates, s - nk, bi, g, kg);
+            const int4 bk = it.rec->bk[bi];  // {j0, nj, l, r16}
+            const int nch = min(8, (bk.w - kg * 64) / 8);
+            const int zr = (int)ceil_div(bk.y, 64);
+            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zr * 1024));
+            const int m0 = it.mb * 128;
+            const int brow = KIND == kGateUp ? ((bk.z * p.E + it.e) * 2 + g) * p.I + m0
+                                             : (bk.z * p.E + it.e) * p.H + m0;
             const CUtensorMap* bmap = KIND == kGateUp ? &maps.m1 : &maps.m2;
             const CUtensorMap* zmap = KIND == kGateUp ? &maps.m2 : &maps.m3;
             const int zcol0 = (KIND == kGateUp ? g * p.R16 : 0) + kg * 64;
             for (int ch = 0; ch < nch; ++ch) {
               tma_load_2d(sbuf + ch * 2048, bmap, &c.full[st], kg * 64 + ch * 8, brow);
-              tma_load_2d(sbuf + 16384 + ch * 4096, zmap, &c.full[st], zcol0 + ch * 8, row0 + c.bj0[bi]);
+              for (int zq = 0; zq < zr; ++zq)
+                tma_load_2d(sbuf + 16384 + ch * 4096 + zq * 1024, zmap, &c.full[st], zcol0 + ch * 8,
+                            it.row0 + bk.x + zq * 64);
             }
           }
         }
-        if (CF::kGather) {
-          if (main_step) {
-            const int kb = s;
-            const uint32_t xs = smem_u32(sbuf + (KIND == kGateUp ? 32768 : 16384));
-            for (int q = tid; q < nrows * 8; q += 128) {
-              const int n = q >> 3, ch = q & 7;
-              const int t = c.tok[n];
-              const int col = kb * 64 + ch * 8;
-              const bool ok = t >= 0 && col < p.H;
-              const uint16_t* src = p.x + (ok ? (int64_t)t * p.H + col : 0);
-              cp_async_16(xs + n * 128 + ((ch ^ (n & 7)) << 4), src, ok ? 16u : 0u);
-            }
-          }
-          cp_async_commit();
-          if (s > 0) {
-            cp_async_wait<1>();
-            fence_proxy_async_smem();
-            mbar_arrive(&c.full[(s - 1) % S]);
-          }
-        }
       }
-      if (CF::kGather && s == nsteps && nsteps > 0) {
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&c.full[(nsteps - 1) % S]);
-      }
-      if (CF::kGather) cp_async_wait<0>();
     }
-  } else if (lane == 0) {
-    // ================================ MMA ===================================
-    for (int s = 0; s < nsteps; ++s) {
-      const int st = s % S, round = s / S;
-      if (!mbar_wait(&c.full[st], round & 1, abort)) break;
+  } else if (warp == 4) {
+    // ============================ MMA (one thread) =============================
+    if (lane == 0) {
+      int gs = 0, il = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++il) {
+        const Item it = load_item<KIND>(p, item);
+        const int b = il % CF::kAccBufs;
+        if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + b * CF::kAccCols;
+        const int nsteps = nk + (kShrink ? 0 : expand_steps(it, kGates));
+        for (int s = 0; s < nsteps; ++s, ++gs) {
+          const int st = gs % S, round = gs / S;
+          if (!mbar_wait(&c.full[st], round & 1, abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sb = smem_u32(smem + st * SB);
+          if (s < nk) {
+            const uint32_t idesc = idesc_bf16_f32(128, it.nrows);
+            if (KIND == kGateUp) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t a = (s > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t bx = sdesc_sw128(sb + 32768 + kk * 32);
+                mma_bf16(acc, sdesc_sw128(sb + kk * 32), bx, idesc, a);
+                mma_bf16(acc + 256, sdesc_sw128(sb + 16384 + kk * 32), bx, idesc, a);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(acc, sdesc_sw128(sb + kk * 32), sdesc_sw128(sb + 16384 + kk * 32), idesc,
+                         (s > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            int bi, g, kg;
+            expand_decode(it, kGates, s - nk, bi, g, kg);
+            const int4 bk = it.rec->bk[bi];
+            const int nch = min(8, (bk.w - kg * 64) / 8);
+            const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + bk.x;
+            const uint32_t idesc = idesc_bf16_f32(128, bk.y);
+            for (int k16 = 0; k16 < nch / 2; ++k16)
+              mma_bf16(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
+                       sdesc_noswz(sb + 16384 + k16 * 2 * 4096, 4096, 128), idesc, 1u);
+          }
+          mma_commit(&c.empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&c.acc_full[b]);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ================================ epilogue =================================
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int m = quarter * 32 + lane;
+    const int et = tid - kEpiWarp0 * 32;  // 0..127
+    int il = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++il) {
+      const Item it = load_item<KIND>(p, item);
+      const int b = il % CF::kAccBufs;
+      if (KIND == kDown) {
+        for (int n = et; n < kTileRows; n += 128) {
+          const int pr = (n < it.nrows) ? p.sorted_ids[it.row0 + n] : (int)p.P;
+          const bool real = pr >= 0 && pr < p.P;
+          c.tok[n] = real ? pr / p.K : -1;
+          c.w[n] = real ? p.topk_weights[pr] : 0.f;
+        }
+      }
+      // one thread waits for the accumulator; the decision is shared through
+      // shared memory so that all 128 epilogue threads take the same branch
+      if (et == 0) {
+        const bool got = mbar_wait(&c.acc_full[b], (il / CF::kAccBufs) & 1, abort);
+        c.epi_go = (got && !*abort) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);  // also publishes tok/w
       tc_fence_after();
-      const uint32_t sb = smem_u32(smem + st * SB);
-      if (s < nk) {
-        const uint32_t idesc = idesc_bf16_f32(128, nrows);
-        if (KIND == kGateUp) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-            const uint64_t bx = sdesc_sw128(sb + 32768 + kk * 32);
-            mma_bf16(tmem, sdesc_sw128(sb + kk * 32), bx, idesc, acc);
-            mma_bf16(tmem + 256, sdesc_sw128(sb + 16384 + kk * 32), bx, idesc, acc);
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, sdesc_sw128(sb + kk * 32), sdesc_sw128(sb + 16384 + kk * 32), idesc,
-                     (s > 0 || kk > 0) ? 1u : 0u);
-        }
-      } else {
-        const int es = c.estep[s - nk];
-        const int bi = es >> 8, g = (es >> 4) & 15, kg = es & 15;
-        const int nch = min(8, (c.br16[bi] - kg * 64) / 8);
-        const uint32_t d = tmem + (KIND == kGateUp ? g * 256 : 0) + c.bj0[bi];
-        const uint32_t idesc = idesc_bf16_f32(128, c.bnj[bi]);
-        for (int k16 = 0; k16 < nch / 2; ++k16)
-          mma_bf16(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
-                   sdesc_noswz(sb + 16384 + k16 * 2 * 4096, 4096, 128), idesc, 1u);
-      }
-      mma_commit(&c.empty[st]);
-    }
-    mma_commit(&c.accum);
-  }
-
-  // ================================ epilogue ================================
-  if (warp < 4) {
-    const bool ok = mbar_wait(&c.accum, 0, abort);
-    tc_fence_after();
-    if (ok && !*abort) {
-      const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-      const int m = warp * 32 + lane;
+      if (!c.epi_go) break;
+      const uint32_t tl = tmem + b * CF::kAccCols + ((uint32_t)(quarter * 32) << 16);
       if (KIND == kGateUp) {
-        const int gi = mb * 128 + m;
-        for (int c0 = 0; c0 < nrows; c0 += 16) {
+        uint16_t* hs = reinterpret_cast<uint16_t*>(epi);
+        constexpr int kHs = 128 + 8;
+        const int i0 = it.mb * 128;
+        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
           float gv[16], uv[16];
           tmem_ld16(tl + c0, gv);
           tmem_ld16(tl + 256 + c0, uv);
-          if (gi < p.I) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              p.h[(int64_t)(row0 + c0 + j) * p.I + gi] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+          for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int q = et + 128 * k;
+            const int n = q >> 4, ch = q & 15;
+            if (i0 + ch * 8 < p.I)
+              *reinterpret_cast<uint4*>(p.h + (int64_t)(it.row0 + c0 + n) * p.I + i0 + ch * 8) =
+                  *reinterpret_cast<const uint4*>(hs + n * kHs + ch * 8);
           }
+          named_bar_sync(1, 128);
         }
       } else if (KIND == kDown) {
-        const int gh = mb * 128 + m;
-        for (int c0 = 0; c0 < nrows; c0 += 16) {
+        float* ds = reinterpret_cast<float*>(epi);
+        constexpr int kDs = 128 + 4;
+        const int h0 = it.mb * 128;
+        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
           float v[16];
           tmem_ld16(tl + c0, v);
-          if (gh < p.H) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = c.tok[c0 + j];
-              if (t >= 0) atomicAdd(p.yacc + (int64_t)t * p.H + gh, c.w[c0 + j] * v[j]);
+          for (int j = 0; j < 16; ++j) ds[j * kDs + m] = v[j];
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int q = et + 128 * k;
+            const int n = q >> 5, quad = q & 31;
+            const int t = c.tok[c0 + n];
+            if (t >= 0 && h0 + quad * 4 < p.H) {
+              const float4 v4 = *reinterpret_cast<const float4*>(ds + n * kDs + quad * 4);
+              const float w = c.w[c0 + n];
+              red_add_v4(p.yacc + (int64_t)t * p.H + h0 + quad * 4, w * v4.x, w * v4.y, w * v4.z, w * v4.w);
             }
           }
+          named_bar_sync(1, 128);
         }
       } else {
-        const int mg = 128 * mb + m;
+        const int r = p.lora_ranks[it.l];
+        const int r16 = (r + 15) & ~15;
+        const float sc = p.scalings[it.l];
+        const int mg = 128 * it.mb + m;
         int g = 0, q = mg;
-        if (KIND == kShrinkGU && mg >= r16_shr) { g = 1; q = mg - r16_shr; }
-        const bool valid = KIND == kShrinkGU ? (mg < 2 * r16_shr) : (mg < r16_shr);
-        for (int c0 = 0; c0 < nrows; c0 += 16) {
+        if (KIND == kShrinkGU && mg >= r16) { g = 1; q = mg - r16; }
+        const bool valid = KIND == kShrinkGU ? (mg < 2 * r16) : (mg < r16);
+        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
           float v[16];
           tmem_ld16(tl + c0, v);
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float z = q < r_shr ? s_shr * v[j] : 0.f;
+              const float z = q < r ? sc * v[j] : 0.f;
               if (KIND == kShrinkGU)
-                p.zgu[(int64_t)(row0 + c0 + j) * (2 * p.R16) + g * p.R16 + q] = f32_to_bf16_bits(z);
+                p.zgu[(int64_t)(it.row0 + c0 + j) * (2 * p.R16) + g * p.R16 + q] = f32_to_bf16_bits(z);
               else
-                p.zd[(int64_t)(row0 + c0 + j) * p.R16 + q] = f32_to_bf16_bits(z);
+                p.zd[(int64_t)(it.row0 + c0 + j) * p.R16 + q] = f32_to_bf16_bits(z);
             }
           }
         }
       }
+      tc_fence_before();
+      named_bar_sync(1, 128);  // tok/w and the staging chunk are free for the next item
+      mbar_arrive(&c.acc_empty[b]);
     }
   }
   if (tid == 0 && *abort) set_status(p.status, MLR_STATUS_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) tmem_dealloc(tmem, CF::kTmemCols);
+  if (warp == 4) tmem_dealloc(tmem, 512);
 }
 
 // Block-wide exclusive scan of per-thread counts; returns this thread's offset.
@@ -401,12 +458,13 @@ __device__ __forceinline__ void chunk_rows(int n, int k, int nt, int& r0, int& n
   nr = min(cs, n - r0);
 }
 
-// One block: base tiles per expert and shrink tiles per LoRA bucket.
+// One block: base tiles per expert (with the adapter buckets each tile meets)
+// and shrink tiles per LoRA bucket.
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lora_ranks, int E, int C,
-            int R, int4* __restrict__ base_tiles, int4* __restrict__ shrink_tiles,
+            int R, TileRec* __restrict__ base_tiles, int4* __restrict__ shrink_tiles,
             int32_t* __restrict__ counts, int32_t* status) {
-  // base tiles: experts shared out in contiguous ranges
+  int bad = 0;
   {
     const int per = (int)ceil_div(E, kPlanThreads);
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
@@ -417,20 +475,34 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
     for (int e = e0; e < e1; ++e) {
       const int s = (int)bstart[e * C], n = (int)bstart[(e + 1) * C] - s;
       const int nt = (int)ceil_div(n, kTileRows);
+      int q = e * C;  // first bucket that may meet the current tile
       for (int k = 0; k < nt; ++k) {
         int r0, nr;
         chunk_rows(n, k, nt, r0, nr);
-        base_tiles[off++] = make_int4(e, s + r0, nr, 0);
+        TileRec& rec = base_tiles[off++];
+        const int t0 = s + r0, t1 = t0 + nr;
+        int nb = 0;
+        while (q < (e + 1) * C && (int)bstart[q + 1] <= t0) ++q;
+        for (int b = q; b < (e + 1) * C && (int)bstart[b] < t1; ++b) {
+          const int l = b - e * C - 1;
+          if (l < 0) continue;
+          const int r = lora_ranks[l];
+          if (r < 0 || r > R) { bad = 1; continue; }
+          if (r == 0) continue;
+          const int s0 = max((int)bstart[b], t0), s1 = min((int)bstart[b + 1], t1);
+          if (s1 <= s0 || nb >= kMaxBuckets) continue;
+          rec.bk[nb++] = make_int4(s0 - t0, s1 - s0, l, (r + 15) & ~15);
+        }
+        rec.head = make_int4(e, t0, nr, nb);
       }
     }
     if (threadIdx.x == 0) counts[0] = total;
   }
-  // shrink tiles: LoRA buckets (class >= 1, 0 < rank <= R)
   {
     const int NB = E * C;
     const int per = (int)ceil_div(NB, kPlanThreads);
     const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
-    int mine = 0, bad = 0;
+    int mine = 0;
     for (int b = b0; b < b1; ++b) {
       const int cl = b % C;
       if (cl == 0) continue;
@@ -439,7 +511,6 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       if (r == 0) continue;
       mine += (int)ceil_div(bstart[b + 1] - bstart[b], kTileRows);
     }
-    if (bad) set_status(status, MLR_STATUS_RANK);
     int total;
     int off = block_offsets(mine, &total);
     for (int b = b0; b < b1; ++b) {
@@ -456,6 +527,26 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       }
     }
     if (threadIdx.x == 0) counts[1] = total;
+  }
+  if (bad) set_status(status, MLR_STATUS_RANK);
+}
+
+// x_sorted[r] = x[sorted_ids[r] / K] for r < npad, zeros for pad rows: one
+// warp per row, 16-byte loads and stores.
+__global__ void __launch_bounds__(kGatherThreads)
+gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
+                const int32_t* __restrict__ npad, int64_t P, int K, int H, int64_t cap,
+                uint16_t* __restrict__ xs) {
+  const int64_t n = min((int64_t)*npad, cap);
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = kGatherThreads / 32;
+  const int chunks = H / 8;  // H is a multiple of 8
+  for (int64_t r = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); r < n; r += (int64_t)gridDim.x * wpb) {
+    const int pr = sorted_ids[r];
+    const bool real = pr >= 0 && pr < P;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(pr / K) * H : 0));
+    uint4* dst = reinterpret_cast<uint4*>(xs + r * H);
+    for (int ch = lane; ch < chunks; ch += 32) dst[ch] = real ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -507,7 +598,7 @@ struct FwdLayout {
   int R16, C, mtiles_gu, mtiles_d;
   int64_t cap, max_base, max_shrink;
   int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_counts, o_zgu, o_h, o_zd,
-      o_yacc, total;
+      o_yacc, o_xs, total;
 };
 
 FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R) {
@@ -533,20 +624,34 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.o_blora = take(f.cap / kBlock * 4);
   f.o_npad = take(16);
   f.o_align = take(f.al.ws_bytes);
-  f.o_base = take(f.max_base * 16);
+  f.o_base = take(f.max_base * (int64_t)sizeof(TileRec));
   f.o_shrink = take(f.max_shrink * 16);
   f.o_counts = take(16);
   f.o_zgu = take(f.cap * 2 * f.R16 * 2);
   f.o_h = take(f.cap * (int64_t)I * 2);
   f.o_zd = take(f.cap * f.R16 * 2);
   f.o_yacc = take((int64_t)T * H * 4);
+  f.o_xs = take(f.cap * (int64_t)H * 2);
   f.total = o;
   f.ok = true;
   return f;
 }
 
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
+// Persistent launch: one CTA per SM (or fewer when there are fewer items).
 template <int KIND>
-int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, int nblk, cudaStream_t stream) {
+int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
   const int smem = smem_bytes<KIND>();
   static bool configured = false;
   if (!configured) {
@@ -555,10 +660,11 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, int nblk, 
       return MLR_ERR_CUDA;
     configured = true;
   }
-  const int64_t grid = max_tiles * nblk;
-  if (grid <= 0) return MLR_OK;
-  if (grid > INT32_MAX) return MLR_ERR_UNSUPPORTED;
-  moe_gemm_kernel<KIND><<<(unsigned)grid, kThreads, smem, stream>>>(maps, p);
+  const int64_t max_items = max_tiles * p.nblk;
+  if (max_items <= 0) return MLR_OK;
+  if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
+  const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
+  moe_gemm_kernel<KIND><<<grid, kThreads, smem, stream>>>(maps, p);
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;
@@ -612,29 +718,32 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   int32_t* blora = reinterpret_cast<int32_t*>(ws + f.o_blora);
   int32_t* npad = reinterpret_cast<int32_t*>(ws + f.o_npad);
   char* aws = ws + f.o_align;
-  int4* base_tiles = reinterpret_cast<int4*>(ws + f.o_base);
+  TileRec* base_tiles = reinterpret_cast<TileRec*>(ws + f.o_base);
   int4* shrink_tiles = reinterpret_cast<int4*>(ws + f.o_shrink);
   int32_t* counts = reinterpret_cast<int32_t*>(ws + f.o_counts);
   uint16_t* zgu = reinterpret_cast<uint16_t*>(ws + f.o_zgu);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + f.o_h);
   uint16_t* zd = reinterpret_cast<uint16_t*>(ws + f.o_zd);
   float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
   const uint32_t* bstart = reinterpret_cast<const uint32_t*>(aws + f.al.bstart_off);
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
   const uint64_t cap = (uint64_t)f.cap;
   bool ok = make_map(&m_gu.m0, w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
-            make_map(&m_sd.m1, hbuf, I, cap, 64, 256, true) &&
+            make_map(&m_gu.m3, xs, H, cap, 64, 64, true) &&
+            make_map(&m_sgu.m1, xs, H, cap, 64, 64, true) &&
+            make_map(&m_sd.m1, hbuf, I, cap, 64, 64, true) &&
             make_map(&m_dn.m0, w_down, I, (uint64_t)E * H, 64, 128, true) &&
-            make_map(&m_dn.m1, hbuf, I, cap, 64, 256, true);
+            make_map(&m_dn.m1, hbuf, I, cap, 64, 64, true);
   if (ok && L > 0) {
     ok = make_map(&m_sgu.m0, lora_a_gu, H, (uint64_t)L * E * 2 * R, 64, 8, true) &&
          make_map(&m_gu.m1, lora_b_gu, R, (uint64_t)L * E * 2 * I, 8, 128, false) &&
-         make_map(&m_gu.m2, zgu, 2 * f.R16, cap, 8, 256, false) &&
+         make_map(&m_gu.m2, zgu, 2 * f.R16, cap, 8, 64, false) &&
          make_map(&m_sd.m0, lora_a_down, I, (uint64_t)L * E * R, 64, 8, true) &&
          make_map(&m_dn.m2, lora_b_down, R, (uint64_t)L * E * H, 8, 128, false) &&
-         make_map(&m_dn.m3, zd, f.R16, cap, 8, 256, false);
+         make_map(&m_dn.m3, zd, f.R16, cap, 8, 64, false);
   }
   if (!ok) return MLR_ERR_CUDA;
 
@@ -648,42 +757,49 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                                                counts, d_status);
   MLR_CHECK_LAUNCH();
   note_launch();
+  {
+    const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
+    const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
+    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, sorted, npad, (int64_t)T * K, K, H, f.cap, xs);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+  }
   prof_mark(prof, 1, stream);
 
   Params p{};
   p.T = T; p.K = K; p.E = E; p.H = H; p.I = I; p.L = L; p.R = R; p.R16 = f.R16; p.C = f.C;
   p.P = (int64_t)T * K;
-  p.x = x;
   p.topk_weights = topk_weights;
   p.lora_ranks = lora_ranks;
   p.scalings = scalings;
   p.sorted_ids = sorted;
-  p.bstart = bstart;
+  p.base_tiles = base_tiles;
+  p.shrink_tiles = shrink_tiles;
   p.zgu = zgu; p.h = hbuf; p.zd = zd; p.yacc = yacc;
   p.status = d_status;
 
   if (L > 0) {
     Params q = p;
-    q.tiles = shrink_tiles; q.n_tiles = counts + 1; q.mtiles = f.mtiles_gu;
-    if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, f.mtiles_gu, stream)) != MLR_OK) return rc;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu;
+    if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 2, stream);
   {
     Params q = p;
-    q.tiles = base_tiles; q.n_tiles = counts; q.mtiles = 1;
-    if ((rc = launch_gemm<kGateUp>(m_gu, q, f.max_base, (int)ceil_div(I, 128), stream)) != MLR_OK) return rc;
+    q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128);
+    if ((rc = launch_gemm<kGateUp>(m_gu, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 3, stream);
   if (L > 0) {
     Params q = p;
-    q.tiles = shrink_tiles; q.n_tiles = counts + 1; q.mtiles = f.mtiles_d;
-    if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, f.mtiles_d, stream)) != MLR_OK) return rc;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_d;
+    if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 4, stream);
   {
     Params q = p;
-    q.tiles = base_tiles; q.n_tiles = counts; q.mtiles = 1;
-    if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, (int)ceil_div(H, 128), stream)) != MLR_OK) return rc;
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 128);
+    if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * H;

@@ -4,7 +4,7 @@
 
 namespace mlr {
 
-constexpr int kProfStages = 7;  // align, plan, shrink_gu, gate_up, shrink_d, down, convert
+constexpr int kProfStages = 7;  // align, plan + x gather, shrink_gu, gate_up, shrink_d, down, convert
 
 void note_launch(int n = 1);
 // Per forward call: returns a slot (>= 0) while recording is on, else -1.
