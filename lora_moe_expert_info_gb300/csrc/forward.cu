@@ -50,18 +50,21 @@ constexpr int kEpiWarp0 = 5;
 constexpr int kThreads = 288;     // 9 warps (warps 1-3 idle)
 constexpr int kGatherThreads = 256;
 constexpr int kPlanThreads = 1024;
-constexpr int kEpiBytes = 16 * (128 + 4) * 4;  // one 16-row fp32 staging chunk
+constexpr int kShrinkRows = 128;  // max sorted rows per shrink tile
+constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging: 32 rows of bf16 h, or 16 rows of fp32
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 
 template <int KIND> struct Cfg;
-template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
+template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512; };
-template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
+template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
 
+// Tensor maps of one GEMM kind.  Shrinks: m0 = LoRA A rows in 64-row boxes,
+// m1 = x_sorted / h rows, m2/m3/m4 = LoRA A rows in 32/16/8-row boxes.
 struct Maps {
-  CUtensorMap m0, m1, m2, m3;
+  CUtensorMap m0, m1, m2, m3, m4;
 };
 
 // Base tile: head {e, row0, nrows, nb} followed by nb buckets {j0, nj, l, r16}.
@@ -72,6 +75,7 @@ struct TileRec {
 
 struct Params {
   int T, K, E, H, I, L, R, R16, C, nblk;
+  int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
   int64_t P;
   const float* topk_weights;
   const int32_t* lora_ranks;
@@ -88,8 +92,8 @@ struct Params {
 };
 
 struct __align__(16) Ctl {
-  uint64_t full[4];
-  uint64_t empty[4];
+  uint64_t full[8];   // one per ring stage (at most 8)
+  uint64_t empty[8];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem;
@@ -101,14 +105,19 @@ struct __align__(16) Ctl {
 
 template <int KIND>
 constexpr int smem_bytes() {
+  static_assert(Cfg<KIND>::kStages <= 8, "ring barriers");
   return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + kEpiBytes + (int)sizeof(Ctl) + 1024;
 }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
+// SiLU(v) = v / (1 + e^-v) with CUDA's fast exponential and fast division
+// (a few ulp of fp32; the result is rounded to bf16 right after).  For
+// v << 0 the denominator overflows and the quotient is 0, the correct limit.
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-// One work item: tile rows, weight block, adapter.
+// One work item: tile rows, weight block, adapter (shrinks: with its rank).
 struct Item {
   int e, l, row0, nrows, nb, mb;
+  int r, r8, r16;
   const TileRec* rec;
 };
 
@@ -120,10 +129,14 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
   if (KIND == kShrinkGU || KIND == kShrinkD) {
     const int4 t = p.shrink_tiles[tile];
     it.e = t.x; it.l = t.y; it.row0 = t.z; it.nrows = t.w; it.nb = 0; it.rec = nullptr;
+    it.r = p.lora_ranks[it.l];
+    it.r8 = (it.r + 7) & ~7;
+    it.r16 = (it.r + 15) & ~15;
   } else {
     it.rec = p.base_tiles + tile;
     const int4 h = it.rec->head;
     it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w;
+    it.r = it.r8 = it.r16 = 0;
   }
   return it;
 }
@@ -134,10 +147,11 @@ __device__ __forceinline__ int expand_steps(const Item& it, int ngates) {
   for (int b = 0; b < it.nb; ++b) n += ngates * ((it.rec->bk[b].w + 63) >> 6);
   return n;
 }
-// Decodes expand step k of an item into (bucket, gate, rank group).
-__device__ __forceinline__ void expand_decode(const Item& it, int ngates, int k, int& bi, int& g, int& kg) {
-  for (bi = 0; bi < it.nb; ++bi) {
-    const int per = (it.rec->bk[bi].w + 63) >> 6;
+// Decodes expand step k of an item into its bucket record, gate and rank group.
+__device__ __forceinline__ void expand_decode(const Item& it, int ngates, int k, int4& bk, int& g, int& kg) {
+  for (int b = 0; b < it.nb; ++b) {
+    bk = it.rec->bk[b];
+    const int per = (bk.w + 63) >> 6;
     if (k < ngates * per) {
       g = k / per;
       kg = k % per;
@@ -145,7 +159,9 @@ __device__ __forceinline__ void expand_decode(const Item& it, int ngates, int k,
     }
     k -= ngates * per;
   }
-  bi = 0; g = 0; kg = 0;
+  bk = make_int4(0, 0, 0, 0);
+  g = 0;
+  kg = 0;
 }
 
 template <int KIND>
@@ -208,26 +224,40 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (main_step) {
             const int kb = s;
             if (kShrink) {
-              // LoRA A rows packed into M in 8-row groups: gate rows then up rows
-              const int r = p.lora_ranks[it.l];
-              const int r8 = (r + 7) & ~7, r16 = (r + 15) & ~15;
-              int ngr = 0;
-              for (int grp = 0; grp < 16; ++grp) {
-                const int m0 = 128 * it.mb + grp * 8;
-                const int g = (KIND == kShrinkGU && m0 >= r16) ? 1 : 0;
-                const int q0 = m0 - g * r16;
-                if (q0 < r8 && (KIND == kShrinkGU || g == 0)) ++ngr;
-              }
-              mbar_arrive_expect_tx(&c.full[st], ngr * 1024 + rbox * 8192);
-              for (int grp = 0; grp < 16; ++grp) {
-                const int m0 = 128 * it.mb + grp * 8;
-                const int g = (KIND == kShrinkGU && m0 >= r16) ? 1 : 0;
-                const int q0 = m0 - g * r16;
-                if (!(q0 < r8 && (KIND == kShrinkGU || g == 0))) continue;
-                const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q0
-                                                  : (it.l * p.E + it.e) * p.R + q0;
-                tma_load_2d(sbuf + grp * 1024, &maps.m0, &c.full[st], kb * 64, row);
-              }
+              // LoRA A rows packed into M: gate rows [0, r8) at packed row 0, up
+              // rows at packed row r16; each run split into boxes of 64/32/16/8
+              // rows, none crossing a 128-row M-block boundary
+              const int r8 = it.r8, r16 = it.r16;
+              const int mlo = 128 * it.mb, mhi = mlo + 128;  // this item's M block
+              int arows = 0;
+              for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
+                for (int q = 0; q < r8;) {
+                  const int pr = g * r16 + q;
+                  int bh = 8;
+                  for (int j = 0; j < 4; ++j) {
+                    const int cand = 64 >> j;
+                    if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; break; }
+                  }
+                  if (pr >= mlo && pr < mhi) arows += bh;
+                  q += bh;
+                }
+              mbar_arrive_expect_tx(&c.full[st], arows * 128 + rbox * 8192);
+              for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
+                for (int q = 0; q < r8;) {
+                  const int pr = g * r16 + q;
+                  int bh = 8, bj = 3;
+                  for (int j = 0; j < 4; ++j) {
+                    const int cand = 64 >> j;
+                    if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; bj = j; break; }
+                  }
+                  if (pr >= mlo && pr < mhi) {
+                    const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q
+                                                      : (it.l * p.E + it.e) * p.R + q;
+                    const CUtensorMap* am = bj == 0 ? &maps.m0 : bj == 1 ? &maps.m2 : bj == 2 ? &maps.m3 : &maps.m4;
+                    tma_load_2d(sbuf + (pr - mlo) * 128, am, &c.full[st], kb * 64, row);
+                  }
+                  q += bh;
+                }
               // B operand: rows of x_sorted (gate_up shrink) or h (down shrink)
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 16384 + q * 8192, &maps.m1, &c.full[st], kb * 64, it.row0 + q * 64);
@@ -246,9 +276,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
-            int bi, g, kg;
-            expand_decode(it, kGates, s - nk, bi, g, kg);
-            const int4 bk = it.rec->bk[bi];  // {j0, nj, l, r16}
+            int4 bk;  // {j0, nj, l, r16}
+            int g, kg;
+            expand_decode(it, kGates, s - nk, bk, g, kg);
             const int nch = min(8, (bk.w - kg * 64) / 8);
             const int zr = (int)ceil_div(bk.y, 64);
             mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zr * 1024));
@@ -302,9 +332,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                          (s > 0 || kk > 0) ? 1u : 0u);
             }
           } else {
-            int bi, g, kg;
-            expand_decode(it, kGates, s - nk, bi, g, kg);
-            const int4 bk = it.rec->bk[bi];
+            int4 bk;
+            int g, kg;
+            expand_decode(it, kGates, s - nk, bk, g, kg);
             const int nch = min(8, (bk.w - kg * 64) / 8);
             const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + bk.x;
             const uint32_t idesc = idesc_bf16_f32(128, bk.y);
@@ -349,16 +379,23 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         uint16_t* hs = reinterpret_cast<uint16_t*>(epi);
         constexpr int kHs = 128 + 8;
         const int i0 = it.mb * 128;
-        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-          float gv[16], uv[16];
-          tmem_ld16(tl + c0, gv);
-          tmem_ld16(tl + 256 + c0, uv);
+        for (int c0 = 0; c0 < it.nrows; c0 += 32) {
+          const int ncol = min(32, it.nrows - c0);  // 32 or 16
+          if (ncol == 32) {
+            float gv[32], uv[32];
+            tmem_ld32(tl + c0, gv);
+            tmem_ld32(tl + 256 + c0, uv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+            for (int j = 0; j < 32; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+          } else {
+            float gv[16], uv[16];
+            tmem_ld16(tl + c0, gv);
+            tmem_ld16(tl + 256 + c0, uv);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+          }
           named_bar_sync(1, 128);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int q = et + 128 * k;
+          for (int q = et; q < ncol * 16; q += 128) {
             const int n = q >> 4, ch = q & 15;
             if (i0 + ch * 8 < p.I)
               *reinterpret_cast<uint4*>(p.h + (int64_t)(it.row0 + c0 + n) * p.I + i0 + ch * 8) =
@@ -390,8 +427,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           named_bar_sync(1, 128);
         }
       } else {
-        const int r = p.lora_ranks[it.l];
-        const int r16 = (r + 15) & ~15;
+        const int r = it.r, r16 = it.r16;
         const float sc = p.scalings[it.l];
         const int mg = 128 * it.mb + m;
         int g = 0, q = mg;
@@ -509,7 +545,7 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       const int r = lora_ranks[cl - 1];
       if (r < 0 || r > R) { bad = 1; continue; }
       if (r == 0) continue;
-      mine += (int)ceil_div(bstart[b + 1] - bstart[b], kTileRows);
+      mine += (int)ceil_div(bstart[b + 1] - bstart[b], kShrinkRows);
     }
     int total;
     int off = block_offsets(mine, &total);
@@ -519,7 +555,7 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       const int r = lora_ranks[cl - 1];
       if (r <= 0 || r > R) continue;
       const int s = (int)bstart[b], n = (int)bstart[b + 1] - s;
-      const int nt = (int)ceil_div(n, kTileRows);
+      const int nt = (int)ceil_div(n, kShrinkRows);
       for (int k = 0; k < nt; ++k) {
         int r0, nr;
         chunk_rows(n, k, nt, r0, nr);
@@ -592,6 +628,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// LoRA A maps with 64/32/16/8-row boxes (m0, m2, m3, m4); a box taller than the
+// tensor is skipped.  The 8-row map always exists (rows = L*E*R >= 8).
+bool make_abox_maps(Maps& m, const void* base, uint64_t cols, uint64_t rows, int* mask) {
+  CUtensorMap* slot[4] = {&m.m0, &m.m2, &m.m3, &m.m4};
+  *mask = 0;
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t bh = 64u >> j;
+    if (bh > rows) continue;
+    if (!make_map(slot[j], base, cols, rows, 64, bh, true)) return false;
+    *mask |= 1 << j;
+  }
+  return (*mask & 8) != 0;
+}
+
 struct FwdLayout {
   bool ok;
   AlignPlan al;
@@ -616,7 +666,7 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.cap = f.al.capacity;
   const int64_t nb_nonempty = f.al.P < f.al.NB ? f.al.P : f.al.NB;
   f.max_base = f.cap / kTileRows + E + 1;
-  f.max_shrink = f.cap / kTileRows + nb_nonempty + 1;
+  f.max_shrink = f.cap / kShrinkRows + nb_nonempty + 1;
   int64_t o = 0;
   auto take = [&](int64_t bytes) { const int64_t r = o; o += round_up(bytes > 0 ? bytes : 1, 256); return r; };
   f.o_sorted = take(f.cap * 4);
@@ -730,6 +780,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
+  int abox_gu = 0, abox_d = 0;
   const uint64_t cap = (uint64_t)f.cap;
   bool ok = make_map(&m_gu.m0, w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
             make_map(&m_gu.m3, xs, H, cap, 64, 64, true) &&
@@ -738,10 +789,10 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
             make_map(&m_dn.m0, w_down, I, (uint64_t)E * H, 64, 128, true) &&
             make_map(&m_dn.m1, hbuf, I, cap, 64, 64, true);
   if (ok && L > 0) {
-    ok = make_map(&m_sgu.m0, lora_a_gu, H, (uint64_t)L * E * 2 * R, 64, 8, true) &&
+    ok = make_abox_maps(m_sgu, lora_a_gu, H, (uint64_t)L * E * 2 * R, &abox_gu) &&
          make_map(&m_gu.m1, lora_b_gu, R, (uint64_t)L * E * 2 * I, 8, 128, false) &&
          make_map(&m_gu.m2, zgu, 2 * f.R16, cap, 8, 64, false) &&
-         make_map(&m_sd.m0, lora_a_down, I, (uint64_t)L * E * R, 64, 8, true) &&
+         make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d) &&
          make_map(&m_dn.m2, lora_b_down, R, (uint64_t)L * E * H, 8, 128, false) &&
          make_map(&m_dn.m3, zd, f.R16, cap, 8, 64, false);
   }
@@ -780,7 +831,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   if (L > 0) {
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu;
     if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 2, stream);
@@ -792,7 +843,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   prof_mark(prof, 3, stream);
   if (L > 0) {
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_d;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d;
     if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 4, stream);
