@@ -61,10 +61,17 @@ template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageByte
 template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
 
-// Tensor maps of one GEMM kind.  Shrinks: m0 = LoRA A rows in 64-row boxes,
-// m1 = x_sorted / h rows, m2/m3/m4 = LoRA A rows in 32/16/8-row boxes.
+// Tensor maps of one GEMM kind, by slot.
+//   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
+//            kRows = chunk-major x_sorted or h rows (one 64-row box = 8 KB contiguous)
+//   shrinks: kA32/kA16/kA8 = LoRA A in 32/16/8-row boxes
+//   base:    kB8/kB4/kB2 = LoRA B stack viewed as [rank chunk][row][8 ranks], 8/4/2 chunks per box
+//            kZ8/kZ4/kZ2 = chunk-major z viewed the same way
+// The TMA engine's cost grows with the number of contiguous global segments it
+// fetches, so every box is chosen to read long contiguous runs.
+enum MapSlot { kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7 };
 struct Maps {
-  CUtensorMap m0, m1, m2, m3, m4;
+  CUtensorMap m[8];
 };
 
 // Base tile: head {e, row0, nrows, nb} followed by nb buckets {j0, nj, l, r16}.
@@ -75,6 +82,9 @@ struct TileRec {
 
 struct Params {
   int T, K, E, H, I, L, R, R16, C, nblk;
+  int cap;    // rows of the sorted buffers (x_sorted, h, z) per 64- or 8-column chunk
+  int zrows;  // rows per z box (min(256, cap))
+  int bmask;  // base GEMMs: bit 0 / 1 set if the 8- / 4-chunk LoRA B and z views exist
   int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
   int64_t P;
   const float* topk_weights;
@@ -253,46 +263,44 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                   if (pr >= mlo && pr < mhi) {
                     const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q
                                                       : (it.l * p.E + it.e) * p.R + q;
-                    const CUtensorMap* am = bj == 0 ? &maps.m0 : bj == 1 ? &maps.m2 : bj == 2 ? &maps.m3 : &maps.m4;
+                    const CUtensorMap* am = &maps.m[bj == 0 ? kW : bj == 1 ? kA32 : bj == 2 ? kA16 : kA8];
                     tma_load_2d(sbuf + (pr - mlo) * 128, am, &c.full[st], kb * 64, row);
                   }
                   q += bh;
                 }
               // B operand: rows of x_sorted (gate_up shrink) or h (down shrink)
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m1, &c.full[st], kb * 64, it.row0 + q * 64);
+                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else if (KIND == kGateUp) {
               mbar_arrive_expect_tx(&c.full[st], 32768 + rbox * 8192);
               const int i0 = it.mb * 128;
-              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, it.e * 2 * p.I + i0);
-              tma_load_2d(sbuf + 16384, &maps.m0, &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+              tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
+              tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 32768 + q * 8192, &maps.m3, &c.full[st], kb * 64, it.row0 + q * 64);
+                tma_load_2d(sbuf + 32768 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else {  // kDown
               mbar_arrive_expect_tx(&c.full[st], 16384 + rbox * 8192);
-              tma_load_2d(sbuf, &maps.m0, &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
+              tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m1, &c.full[st], kb * 64, it.row0 + q * 64);
+                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
             int4 bk;  // {j0, nj, l, r16}
             int g, kg;
             expand_decode(it, kGates, s - nk, bk, g, kg);
-            const int nch = min(8, (bk.w - kg * 64) / 8);
-            const int zr = (int)ceil_div(bk.y, 64);
-            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zr * 1024));
+            const int nch = min(8, (bk.w - kg * 64) / 8);  // rank chunks of 8 (even)
+            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + p.zrows * 16));
             const int m0 = it.mb * 128;
             const int brow = KIND == kGateUp ? ((bk.z * p.E + it.e) * 2 + g) * p.I + m0
                                              : (bk.z * p.E + it.e) * p.H + m0;
-            const CUtensorMap* bmap = KIND == kGateUp ? &maps.m1 : &maps.m2;
-            const CUtensorMap* zmap = KIND == kGateUp ? &maps.m2 : &maps.m3;
-            const int zcol0 = (KIND == kGateUp ? g * p.R16 : 0) + kg * 64;
-            for (int ch = 0; ch < nch; ++ch) {
-              tma_load_2d(sbuf + ch * 2048, bmap, &c.full[st], kg * 64 + ch * 8, brow);
-              for (int zq = 0; zq < zr; ++zq)
-                tma_load_2d(sbuf + 16384 + ch * 4096 + zq * 1024, zmap, &c.full[st], zcol0 + ch * 8,
-                            it.row0 + bk.x + zq * 64);
+            const int zc0 = ((KIND == kGateUp ? g * p.R16 : 0) + kg * 64) >> 3;
+            for (int ch = 0; ch < nch;) {
+              const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
+              const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2), zs = nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2);
+              tma_load_3d(sbuf + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
+              tma_load_3d(sbuf + 16384 + ch * p.zrows * 16, &maps.m[zs], &c.full[st], 0, it.row0 + bk.x, zc0 + ch);
+              ch += nc;
             }
           }
         }
@@ -340,7 +348,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const uint32_t idesc = idesc_bf16_f32(128, bk.y);
             for (int k16 = 0; k16 < nch / 2; ++k16)
               mma_bf16(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
-                       sdesc_noswz(sb + 16384 + k16 * 2 * 4096, 4096, 128), idesc, 1u);
+                       sdesc_noswz(sb + 16384 + k16 * 2 * p.zrows * 16, p.zrows * 16, 128), idesc, 1u);
           }
           mma_commit(&c.empty[st]);
         }
@@ -395,11 +403,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           }
           named_bar_sync(1, 128);
+          const int icap = (int)round_up(p.I, 64);
           for (int q = et; q < ncol * 16; q += 128) {
             const int n = q >> 4, ch = q & 15;
-            if (i0 + ch * 8 < p.I)
-              *reinterpret_cast<uint4*>(p.h + (int64_t)(it.row0 + c0 + n) * p.I + i0 + ch * 8) =
-                  *reinterpret_cast<const uint4*>(hs + n * kHs + ch * 8);
+            const int i = i0 + ch * 8;
+            if (i < icap) {  // h is chunk-major: [I/64][cap][64]; the tail past I is zero
+              const uint4 v = i < p.I ? *reinterpret_cast<const uint4*>(hs + n * kHs + ch * 8) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + c0 + n) * 64 + (i & 63)) = v;
+            }
           }
           named_bar_sync(1, 128);
         }
@@ -440,10 +451,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float z = q < r ? sc * v[j] : 0.f;
-              if (KIND == kShrinkGU)
-                p.zgu[(int64_t)(it.row0 + c0 + j) * (2 * p.R16) + g * p.R16 + q] = f32_to_bf16_bits(z);
-              else
-                p.zd[(int64_t)(it.row0 + c0 + j) * p.R16 + q] = f32_to_bf16_bits(z);
+              // z is chunk-major: [columns/8][cap][8]
+              const int col = (KIND == kShrinkGU ? g * p.R16 : 0) + q;
+              uint16_t* zb = KIND == kShrinkGU ? p.zgu : p.zd;
+              zb[((int64_t)(col >> 3) * p.cap + it.row0 + c0 + j) * 8 + (col & 7)] = f32_to_bf16_bits(z);
             }
           }
         }
@@ -567,7 +578,8 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
   if (bad) set_status(status, MLR_STATUS_RANK);
 }
 
-// x_sorted[r] = x[sorted_ids[r] / K] for r < npad, zeros for pad rows: one
+// x_sorted row r = x[sorted_ids[r] / K] for r < npad (zeros for pad rows),
+// stored chunk-major, [H/64][cap][64], with zeros past H in the last chunk: one
 // warp per row, 16-byte loads and stores.
 __global__ void __launch_bounds__(kGatherThreads)
 gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
@@ -576,13 +588,15 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sort
   const int64_t n = min((int64_t)*npad, cap);
   const int lane = threadIdx.x & 31;
   const int64_t wpb = kGatherThreads / 32;
-  const int chunks = H / 8;  // H is a multiple of 8
+  const int pieces = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
   for (int64_t r = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); r < n; r += (int64_t)gridDim.x * wpb) {
     const int pr = sorted_ids[r];
     const bool real = pr >= 0 && pr < P;
     const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(pr / K) * H : 0));
-    uint4* dst = reinterpret_cast<uint4*>(xs + r * H);
-    for (int ch = lane; ch < chunks; ch += 32) dst[ch] = real ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+    for (int q = lane; q < pieces; q += 32) {
+      const uint4 v = (real && q * 8 < H) ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(xs + ((int64_t)(q >> 3) * cap + r) * 64 + (q & 7) * 8) = v;
+    }
   }
 }
 
@@ -631,7 +645,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 // LoRA A maps with 64/32/16/8-row boxes (m0, m2, m3, m4); a box taller than the
 // tensor is skipped.  The 8-row map always exists (rows = L*E*R >= 8).
 bool make_abox_maps(Maps& m, const void* base, uint64_t cols, uint64_t rows, int* mask) {
-  CUtensorMap* slot[4] = {&m.m0, &m.m2, &m.m3, &m.m4};
+  CUtensorMap* slot[4] = {&m.m[kW], &m.m[kA32], &m.m[kA16], &m.m[kA8]};
   *mask = 0;
   for (int j = 0; j < 4; ++j) {
     const uint32_t bh = 64u >> j;
@@ -640,6 +654,20 @@ bool make_abox_maps(Maps& m, const void* base, uint64_t cols, uint64_t rows, int
     *mask |= 1 << j;
   }
   return (*mask & 8) != 0;
+}
+
+// 3-D bf16 view {d0, d1, d2} with byte strides s1 (dim 1) and s2 (dim 2), no swizzle.
+bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+               uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct FwdLayout {
@@ -654,8 +682,8 @@ struct FwdLayout {
 FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R) {
   FwdLayout f{};
   f.ok = false;
-  if (T < 0 || K < 1 || E < 1 || H < 64 || I < 64 || L < 0 || R < 0) return f;
-  if (H % 8 || I % 8 || R % 8 || R > 256 || (L > 0 && R < 8)) return f;
+  if (T < 0 || K < 1 || E < 1 || H < 128 || I < 64 || L < 0 || R < 0) return f;
+  if (H % 8 || I % 8 || R > 256 || (L > 0 && (R % 16 != 0 || R < 16))) return f;
   f.al = align_plan(T, K, E, L, kBlock);
   if (!f.al.ok) return f;
   f.R16 = (int)round_up(R, 16);
@@ -678,10 +706,10 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.o_shrink = take(f.max_shrink * 16);
   f.o_counts = take(16);
   f.o_zgu = take(f.cap * 2 * f.R16 * 2);
-  f.o_h = take(f.cap * (int64_t)I * 2);
+  f.o_h = take(f.cap * round_up(I, 64) * 2);
   f.o_zd = take(f.cap * f.R16 * 2);
   f.o_yacc = take((int64_t)T * H * 4);
-  f.o_xs = take(f.cap * (int64_t)H * 2);
+  f.o_xs = take(f.cap * round_up(H, 64) * 2);
   f.total = o;
   f.ok = true;
   return f;
@@ -780,21 +808,33 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
-  int abox_gu = 0, abox_d = 0;
+  int abox_gu = 0, abox_d = 0, bmask = 0;
   const uint64_t cap = (uint64_t)f.cap;
-  bool ok = make_map(&m_gu.m0, w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
-            make_map(&m_gu.m3, xs, H, cap, 64, 64, true) &&
-            make_map(&m_sgu.m1, xs, H, cap, 64, 64, true) &&
-            make_map(&m_sd.m1, hbuf, I, cap, 64, 64, true) &&
-            make_map(&m_dn.m0, w_down, I, (uint64_t)E * H, 64, 128, true) &&
-            make_map(&m_dn.m1, hbuf, I, cap, 64, 64, true);
+  const uint64_t hk = (uint64_t)ceil_div(H, 64), ik = (uint64_t)ceil_div(I, 64);
+  const uint32_t zrows = (uint32_t)(f.cap < 256 ? f.cap : 256);
+  bool ok = make_map(&m_gu.m[kW], w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
+            make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
+            make_map(&m_sgu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
+            make_map(&m_sd.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
+            make_map(&m_dn.m[kW], w_down, I, (uint64_t)E * H, 64, 128, true) &&
+            make_map(&m_dn.m[kRows], hbuf, 64, ik * cap, 64, 64, true);
   if (ok && L > 0) {
     ok = make_abox_maps(m_sgu, lora_a_gu, H, (uint64_t)L * E * 2 * R, &abox_gu) &&
-         make_map(&m_gu.m1, lora_b_gu, R, (uint64_t)L * E * 2 * I, 8, 128, false) &&
-         make_map(&m_gu.m2, zgu, 2 * f.R16, cap, 8, 64, false) &&
-         make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d) &&
-         make_map(&m_dn.m2, lora_b_down, R, (uint64_t)L * E * H, 8, 128, false) &&
-         make_map(&m_dn.m3, zd, f.R16, cap, 8, 64, false);
+         make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d);
+    const int nc[3] = {8, 4, 2};
+    const int bslot[3] = {kB8, kB4, kB2}, zslot[3] = {kZ8, kZ4, kZ2};
+    for (int j = 0; ok && j < 3; ++j) {
+      if (nc[j] > R / 8) continue;  // a box may not span more rank chunks than exist
+      if (j < 2) bmask |= 1 << j;
+      // LoRA B stacks as [rank chunk][row][8]: each row's ranks are contiguous
+      ok = make_map3(&m_gu.m[bslot[j]], lora_b_gu, 8, (uint64_t)L * E * 2 * I, (uint64_t)R / 8, (uint64_t)R * 2, 16,
+                     8, 128, nc[j]) &&
+           make_map3(&m_dn.m[bslot[j]], lora_b_down, 8, (uint64_t)L * E * H, (uint64_t)R / 8, (uint64_t)R * 2, 16,
+                     8, 128, nc[j]) &&
+           // chunk-major z: [column/8][cap][8]
+           make_map3(&m_gu.m[zslot[j]], zgu, 8, cap, (uint64_t)2 * f.R16 / 8, 16, cap * 16, 8, zrows, nc[j]) &&
+           make_map3(&m_dn.m[zslot[j]], zd, 8, cap, (uint64_t)f.R16 / 8, 16, cap * 16, 8, zrows, nc[j]);
+    }
   }
   if (!ok) return MLR_ERR_CUDA;
 
@@ -819,6 +859,9 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   Params p{};
   p.T = T; p.K = K; p.E = E; p.H = H; p.I = I; p.L = L; p.R = R; p.R16 = f.R16; p.C = f.C;
+  p.cap = f.cap;
+  p.zrows = (int)zrows;
+  p.bmask = bmask;
   p.P = (int64_t)T * K;
   p.topk_weights = topk_weights;
   p.lora_ranks = lora_ranks;

@@ -112,8 +112,8 @@ def test_tiny_lora_delta_sensitivity(cuda_device):
 
 @pytest.mark.parametrize("seed", [0, 1])
 def test_ragged_shapes(cuda_device, seed):
-    # H, I not multiples of 64/128, ranks not multiples of 8, R16 > R, skewed routing
-    c = custom_case(cuda_device, T=203, K=3, E=5, H=200, I=136, L=4, R=24, ranks=[12, 0, 24, 5],
+    # H, I not multiples of 64/128, ranks not multiples of 8 or 16, skewed routing
+    c = custom_case(cuda_device, T=203, K=3, E=5, H=200, I=136, L=4, R=32, ranks=[12, 0, 24, 5],
                     seg_lens=[17, 60, 1, 90, 35], adapters=[0, 3, -1, 2, 1], seed=seed,
                     lora_std="fan_in", expert_bias=1.0)
     none = np.full_like(c.mapping, -1)
