@@ -2,8 +2,10 @@
 // stable, each bucket padded to block_size (sglang PR #14105 page, 实现拆解:
 // moe_lora_align_block_size "sorts tokens by LoRA adapter and expert id").
 //
-// key(p) = e * (L+1) + (lora + 1); NB = E * (L+1) buckets.  Pairs are split
-// into G contiguous chunks of up to 32768 pairs.  Four launches:
+// key(p) = e * (L+1) + (lora + 1); NB = E * (L+1) buckets.  Up to 32768 pairs
+// and 8192 buckets, one block does everything in shared memory (align_block).
+// Otherwise pairs are split into G contiguous chunks of up to 32768 pairs and
+// four launches follow:
 //   1. count    : per chunk, a shared-memory histogram over NB buckets
 //                 -> cnt[g][b]
 //   2. colscan  : per bucket, exclusive prefix over chunks (in place) and the
@@ -26,56 +28,6 @@ constexpr int kMaxItems = 32;                         // pairs per thread per ch
 constexpr int kMaxChunk = kThreads * kMaxItems;       // 32768 (fits uint16 indices)
 constexpr int kColThreads = 256;
 
-__device__ __forceinline__ int pair_key(const int32_t* __restrict__ topk_ids,
-                                        const int32_t* __restrict__ mapping, int64_t p, int topk,
-                                        int E, int C, int L, int& bad) {
-  const int e = __ldg(topk_ids + p);
-  const int l = __ldg(mapping + p / topk);
-  if (e < 0 || e >= E || l < -1 || l >= L) {
-    bad |= MLR_STATUS_INDEX;
-    return -1;
-  }
-  return e * C + (l + 1);
-}
-
-// Block-wide exclusive scan of s[0..n) in place; s[n] receives the total.
-__device__ void block_exclusive_scan(uint32_t* s, int n) {
-  __shared__ uint32_t warp_tot[32];
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
-  uint32_t local = 0;
-  for (int b = b0; b < b1; ++b) local += s[b];
-  // inclusive warp scan of the per-thread sums
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t inc = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    uint32_t w = lane < nw ? warp_tot[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += v;
-    }
-    if (lane < nw) warp_tot[lane] = w;  // inclusive warp totals
-  }
-  __syncthreads();
-  uint32_t run = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0u);
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t c = s[b];
-    s[b] = run;
-    run += c;
-  }
-  if (threadIdx.x == blockDim.x - 1) s[n] = run;
-  __syncthreads();
-}
-
 __global__ void __launch_bounds__(kThreads)
 align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
                    int64_t P, int topk, int E, int L, int chunk, uint32_t* __restrict__ cnt,
@@ -88,7 +40,7 @@ align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
   const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
   int bad = 0;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const int key = pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
+    const int key = align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
     if (key >= 0) atomicAdd(&hist[key], 1u);
   }
   if (bad) set_status(d_status, bad);
@@ -103,12 +55,13 @@ align_colscan_kernel(uint32_t* __restrict__ cnt, int G, int NB, uint32_t* __rest
   if (b >= NB) return;
   uint32_t run = 0;
   int g = 0;
-  for (; g + 4 <= G; g += 4) {
-    uint32_t c[4];
+  // 16 loads in flight per round trip to L2
+  for (; g + 16 <= G; g += 16) {
+    uint32_t c[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] = cnt[(int64_t)(g + q) * NB + b];
+    for (int q = 0; q < 16; ++q) c[q] = cnt[(int64_t)(g + q) * NB + b];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 16; ++q) {
       cnt[(int64_t)(g + q) * NB + b] = run;
       run += c[q];
     }
@@ -194,13 +147,13 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
       const int j = it * kThreads + threadIdx.x;
       ks[it] = 0xFFFFFFFFu;
       if (j < n) {
-        const int key = pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
+        const int key = align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
         if (key >= 0) ks[it] = ((uint32_t)key << 16) | atomicAdd(&off[key], 1u);
       }
       __syncthreads();  // rounds are ordered: a bucket's slots follow round order
     }
   }
-  block_exclusive_scan(off, NB);
+  align_block_scan(off, NB);
 #pragma unroll
   for (int it = 0; it < kMaxItems; ++it)
     if (it < rounds && ks[it] != 0xFFFFFFFFu)
@@ -228,19 +181,36 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
     }
   }
 
-  // pad sentinels and per-block labels: buckets are shared out over all threads
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const int64_t cap_blocks = capacity / block_size;
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < NB; b += nthreads) {
-    const int64_t s = bstart[b], e = bstart[b + 1];
+  // Pad sentinels and per-block labels: one warp per bucket over the whole
+  // grid, lanes writing consecutive entries.  Padded positions are below
+  // P + NB * block_size < 2^31 (align_plan checks the bound).
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int64_t cap64 = capacity < INT32_MAX ? capacity : INT32_MAX;
+  const int cap = (int)cap64, cap_blocks = (int)(cap64 / block_size);
+  for (int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < NB; b += nwarps) {
+    const int s = (int)bstart[b], e = (int)bstart[b + 1];
     if (s == e) continue;
-    for (int64_t q = s + btotal[b]; q < e && q < capacity; ++q) sorted_ids[q] = (int32_t)P;
-    const int expert = (int)(b / C), lora = (int)(b % C) - 1;
-    for (int64_t blk = s / block_size; blk < e / block_size && blk < cap_blocks; ++blk) {
+    for (int q = s + (int)btotal[b] + lane; q < e && q < cap; q += 32) sorted_ids[q] = (int32_t)P;
+    const int expert = b / C, lora = b - expert * C - 1;
+    for (int blk = s / block_size + lane; blk < e / block_size && blk < cap_blocks; blk += 32) {
       block_expert[blk] = expert;
       block_lora[blk] = lora;
     }
   }
+}
+
+// Single-block path: the whole align in one launch.
+__global__ void __launch_bounds__(kAlignBlockThreads)
+align_block_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping, int P,
+                   int topk, int E, int L, int block_size, int32_t* __restrict__ sorted_ids,
+                   int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
+                   int32_t* __restrict__ num_post_pad, uint32_t* __restrict__ bstart,
+                   int64_t capacity, int32_t* d_status) {
+  extern __shared__ __align__(16) unsigned char align_smem[];
+  const AlignBlockSmem sm = align_block_carve(align_smem, E * (L + 1), P);
+  align_block(topk_ids, mapping, P, topk, E, L, block_size, sm, sorted_ids, block_expert, block_lora,
+              num_post_pad, bstart, capacity, d_status);
 }
 
 }  // namespace
@@ -284,6 +254,19 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.cnt_off);
   uint32_t* btotal = reinterpret_cast<uint32_t*>(ws + pl.btotal_off);
   uint32_t* bstart = reinterpret_cast<uint32_t*>(ws + pl.bstart_off);
+  if (align_block_ok(pl)) {
+    const size_t sm = align_block_smem(pl);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(align_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm) != cudaSuccess)
+      return MLR_ERR_CUDA;
+    align_block_kernel<<<1, kAlignBlockThreads, sm, stream>>>(
+        topk_ids, mapping, (int)pl.P, topk, E, L, block_size, sorted_ids, block_expert, block_lora,
+        num_post_pad, bstart, capacity, d_status);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+    return MLR_OK;
+  }
   const size_t sm_count = align_smem_count(pl), sm_scatter = align_smem_scatter(pl);
   if (sm_scatter > 48 * 1024) {
     if (cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

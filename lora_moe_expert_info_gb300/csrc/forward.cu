@@ -63,15 +63,25 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 
 // Tensor maps of one GEMM kind, by slot.
 //   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
-//            kRows = chunk-major x_sorted or h rows (one 64-row box = 8 KB contiguous)
+//            kRows / kRows128 / kRows256 = chunk-major x_sorted or h rows in
+//            64/128/256-row boxes (one box = one contiguous run)
 //   shrinks: kA32/kA16/kA8 = LoRA A in 32/16/8-row boxes
+//            kA3x16/kA3x32/kA3x64 (gate_up shrink) = LoRA A viewed as
+//            [(l,e,gate|up)][rank][k]: one box holds the gate and up rank rows
 //   base:    kB8/kB4/kB2 = LoRA B stack viewed as [rank chunk][row][8 ranks], 8/4/2 chunks per box
 //            kZ8/kZ4/kZ2 = chunk-major z viewed the same way
-// The TMA engine's cost grows with the number of contiguous global segments it
-// fetches, so every box is chosen to read long contiguous runs.
-enum MapSlot { kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7 };
+//            kW3 (gate_up) = W_gate_up viewed as [(e,gate|up)][row][k]: one
+//            box holds a 128-row block of gate and of up
+// Each TMA box costs the SM's copy engine a roughly fixed time whatever its
+// size (measured on GB300 from L2: 8 KB and 32 KB boxes take about the same
+// time), so every operand of a K step is fetched with as few boxes as possible.
+enum MapSlot {
+  kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
+  kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
+  kRows128 = 8, kRows256 = 9, kW3 = 10, kNumMaps = 11
+};
 struct Maps {
-  CUtensorMap m[8];
+  CUtensorMap m[kNumMaps];
 };
 
 // Base tile: head {e, row0, nrows, nb} followed by nb buckets {j0, nj, l, r16}.
@@ -86,6 +96,9 @@ struct Params {
   int zrows;  // rows per z box (min(256, cap))
   int bmask;  // base GEMMs: bit 0 / 1 set if the 8- / 4-chunk LoRA B and z views exist
   int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
+  int a3_mask;    // gate_up shrink: bit j set if the gate+up LoRA A map with (16 << j)-row boxes exists
+  int rmask;      // bit 0 / 1 set if the 128- / 256-row maps of the row operand exist
+  int w3;         // gate_up: 1 if the gate+up weight map exists
   int64_t P;
   const float* topk_weights;
   const int32_t* lora_ranks;
@@ -128,6 +141,8 @@ __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + _
 struct Item {
   int e, l, row0, nrows, nb, mb;
   int r, r8, r16;
+  int po;   // shrinks: packed M row of the first up rank (gate ranks start at row 0)
+  int a3;   // gate_up shrink: rows per gate/up half of the one-box LoRA A load, or 0
   const TileRec* rec;
 };
 
@@ -142,11 +157,18 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
     it.r = p.lora_ranks[it.l];
     it.r8 = (it.r + 7) & ~7;
     it.r16 = (it.r + 15) & ~15;
+    it.po = it.r16;
+    it.a3 = 0;
+    if (KIND == kShrinkGU && it.r16 <= 64) {
+      const int j = it.r16 <= 16 ? 0 : (it.r16 <= 32 ? 1 : 2);
+      if ((p.a3_mask >> j) & 1) it.a3 = it.po = 16 << j;
+    }
   } else {
     it.rec = p.base_tiles + tile;
     const int4 h = it.rec->head;
     it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w;
     it.r = it.r8 = it.r16 = 0;
+    it.po = it.a3 = 0;
   }
   return it;
 }
@@ -228,8 +250,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         const bool main_step = s < nk;
-        // row tiles of x_sorted / h are loaded as 64-row boxes
-        const int rbox = (int)ceil_div(it.nrows, 64);
+        // the row tile of x_sorted / h: one 64/128/256-row box where the map
+        // exists, else 64-row boxes
+        const int hb = it.nrows <= 64 ? 64 : (it.nrows <= 128 && (p.rmask & 1)) ? 128
+                                         : (it.nrows <= 256 && (p.rmask & 2)) ? 256 : 0;
+        const int rbox = hb ? 1 : (int)ceil_div(it.nrows, 64);
+        const int rbytes = hb ? hb * 128 : rbox * 8192;
+        const CUtensorMap* rmap = &maps.m[hb == 128 ? kRows128 : hb == 256 ? kRows256 : kRows];
         if (lane == 0) {
           if (main_step) {
             const int kb = s;
@@ -240,6 +267,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               const int r8 = it.r8, r16 = it.r16;
               const int mlo = 128 * it.mb, mhi = mlo + 128;  // this item's M block
               int arows = 0;
+              if (it.a3) {
+                // gate and up rank rows in one box: up rows start at packed row a3
+                arows = it.mb == 0 ? 2 * it.a3 : 0;
+              } else
               for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
                 for (int q = 0; q < r8;) {
                   const int pr = g * r16 + q;
@@ -251,7 +282,12 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                   if (pr >= mlo && pr < mhi) arows += bh;
                   q += bh;
                 }
-              mbar_arrive_expect_tx(&c.full[st], arows * 128 + rbox * 8192);
+              mbar_arrive_expect_tx(&c.full[st], arows * 128 + rbytes);
+              if (it.a3) {
+                if (it.mb == 0)
+                  tma_load_3d(sbuf, &maps.m[it.a3 == 16 ? kA3x16 : it.a3 == 32 ? kA3x32 : kA3x64], &c.full[st],
+                              kb * 64, 0, (it.l * p.E + it.e) * 2);
+              } else
               for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
                 for (int q = 0; q < r8;) {
                   const int pr = g * r16 + q;
@@ -270,19 +306,23 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 }
               // B operand: rows of x_sorted (gate_up shrink) or h (down shrink)
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else if (KIND == kGateUp) {
-              mbar_arrive_expect_tx(&c.full[st], 32768 + rbox * 8192);
+              mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
               const int i0 = it.mb * 128;
-              tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
-              tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+              if (p.w3) {
+                tma_load_3d(sbuf, &maps.m[kW3], &c.full[st], kb * 64, i0, it.e * 2);
+              } else {
+                tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
+                tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+              }
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 32768 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+                tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else {  // kDown
-              mbar_arrive_expect_tx(&c.full[st], 16384 + rbox * 8192);
+              mbar_arrive_expect_tx(&c.full[st], 16384 + rbytes);
               tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, &maps.m[kRows], &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
@@ -442,8 +482,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const float sc = p.scalings[it.l];
         const int mg = 128 * it.mb + m;
         int g = 0, q = mg;
-        if (KIND == kShrinkGU && mg >= r16) { g = 1; q = mg - r16; }
-        const bool valid = KIND == kShrinkGU ? (mg < 2 * r16) : (mg < r16);
+        if (KIND == kShrinkGU && mg >= it.po) { g = 1; q = mg - it.po; }
+        // rows q in [r16, po) of the gate half hold no rank of this adapter
+        const bool valid = q < r16 && (KIND == kShrinkGU ? mg < 2 * it.po : true);
         for (int c0 = 0; c0 < it.nrows; c0 += 16) {
           float v[16];
           tmem_ld16(tl + c0, v);
@@ -500,28 +541,29 @@ __device__ int block_offsets(int mine, int* total) {
 }
 
 __device__ __forceinline__ void chunk_rows(int n, int k, int nt, int& r0, int& nr) {
-  const int cs = (int)round_up(ceil_div(n, nt), kBlock);
+  const int cs = ((n + nt - 1) / nt + kBlock - 1) / kBlock * kBlock;
   r0 = k * cs;
   nr = min(cs, n - r0);
 }
 
 // One block: base tiles per expert (with the adapter buckets each tile meets)
-// and shrink tiles per LoRA bucket.
-__global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lora_ranks, int E, int C,
-            int R, TileRec* __restrict__ base_tiles, int4* __restrict__ shrink_tiles,
-            int32_t* __restrict__ counts, int32_t* status) {
+// and shrink tiles per LoRA bucket, from the padded bucket starts (global or
+// shared memory).
+__device__ void plan_block(const uint32_t* bstart, const int32_t* __restrict__ lora_ranks, int E,
+                           int C, int R, TileRec* __restrict__ base_tiles,
+                           int4* __restrict__ shrink_tiles, int32_t* __restrict__ counts,
+                           int32_t* status) {
   int bad = 0;
   {
-    const int per = (int)ceil_div(E, kPlanThreads);
+    const int per = (E + kPlanThreads - 1) / kPlanThreads;
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
     int mine = 0;
-    for (int e = e0; e < e1; ++e) mine += (int)ceil_div(bstart[(e + 1) * C] - bstart[e * C], kTileRows);
+    for (int e = e0; e < e1; ++e) mine += ((int)(bstart[(e + 1) * C] - bstart[e * C]) + kTileRows - 1) / kTileRows;
     int total;
     int off = block_offsets(mine, &total);
     for (int e = e0; e < e1; ++e) {
       const int s = (int)bstart[e * C], n = (int)bstart[(e + 1) * C] - s;
-      const int nt = (int)ceil_div(n, kTileRows);
+      const int nt = (n + kTileRows - 1) / kTileRows;
       int q = e * C;  // first bucket that may meet the current tile
       for (int k = 0; k < nt; ++k) {
         int r0, nr;
@@ -547,7 +589,7 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
   }
   {
     const int NB = E * C;
-    const int per = (int)ceil_div(NB, kPlanThreads);
+    const int per = (NB + kPlanThreads - 1) / kPlanThreads;
     const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
     int mine = 0;
     for (int b = b0; b < b1; ++b) {
@@ -556,7 +598,7 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       const int r = lora_ranks[cl - 1];
       if (r < 0 || r > R) { bad = 1; continue; }
       if (r == 0) continue;
-      mine += (int)ceil_div(bstart[b + 1] - bstart[b], kShrinkRows);
+      mine += ((int)(bstart[b + 1] - bstart[b]) + kShrinkRows - 1) / kShrinkRows;
     }
     int total;
     int off = block_offsets(mine, &total);
@@ -566,7 +608,7 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
       const int r = lora_ranks[cl - 1];
       if (r <= 0 || r > R) continue;
       const int s = (int)bstart[b], n = (int)bstart[b + 1] - s;
-      const int nt = (int)ceil_div(n, kShrinkRows);
+      const int nt = (n + kShrinkRows - 1) / kShrinkRows;
       for (int k = 0; k < nt; ++k) {
         int r0, nr;
         chunk_rows(n, k, nt, r0, nr);
@@ -576,6 +618,31 @@ plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lor
     if (threadIdx.x == 0) counts[1] = total;
   }
   if (bad) set_status(status, MLR_STATUS_RANK);
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lora_ranks, int E, int C,
+            int R, TileRec* __restrict__ base_tiles, int4* __restrict__ shrink_tiles,
+            int32_t* __restrict__ counts, int32_t* status) {
+  plan_block(bstart, lora_ranks, E, C, R, base_tiles, shrink_tiles, counts, status);
+}
+
+// Small batches: the single-block align followed by the tile plan, in one
+// launch; the plan reads the bucket starts from shared memory.
+__global__ void __launch_bounds__(kPlanThreads)
+align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping, int P,
+                  int topk, int E, int L, int R, const int32_t* __restrict__ lora_ranks,
+                  int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
+                  int32_t* __restrict__ block_lora, int32_t* __restrict__ num_post_pad,
+                  uint32_t* __restrict__ bstart, int64_t capacity, TileRec* __restrict__ base_tiles,
+                  int4* __restrict__ shrink_tiles, int32_t* __restrict__ counts, int32_t* status) {
+  static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
+  extern __shared__ __align__(16) unsigned char ap_smem[];
+  const int C = L + 1, NB = E * C;
+  const AlignBlockSmem sm = align_block_carve(ap_smem, NB, P);
+  align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, sorted_ids, block_expert, block_lora,
+              num_post_pad, bstart, capacity, status);
+  plan_block(sm.start, lora_ranks, E, C, R, base_tiles, shrink_tiles, counts, status);
 }
 
 // x_sorted row r = x[sorted_ids[r] / K] for r < npad (zeros for pad rows),
@@ -656,9 +723,9 @@ bool make_abox_maps(Maps& m, const void* base, uint64_t cols, uint64_t rows, int
   return (*mask & 8) != 0;
 }
 
-// 3-D bf16 view {d0, d1, d2} with byte strides s1 (dim 1) and s2 (dim 2), no swizzle.
+// 3-D bf16 view {d0, d1, d2} with byte strides s1 (dim 1) and s2 (dim 2).
 bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-               uint32_t b0, uint32_t b1, uint32_t b2) {
+               uint32_t b0, uint32_t b1, uint32_t b2, bool swizzle128 = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {d0, d1, d2};
@@ -666,8 +733,24 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-operand maps with 128- and 256-row boxes over a chunk-major buffer of
+// `rows` 64-column rows; returns the mask of the maps made (a box taller than
+// the buffer is skipped).
+bool make_row_maps(Maps& m, const void* base, uint64_t rows, int* mask) {
+  *mask = 0;
+  if (rows >= 128) {
+    if (!make_map(&m.m[kRows128], base, 64, rows, 64, 128, true)) return false;
+    *mask |= 1;
+  }
+  if (rows >= 256) {
+    if (!make_map(&m.m[kRows256], base, 64, rows, 64, 256, true)) return false;
+    *mask |= 2;
+  }
+  return true;
 }
 
 struct FwdLayout {
@@ -804,11 +887,12 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   uint16_t* zd = reinterpret_cast<uint16_t*>(ws + f.o_zd);
   float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
-  const uint32_t* bstart = reinterpret_cast<const uint32_t*>(aws + f.al.bstart_off);
+  uint32_t* bstart = reinterpret_cast<uint32_t*>(aws + f.al.bstart_off);
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
-  int abox_gu = 0, abox_d = 0, bmask = 0;
+  int abox_gu = 0, abox_d = 0, bmask = 0, a3_gu = 0, w3 = 0;
+  int rm_sgu = 0, rm_gu = 0, rm_sd = 0, rm_dn = 0;
   const uint64_t cap = (uint64_t)f.cap;
   const uint64_t hk = (uint64_t)ceil_div(H, 64), ik = (uint64_t)ceil_div(I, 64);
   const uint32_t zrows = (uint32_t)(f.cap < 256 ? f.cap : 256);
@@ -817,7 +901,27 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
             make_map(&m_sgu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
             make_map(&m_sd.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
             make_map(&m_dn.m[kW], w_down, I, (uint64_t)E * H, 64, 128, true) &&
-            make_map(&m_dn.m[kRows], hbuf, 64, ik * cap, 64, 64, true);
+            make_map(&m_dn.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
+            make_row_maps(m_gu, xs, hk * cap, &rm_gu) && make_row_maps(m_sgu, xs, hk * cap, &rm_sgu) &&
+            make_row_maps(m_sd, hbuf, ik * cap, &rm_sd) && make_row_maps(m_dn, hbuf, ik * cap, &rm_dn);
+  rm_sgu &= 1;  // shrink tiles hold at most 128 rows
+  rm_sd &= 1;
+  if (ok && I >= 128) {
+    // W_gate_up as [(e, gate|up)][row][k]: a box {64, 128, 2} is a 128-row block of gate and of up
+    ok = make_map3(&m_gu.m[kW3], w_gate_up, H, I, (uint64_t)E * 2, (uint64_t)H * 2, (uint64_t)I * H * 2, 64, 128, 2,
+                   true);
+    w3 = 1;
+  }
+  if (ok && L > 0) {
+    // LoRA A_gu as [(l, e, gate|up)][rank][k]: a box {64, rb, 2} holds rb gate and rb up rank rows
+    for (int j = 0; ok && j < 3; ++j) {
+      const int rb = 16 << j;
+      if (rb > R) continue;
+      ok = make_map3(&m_sgu.m[kA3x16 + j], lora_a_gu, H, R, (uint64_t)L * E * 2, (uint64_t)H * 2,
+                     (uint64_t)R * H * 2, 64, rb, 2, true);
+      a3_gu |= 1 << j;
+    }
+  }
   if (ok && L > 0) {
     ok = make_abox_maps(m_sgu, lora_a_gu, H, (uint64_t)L * E * 2 * R, &abox_gu) &&
          make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d);
@@ -840,14 +944,30 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   const int prof = prof_call_begin(stream);
   if (cudaMemsetAsync(yacc, 0, (size_t)T * H * 4, stream) != cudaSuccess) return MLR_ERR_CUDA;
-  int rc = align_launch(f.al, topk_ids, token_lora_mapping, K, E, L, kBlock, sorted, bexp, blora, npad,
-                        f.cap, aws, d_status, stream);
-  if (rc != MLR_OK) return rc;
-  prof_mark(prof, 0, stream);
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(bstart, lora_ranks, E, f.C, R, base_tiles, shrink_tiles,
-                                               counts, d_status);
-  MLR_CHECK_LAUNCH();
-  note_launch();
+  int rc = MLR_OK;
+  if (align_block_ok(f.al)) {
+    // one launch: align and tile plan (the plan is timed with the align)
+    const size_t sm = align_block_smem(f.al);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm) != cudaSuccess)
+      return MLR_ERR_CUDA;
+    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(
+        topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R, lora_ranks, sorted, bexp, blora, npad,
+        bstart, f.cap, base_tiles, shrink_tiles, counts, d_status);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+    prof_mark(prof, 0, stream);
+  } else {
+    rc = align_launch(f.al, topk_ids, token_lora_mapping, K, E, L, kBlock, sorted, bexp, blora, npad,
+                      f.cap, aws, d_status, stream);
+    if (rc != MLR_OK) return rc;
+    prof_mark(prof, 0, stream);
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(bstart, lora_ranks, E, f.C, R, base_tiles, shrink_tiles,
+                                                 counts, d_status);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+  }
   {
     const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
@@ -874,25 +994,25 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   if (L > 0) {
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu; q.a3_mask = a3_gu; q.rmask = rm_sgu;
     if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 2, stream);
   {
     Params q = p;
-    q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128);
+    q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128); q.rmask = rm_gu; q.w3 = w3;
     if ((rc = launch_gemm<kGateUp>(m_gu, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 3, stream);
   if (L > 0) {
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d; q.rmask = rm_sd;
     if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 4, stream);
   {
     Params q = p;
-    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 128);
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 128); q.rmask = rm_dn;
     if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);

@@ -46,6 +46,9 @@ def _random(seed, T, K, E, L, p_none=0.1, distinct=True):
     (4, 50, 4, 3, 1, 1), (5, 20, 8, 16, 6, 8), (7, 40, 2, 2, 0, 5), (8, 25, 6, 3, 7, 64),
     (9, 5000, 8, 64, 8, 16), (10, 4097, 8, 256, 4, 64), (11, 1000, 1, 1, 0, 16),
     (12, 30000, 2, 2, 1, 16), (13, 3, 4, 100, 399, 4096),
+    # the limits of the single-block path: 16384 pairs, 8192 buckets (and one past each)
+    (14, 2048, 8, 64, 7, 16), (15, 2049, 8, 64, 7, 16), (16, 100, 4, 128, 63, 16),
+    (17, 100, 4, 128, 64, 16),
 ])
 def test_random_cases(cuda_device, seed, T, K, E, L, bs):
     topk, mapping = _random(seed, T, K, E, L, distinct=(seed % 2 == 0))
@@ -62,6 +65,13 @@ def test_single_bucket_long_runs(cuda_device):
     T, K = 40000, 2
     topk = np.zeros((T, K), np.int32)
     _compare(cuda_device, topk, np.full(T, 1, np.int32), 1, 2, 16)
+
+
+def test_single_bucket_long_runs_one_block(cuda_device):
+    # 16384 pairs in one bucket: every round of the single-block path is one run
+    T, K = 8192, 2
+    topk = np.zeros((T, K), np.int32)
+    _compare(cuda_device, topk, np.full(T, 0, np.int32), 1, 1, 16)
 
 
 def test_all_minus_one(cuda_device):

@@ -123,6 +123,19 @@ def test_ragged_shapes(cuda_device, seed):
     assert within(y, r) <= 0 and within(y0, r0) <= 0
 
 
+@pytest.mark.parametrize("I", [64, 192])
+def test_padded_rank_boxes(cuda_device, I):
+    # ranks 40 and 48 round to 48 and load as 64-row LoRA A boxes (rows 48-63 are
+    # rank padding); I = 64 also takes the two-box weight load of gate_up
+    c = custom_case(cuda_device, T=150, K=2, E=4, H=128, I=I, L=3, R=64, ranks=[40, 48, 64],
+                    seg_lens=[50, 60, 40], adapters=[0, 1, 2], lora_std="fan_in", seed=3)
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
 def test_single_expert_top1(cuda_device):
     c = custom_case(cuda_device, T=40, K=1, E=1, H=128, I=128, L=2, R=16, ranks=[16, 8],
                     seg_lens=[25, 15], adapters=[1, 0], lora_std="fan_in")
@@ -154,6 +167,14 @@ def test_many_tiles_per_expert(cuda_device):
     r, r0 = c.ref(), c.ref(mapping=none)
     assert np.abs(r - r0).max() > 0.5
     assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
+def test_chunked_align_path(cuda_device):
+    # 33,600 pairs: past the single-block align (16,384 pairs), so the chunked
+    # align and the separate plan launch run
+    c = custom_case(cuda_device, T=4200, K=8, E=16, H=128, I=128, L=4, R=16, ranks=[16, 8, 0, 16],
+                    seg_lens=[1000, 1200, 900, 1100], adapters=[0, 1, 2, -1], lora_std="fan_in")
+    assert within(c.gpu(), c.ref()) <= 0
 
 
 def test_repeated_calls_identical_metadata(cuda_device):
