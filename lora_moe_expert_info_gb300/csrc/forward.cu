@@ -84,7 +84,9 @@ struct Maps {
   CUtensorMap m[kNumMaps];
 };
 
-// Base tile: head {e, row0, nrows, nb} followed by nb buckets {j0, nj, l, r16}.
+// Base tile: head {e, row0, nrows, nb | nexp_gu << 8 | nexp_d << 16} followed by
+// nb buckets {j0, nj, l, r16}; nexp_* = the tile's LoRA expand steps in the
+// gate_up (2 per 64 ranks of a bucket) and down (1 per 64 ranks) GEMMs.
 struct TileRec {
   int4 head;
   int4 bk[kMaxBuckets];
@@ -115,6 +117,7 @@ struct Params {
 };
 
 struct __align__(16) Ctl {
+  TileRec rec_p, rec_m;  // the current base tile of the producer / MMA warp
   uint64_t full[8];   // one per ring stage (at most 8)
   uint64_t empty[8];
   uint64_t acc_full[2];
@@ -139,7 +142,7 @@ __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + _
 
 // One work item: tile rows, weight block, adapter (shrinks: with its rank).
 struct Item {
-  int e, l, row0, nrows, nb, mb;
+  int e, l, row0, nrows, nb, mb, nexp;
   int r, r8, r16;
   int po;   // shrinks: packed M row of the first up rank (gate ranks start at row 0)
   int a3;   // gate_up shrink: rows per gate/up half of the one-box LoRA A load, or 0
@@ -153,7 +156,7 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
   it.mb = item % p.nblk;
   if (KIND == kShrinkGU || KIND == kShrinkD) {
     const int4 t = p.shrink_tiles[tile];
-    it.e = t.x; it.l = t.y; it.row0 = t.z; it.nrows = t.w; it.nb = 0; it.rec = nullptr;
+    it.e = t.x; it.l = t.y; it.row0 = t.z; it.nrows = t.w; it.nb = 0; it.nexp = 0; it.rec = nullptr;
     it.r = p.lora_ranks[it.l];
     it.r8 = (it.r + 7) & ~7;
     it.r16 = (it.r + 15) & ~15;
@@ -166,35 +169,49 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
   } else {
     it.rec = p.base_tiles + tile;
     const int4 h = it.rec->head;
-    it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w;
+    it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w & 0xff;
+    it.nexp = KIND == kGateUp ? (h.w >> 8) & 0xff : (h.w >> 16) & 0xff;
     it.r = it.r8 = it.r16 = 0;
     it.po = it.a3 = 0;
   }
   return it;
 }
 
-// Expand steps of a base item: per bucket, per gate (2 for gate_up), per 64 ranks.
-__device__ __forceinline__ int expand_steps(const Item& it, int ngates) {
-  int n = 0;
-  for (int b = 0; b < it.nb; ++b) n += ngates * ((it.rec->bk[b].w + 63) >> 6);
-  return n;
+// load_item for a whole warp: a base tile record is copied to shared memory
+// with one coalesced load (instead of one dependent load per bucket) and the
+// item reads it from there.  All 32 lanes call this.
+template <int KIND>
+__device__ __forceinline__ Item load_item_warp(const Params& p, int item, TileRec* srec, int lane) {
+  if (KIND == kShrinkGU || KIND == kShrinkD) return load_item<KIND>(p, item);
+  const int4* src = reinterpret_cast<const int4*>(p.base_tiles + item / p.nblk);
+  __syncwarp();  // the previous item's reads of srec are done
+  if (lane <= kMaxBuckets) reinterpret_cast<int4*>(srec)[lane] = src[lane];
+  __syncwarp();
+  Item it;
+  it.mb = item % p.nblk;
+  it.rec = srec;
+  const int4 h = srec->head;
+  it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w & 0xff;
+  it.nexp = KIND == kGateUp ? (h.w >> 8) & 0xff : (h.w >> 16) & 0xff;
+  it.r = it.r8 = it.r16 = 0;
+  it.po = it.a3 = 0;
+  return it;
 }
-// Decodes expand step k of an item into its bucket record, gate and rank group.
-__device__ __forceinline__ void expand_decode(const Item& it, int ngates, int k, int4& bk, int& g, int& kg) {
-  for (int b = 0; b < it.nb; ++b) {
-    bk = it.rec->bk[b];
-    const int per = (bk.w + 63) >> 6;
-    if (k < ngates * per) {
-      g = k / per;
-      kg = k % per;
-      return;
+
+// Walks the expand steps of a base item in order: per bucket, per gate (2 for
+// gate_up), per 64 ranks.  Producer and MMA warp walk the same sequence.
+struct ExpandCursor {
+  int b = 0, g = 0, kg = 0;
+  __device__ __forceinline__ void next(const TileRec* rec, int ngates) {
+    if (++kg == (rec->bk[b].w + 63) >> 6) {
+      kg = 0;
+      if (++g == ngates) {
+        g = 0;
+        ++b;
+      }
     }
-    k -= ngates * per;
   }
-  bk = make_int4(0, 0, 0, 0);
-  g = 0;
-  kg = 0;
-}
+};
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -242,8 +259,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     int gs = 0;  // global step counter of this CTA (ring position)
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const Item it = load_item<KIND>(p, item);
-      const int nsteps = nk + (kShrink ? 0 : expand_steps(it, kGates));
+      const Item it = load_item_warp<KIND>(p, item, &c.rec_p, lane);
+      const int nsteps = nk + it.nexp;
+      ExpandCursor cur;
       for (int s = 0; s < nsteps; ++s, ++gs) {
         const int st = gs % S, round = gs / S;
         uint8_t* sbuf = smem + st * SB;
@@ -326,9 +344,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
-            int4 bk;  // {j0, nj, l, r16}
-            int g, kg;
-            expand_decode(it, kGates, s - nk, bk, g, kg);
+            const int4 bk = it.rec->bk[cur.b];  // {j0, nj, l, r16}
+            const int g = cur.g, kg = cur.kg;
+            cur.next(it.rec, kGates);
             const int nch = min(8, (bk.w - kg * 64) / 8);  // rank chunks of 8 (even)
             mbar_arrive_expect_tx(&c.full[st], nch * (2048 + p.zrows * 16));
             const int m0 = it.mb * 128;
@@ -347,17 +365,18 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       }
     }
   } else if (warp == 4) {
-    // ============================ MMA (one thread) =============================
-    if (lane == 0) {
-      int gs = 0, il = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++il) {
-        const Item it = load_item<KIND>(p, item);
+    // ================== MMA (the warp loads items, one thread issues) ==================
+    int gs = 0, il = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++il) {
+      const Item it = load_item_warp<KIND>(p, item, &c.rec_m, lane);
+      if (lane == 0) {
         const int b = il % CF::kAccBufs;
-        if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort)) break;
+        if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort)) ok = false;
         tc_fence_after();
         const uint32_t acc = tmem + b * CF::kAccCols;
-        const int nsteps = nk + (kShrink ? 0 : expand_steps(it, kGates));
+        const int nsteps = ok ? nk + it.nexp : 0;
+        ExpandCursor cur;
         for (int s = 0; s < nsteps; ++s, ++gs) {
           const int st = gs % S, round = gs / S;
           if (!mbar_wait(&c.full[st], round & 1, abort)) { ok = false; break; }
@@ -380,9 +399,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                          (s > 0 || kk > 0) ? 1u : 0u);
             }
           } else {
-            int4 bk;
-            int g, kg;
-            expand_decode(it, kGates, s - nk, bk, g, kg);
+            const int4 bk = it.rec->bk[cur.b];
+            const int g = cur.g, kg = cur.kg;
+            cur.next(it.rec, kGates);
             const int nch = min(8, (bk.w - kg * 64) / 8);
             const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + bk.x;
             const uint32_t idesc = idesc_bf16_f32(128, bk.y);
@@ -392,9 +411,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           }
           mma_commit(&c.empty[st]);
         }
-        if (!ok) break;
-        mma_commit(&c.acc_full[b]);
+        if (ok) mma_commit(&c.acc_full[b]);
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
   } else if (warp >= kEpiWarp0) {
     // ================================ epilogue =================================
@@ -582,7 +601,13 @@ __device__ void plan_block(const uint32_t* bstart, const int32_t* __restrict__ l
           if (s1 <= s0 || nb >= kMaxBuckets) continue;
           rec.bk[nb++] = make_int4(s0 - t0, s1 - s0, l, (r + 15) & ~15);
         }
-        rec.head = make_int4(e, t0, nr, nb);
+        int nexp_gu = 0, nexp_d = 0;
+        for (int j = 0; j < nb; ++j) {
+          const int per = (rec.bk[j].w + 63) >> 6;
+          nexp_gu += 2 * per;
+          nexp_d += per;
+        }
+        rec.head = make_int4(e, t0, nr, nb | (nexp_gu << 8) | (nexp_d << 16));
       }
     }
     if (threadIdx.x == 0) counts[0] = total;
