@@ -45,7 +45,7 @@ namespace {
 
 constexpr int kBlock = 16;        // internal align block = MMA N granularity
 constexpr int kTileRows = 256;    // max sorted rows per tile (MMA N)
-constexpr int kMaxBuckets = 16;   // adapter buckets meeting one tile (each >= 16 rows)
+constexpr int kInlinePieces = 30;  // LoRA pieces stored inside a base-tile record
 constexpr int kEpiWarp0 = 5;
 constexpr int kThreads = 288;     // 9 warps (warps 1-3 idle)
 constexpr int kGatherThreads = 256;
@@ -69,7 +69,8 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 //            kA3x16/kA3x32/kA3x64 (gate_up shrink) = LoRA A viewed as
 //            [(l,e,gate|up)][rank][k]: one box holds the gate and up rank rows
 //   base:    kB8/kB4/kB2 = LoRA B stack viewed as [rank chunk][row][8 ranks], 8/4/2 chunks per box
-//            kZ8/kZ4/kZ2 = chunk-major z viewed the same way
+//            kZ8/kZ4/kZ2 = chunk-major z viewed the same way, zrows-row boxes;
+//            kZ8s/kZ4s/kZ2s the same with 64-row boxes (pieces of <= 64 rows)
 //            kW3 (gate_up) = W_gate_up viewed as [(e,gate|up)][row][k]: one
 //            box holds a 128-row block of gate and of up
 // Each TMA box costs the SM's copy engine a roughly fixed time whatever its
@@ -78,24 +79,48 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 enum MapSlot {
   kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
   kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
-  kRows128 = 8, kRows256 = 9, kW3 = 10, kNumMaps = 11
+  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kNumMaps = 14
 };
 struct Maps {
   CUtensorMap m[kNumMaps];
 };
 
-// Base tile: head {e, row0, nrows, nb | nexp_gu << 8 | nexp_d << 16} followed by
-// nb buckets {j0, nj, l, r16}; nexp_* = the tile's LoRA expand steps in the
-// gate_up (2 per 64 ranks of a bucket) and down (1 per 64 ranks) GEMMs.
+// Row space.  The GEMMs work on the dense sorted order: the pairs of every
+// (expert, adapter) bucket in align order, buckets back to back with no
+// padding (row u of x_sorted / h = the u-th pair).  A LoRA bucket b with dense
+// rows [us, ue) owns a z region of rows [floor16(us), ceil16(ue)) in z space,
+// starting at z row zstart[b]; its rows outside [us, ue) hold zeros.  An
+// expand MMA therefore covers a 16-aligned column range and adds exactly zero
+// to the columns of rows outside its bucket.
+//
+// Base tile: columns [0, N) = dense rows [row0, row0 + N) (row0 16-aligned, N a
+// multiple of 16 and <= 256); only columns [lo, hi) belong to expert e.  Its
+// LoRA expand work is np pieces {j0 | nj << 16, l, r16, zrow}: the 16-aligned
+// column range [j0, j0 + nj) of one bucket, whose z rows start at zrow.  All
+// pieces are at pieces[poff..]; the first kInlinePieces are also stored in the
+// record so that one warp-wide load brings a whole typical tile.
 struct TileRec {
-  int4 head;
-  int4 bk[kMaxBuckets];
+  int4 head;  // {e, row0, N, poff}
+  int4 info;  // {lo, hi, np, nexp_gu | nexp_d << 16}: expand steps of gate_up (2 per
+              // 64 ranks of a piece) and of down (1 per 64 ranks)
+  int4 pc[kInlinePieces];
+};
+static_assert(sizeof(TileRec) == 32 * 16, "one int4 per lane");
+
+// Shrink tile: columns [0, N) = dense rows [row0, row0 + N) of one bucket's z
+// region (row0 16-aligned, N <= 128), written to z rows zrow0 + column; bucket
+// members are columns [mlo, mhi), the other columns get zeros.
+struct ShrinkRec {
+  int4 a;  // {e, l, row0, N}
+  int4 b;  // {zrow0, mlo, mhi, 0}
 };
 
 struct Params {
   int T, K, E, H, I, L, R, R16, C, nblk;
-  int cap;    // rows of the sorted buffers (x_sorted, h, z) per 64- or 8-column chunk
-  int zrows;  // rows per z box (min(256, cap))
+  int cap;    // rows of x_sorted / h per 64-column chunk (dense rows plus slack)
+  int zcap;   // rows of z_gu / z_d per 8-column chunk
+  int zrows;  // rows per z box (min(256, zcap))
+  int zshort; // 1 if the 64-row z maps exist
   int bmask;  // base GEMMs: bit 0 / 1 set if the 8- / 4-chunk LoRA B and z views exist
   int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
   int a3_mask;    // gate_up shrink: bit j set if the gate+up LoRA A map with (16 << j)-row boxes exists
@@ -105,13 +130,14 @@ struct Params {
   const float* topk_weights;
   const int32_t* lora_ranks;
   const float* scalings;
-  const int32_t* sorted_ids;
+  const int32_t* usorted;  // pair id of each dense row
   const TileRec* base_tiles;
-  const int4* shrink_tiles;  // {e, l, row0, nrows}
+  const int4* pieces;
+  const ShrinkRec* shrink_tiles;
   const int32_t* n_tiles;
-  uint16_t* zgu;  // [cap, 2*R16]
-  uint16_t* h;    // [cap, I]
-  uint16_t* zd;   // [cap, R16]
+  uint16_t* zgu;  // [2*R16/8][zcap][8]
+  uint16_t* h;    // [I/64][cap][64]
+  uint16_t* zd;   // [R16/8][zcap][8]
   float* yacc;    // [T, H]
   int32_t* status;
 };
@@ -142,12 +168,29 @@ __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + _
 
 // One work item: tile rows, weight block, adapter (shrinks: with its rank).
 struct Item {
-  int e, l, row0, nrows, nb, mb, nexp;
+  int e, l, row0, nrows, mb, nexp;
+  int np, lo, hi;          // base: LoRA pieces, columns of expert e
+  int zrow0, mlo, mhi;     // shrinks: z row of column 0, bucket member columns
   int r, r8, r16;
   int po;   // shrinks: packed M row of the first up rank (gate ranks start at row 0)
   int a3;   // gate_up shrink: rows per gate/up half of the one-box LoRA A load, or 0
-  const TileRec* rec;
+  const int4* pc;          // base: first kInlinePieces pieces (shared or global memory)
+  const int4* pg;          // base: all pieces (global memory)
+  __device__ __forceinline__ int4 piece(int k) const { return k < kInlinePieces ? pc[k] : pg[k]; }
 };
+
+template <int KIND>
+__device__ __forceinline__ void item_base(Item& it, const TileRec* rec, const Params& p) {
+  const int4 h = rec->head, f = rec->info;
+  it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z;
+  it.pg = p.pieces + h.w;
+  it.pc = rec->pc;
+  it.lo = f.x; it.hi = f.y; it.np = f.z;
+  it.nexp = KIND == kGateUp ? (f.w & 0xffff) : (f.w >> 16);
+  it.zrow0 = it.mlo = it.mhi = 0;
+  it.r = it.r8 = it.r16 = 0;
+  it.po = it.a3 = 0;
+}
 
 template <int KIND>
 __device__ __forceinline__ Item load_item(const Params& p, int item) {
@@ -155,8 +198,12 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
   const int tile = item / p.nblk;
   it.mb = item % p.nblk;
   if (KIND == kShrinkGU || KIND == kShrinkD) {
-    const int4 t = p.shrink_tiles[tile];
-    it.e = t.x; it.l = t.y; it.row0 = t.z; it.nrows = t.w; it.nb = 0; it.nexp = 0; it.rec = nullptr;
+    const ShrinkRec& t = p.shrink_tiles[tile];
+    const int4 a = t.a, b = t.b;
+    it.e = a.x; it.l = a.y; it.row0 = a.z; it.nrows = a.w;
+    it.zrow0 = b.x; it.mlo = b.y; it.mhi = b.z;
+    it.nexp = it.np = it.lo = it.hi = 0;
+    it.pc = it.pg = nullptr;
     it.r = p.lora_ranks[it.l];
     it.r8 = (it.r + 7) & ~7;
     it.r16 = (it.r + 15) & ~15;
@@ -167,43 +214,37 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
       if ((p.a3_mask >> j) & 1) it.a3 = it.po = 16 << j;
     }
   } else {
-    it.rec = p.base_tiles + tile;
-    const int4 h = it.rec->head;
-    it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w & 0xff;
-    it.nexp = KIND == kGateUp ? (h.w >> 8) & 0xff : (h.w >> 16) & 0xff;
-    it.r = it.r8 = it.r16 = 0;
-    it.po = it.a3 = 0;
+    item_base<KIND>(it, p.base_tiles + tile, p);
   }
   return it;
 }
 
-// load_item for a whole warp: a base tile record is copied to shared memory
-// with one coalesced load (instead of one dependent load per bucket) and the
-// item reads it from there.  All 32 lanes call this.
+// load_item for a whole warp: a base tile record (512 bytes) is copied to
+// shared memory with one coalesced load and the item reads it from there.  All
+// 32 lanes call this.
 template <int KIND>
 __device__ __forceinline__ Item load_item_warp(const Params& p, int item, TileRec* srec, int lane) {
   if (KIND == kShrinkGU || KIND == kShrinkD) return load_item<KIND>(p, item);
   const int4* src = reinterpret_cast<const int4*>(p.base_tiles + item / p.nblk);
   __syncwarp();  // the previous item's reads of srec are done
-  if (lane <= kMaxBuckets) reinterpret_cast<int4*>(srec)[lane] = src[lane];
+  reinterpret_cast<int4*>(srec)[lane] = src[lane];
   __syncwarp();
   Item it;
   it.mb = item % p.nblk;
-  it.rec = srec;
-  const int4 h = srec->head;
-  it.e = h.x; it.l = -1; it.row0 = h.y; it.nrows = h.z; it.nb = h.w & 0xff;
-  it.nexp = KIND == kGateUp ? (h.w >> 8) & 0xff : (h.w >> 16) & 0xff;
-  it.r = it.r8 = it.r16 = 0;
-  it.po = it.a3 = 0;
+  item_base<KIND>(it, srec, p);
   return it;
 }
+
+// Rows of the z box of an expand piece of nj columns: 64 when the short maps
+// exist and suffice, else zrows.
+__device__ __forceinline__ int z_box_rows(const Params& p, int nj) { return (nj <= 64 && p.zshort) ? 64 : p.zrows; }
 
 // Walks the expand steps of a base item in order: per bucket, per gate (2 for
 // gate_up), per 64 ranks.  Producer and MMA warp walk the same sequence.
 struct ExpandCursor {
   int b = 0, g = 0, kg = 0;
-  __device__ __forceinline__ void next(const TileRec* rec, int ngates) {
-    if (++kg == (rec->bk[b].w + 63) >> 6) {
+  __device__ __forceinline__ void next(int r16, int ngates) {  // r16 of piece b
+    if (++kg == (r16 + 63) >> 6) {
       kg = 0;
       if (++g == ngates) {
         g = 0;
@@ -343,21 +384,24 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             }
           } else {
-            // expand step: LoRA B chunk (A operand) + z rows of the bucket (B operand)
-            const int4 bk = it.rec->bk[cur.b];  // {j0, nj, l, r16}
+            // expand step: LoRA B chunk (A operand) + z rows of the piece (B operand)
+            const int4 pc = it.piece(cur.b);  // {j0 | nj << 16, l, r16, zrow}
+            const int pl = pc.y, pr16 = pc.z, zrow = pc.w;
             const int g = cur.g, kg = cur.kg;
-            cur.next(it.rec, kGates);
-            const int nch = min(8, (bk.w - kg * 64) / 8);  // rank chunks of 8 (even)
-            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + p.zrows * 16));
+            cur.next(pr16, kGates);
+            const int nch = min(8, (pr16 - kg * 64) / 8);  // rank chunks of 8 (even)
+            const int zh = z_box_rows(p, pc.x >> 16);
+            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zh * 16));
             const int m0 = it.mb * 128;
-            const int brow = KIND == kGateUp ? ((bk.z * p.E + it.e) * 2 + g) * p.I + m0
-                                             : (bk.z * p.E + it.e) * p.H + m0;
+            const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
+                                             : (pl * p.E + it.e) * p.H + m0;
             const int zc0 = ((KIND == kGateUp ? g * p.R16 : 0) + kg * 64) >> 3;
             for (int ch = 0; ch < nch;) {
               const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
-              const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2), zs = nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2);
+              const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
+              const int zs = zh == 64 ? (nc == 8 ? kZ8s : (nc == 4 ? kZ4s : kZ2s)) : (nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2));
               tma_load_3d(sbuf + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
-              tma_load_3d(sbuf + 16384 + ch * p.zrows * 16, &maps.m[zs], &c.full[st], 0, it.row0 + bk.x, zc0 + ch);
+              tma_load_3d(sbuf + 16384 + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
               ch += nc;
             }
           }
@@ -399,15 +443,16 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                          (s > 0 || kk > 0) ? 1u : 0u);
             }
           } else {
-            const int4 bk = it.rec->bk[cur.b];
+            const int4 pc = it.piece(cur.b);
             const int g = cur.g, kg = cur.kg;
-            cur.next(it.rec, kGates);
-            const int nch = min(8, (bk.w - kg * 64) / 8);
-            const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + bk.x;
-            const uint32_t idesc = idesc_bf16_f32(128, bk.y);
+            cur.next(pc.z, kGates);
+            const int nch = min(8, (pc.z - kg * 64) / 8);
+            const int zh = z_box_rows(p, pc.x >> 16);
+            const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + (pc.x & 0xffff);
+            const uint32_t idesc = idesc_bf16_f32(128, pc.x >> 16);
             for (int k16 = 0; k16 < nch / 2; ++k16)
               mma_bf16(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
-                       sdesc_noswz(sb + 16384 + k16 * 2 * p.zrows * 16, p.zrows * 16, 128), idesc, 1u);
+                       sdesc_noswz(sb + 16384 + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
           }
           mma_commit(&c.empty[st]);
         }
@@ -426,7 +471,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       const int b = il % CF::kAccBufs;
       if (KIND == kDown) {
         for (int n = et; n < kTileRows; n += 128) {
-          const int pr = (n < it.nrows) ? p.sorted_ids[it.row0 + n] : (int)p.P;
+          const int pr = (n >= it.lo && n < it.hi) ? p.usorted[it.row0 + n] : (int)p.P;
           const bool real = pr >= 0 && pr < p.P;
           c.tok[n] = real ? pr / p.K : -1;
           c.w[n] = real ? p.topk_weights[pr] : 0.f;
@@ -466,7 +511,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           for (int q = et; q < ncol * 16; q += 128) {
             const int n = q >> 4, ch = q & 15;
             const int i = i0 + ch * 8;
-            if (i < icap) {  // h is chunk-major: [I/64][cap][64]; the tail past I is zero
+            const int col = c0 + n;
+            // h is chunk-major: [I/64][cap][64]; the tail past I is zero.  Only
+            // this expert's columns are stored (the others belong to other tiles).
+            if (i < icap && col >= it.lo && col < it.hi) {
               const uint4 v = i < p.I ? *reinterpret_cast<const uint4*>(hs + n * kHs + ch * 8) : make_uint4(0, 0, 0, 0);
               *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + c0 + n) * 64 + (i & 63)) = v;
             }
@@ -510,11 +558,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float z = q < r ? sc * v[j] : 0.f;
-              // z is chunk-major: [columns/8][cap][8]
+              // columns outside the bucket (and ranks past r) are written as zeros
+              const int n = c0 + j;
+              const float z = (q < r && n >= it.mlo && n < it.mhi) ? sc * v[j] : 0.f;
+              // z is chunk-major: [columns/8][zcap][8]
               const int col = (KIND == kShrinkGU ? g * p.R16 : 0) + q;
               uint16_t* zb = KIND == kShrinkGU ? p.zgu : p.zd;
-              zb[((int64_t)(col >> 3) * p.cap + it.row0 + c0 + j) * 8 + (col & 7)] = f32_to_bf16_bits(z);
+              zb[((int64_t)(col >> 3) * p.zcap + it.zrow0 + n) * 8 + (col & 7)] = f32_to_bf16_bits(z);
             }
           }
         }
@@ -559,85 +609,121 @@ __device__ int block_offsets(int mine, int* total) {
   return off;
 }
 
-__device__ __forceinline__ void chunk_rows(int n, int k, int nt, int& r0, int& nr) {
-  const int cs = ((n + nt - 1) / nt + kBlock - 1) / kBlock * kBlock;
-  r0 = k * cs;
-  nr = min(cs, n - r0);
+__device__ __forceinline__ int floor16(int v) { return v & ~15; }
+__device__ __forceinline__ int ceil16(int v) { return (v + 15) & ~15; }
+// Rows per base tile of an expert spanning `span` rows (a multiple of 16):
+// ceil(span / 256) tiles of equal size, rounded up to 16 (the count of tiles is
+// then ceil(span / tile_rows), every tile non-empty and at most 256 rows).
+__device__ __forceinline__ int tile_rows(int span) {
+  const int nt = (span + kTileRows - 1) / kTileRows;
+  return ceil16((span + nt - 1) / nt);
 }
 
-// One block: base tiles per expert (with the adapter buckets each tile meets)
-// and shrink tiles per LoRA bucket, from the padded bucket starts (global or
-// shared memory).
-__device__ void plan_block(const uint32_t* bstart, const int32_t* __restrict__ lora_ranks, int E,
-                           int C, int R, TileRec* __restrict__ base_tiles,
-                           int4* __restrict__ shrink_tiles, int32_t* __restrict__ counts,
+// One block of kPlanThreads threads.  us[0..NB] (shared memory) holds the dense
+// bucket starts (exclusive scan of the bucket sizes, us[NB] = P); zs[0..NB] is
+// shared scratch.  Writes the dense starts to ustart_out, the base tiles with
+// their LoRA pieces, the shrink tiles, counts[0] = base tiles and counts[1] =
+// shrink tiles.
+__device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __restrict__ lora_ranks,
+                           int E, int C, int R, uint32_t* __restrict__ ustart_out,
+                           TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
+                           ShrinkRec* __restrict__ shrink_tiles, int32_t* __restrict__ counts,
                            int32_t* status) {
+  const int NB = E * C;
   int bad = 0;
+  // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
+  for (int b = threadIdx.x; b < NB; b += kPlanThreads) {
+    ustart_out[b] = us[b];
+    const int cl = b % C;
+    int zl = 0;
+    if (cl > 0) {
+      const int r = lora_ranks[cl - 1];
+      if (r < 0 || r > R) bad = 1;
+      else if (r > 0 && us[b + 1] > us[b]) zl = ceil16((int)us[b + 1]) - floor16((int)us[b]);
+    }
+    zs[b] = (uint32_t)zl;
+  }
+  if (threadIdx.x == 0) ustart_out[NB] = us[NB];
+  __syncthreads();
+  align_block_scan(zs, NB);  // zs[b]: first z row of bucket b's region
+  auto rank16 = [&](int b) -> int {  // rank rounded to 16 of a LoRA bucket, or 0
+    const int cl = b % C;
+    if (cl == 0) return 0;
+    const int r = lora_ranks[cl - 1];
+    return (r > 0 && r <= R) ? (r + 15) & ~15 : 0;
+  };
+  // ---- base tiles: per expert, equal tiles of <= 256 rows from floor16(first row) ----
   {
     const int per = (E + kPlanThreads - 1) / kPlanThreads;
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
-    int mine = 0;
-    for (int e = e0; e < e1; ++e) mine += ((int)(bstart[(e + 1) * C] - bstart[e * C]) + kTileRows - 1) / kTileRows;
-    int total;
-    int off = block_offsets(mine, &total);
+    int my_t = 0, my_p = 0;
     for (int e = e0; e < e1; ++e) {
-      const int s = (int)bstart[e * C], n = (int)bstart[(e + 1) * C] - s;
-      const int nt = (n + kTileRows - 1) / kTileRows;
-      int q = e * C;  // first bucket that may meet the current tile
-      for (int k = 0; k < nt; ++k) {
-        int r0, nr;
-        chunk_rows(n, k, nt, r0, nr);
-        TileRec& rec = base_tiles[off++];
-        const int t0 = s + r0, t1 = t0 + nr;
-        int nb = 0;
-        while (q < (e + 1) * C && (int)bstart[q + 1] <= t0) ++q;
-        for (int b = q; b < (e + 1) * C && (int)bstart[b] < t1; ++b) {
-          const int l = b - e * C - 1;
-          if (l < 0) continue;
-          const int r = lora_ranks[l];
-          if (r < 0 || r > R) { bad = 1; continue; }
-          if (r == 0) continue;
-          const int s0 = max((int)bstart[b], t0), s1 = min((int)bstart[b + 1], t1);
-          if (s1 <= s0 || nb >= kMaxBuckets) continue;
-          rec.bk[nb++] = make_int4(s0 - t0, s1 - s0, l, (r + 15) & ~15);
-        }
-        int nexp_gu = 0, nexp_d = 0;
-        for (int j = 0; j < nb; ++j) {
-          const int per = (rec.bk[j].w + 63) >> 6;
-          nexp_gu += 2 * per;
-          nexp_d += per;
-        }
-        rec.head = make_int4(e, t0, nr, nb | (nexp_gu << 8) | (nexp_d << 16));
+      const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
+      if (ue1 == ue0) continue;
+      const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
+      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      my_t += nt;
+      for (int b = e * C + 1; b < (e + 1) * C; ++b) {
+        if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+        const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
+        my_p += (z1 - 1 - r0) / ts - (z0 - r0) / ts + 1;  // tiles it meets
       }
     }
-    if (threadIdx.x == 0) counts[0] = total;
+    int total_t, total_p;
+    int toff = block_offsets(my_t, &total_t);
+    int poff = block_offsets(my_p, &total_p);
+    for (int e = e0; e < e1; ++e) {
+      const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
+      if (ue1 == ue0) continue;
+      // nt tiles of equal size (a multiple of 16) over [floor16(first row), ceil16(end))
+      const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
+      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      for (int k = 0; k < nt; ++k) {
+        const int row0 = r0 + k * ts;
+        const int N = min(ts, r0 + span - row0);
+        TileRec& rec = base_tiles[toff++];
+        int np = 0, nexp_gu = 0, nexp_d = 0;
+        for (int b = e * C + 1; b < (e + 1) * C; ++b) {
+          const int r16 = rank16(b);
+          if (r16 == 0 || us[b + 1] == us[b]) continue;
+          const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
+          const int a0 = max(z0, row0), a1 = min(z1, row0 + N);
+          if (a1 <= a0) continue;
+          const int4 pc = make_int4((a0 - row0) | ((a1 - a0) << 16), b % C - 1, r16, (int)zs[b] + (a0 - z0));
+          pieces[poff + np] = pc;
+          if (np < kInlinePieces) rec.pc[np] = pc;
+          ++np;
+          nexp_gu += 2 * ((r16 + 63) >> 6);
+          nexp_d += (r16 + 63) >> 6;
+        }
+        rec.head = make_int4(e, row0, N, poff);
+        rec.info = make_int4(max(ue0, row0) - row0, min(ue1, row0 + N) - row0, np, nexp_gu | (nexp_d << 16));
+        poff += np;
+      }
+    }
+    if (threadIdx.x == 0) counts[0] = total_t;
   }
+  // ---- shrink tiles: each LoRA bucket's z region in pieces of <= 128 rows ----
   {
-    const int NB = E * C;
     const int per = (NB + kPlanThreads - 1) / kPlanThreads;
     const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
     int mine = 0;
     for (int b = b0; b < b1; ++b) {
-      const int cl = b % C;
-      if (cl == 0) continue;
-      const int r = lora_ranks[cl - 1];
-      if (r < 0 || r > R) { bad = 1; continue; }
-      if (r == 0) continue;
-      mine += ((int)(bstart[b + 1] - bstart[b]) + kShrinkRows - 1) / kShrinkRows;
+      if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+      mine += (ceil16((int)us[b + 1]) - floor16((int)us[b]) + kShrinkRows - 1) / kShrinkRows;
     }
     int total;
     int off = block_offsets(mine, &total);
     for (int b = b0; b < b1; ++b) {
-      const int cl = b % C;
-      if (cl == 0) continue;
-      const int r = lora_ranks[cl - 1];
-      if (r <= 0 || r > R) continue;
-      const int s = (int)bstart[b], n = (int)bstart[b + 1] - s;
-      const int nt = (n + kShrinkRows - 1) / kShrinkRows;
-      for (int k = 0; k < nt; ++k) {
-        int r0, nr;
-        chunk_rows(n, k, nt, r0, nr);
-        shrink_tiles[off++] = make_int4(b / C, cl - 1, s + r0, nr);
+      if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+      const int bs = (int)us[b], be = (int)us[b + 1];
+      const int z0 = floor16(bs), z1 = ceil16(be);
+      for (int row0 = z0; row0 < z1; row0 += kShrinkRows) {
+        const int N = min(kShrinkRows, z1 - row0);
+        ShrinkRec t;
+        t.a = make_int4(b / C, b % C - 1, row0, N);
+        t.b = make_int4((int)zs[b] + (row0 - z0), max(bs - row0, 0), min(be - row0, N), 0);
+        shrink_tiles[off++] = t;
       }
     }
     if (threadIdx.x == 0) counts[1] = total;
@@ -645,51 +731,76 @@ __device__ void plan_block(const uint32_t* bstart, const int32_t* __restrict__ l
   if (bad) set_status(status, MLR_STATUS_RANK);
 }
 
+// Chunked-align path: bucket sizes btotal[NB] -> dense starts, then the plan.
+// Dynamic shared memory: 2 * (NB + 1) uint32.
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const uint32_t* __restrict__ bstart, const int32_t* __restrict__ lora_ranks, int E, int C,
-            int R, TileRec* __restrict__ base_tiles, int4* __restrict__ shrink_tiles,
+plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lora_ranks, int E, int C,
+            int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
+            int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
             int32_t* __restrict__ counts, int32_t* status) {
-  plan_block(bstart, lora_ranks, E, C, R, base_tiles, shrink_tiles, counts, status);
+  extern __shared__ __align__(16) unsigned char plan_smem[];
+  const int NB = E * C;
+  uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
+  uint32_t* zs = us + round_up(NB + 1, 4);
+  for (int b = threadIdx.x; b < NB; b += kPlanThreads) us[b] = btotal[b];
+  __syncthreads();
+  align_block_scan(us, NB);
+  plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, counts, status);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
-// launch; the plan reads the bucket starts from shared memory.
+// launch.  After the align, its shared count array holds the dense bucket
+// starts; the z-region scan uses kAlignPlanExtra more bytes of shared memory.
 __global__ void __launch_bounds__(kPlanThreads)
 align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping, int P,
                   int topk, int E, int L, int R, const int32_t* __restrict__ lora_ranks,
                   int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
                   int32_t* __restrict__ block_lora, int32_t* __restrict__ num_post_pad,
-                  uint32_t* __restrict__ bstart, int64_t capacity, TileRec* __restrict__ base_tiles,
-                  int4* __restrict__ shrink_tiles, int32_t* __restrict__ counts, int32_t* status) {
+                  uint32_t* __restrict__ bstart, int64_t capacity, uint32_t* __restrict__ ustart,
+                  TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
+                  ShrinkRec* __restrict__ shrink_tiles, int32_t* __restrict__ counts, int32_t* status,
+                  int zs_offset) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
   const AlignBlockSmem sm = align_block_carve(ap_smem, NB, P);
   align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, sorted_ids, block_expert, block_lora,
               num_post_pad, bstart, capacity, status);
-  plan_block(sm.start, lora_ranks, E, C, R, base_tiles, shrink_tiles, counts, status);
+  plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
+             base_tiles, pieces, shrink_tiles, counts, status);
 }
 
-// x_sorted row r = x[sorted_ids[r] / K] for r < npad (zeros for pad rows),
-// stored chunk-major, [H/64][cap][64], with zeros past H in the last chunk: one
-// warp per row, 16-byte loads and stores.
+// Dense x_sorted: the pair at padded align position q (bucket b, index q -
+// bstart[b]) goes to dense row ustart[b] + q - bstart[b]; its x row is copied
+// there (chunk-major [H/64][cap][64], zeros past H) and its pair id to usorted.
+// Rows [P, cap) are zero.  One warp per row, 16-byte loads and stores.
 __global__ void __launch_bounds__(kGatherThreads)
 gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
-                const int32_t* __restrict__ npad, int64_t P, int K, int H, int64_t cap,
-                uint16_t* __restrict__ xs) {
-  const int64_t n = min((int64_t)*npad, cap);
+                const int32_t* __restrict__ block_expert, const int32_t* __restrict__ block_lora,
+                const uint32_t* __restrict__ bstart, const uint32_t* __restrict__ ustart,
+                const int32_t* __restrict__ npad, int64_t acap, int C, int64_t P, int K, int H,
+                int64_t cap, uint16_t* __restrict__ xs, int32_t* __restrict__ usorted) {
+  const int64_t n = min((int64_t)*npad, acap);
   const int lane = threadIdx.x & 31;
   const int64_t wpb = kGatherThreads / 32;
-  const int pieces = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
-  for (int64_t r = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); r < n; r += (int64_t)gridDim.x * wpb) {
-    const int pr = sorted_ids[r];
-    const bool real = pr >= 0 && pr < P;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(pr / K) * H : 0));
-    for (int q = lane; q < pieces; q += 32) {
-      const uint4 v = (real && q * 8 < H) ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(xs + ((int64_t)(q >> 3) * cap + r) * 64 + (q & 7) * 8) = v;
+  const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
+  const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
+  for (int64_t q = w0; q < n; q += ws) {
+    const int pr = sorted_ids[q];
+    if (pr < 0 || pr >= P) continue;  // pad
+    const int b = block_expert[q / kBlock] * C + block_lora[q / kBlock] + 1;
+    const int64_t u = (int64_t)ustart[b] + (q - (int64_t)bstart[b]);
+    if (u < 0 || u >= P) continue;
+    if (lane == 0) usorted[u] = pr;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(pr / K) * H);
+    for (int c = lane; c < pieces16; c += 32) {
+      const uint4 v = c * 8 < H ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v;
     }
   }
+  for (int64_t u = P + w0; u < cap; u += ws)
+    for (int c = lane; c < pieces16; c += 32)
+      *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void convert_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, int64_t n) {
@@ -778,13 +889,15 @@ bool make_row_maps(Maps& m, const void* base, uint64_t rows, int* mask) {
   return true;
 }
 
+constexpr int kMaxForwardBuckets = 16384;  // E * (L + 1): the plan keeps two scans of it in shared memory
+
 struct FwdLayout {
   bool ok;
   AlignPlan al;
   int R16, C, mtiles_gu, mtiles_d;
-  int64_t cap, max_base, max_shrink;
-  int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_counts, o_zgu, o_h, o_zd,
-      o_yacc, o_xs, total;
+  int64_t cap, zcap, max_base, max_shrink, max_pieces;
+  int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_pieces, o_ustart, o_usorted,
+      o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, total;
 };
 
 FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R) {
@@ -793,29 +906,38 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   if (T < 0 || K < 1 || E < 1 || H < 128 || I < 64 || L < 0 || R < 0) return f;
   if (H % 8 || I % 8 || R > 256 || (L > 0 && (R % 16 != 0 || R < 16))) return f;
   f.al = align_plan(T, K, E, L, kBlock);
-  if (!f.al.ok) return f;
+  if (!f.al.ok || f.al.NB > kMaxForwardBuckets) return f;
   f.R16 = (int)round_up(R, 16);
   if (f.R16 == 0) f.R16 = 16;
   f.C = L + 1;
   f.mtiles_gu = (int)ceil_div(2 * f.R16, 128);
   f.mtiles_d = (int)ceil_div(f.R16, 128);
-  f.cap = f.al.capacity;
-  const int64_t nb_nonempty = f.al.P < f.al.NB ? f.al.P : f.al.NB;
-  f.max_base = f.cap / kTileRows + E + 1;
-  f.max_shrink = f.cap / kShrinkRows + nb_nonempty + 1;
+  const int64_t P = f.al.P;
+  const int64_t nb_nonempty = P < f.al.NB ? P : f.al.NB;
+  // dense rows plus room for a 256-row box from the last 16-aligned tile start
+  f.cap = round_up(P, 16) + kTileRows;
+  // z regions: each non-empty LoRA bucket adds < 32 rows of 16-row alignment
+  f.zcap = round_up(P + 32 * nb_nonempty, 16) + kTileRows;
+  f.max_base = P / kTileRows + 2 * (int64_t)E + 1;
+  f.max_shrink = (P + 32 * nb_nonempty) / kShrinkRows + nb_nonempty + 1;
+  f.max_pieces = nb_nonempty + f.max_base;
+  if (f.cap * round_up(H > I ? H : I, 64) >= ((int64_t)1 << 31) || f.zcap * 2 * f.R16 >= ((int64_t)1 << 31)) return f;
   int64_t o = 0;
   auto take = [&](int64_t bytes) { const int64_t r = o; o += round_up(bytes > 0 ? bytes : 1, 256); return r; };
-  f.o_sorted = take(f.cap * 4);
-  f.o_bexp = take(f.cap / kBlock * 4);
-  f.o_blora = take(f.cap / kBlock * 4);
+  f.o_sorted = take(f.al.capacity * 4);
+  f.o_bexp = take(f.al.capacity / kBlock * 4);
+  f.o_blora = take(f.al.capacity / kBlock * 4);
   f.o_npad = take(16);
   f.o_align = take(f.al.ws_bytes);
   f.o_base = take(f.max_base * (int64_t)sizeof(TileRec));
-  f.o_shrink = take(f.max_shrink * 16);
+  f.o_shrink = take(f.max_shrink * (int64_t)sizeof(ShrinkRec));
+  f.o_pieces = take(f.max_pieces * 16);
+  f.o_ustart = take(((int64_t)f.al.NB + 1) * 4);
+  f.o_usorted = take(f.cap * 4);
   f.o_counts = take(16);
-  f.o_zgu = take(f.cap * 2 * f.R16 * 2);
+  f.o_zgu = take(f.zcap * 2 * f.R16 * 2);
   f.o_h = take(f.cap * round_up(I, 64) * 2);
-  f.o_zd = take(f.cap * f.R16 * 2);
+  f.o_zd = take(f.zcap * f.R16 * 2);
   f.o_yacc = take((int64_t)T * H * 4);
   f.o_xs = take(f.cap * round_up(H, 64) * 2);
   f.total = o;
@@ -905,7 +1027,10 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   int32_t* npad = reinterpret_cast<int32_t*>(ws + f.o_npad);
   char* aws = ws + f.o_align;
   TileRec* base_tiles = reinterpret_cast<TileRec*>(ws + f.o_base);
-  int4* shrink_tiles = reinterpret_cast<int4*>(ws + f.o_shrink);
+  ShrinkRec* shrink_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_shrink);
+  int4* pieces = reinterpret_cast<int4*>(ws + f.o_pieces);
+  uint32_t* ustart = reinterpret_cast<uint32_t*>(ws + f.o_ustart);
+  int32_t* usorted = reinterpret_cast<int32_t*>(ws + f.o_usorted);
   int32_t* counts = reinterpret_cast<int32_t*>(ws + f.o_counts);
   uint16_t* zgu = reinterpret_cast<uint16_t*>(ws + f.o_zgu);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + f.o_h);
@@ -913,14 +1038,15 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
   uint32_t* bstart = reinterpret_cast<uint32_t*>(aws + f.al.bstart_off);
+  const uint32_t* btotal = reinterpret_cast<const uint32_t*>(aws + f.al.btotal_off);
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
   int abox_gu = 0, abox_d = 0, bmask = 0, a3_gu = 0, w3 = 0;
   int rm_sgu = 0, rm_gu = 0, rm_sd = 0, rm_dn = 0;
-  const uint64_t cap = (uint64_t)f.cap;
+  const uint64_t cap = (uint64_t)f.cap, zcap = (uint64_t)f.zcap;
   const uint64_t hk = (uint64_t)ceil_div(H, 64), ik = (uint64_t)ceil_div(I, 64);
-  const uint32_t zrows = (uint32_t)(f.cap < 256 ? f.cap : 256);
+  const uint32_t zrows = (uint32_t)(f.zcap < 256 ? f.zcap : 256);
   bool ok = make_map(&m_gu.m[kW], w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
             make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
             make_map(&m_sgu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
@@ -951,7 +1077,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
     ok = make_abox_maps(m_sgu, lora_a_gu, H, (uint64_t)L * E * 2 * R, &abox_gu) &&
          make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d);
     const int nc[3] = {8, 4, 2};
-    const int bslot[3] = {kB8, kB4, kB2}, zslot[3] = {kZ8, kZ4, kZ2};
+    const int bslot[3] = {kB8, kB4, kB2}, zslot[3] = {kZ8, kZ4, kZ2}, zsslot[3] = {kZ8s, kZ4s, kZ2s};
     for (int j = 0; ok && j < 3; ++j) {
       if (nc[j] > R / 8) continue;  // a box may not span more rank chunks than exist
       if (j < 2) bmask |= 1 << j;
@@ -960,9 +1086,11 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                      8, 128, nc[j]) &&
            make_map3(&m_dn.m[bslot[j]], lora_b_down, 8, (uint64_t)L * E * H, (uint64_t)R / 8, (uint64_t)R * 2, 16,
                      8, 128, nc[j]) &&
-           // chunk-major z: [column/8][cap][8]
-           make_map3(&m_gu.m[zslot[j]], zgu, 8, cap, (uint64_t)2 * f.R16 / 8, 16, cap * 16, 8, zrows, nc[j]) &&
-           make_map3(&m_dn.m[zslot[j]], zd, 8, cap, (uint64_t)f.R16 / 8, 16, cap * 16, 8, zrows, nc[j]);
+           // chunk-major z: [column/8][zcap][8]
+           make_map3(&m_gu.m[zslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
+           make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
+           make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]) &&
+           make_map3(&m_dn.m[zsslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
     }
   }
   if (!ok) return MLR_ERR_CUDA;
@@ -970,33 +1098,40 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   const int prof = prof_call_begin(stream);
   if (cudaMemsetAsync(yacc, 0, (size_t)T * H * 4, stream) != cudaSuccess) return MLR_ERR_CUDA;
   int rc = MLR_OK;
+  const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
   if (align_block_ok(f.al)) {
     // one launch: align and tile plan (the plan is timed with the align)
-    const size_t sm = align_block_smem(f.al);
+    const size_t zs_off = align_block_smem(f.al), sm = zs_off + scan_bytes;
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(
         topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R, lora_ranks, sorted, bexp, blora, npad,
-        bstart, f.cap, base_tiles, shrink_tiles, counts, d_status);
+        bstart, f.al.capacity, ustart, base_tiles, pieces, shrink_tiles, counts, d_status, (int)zs_off);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
   } else {
     rc = align_launch(f.al, topk_ids, token_lora_mapping, K, E, L, kBlock, sorted, bexp, blora, npad,
-                      f.cap, aws, d_status, stream);
+                      f.al.capacity, aws, d_status, stream);
     if (rc != MLR_OK) return rc;
     prof_mark(prof, 0, stream);
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(bstart, lora_ranks, E, f.C, R, base_tiles, shrink_tiles,
-                                                 counts, d_status);
+    const size_t sm = 2 * scan_bytes;
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+      return MLR_ERR_CUDA;
+    plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
+                                                  shrink_tiles, counts, d_status);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
   {
-    const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
+    const int64_t blocks = ceil_div(f.al.capacity > f.cap ? f.al.capacity : f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
-    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, sorted, npad, (int64_t)T * K, K, H, f.cap, xs);
+    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, sorted, bexp, blora, bstart, ustart, npad,
+                                                         f.al.capacity, f.C, (int64_t)T * K, K, H, f.cap,
+                                                         xs, usorted);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -1004,15 +1139,18 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   Params p{};
   p.T = T; p.K = K; p.E = E; p.H = H; p.I = I; p.L = L; p.R = R; p.R16 = f.R16; p.C = f.C;
-  p.cap = f.cap;
+  p.cap = (int)f.cap;
+  p.zcap = (int)f.zcap;
   p.zrows = (int)zrows;
+  p.zshort = zrows >= 64 ? 1 : 0;  // zcap >= 256, so the 64-row maps always exist
   p.bmask = bmask;
   p.P = (int64_t)T * K;
   p.topk_weights = topk_weights;
   p.lora_ranks = lora_ranks;
   p.scalings = scalings;
-  p.sorted_ids = sorted;
+  p.usorted = usorted;
   p.base_tiles = base_tiles;
+  p.pieces = pieces;
   p.shrink_tiles = shrink_tiles;
   p.zgu = zgu; p.h = hbuf; p.zd = zd; p.yacc = yacc;
   p.status = d_status;
