@@ -180,8 +180,9 @@ size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t 
  * padding must be finite (the adapter pool keeps it zero).  Accumulation is
  * fp32; the gate/up activation and the LoRA intermediates are rounded to bf16.
  * Runs the align internally (block 16).  Requirements: H, I multiples of 8,
- * H >= 128, I >= 64, R a multiple of 16 in [16, 256] when L > 0, every base
- * pointer 16-byte aligned.
+ * H >= 128, I >= 64, R a multiple of 16 in [16, 256] when L > 0,
+ * E * (L + 1) <= 16384, every base pointer 16-byte aligned.  Sizes outside
+ * these return MLR_ERR_UNSUPPORTED (and fused_moe_lora_workspace_bytes 0).
  * The top-k combine uses fp32 atomics, so y may differ in the last bits between runs.
  */
 int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,

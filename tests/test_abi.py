@@ -85,6 +85,20 @@ def test_align_host_checks(lib):
         == mlr.MLR_ERR_INVALID
 
 
+def test_forward_host_checks(lib):
+    ws = lib.fused_moe_lora_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(4096, 8, 128, 2048, 768, 8, 64) > 0
+    assert ws(64, 2, 8, 256, 512, 4, 24) == 0          # R not a multiple of 16
+    assert ws(64, 2, 8, 120, 512, 4, 16) == 0          # H below 128
+    assert ws(64, 2, 256, 256, 512, 63, 16) > 0        # E*(L+1) = 16384: the limit
+    assert ws(64, 2, 256, 256, 512, 64, 16) == 0       # E*(L+1) = 16640: above it
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the call returns before any launch
+    f = lib.fused_moe_lora_forward
+    args = [fake] * 12 + [64, 2, 256, 256, 512, 64, 16, fake, fake, ctypes.c_size_t(1 << 30), None, None]
+    assert f(*args) == mlr.MLR_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
     assert b"under-covers" in lib.moe_lora_status_string(mlr.MLR_ERR_UNDERCOVERED)
     assert lib.moe_lora_status_string(0) == b"ok"
