@@ -63,8 +63,8 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 
 // Tensor maps of one GEMM kind, by slot.
 //   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
-//            kRows / kRows128 / kRows256 = chunk-major x_sorted or h rows in
-//            64/128/256-row boxes (one box = one contiguous run)
+//            kRows / kRows128 / kRows192 / kRows256 = chunk-major x_sorted or h
+//            rows in 64/128/192/256-row boxes (one box = one contiguous run)
 //   shrinks: kA32/kA16/kA8 = LoRA A in 32/16/8-row boxes
 //            kA3x16/kA3x32/kA3x64 (gate_up shrink) = LoRA A viewed as
 //            [(l,e,gate|up)][rank][k]: one box holds the gate and up rank rows
@@ -79,7 +79,7 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 enum MapSlot {
   kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
   kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
-  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kNumMaps = 14
+  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14, kNumMaps = 15
 };
 struct Maps {
   CUtensorMap m[kNumMaps];
@@ -124,7 +124,7 @@ struct Params {
   int bmask;  // base GEMMs: bit 0 / 1 set if the 8- / 4-chunk LoRA B and z views exist
   int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
   int a3_mask;    // gate_up shrink: bit j set if the gate+up LoRA A map with (16 << j)-row boxes exists
-  int rmask;      // bit 0 / 1 set if the 128- / 256-row maps of the row operand exist
+  int rmask;      // bit 0 / 1 / 2 set if the 128- / 256- / 192-row maps of the row operand exist
   int w3;         // gate_up: 1 if the gate+up weight map exists
   int64_t P;
   const float* topk_weights;
@@ -309,13 +309,15 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         const bool main_step = s < nk;
-        // the row tile of x_sorted / h: one 64/128/256-row box where the map
-        // exists, else 64-row boxes
+        // the row tile of x_sorted / h: one 64/128/192/256-row box where the
+        // map exists, else 64-row boxes
         const int hb = it.nrows <= 64 ? 64 : (it.nrows <= 128 && (p.rmask & 1)) ? 128
+                                         : (it.nrows <= 192 && (p.rmask & 4)) ? 192
                                          : (it.nrows <= 256 && (p.rmask & 2)) ? 256 : 0;
         const int rbox = hb ? 1 : (int)ceil_div(it.nrows, 64);
         const int rbytes = hb ? hb * 128 : rbox * 8192;
-        const CUtensorMap* rmap = &maps.m[hb == 128 ? kRows128 : hb == 256 ? kRows256 : kRows];
+        const CUtensorMap* rmap =
+            &maps.m[hb == 128 ? kRows128 : hb == 192 ? kRows192 : hb == 256 ? kRows256 : kRows];
         if (lane == 0) {
           if (main_step) {
             const int kb = s;
@@ -873,18 +875,17 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-operand maps with 128- and 256-row boxes over a chunk-major buffer of
-// `rows` 64-column rows; returns the mask of the maps made (a box taller than
-// the buffer is skipped).
+// Row-operand maps with 128-, 256- and 192-row boxes over a chunk-major buffer
+// of `rows` 64-column rows; returns the mask of the maps made (a box taller
+// than the buffer is skipped).
 bool make_row_maps(Maps& m, const void* base, uint64_t rows, int* mask) {
   *mask = 0;
-  if (rows >= 128) {
-    if (!make_map(&m.m[kRows128], base, 64, rows, 64, 128, true)) return false;
-    *mask |= 1;
-  }
-  if (rows >= 256) {
-    if (!make_map(&m.m[kRows256], base, 64, rows, 64, 256, true)) return false;
-    *mask |= 2;
+  const int slot[3] = {kRows128, kRows256, kRows192};
+  const uint32_t height[3] = {128, 256, 192};
+  for (int j = 0; j < 3; ++j) {
+    if (rows < height[j]) continue;
+    if (!make_map(&m.m[slot[j]], base, 64, rows, 64, height[j], true)) return false;
+    *mask |= 1 << j;
   }
   return true;
 }
