@@ -51,6 +51,8 @@ constexpr int kThreads = 288;     // 9 warps (warps 1-3 idle)
 constexpr int kGatherThreads = 256;
 constexpr int kPlanThreads = 1024;
 constexpr int kShrinkRows = 128;  // max sorted rows per shrink tile
+constexpr int kGemvRows = 4;      // buckets with at most this many pairs take the CUDA-core shrink
+constexpr int kGemvThreads = 256;
 constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging: 32 rows of bf16 h, or 16 rows of fp32
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
@@ -624,13 +626,13 @@ __device__ __forceinline__ int tile_rows(int span) {
 // One block of kPlanThreads threads.  us[0..NB] (shared memory) holds the dense
 // bucket starts (exclusive scan of the bucket sizes, us[NB] = P); zs[0..NB] is
 // shared scratch.  Writes the dense starts to ustart_out, the base tiles with
-// their LoRA pieces, the shrink tiles, counts[0] = base tiles and counts[1] =
-// shrink tiles.
+// their LoRA pieces, the shrink tiles (tensor-core and CUDA-core), counts[0] =
+// base tiles, counts[1] = tensor-core shrink tiles, counts[2] = CUDA-core ones.
 __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __restrict__ lora_ranks,
                            int E, int C, int R, uint32_t* __restrict__ ustart_out,
                            TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
-                           ShrinkRec* __restrict__ shrink_tiles, int32_t* __restrict__ counts,
-                           int32_t* status) {
+                           ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
+                           int32_t* __restrict__ counts, int32_t* status) {
   const int NB = E * C;
   int bad = 0;
   // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
@@ -705,30 +707,38 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
     }
     if (threadIdx.x == 0) counts[0] = total_t;
   }
-  // ---- shrink tiles: each LoRA bucket's z region in pieces of <= 128 rows ----
+  // ---- shrink tiles: each LoRA bucket's z region in pieces of <= 128 rows;
+  //      buckets of <= kGemvRows pairs go whole to the CUDA-core shrink ----
   {
     const int per = (NB + kPlanThreads - 1) / kPlanThreads;
     const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
-    int mine = 0;
+    int mine = 0, mine_g = 0;
     for (int b = b0; b < b1; ++b) {
       if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
-      mine += (ceil16((int)us[b + 1]) - floor16((int)us[b]) + kShrinkRows - 1) / kShrinkRows;
+      if ((int)(us[b + 1] - us[b]) <= kGemvRows) ++mine_g;
+      else mine += (ceil16((int)us[b + 1]) - floor16((int)us[b]) + kShrinkRows - 1) / kShrinkRows;
     }
-    int total;
+    int total, total_g;
     int off = block_offsets(mine, &total);
+    int off_g = block_offsets(mine_g, &total_g);
     for (int b = b0; b < b1; ++b) {
       if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
       const int bs = (int)us[b], be = (int)us[b + 1];
       const int z0 = floor16(bs), z1 = ceil16(be);
+      const bool small = be - bs <= kGemvRows;  // region of <= 32 rows: one tile
       for (int row0 = z0; row0 < z1; row0 += kShrinkRows) {
         const int N = min(kShrinkRows, z1 - row0);
         ShrinkRec t;
         t.a = make_int4(b / C, b % C - 1, row0, N);
         t.b = make_int4((int)zs[b] + (row0 - z0), max(bs - row0, 0), min(be - row0, N), 0);
-        shrink_tiles[off++] = t;
+        if (small) gemv_tiles[off_g++] = t;
+        else shrink_tiles[off++] = t;
       }
     }
-    if (threadIdx.x == 0) counts[1] = total;
+    if (threadIdx.x == 0) {
+      counts[1] = total;
+      counts[2] = total_g;
+    }
   }
   if (bad) set_status(status, MLR_STATUS_RANK);
 }
@@ -739,7 +749,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lora_ranks, int E, int C,
             int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
-            int32_t* __restrict__ counts, int32_t* status) {
+            ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status) {
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -747,7 +757,8 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
   for (int b = threadIdx.x; b < NB; b += kPlanThreads) us[b] = btotal[b];
   __syncthreads();
   align_block_scan(us, NB);
-  plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, counts, status);
+  plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts,
+             status);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
@@ -760,8 +771,8 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
                   int32_t* __restrict__ block_lora, int32_t* __restrict__ num_post_pad,
                   uint32_t* __restrict__ bstart, int64_t capacity, uint32_t* __restrict__ ustart,
                   TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
-                  ShrinkRec* __restrict__ shrink_tiles, int32_t* __restrict__ counts, int32_t* status,
-                  int zs_offset) {
+                  ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
+                  int32_t* __restrict__ counts, int32_t* status, int zs_offset) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
@@ -769,7 +780,7 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
   align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, sorted_ids, block_expert, block_lora,
               num_post_pad, bstart, capacity, status);
   plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
-             base_tiles, pieces, shrink_tiles, counts, status);
+             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status);
 }
 
 // Dense x_sorted: the pair at padded align position q (bucket b, index q -
@@ -803,6 +814,122 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sort
   for (int64_t u = P + w0; u < cap; u += ws)
     for (int c = lane; c < pieces16; c += 32)
       *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = make_uint4(0, 0, 0, 0);
+}
+
+// The shrink of a small bucket (<= kGemvRows pairs) on CUDA cores: z = s_l A x
+// for its member rows, an HBM-bound matrix-vector product.  Each warp streams
+// whole rank rows of A with 16-byte loads and dots them with the member rows,
+// staged in shared memory; every other entry of the bucket's z region (the
+// non-member rows, the ranks past r) is written as zero.  NG = 2: the gate_up
+// shrink (A_gu [L, E, 2, R, K], rows of x_sorted); NG = 1: the down shrink
+// (A_d [L, E, R, K], rows of h).  K is a multiple of 8; rows are chunk-major
+// [ceil(K/64)][cap][64] with zeros past K.  Dynamic shared memory:
+// kGemvRows * round_up(K, 64) bf16.
+// acc[i] += A row . member row i (i < M) over k in [0, Kd), lane-strided in
+// 16-byte pieces with kBatch loads in flight; A is unpacked once per piece.
+template <int M>
+__device__ __forceinline__ void gemv_dot(const uint16_t* __restrict__ arow, const uint16_t* xr, int Kp, int Kd,
+                                         int lane, float (&acc)[kGemvRows]) {
+  constexpr int kBatch = 8;  // a 4 KB rank row per warp
+  for (int k0 = lane * 8; k0 < Kd; k0 += 32 * 8 * kBatch) {
+    uint4 av[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int k = k0 + j * 256;
+      av[j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow + k)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int k = k0 + j * 256;
+      if (k < Kd) {
+        const uint32_t aw[4] = {av[j].x, av[j].y, av[j].z, av[j].w};
+        float af[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          af[2 * w] = __uint_as_float(aw[w] << 16);
+          af[2 * w + 1] = __uint_as_float(aw[w] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xr + i * Kp + k);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            acc[i] = fmaf(af[2 * w], __uint_as_float(xw[w] << 16), acc[i]);
+            acc[i] = fmaf(af[2 * w + 1], __uint_as_float(xw[w] & 0xffff0000u), acc[i]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kGemvThreads)
+shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restrict__ n_tiles,
+                   const uint16_t* __restrict__ a, const uint16_t* __restrict__ rows, int Kd, int64_t cap,
+                   int E, int R, int R16, const int32_t* __restrict__ lora_ranks,
+                   const float* __restrict__ scalings, uint16_t* __restrict__ z, int64_t zcap) {
+  constexpr int kUnitRows = 2 * kGemvThreads / 32;  // rank rows per work unit (2 per warp)
+  extern __shared__ __align__(16) uint16_t xr[];  // [kGemvRows][Kp]
+  const int units = (NG * R + kUnitRows - 1) / kUnitRows;  // work units per bucket (upper bound)
+  const int nu = *n_tiles * units;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Kp = (Kd + 63) & ~63, kp8 = Kp / 8;
+  for (int unit = blockIdx.x; unit < nu; unit += gridDim.x) {
+    const int tile = unit / units, grp = unit - tile * units;
+    const int r = lora_ranks[tiles[tile].a.y];
+    if (grp * kUnitRows >= NG * r && grp > 0) continue;  // no rank rows left for this unit
+    const ShrinkRec t = tiles[tile];
+    const int e = t.a.x, l = t.a.y, row0 = t.a.z, N = t.a.w;
+    const int zrow0 = t.b.x, mlo = t.b.y, mhi = t.b.z;
+    const int m = mhi - mlo;
+    const int r16 = (r + 15) & ~15;
+    const float sc = scalings[l];
+    __syncthreads();  // the previous unit's reads of xr are done
+    for (int idx = threadIdx.x; idx < m * kp8; idx += kGemvThreads) {
+      const int i = idx / kp8, c = idx - i * kp8;  // 16-byte piece c of member row i
+      const int64_t u = (int64_t)row0 + mlo + i;
+      *reinterpret_cast<uint4*>(xr + i * Kp + c * 8) =
+          *reinterpret_cast<const uint4*>(rows + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8);
+    }
+    __syncthreads();
+    const int task_end = min(NG * r, (grp + 1) * kUnitRows);
+    for (int task = grp * kUnitRows + warp; task < task_end; task += kGemvThreads / 32) {
+      const int g = task / r, q = task - g * r;
+      const uint16_t* arow = a + ((((int64_t)l * E + e) * NG + g) * R + q) * (int64_t)Kd;
+      float acc[kGemvRows];
+#pragma unroll
+      for (int i = 0; i < kGemvRows; ++i) acc[i] = 0.f;
+      static_assert(kGemvRows == 4, "one case per member count");
+      switch (m) {  // uniform per CTA
+        case 1: gemv_dot<1>(arow, xr, Kp, Kd, lane, acc); break;
+        case 2: gemv_dot<2>(arow, xr, Kp, Kd, lane, acc); break;
+        case 3: gemv_dot<3>(arow, xr, Kp, Kd, lane, acc); break;
+        default: gemv_dot<4>(arow, xr, Kp, Kd, lane, acc); break;
+      }
+#pragma unroll
+      for (int i = 0; i < kGemvRows; ++i)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+      if (lane < m) {
+        float v = acc[0];
+#pragma unroll
+        for (int i = 1; i < kGemvRows; ++i)
+          if (lane == i) v = acc[i];
+        const int col = g * R16 + q;
+        z[((int64_t)(col >> 3) * zcap + zrow0 + mlo + lane) * 8 + (col & 7)] = f32_to_bf16_bits(sc * v);
+      }
+    }
+    // the rest of the region (first unit): non-member columns for every rank,
+    // member columns past r
+    for (int idx = threadIdx.x; grp == 0 && idx < NG * r16 * N; idx += kGemvThreads) {
+      const int n = idx % N, rest = idx / N, q = rest % r16, g = rest / r16;
+      if (n >= mlo && n < mhi && q < r) continue;
+      const int col = g * R16 + q;
+      z[((int64_t)(col >> 3) * zcap + zrow0 + n) * 8 + (col & 7)] = 0;
+    }
+  }
 }
 
 __global__ void convert_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, int64_t n) {
@@ -896,8 +1023,8 @@ struct FwdLayout {
   bool ok;
   AlignPlan al;
   int R16, C, mtiles_gu, mtiles_d;
-  int64_t cap, zcap, max_base, max_shrink, max_pieces;
-  int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_pieces, o_ustart, o_usorted,
+  int64_t cap, zcap, max_base, max_shrink, max_pieces, max_gemv;
+  int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted,
       o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, total;
 };
 
@@ -922,6 +1049,7 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.max_base = P / kTileRows + 2 * (int64_t)E + 1;
   f.max_shrink = (P + 32 * nb_nonempty) / kShrinkRows + nb_nonempty + 1;
   f.max_pieces = nb_nonempty + f.max_base;
+  f.max_gemv = nb_nonempty;
   if (f.cap * round_up(H > I ? H : I, 64) >= ((int64_t)1 << 31) || f.zcap * 2 * f.R16 >= ((int64_t)1 << 31)) return f;
   int64_t o = 0;
   auto take = [&](int64_t bytes) { const int64_t r = o; o += round_up(bytes > 0 ? bytes : 1, 256); return r; };
@@ -932,6 +1060,7 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.o_align = take(f.al.ws_bytes);
   f.o_base = take(f.max_base * (int64_t)sizeof(TileRec));
   f.o_shrink = take(f.max_shrink * (int64_t)sizeof(ShrinkRec));
+  f.o_gemv = take(f.max_gemv * (int64_t)sizeof(ShrinkRec));
   f.o_pieces = take(f.max_pieces * 16);
   f.o_ustart = take(((int64_t)f.al.NB + 1) * 4);
   f.o_usorted = take(f.cap * 4);
@@ -974,6 +1103,31 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
   const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
   moe_gemm_kernel<KIND><<<grid, kThreads, smem, stream>>>(maps, p);
+  MLR_CHECK_LAUNCH();
+  note_launch();
+  return MLR_OK;
+}
+
+// CUDA-core shrink of the small buckets: each CTA takes listed buckets in a
+// grid-stride loop up to the device-side count.
+template <int NG>
+int launch_gemv(const ShrinkRec* tiles, const int32_t* n_tiles, int64_t max_tiles, const void* a, const uint16_t* rows,
+                int Kd, const FwdLayout& f, int E, int R, const int32_t* lora_ranks, const float* scalings,
+                uint16_t* z, cudaStream_t stream) {
+  if (max_tiles <= 0) return MLR_OK;
+  const int smem = kGemvRows * (int)round_up(Kd, 64) * 2;
+  static int configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    if (cudaFuncSetAttribute(shrink_gemv_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return MLR_ERR_CUDA;
+    configured = smem;
+  }
+  const int64_t units = max_tiles * ((NG * R + 2 * kGemvThreads / 32 - 1) / (2 * kGemvThreads / 32));
+  const int64_t grid = units < 6 * (int64_t)sm_count() ? units : 6 * (int64_t)sm_count();
+  shrink_gemv_kernel<NG><<<(unsigned)grid, kGemvThreads, smem, stream>>>(
+      tiles, n_tiles, static_cast<const uint16_t*>(a), rows, Kd, f.cap, E, R, f.R16, lora_ranks, scalings, z,
+      f.zcap);
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;
@@ -1029,6 +1183,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   char* aws = ws + f.o_align;
   TileRec* base_tiles = reinterpret_cast<TileRec*>(ws + f.o_base);
   ShrinkRec* shrink_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_shrink);
+  ShrinkRec* gemv_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_gemv);
   int4* pieces = reinterpret_cast<int4*>(ws + f.o_pieces);
   uint32_t* ustart = reinterpret_cast<uint32_t*>(ws + f.o_ustart);
   int32_t* usorted = reinterpret_cast<int32_t*>(ws + f.o_usorted);
@@ -1109,7 +1264,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
       return MLR_ERR_CUDA;
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(
         topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R, lora_ranks, sorted, bexp, blora, npad,
-        bstart, f.al.capacity, ustart, base_tiles, pieces, shrink_tiles, counts, d_status, (int)zs_off);
+        bstart, f.al.capacity, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts, d_status,
+        (int)zs_off);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
@@ -1123,7 +1279,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
-                                                  shrink_tiles, counts, d_status);
+                                                  shrink_tiles, gemv_tiles, counts, d_status);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -1157,6 +1313,9 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   p.status = d_status;
 
   if (L > 0) {
+    if ((rc = launch_gemv<2>(gemv_tiles, counts + 2, f.max_gemv, lora_a_gu, xs, H, f, E, R, lora_ranks, scalings,
+                             zgu, stream)) != MLR_OK)
+      return rc;
     Params q = p;
     q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu; q.a3_mask = a3_gu; q.rmask = rm_sgu;
     if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, stream)) != MLR_OK) return rc;
@@ -1169,6 +1328,9 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   }
   prof_mark(prof, 3, stream);
   if (L > 0) {
+    if ((rc = launch_gemv<1>(gemv_tiles, counts + 2, f.max_gemv, lora_a_down, hbuf, I, f, E, R, lora_ranks,
+                             scalings, zd, stream)) != MLR_OK)
+      return rc;
     Params q = p;
     q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d; q.rmask = rm_sd;
     if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, stream)) != MLR_OK) return rc;

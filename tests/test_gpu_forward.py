@@ -136,6 +136,33 @@ def test_padded_rank_boxes(cuda_device, I):
     assert within(y, r) <= 0 and within(y0, r0) <= 0
 
 
+def test_small_bucket_sizes(cuda_device):
+    # (expert, adapter) buckets of exactly 1, 2, 3, 4 and 5 pairs: 1-4 take the
+    # CUDA-core shrink, 5 the tensor-core one; ranks 16 and 48 (48 uses a padded box)
+    T, K, E, L, R, H, I = 15, 1, 4, 2, 48, 128, 128
+    cfg = workloads.custom_config(hidden=H, intermediate=I, num_experts=E, topk=K, num_loras=L,
+                                  max_rank=R, num_tokens=T)
+    experts = [0] + [1] * 2 + [2] * 3 + [3] * 4 + [0] * 5
+    adapters = [0] + [0] * 2 + [1] * 3 + [1] * 4 + [1] * 5
+    ids = torch.tensor(experts, dtype=torch.int32, device=cuda_device).view(T, 1)
+    wts = torch.ones(T, 1, dtype=torch.float32, device=cuda_device)
+    lens = torch.ones(T, dtype=torch.int32)
+    ip = torch.arange(T + 1, dtype=torch.int32)
+    ranks = torch.tensor([16, 48], dtype=torch.int32)
+    b = workloads.Batch(lens.to(cuda_device), ip.to(cuda_device),
+                        torch.tensor(adapters, dtype=torch.int32, device=cuda_device), ranks.to(cuda_device),
+                        torch.tensor([0.5, 0.5], dtype=torch.float32, device=cuda_device), ids, wts)
+    w = workloads.make_weights(cfg, ranks, device=cuda_device, seed=5, lora_std="fan_in")
+    x = torch.randn(T, H, generator=torch.Generator(device=cuda_device).manual_seed(9), device=cuda_device,
+                    dtype=torch.bfloat16)
+    c = Case(cfg, b, w, x, cuda_device)
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
 def test_single_expert_top1(cuda_device):
     c = custom_case(cuda_device, T=40, K=1, E=1, H=128, I=128, L=2, R=16, ranks=[16, 8],
                     seg_lens=[25, 15], adapters=[1, 0], lora_std="fan_in")
