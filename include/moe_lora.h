@@ -206,9 +206,10 @@ int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const flo
  *   recorded events complete, writes the summed milliseconds of each stage over
  *   the recorded calls into stage_ms[0..min(max_stages, *n_stages)), the number of
  *   recorded calls into *n_calls (host pointers), and stops recording.
- * moe_lora_profile_stage_name(i): "align", "plan_gather" (tile plan and the copy of x into
- *   sorted row order), "shrink_gate_up", "gate_up",
- *   "shrink_down", "down", "convert" (static storage; NULL past the last stage).
+ * moe_lora_profile_stage_name(i): "align_plan" (the (expert, adapter) align in
+ *   dense order and the tile plan), "gather" (x copied into sorted row order; zeroes the fp32
+ *   accumulator), "shrink_gate_up", "gate_up", "shrink_down", "down", "convert"
+ *   (static storage; NULL past the last stage).
  * moe_lora_launch_count(): kernels this library has launched in this process.
  */
 int moe_lora_profile_begin(int32_t max_calls);

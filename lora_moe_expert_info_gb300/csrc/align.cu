@@ -127,7 +127,9 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
                      const uint32_t* __restrict__ cnt, const uint32_t* __restrict__ btotal,
                      const uint32_t* __restrict__ bstart, int32_t* __restrict__ sorted_ids,
                      int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
-                     int64_t capacity) {
+                     int64_t capacity, const uint32_t* __restrict__ dense_start) {
+  // dense_start != nullptr: the dense order (no padding, no labels) for the
+  // forward; sorted_ids then receives pair ids at dense_start[b] + rank.
   extern __shared__ uint32_t smem[];
   const int C = L + 1, NB = E * C;
   uint32_t* off = smem;                                             // [NB + 1]
@@ -176,10 +178,11 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
       }
       const int round_start = m + 1;
       for (m = pos + 1; m < hi && (stage[m] >> 10) == (uint32_t)it; ++m) less += stage[m] < j;
-      const int64_t dst = (int64_t)bstart[k] + crow[k] + (round_start - lo) + less;
+      const int64_t dst = (int64_t)(dense_start ? dense_start[k] : bstart[k]) + crow[k] + (round_start - lo) + less;
       if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + j);
     }
   }
+  if (dense_start) return;
 
   // Pad sentinels and per-block labels: one warp per bucket over the whole
   // grid, lanes writing consecutive entries.  Padded positions are below
@@ -295,10 +298,51 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
   if (pl.G > 0) {
     align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(
         topk_ids, mapping, pl.P, topk, E, L, pl.chunk, block_size, cnt, btotal, bstart, sorted_ids,
-        block_expert, block_lora, capacity);
+        block_expert, block_lora, capacity, nullptr);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
+  return MLR_OK;
+}
+
+int align_dense_count(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk, int E,
+                      int L, void* workspace, int32_t* d_status, cudaStream_t stream) {
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + pl.cnt_off);
+  uint32_t* btotal = reinterpret_cast<uint32_t*>(ws + pl.btotal_off);
+  const size_t sm_count = align_smem_count(pl);
+  if (sm_count > 48 * 1024 &&
+      cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_count) !=
+          cudaSuccess)
+    return MLR_ERR_CUDA;
+  if (pl.G > 0) {
+    align_count_kernel<<<pl.G, kThreads, sm_count, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk, cnt,
+                                                             d_status);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+  }
+  align_colscan_kernel<<<(int)ceil_div(pl.NB, kColThreads), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
+  MLR_CHECK_LAUNCH();
+  note_launch();
+  return MLR_OK;
+}
+
+int align_dense_scatter(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk, int E,
+                        int L, const void* workspace, const uint32_t* dense_start, int32_t* dense_sorted,
+                        cudaStream_t stream) {
+  if (pl.G == 0) return MLR_OK;
+  const char* ws = static_cast<const char*>(workspace);
+  const uint32_t* cnt = reinterpret_cast<const uint32_t*>(ws + pl.cnt_off);
+  const size_t sm_scatter = align_smem_scatter(pl);
+  if (sm_scatter > 48 * 1024 &&
+      cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter) !=
+          cudaSuccess)
+    return MLR_ERR_CUDA;
+  align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk, 1,
+                                                               cnt, nullptr, nullptr, dense_sorted, nullptr, nullptr,
+                                                               pl.P, dense_start);
+  MLR_CHECK_LAUNCH();
+  note_launch();
   return MLR_OK;
 }
 

@@ -632,7 +632,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
                            int E, int C, int R, uint32_t* __restrict__ ustart_out,
                            TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                            ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                           int32_t* __restrict__ counts, int32_t* status) {
+                           int32_t* __restrict__ counts, int32_t* status, int gemv_rows) {
   const int NB = E * C;
   int bad = 0;
   // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
@@ -708,14 +708,15 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
     if (threadIdx.x == 0) counts[0] = total_t;
   }
   // ---- shrink tiles: each LoRA bucket's z region in pieces of <= 128 rows;
-  //      buckets of <= kGemvRows pairs go whole to the CUDA-core shrink ----
+  //      buckets of <= gemv_rows (0 or kGemvRows) pairs go whole to the
+  //      CUDA-core shrink ----
   {
     const int per = (NB + kPlanThreads - 1) / kPlanThreads;
     const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
     int mine = 0, mine_g = 0;
     for (int b = b0; b < b1; ++b) {
       if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
-      if ((int)(us[b + 1] - us[b]) <= kGemvRows) ++mine_g;
+      if ((int)(us[b + 1] - us[b]) <= gemv_rows) ++mine_g;
       else mine += (ceil16((int)us[b + 1]) - floor16((int)us[b]) + kShrinkRows - 1) / kShrinkRows;
     }
     int total, total_g;
@@ -725,7 +726,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
       const int bs = (int)us[b], be = (int)us[b + 1];
       const int z0 = floor16(bs), z1 = ceil16(be);
-      const bool small = be - bs <= kGemvRows;  // region of <= 32 rows: one tile
+      const bool small = be - bs <= gemv_rows;  // region of <= 32 rows: one tile
       for (int row0 = z0; row0 < z1; row0 += kShrinkRows) {
         const int N = min(kShrinkRows, z1 - row0);
         ShrinkRec t;
@@ -749,7 +750,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lora_ranks, int E, int C,
             int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
-            ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status) {
+            ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status,
+            int gemv_rows) {
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -758,73 +760,54 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
   __syncthreads();
   align_block_scan(us, NB);
   plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts,
-             status);
+             status, gemv_rows);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
-// launch.  After the align, its shared count array holds the dense bucket
-// starts; the z-region scan uses kAlignPlanExtra more bytes of shared memory.
+// launch.  The align writes the dense order to usorted and leaves the dense
+// bucket starts in its shared count array; the z-region scan uses
+// (NB + 1) * 4 more bytes of shared memory at zs_offset.
 __global__ void __launch_bounds__(kPlanThreads)
 align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping, int P,
                   int topk, int E, int L, int R, const int32_t* __restrict__ lora_ranks,
-                  int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
-                  int32_t* __restrict__ block_lora, int32_t* __restrict__ num_post_pad,
-                  uint32_t* __restrict__ bstart, int64_t capacity, uint32_t* __restrict__ ustart,
+                  int32_t* __restrict__ usorted, uint32_t* __restrict__ ustart,
                   TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                   ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                  int32_t* __restrict__ counts, int32_t* status, int zs_offset) {
+                  int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
   const AlignBlockSmem sm = align_block_carve(ap_smem, NB, P);
-  align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, sorted_ids, block_expert, block_lora,
-              num_post_pad, bstart, capacity, status);
+  align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, nullptr, nullptr, nullptr, nullptr, nullptr, P,
+              status, usorted);
   plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
-             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status);
+             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows);
 }
 
-// Dense x_sorted: the pair at padded align position q (bucket b, index q -
-// bstart[b]) goes to dense row ustart[b] + q - bstart[b]; its x row is copied
-// there (chunk-major [H/64][cap][64], zeros past H) and its pair id to usorted.
-// Rows [P, cap) are zero.  One warp per row, 16-byte loads and stores.
+// Dense x_sorted: row u < n = ustart[NB] (the valid pairs) is x[usorted[u] / K]
+// (chunk-major [H/64][cap][64], zeros past H); rows [n, cap) are zero.  One
+// warp per row, 16-byte loads and stores.  The same launch zeroes y_acc.
 __global__ void __launch_bounds__(kGatherThreads)
-gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_ids,
-                const int32_t* __restrict__ block_expert, const int32_t* __restrict__ block_lora,
-                const uint32_t* __restrict__ bstart, const uint32_t* __restrict__ ustart,
-                const int32_t* __restrict__ npad, int64_t acap, int C, int64_t P, int K, int H,
-                int64_t cap, uint16_t* __restrict__ xs, int32_t* __restrict__ usorted) {
-  const int64_t n = min((int64_t)*npad, acap);
+gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usorted,
+                const uint32_t* __restrict__ n_valid, int K, int H, int64_t cap, uint16_t* __restrict__ xs,
+                float* __restrict__ yacc, int64_t yacc_n4) {
+  const int64_t n = *n_valid;
   const int lane = threadIdx.x & 31;
   const int64_t wpb = kGatherThreads / 32;
   const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
   const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
-  for (int64_t q = w0; q < n; q += ws) {
-    const int pr = sorted_ids[q];
-    if (pr < 0 || pr >= P) continue;  // pad
-    const int b = block_expert[q / kBlock] * C + block_lora[q / kBlock] + 1;
-    const int64_t u = (int64_t)ustart[b] + (q - (int64_t)bstart[b]);
-    if (u < 0 || u >= P) continue;
-    if (lane == 0) usorted[u] = pr;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(pr / K) * H);
+  for (int64_t u = w0; u < cap; u += ws) {
+    const bool real = u < n;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(usorted[u] / K) * H : 0));
     for (int c = lane; c < pieces16; c += 32) {
-      const uint4 v = c * 8 < H ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      const uint4 v = (real && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v;
     }
   }
-  for (int64_t u = P + w0; u < cap; u += ws)
-    for (int c = lane; c < pieces16; c += 32)
-      *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = make_uint4(0, 0, 0, 0);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < yacc_n4; i += (int64_t)gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// The shrink of a small bucket (<= kGemvRows pairs) on CUDA cores: z = s_l A x
-// for its member rows, an HBM-bound matrix-vector product.  Each warp streams
-// whole rank rows of A with 16-byte loads and dots them with the member rows,
-// staged in shared memory; every other entry of the bucket's z region (the
-// non-member rows, the ranks past r) is written as zero.  NG = 2: the gate_up
-// shrink (A_gu [L, E, 2, R, K], rows of x_sorted); NG = 1: the down shrink
-// (A_d [L, E, R, K], rows of h).  K is a multiple of 8; rows are chunk-major
-// [ceil(K/64)][cap][64] with zeros past K.  Dynamic shared memory:
-// kGemvRows * round_up(K, 64) bf16.
 // acc[i] += A row . member row i (i < M) over k in [0, Kd), lane-strided in
 // 16-byte pieces with kBatch loads in flight; A is unpacked once per piece.
 template <int M>
@@ -1024,7 +1007,7 @@ struct FwdLayout {
   AlignPlan al;
   int R16, C, mtiles_gu, mtiles_d;
   int64_t cap, zcap, max_base, max_shrink, max_pieces, max_gemv;
-  int64_t o_sorted, o_bexp, o_blora, o_npad, o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted,
+  int64_t o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted,
       o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, total;
 };
 
@@ -1053,10 +1036,6 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   if (f.cap * round_up(H > I ? H : I, 64) >= ((int64_t)1 << 31) || f.zcap * 2 * f.R16 >= ((int64_t)1 << 31)) return f;
   int64_t o = 0;
   auto take = [&](int64_t bytes) { const int64_t r = o; o += round_up(bytes > 0 ? bytes : 1, 256); return r; };
-  f.o_sorted = take(f.al.capacity * 4);
-  f.o_bexp = take(f.al.capacity / kBlock * 4);
-  f.o_blora = take(f.al.capacity / kBlock * 4);
-  f.o_npad = take(16);
   f.o_align = take(f.al.ws_bytes);
   f.o_base = take(f.max_base * (int64_t)sizeof(TileRec));
   f.o_shrink = take(f.max_shrink * (int64_t)sizeof(ShrinkRec));
@@ -1176,10 +1155,6 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLR_ERR_INVALID;
 
   char* ws = static_cast<char*>(workspace);
-  int32_t* sorted = reinterpret_cast<int32_t*>(ws + f.o_sorted);
-  int32_t* bexp = reinterpret_cast<int32_t*>(ws + f.o_bexp);
-  int32_t* blora = reinterpret_cast<int32_t*>(ws + f.o_blora);
-  int32_t* npad = reinterpret_cast<int32_t*>(ws + f.o_npad);
   char* aws = ws + f.o_align;
   TileRec* base_tiles = reinterpret_cast<TileRec*>(ws + f.o_base);
   ShrinkRec* shrink_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_shrink);
@@ -1193,7 +1168,6 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   uint16_t* zd = reinterpret_cast<uint16_t*>(ws + f.o_zd);
   float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
-  uint32_t* bstart = reinterpret_cast<uint32_t*>(aws + f.al.bstart_off);
   const uint32_t* btotal = reinterpret_cast<const uint32_t*>(aws + f.al.btotal_off);
 
   // tensor maps
@@ -1252,43 +1226,48 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   if (!ok) return MLR_ERR_CUDA;
 
   const int prof = prof_call_begin(stream);
-  if (cudaMemsetAsync(yacc, 0, (size_t)T * H * 4, stream) != cudaSuccess) return MLR_ERR_CUDA;
   int rc = MLR_OK;
+  // the CUDA-core shrink pays off when buckets average a few pairs (decode)
+  const int64_t nb_nonempty = f.al.P < f.al.NB ? f.al.P : f.al.NB;
+  const int gemv_rows = (L > 0 && f.al.P < 8 * nb_nonempty) ? kGemvRows : 0;
   const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
   if (align_block_ok(f.al)) {
-    // one launch: align and tile plan (the plan is timed with the align)
+    // one launch: the dense align and the tile plan (timed as the align stage)
     const size_t zs_off = align_block_smem(f.al), sm = zs_off + scan_bytes;
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(
-        topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R, lora_ranks, sorted, bexp, blora, npad,
-        bstart, f.al.capacity, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts, d_status,
-        (int)zs_off);
+    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
+                                                       lora_ranks, usorted, ustart, base_tiles, pieces,
+                                                       shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
+                                                       gemv_rows);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
   } else {
-    rc = align_launch(f.al, topk_ids, token_lora_mapping, K, E, L, kBlock, sorted, bexp, blora, npad,
-                      f.al.capacity, aws, d_status, stream);
-    if (rc != MLR_OK) return rc;
-    prof_mark(prof, 0, stream);
+    // chunked: per-chunk counts, the plan (which scans the bucket sizes into
+    // the dense starts), then the dense scatter
+    if ((rc = align_dense_count(f.al, topk_ids, token_lora_mapping, K, E, L, aws, d_status, stream)) != MLR_OK)
+      return rc;
     const size_t sm = 2 * scan_bytes;
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
-                                                  shrink_tiles, gemv_tiles, counts, d_status);
+                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows);
     MLR_CHECK_LAUNCH();
     note_launch();
+    if ((rc = align_dense_scatter(f.al, topk_ids, token_lora_mapping, K, E, L, aws, ustart, usorted, stream)) !=
+        MLR_OK)
+      return rc;
+    prof_mark(prof, 0, stream);
   }
   {
-    const int64_t blocks = ceil_div(f.al.capacity > f.cap ? f.al.capacity : f.cap, kGatherThreads / 32);
+    const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
-    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, sorted, bexp, blora, bstart, ustart, npad,
-                                                         f.al.capacity, f.C, (int64_t)T * K, K, H, f.cap,
-                                                         xs, usorted);
+    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, yacc,
+                                                         (int64_t)T * H / 4);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -1313,7 +1292,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   p.status = d_status;
 
   if (L > 0) {
-    if ((rc = launch_gemv<2>(gemv_tiles, counts + 2, f.max_gemv, lora_a_gu, xs, H, f, E, R, lora_ranks, scalings,
+    if (gemv_rows > 0 &&
+        (rc = launch_gemv<2>(gemv_tiles, counts + 2, f.max_gemv, lora_a_gu, xs, H, f, E, R, lora_ranks, scalings,
                              zgu, stream)) != MLR_OK)
       return rc;
     Params q = p;
@@ -1328,7 +1308,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   }
   prof_mark(prof, 3, stream);
   if (L > 0) {
-    if ((rc = launch_gemv<1>(gemv_tiles, counts + 2, f.max_gemv, lora_a_down, hbuf, I, f, E, R, lora_ranks,
+    if (gemv_rows > 0 &&
+        (rc = launch_gemv<1>(gemv_tiles, counts + 2, f.max_gemv, lora_a_down, hbuf, I, f, E, R, lora_ranks,
                              scalings, zd, stream)) != MLR_OK)
       return rc;
     Params q = p;

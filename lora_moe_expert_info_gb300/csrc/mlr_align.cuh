@@ -30,6 +30,17 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
                  int32_t* block_lora, int32_t* num_post_pad, int64_t capacity, void* workspace,
                  int32_t* d_status, cudaStream_t stream);
 
+// The dense order for the forward on the chunked path, in two parts around the
+// caller's scan of the bucket sizes: align_dense_count leaves the per-chunk
+// counts (column-scanned) and btotal[NB] (bucket sizes) in the workspace;
+// align_dense_scatter then writes each valid pair id to
+// dense_sorted[dense_start[b] + its stable rank in bucket b].
+int align_dense_count(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk, int E,
+                      int L, void* workspace, int32_t* d_status, cudaStream_t stream);
+int align_dense_scatter(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk, int E,
+                        int L, const void* workspace, const uint32_t* dense_start, int32_t* dense_sorted,
+                        cudaStream_t stream);
+
 
 // ---------------------------------------------------------------------------
 // Single-block align.  Up to 16384 pairs (16 per thread of a 1024-thread
@@ -105,9 +116,11 @@ static __device__ void align_block_scan(uint32_t* s, int n) {
 
 // The whole align in one block of kAlignBlockThreads threads (align_block_ok
 // holds).  smem points at align_block_smem bytes of dynamic shared memory.
-// On return (after a barrier) start holds the padded bucket starts
-// (start[NB] = total), also copied to bstart_out if given, and the outputs are
-// written as by the chunked path.
+// On return (after a barrier) cnt holds the exclusive scan of the bucket sizes
+// (cnt[NB] = valid pairs).  With dense_out == nullptr, start holds the padded
+// bucket starts (start[NB] = total), also copied to bstart_out if given, and the
+// outputs are written as by the chunked path.  With dense_out, only the dense
+// order is written: dense_out[u] = the u-th pair in bucket order.
 struct AlignBlockSmem {
   uint32_t* cnt;    // [NB+1] per-bucket counts, then first slot of each bucket
   uint32_t* start;  // [NB+1] padded bucket starts
@@ -129,7 +142,8 @@ static __device__ void align_block(const int32_t* __restrict__ topk_ids,
                                    int32_t* __restrict__ sorted_ids,
                                    int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
                                    int32_t* __restrict__ num_post_pad, uint32_t* __restrict__ bstart_out,
-                                   int64_t capacity, int32_t* d_status) {
+                                   int64_t capacity, int32_t* d_status,
+                                   int32_t* __restrict__ dense_out = nullptr) {
   uint32_t* cnt = sm.cnt;
   uint32_t* start = sm.start;
   uint16_t* stage = sm.stage;
@@ -179,7 +193,7 @@ static __device__ void align_block(const int32_t* __restrict__ topk_ids,
   __syncthreads();
   align_block_scan(cnt, NB);    // cnt[b]: first slot of bucket b in stage / order
   align_block_scan(start, NB);  // start[b]: first block of bucket b
-  if (tid == 0) {
+  if (tid == 0 && dense_out == nullptr) {
     const int64_t total = (int64_t)start[NB] * block_size;
     *num_post_pad = (int32_t)total;
     if (total > capacity) set_status(d_status, MLR_STATUS_CAPACITY);
@@ -210,6 +224,12 @@ static __device__ void align_block(const int32_t* __restrict__ topk_ids,
     }
   }
   __syncthreads();
+  if (dense_out != nullptr) {
+    // the dense order (no padding, no labels): order itself, written out
+    for (int u = tid; u < (int)cnt[NB]; u += kAlignBlockThreads) dense_out[u] = order[u];
+    __syncthreads();
+    return;
+  }
   // Output.  Labels, and an owner table block -> bucket in stage (no longer
   // needed; a bucket has at least as many pairs as blocks, so P entries hold
   // every block), are written bucket-parallel; sorted ids and pad sentinels

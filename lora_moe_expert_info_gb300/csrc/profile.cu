@@ -14,7 +14,7 @@ bool g_on = false;
 int g_max_calls = 0, g_calls = 0;
 std::vector<cudaEvent_t> g_events;  // [max_calls][kProfStages + 1]
 
-const char* kStageNames[kProfStages] = {"align", "plan_gather", "shrink_gate_up", "gate_up",
+const char* kStageNames[kProfStages] = {"align_plan", "gather", "shrink_gate_up", "gate_up",
                                         "shrink_down", "down", "convert"};
 
 }  // namespace
