@@ -796,12 +796,22 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usor
   const int64_t wpb = kGatherThreads / 32;
   const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
   const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
+  constexpr int kBatch = 8;  // 16-byte loads in flight per lane (4 KB per warp)
   for (int64_t u = w0; u < cap; u += ws) {
     const bool real = u < n;
     const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(usorted[u] / K) * H : 0));
-    for (int c = lane; c < pieces16; c += 32) {
-      const uint4 v = (real && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v;
+    for (int c0 = lane; c0 < pieces16; c0 += 32 * kBatch) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = c0 + 32 * j;
+        v[j] = (real && c < pieces16 && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = c0 + 32 * j;
+        if (c < pieces16) *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
+      }
     }
   }
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < yacc_n4; i += (int64_t)gridDim.x * blockDim.x)
