@@ -58,9 +58,11 @@ constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging: 32 rows of bf16 h, or
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 
 template <int KIND> struct Cfg;
-template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
+// The shrinks stage two 64-wide K chunks per ring slot (LoRA A in [0, 32 KB),
+// the x / h rows in [32 KB, 64 KB)): twice the bytes per TMA box.
+template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512; };
-template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
+template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
 
 // Tensor maps of one GEMM kind, by slot.
@@ -68,6 +70,10 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 //            kRows / kRows128 / kRows192 / kRows256 = chunk-major x_sorted or h
 //            rows in 64/128/192/256-row boxes (one box = one contiguous run)
 //   shrinks: kA32/kA16/kA8 = LoRA A in 32/16/8-row boxes
+//            kX2x64 / kX2x128 = x_sorted or h as [chunk][row][64]: one box holds
+//            64 or 128 rows of two consecutive 64-wide K chunks
+//            kAW16/32/64 ("wide") = LoRA A rows of two K chunks in one box, rb =
+//            16/32/64 rank rows (gate_up: [chunk][gate|up][rank][64])
 //            kA3x16/kA3x32/kA3x64 (gate_up shrink) = LoRA A viewed as
 //            [(l,e,gate|up)][rank][k]: one box holds the gate and up rank rows
 //   base:    kB8/kB4/kB2 = LoRA B stack viewed as [rank chunk][row][8 ranks], 8/4/2 chunks per box
@@ -81,6 +87,7 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageByte
 enum MapSlot {
   kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
   kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
+  kX2x64 = 9, kX2x128 = 10, kAW16 = 11, kAW32 = 12, kAW64 = 13,  // shrinks: two-chunk boxes
   kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14, kNumMaps = 15
 };
 struct Maps {
@@ -126,6 +133,7 @@ struct Params {
   int bmask;  // base GEMMs: bit 0 / 1 set if the 8- / 4-chunk LoRA B and z views exist
   int abox_mask;  // shrinks: bit j set if the LoRA A map with (64 >> j)-row boxes exists
   int a3_mask;    // gate_up shrink: bit j set if the gate+up LoRA A map with (16 << j)-row boxes exists
+  int aw_mask;    // shrinks: bit j set if the wide LoRA A map with (16 << j)-row boxes exists
   int rmask;      // bit 0 / 1 / 2 set if the 128- / 256- / 192-row maps of the row operand exist
   int w3;         // gate_up: 1 if the gate+up weight map exists
   int64_t P;
@@ -176,6 +184,7 @@ struct Item {
   int r, r8, r16;
   int po;   // shrinks: packed M row of the first up rank (gate ranks start at row 0)
   int a3;   // gate_up shrink: rows per gate/up half of the one-box LoRA A load, or 0
+  int aw;   // shrinks: rank rows per gate/up half of the wide (two-chunk) A box, or 0
   const int4* pc;          // base: first kInlinePieces pieces (shared or global memory)
   const int4* pg;          // base: all pieces (global memory)
   __device__ __forceinline__ int4 piece(int k) const { return k < kInlinePieces ? pc[k] : pg[k]; }
@@ -191,7 +200,7 @@ __device__ __forceinline__ void item_base(Item& it, const TileRec* rec, const Pa
   it.nexp = KIND == kGateUp ? (f.w & 0xffff) : (f.w >> 16);
   it.zrow0 = it.mlo = it.mhi = 0;
   it.r = it.r8 = it.r16 = 0;
-  it.po = it.a3 = 0;
+  it.po = it.a3 = it.aw = 0;
 }
 
 template <int KIND>
@@ -210,10 +219,11 @@ __device__ __forceinline__ Item load_item(const Params& p, int item) {
     it.r8 = (it.r + 7) & ~7;
     it.r16 = (it.r + 15) & ~15;
     it.po = it.r16;
-    it.a3 = 0;
-    if (KIND == kShrinkGU && it.r16 <= 64) {
+    it.a3 = it.aw = 0;
+    if (it.r16 <= 64) {
       const int j = it.r16 <= 16 ? 0 : (it.r16 <= 32 ? 1 : 2);
-      if ((p.a3_mask >> j) & 1) it.a3 = it.po = 16 << j;
+      if (KIND == kShrinkGU && ((p.a3_mask >> j) & 1)) it.a3 = it.po = 16 << j;
+      if ((p.aw_mask >> j) & 1) it.aw = it.po = 16 << j;  // also for the down shrink (po unused there)
     }
   } else {
     item_base<KIND>(it, p.base_tiles + tile, p);
@@ -240,6 +250,14 @@ __device__ __forceinline__ Item load_item_warp(const Params& p, int item, TileRe
 // Rows of the z box of an expand piece of nj columns: 64 when the short maps
 // exist and suffice, else zrows.
 __device__ __forceinline__ int z_box_rows(const Params& p, int nj) { return (nj <= 64 && p.zshort) ? 64 : p.zrows; }
+
+// Bytes between the LoRA A tiles of a shrink stage's two K chunks: the packed
+// gate+up (or down) rank rows of the wide / a3 boxes, else a full 128-row M block.
+template <int KIND>
+__device__ __forceinline__ int shrink_a_stride(const Item& it) {
+  const int rb = it.aw ? it.aw : it.a3;
+  return rb ? (KIND == kShrinkGU ? 2 : 1) * rb * 128 : 16384;
+}
 
 // Walks the expand steps of a base item in order: per bucket, per gate (2 for
 // gate_up), per 64 ranks.  Producer and MMA warp walk the same sequence.
@@ -273,7 +291,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   uint8_t* epi = smem + S * SB;
   Ctl& c = *reinterpret_cast<Ctl*>(epi + kEpiBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, 64);
+  const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, 64);  // 64-wide K chunks
+  const int nks = kShrink ? (nk + 1) / 2 : nk;  // main steps (a shrink step covers two chunks)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -303,14 +322,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const Item it = load_item_warp<KIND>(p, item, &c.rec_p, lane);
-      const int nsteps = nk + it.nexp;
+      const int nsteps = nks + it.nexp;
       ExpandCursor cur;
       for (int s = 0; s < nsteps; ++s, ++gs) {
         const int st = gs % S, round = gs / S;
         uint8_t* sbuf = smem + st * SB;
         const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-        const bool main_step = s < nk;
+        const bool main_step = s < nks;
         // the row tile of x_sorted / h: one 64/128/192/256-row box where the
         // map exists, else 64-row boxes
         const int hb = it.nrows <= 64 ? 64 : (it.nrows <= 128 && (p.rmask & 1)) ? 128
@@ -324,52 +343,68 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (main_step) {
             const int kb = s;
             if (kShrink) {
-              // LoRA A rows packed into M: gate rows [0, r8) at packed row 0, up
-              // rows at packed row r16; each run split into boxes of 64/32/16/8
-              // rows, none crossing a 128-row M-block boundary
+              // Two K chunks c0, c0 + 1.  LoRA A rows packed into M: gate rows
+              // [0, r8) at packed row 0, up rows at packed row po; chunk kc's A
+              // tile starts at kc * ast.  The wide map loads both chunks (and
+              // gate and up) in one box; otherwise each chunk is loaded alone,
+              // gate+up in one box (a3) or runs of 64/32/16/8-row boxes that
+              // never cross a 128-row M-block boundary.
+              const int c0 = 2 * kb;
               const int r8 = it.r8, r16 = it.r16;
               const int mlo = 128 * it.mb, mhi = mlo + 128;  // this item's M block
-              int arows = 0;
-              if (it.a3) {
-                // gate and up rank rows in one box: up rows start at packed row a3
-                arows = it.mb == 0 ? 2 * it.a3 : 0;
-              } else
-              for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
-                for (int q = 0; q < r8;) {
-                  const int pr = g * r16 + q;
-                  int bh = 8;
-                  for (int j = 0; j < 4; ++j) {
-                    const int cand = 64 >> j;
-                    if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; break; }
+              const int ast = shrink_a_stride<KIND>(it);
+              int abytes = 0;
+              if (it.aw || it.a3) {
+                abytes = it.mb == 0 ? 2 * ast : 0;
+              } else {
+                for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
+                  for (int q = 0; q < r8;) {
+                    const int pr = g * r16 + q;
+                    int bh = 8;
+                    for (int j = 0; j < 4; ++j) {
+                      const int cand = 64 >> j;
+                      if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; break; }
+                    }
+                    if (pr >= mlo && pr < mhi) abytes += 2 * bh * 128;
+                    q += bh;
                   }
-                  if (pr >= mlo && pr < mhi) arows += bh;
-                  q += bh;
+              }
+              const int xh = it.nrows <= 64 ? 64 : 128;  // x / h rows per chunk
+              mbar_arrive_expect_tx(&c.full[st], abytes + 2 * xh * 128);
+              if (it.aw) {
+                if (it.mb == 0) {
+                  const CUtensorMap* am = &maps.m[it.aw == 16 ? kAW16 : it.aw == 32 ? kAW32 : kAW64];
+                  if (KIND == kShrinkGU) tma_load_4d(sbuf, am, &c.full[st], 0, 0, (it.l * p.E + it.e) * 2, c0);
+                  else tma_load_3d(sbuf, am, &c.full[st], 0, (it.l * p.E + it.e) * p.R, c0);
                 }
-              mbar_arrive_expect_tx(&c.full[st], arows * 128 + rbytes);
-              if (it.a3) {
-                if (it.mb == 0)
-                  tma_load_3d(sbuf, &maps.m[it.a3 == 16 ? kA3x16 : it.a3 == 32 ? kA3x32 : kA3x64], &c.full[st],
-                              kb * 64, 0, (it.l * p.E + it.e) * 2);
-              } else
-              for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
-                for (int q = 0; q < r8;) {
-                  const int pr = g * r16 + q;
-                  int bh = 8, bj = 3;
-                  for (int j = 0; j < 4; ++j) {
-                    const int cand = 64 >> j;
-                    if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; bj = j; break; }
+              } else {
+                for (int kc = 0; kc < 2; ++kc) {
+                  if (it.a3) {
+                    if (it.mb == 0)
+                      tma_load_3d(sbuf + kc * ast, &maps.m[it.a3 == 16 ? kA3x16 : it.a3 == 32 ? kA3x32 : kA3x64],
+                                  &c.full[st], (c0 + kc) * 64, 0, (it.l * p.E + it.e) * 2);
+                    continue;
                   }
-                  if (pr >= mlo && pr < mhi) {
-                    const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q
-                                                      : (it.l * p.E + it.e) * p.R + q;
-                    const CUtensorMap* am = &maps.m[bj == 0 ? kW : bj == 1 ? kA32 : bj == 2 ? kA16 : kA8];
-                    tma_load_2d(sbuf + (pr - mlo) * 128, am, &c.full[st], kb * 64, row);
-                  }
-                  q += bh;
+                  for (int g = 0; g < (KIND == kShrinkGU ? 2 : 1); ++g)
+                    for (int q = 0; q < r8;) {
+                      const int pr = g * r16 + q;
+                      int bh = 8, bj = 3;
+                      for (int j = 0; j < 4; ++j) {
+                        const int cand = 64 >> j;
+                        if ((p.abox_mask >> j) & 1 && cand <= r8 - q && (pr >> 7) == ((pr + cand - 1) >> 7)) { bh = cand; bj = j; break; }
+                      }
+                      if (pr >= mlo && pr < mhi) {
+                        const int row = KIND == kShrinkGU ? ((it.l * p.E + it.e) * 2 + g) * p.R + q
+                                                          : (it.l * p.E + it.e) * p.R + q;
+                        const CUtensorMap* am = &maps.m[bj == 0 ? kW : bj == 1 ? kA32 : bj == 2 ? kA16 : kA8];
+                        tma_load_2d(sbuf + kc * ast + (pr - mlo) * 128, am, &c.full[st], (c0 + kc) * 64, row);
+                      }
+                      q += bh;
+                    }
                 }
-              // B operand: rows of x_sorted (gate_up shrink) or h (down shrink)
-              for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+              }
+              // B operand: rows of x_sorted (gate_up shrink) or h (down shrink), both chunks
+              tma_load_3d(sbuf + 32768, &maps.m[xh == 64 ? kX2x64 : kX2x128], &c.full[st], 0, it.row0, c0);
             } else if (KIND == kGateUp) {
               mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
               const int i0 = it.mb * 128;
@@ -423,14 +458,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort)) ok = false;
         tc_fence_after();
         const uint32_t acc = tmem + b * CF::kAccCols;
-        const int nsteps = ok ? nk + it.nexp : 0;
+        const int nsteps = ok ? nks + it.nexp : 0;
         ExpandCursor cur;
         for (int s = 0; s < nsteps; ++s, ++gs) {
           const int st = gs % S, round = gs / S;
           if (!mbar_wait(&c.full[st], round & 1, abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sb = smem_u32(smem + st * SB);
-          if (s < nk) {
+          if (s < nks) {
             const uint32_t idesc = idesc_bf16_f32(128, it.nrows);
             if (KIND == kGateUp) {
 #pragma unroll
@@ -440,6 +475,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 mma_bf16(acc, sdesc_sw128(sb + kk * 32), bx, idesc, a);
                 mma_bf16(acc + 256, sdesc_sw128(sb + 16384 + kk * 32), bx, idesc, a);
               }
+            } else if (kShrink) {
+              const int ast = shrink_a_stride<KIND>(it), xst = (it.nrows <= 64 ? 64 : 128) * 128;
+#pragma unroll
+              for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_bf16(acc, sdesc_sw128(sb + kc * ast + kk * 32), sdesc_sw128(sb + 32768 + kc * xst + kk * 32),
+                           idesc, (s > 0 || kc > 0 || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
@@ -995,6 +1038,20 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 view {d0..d3} with byte strides s1..s3, 128-byte swizzle.
+bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&d)[4], const uint64_t (&st)[3],
+               const uint32_t (&b)[4]) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {d[0], d[1], d[2], d[3]};
+  cuuint64_t strides[3] = {st[0], st[1], st[2]};
+  cuuint32_t box[4] = {b[0], b[1], b[2], b[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-operand maps with 128-, 256- and 192-row boxes over a chunk-major buffer
 // of `rows` 64-column rows; returns the mask of the maps made (a box taller
 // than the buffer is skipped).
@@ -1182,7 +1239,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
-  int abox_gu = 0, abox_d = 0, bmask = 0, a3_gu = 0, w3 = 0;
+  int abox_gu = 0, abox_d = 0, bmask = 0, a3_gu = 0, w3 = 0, aw_gu = 0, aw_d = 0;
   int rm_sgu = 0, rm_gu = 0, rm_sd = 0, rm_dn = 0;
   const uint64_t cap = (uint64_t)f.cap, zcap = (uint64_t)f.zcap;
   const uint64_t hk = (uint64_t)ceil_div(H, 64), ik = (uint64_t)ceil_div(I, 64);
@@ -1202,6 +1259,32 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
     ok = make_map3(&m_gu.m[kW3], w_gate_up, H, I, (uint64_t)E * 2, (uint64_t)H * 2, (uint64_t)I * H * 2, 64, 128, 2,
                    true);
     w3 = 1;
+  }
+  // shrinks: x_sorted / h as [chunk][row][64]; a box of 64 or 128 rows covers two K chunks
+  ok = ok && make_map3(&m_sgu.m[kX2x64], xs, 64, cap, hk, 128, cap * 128, 64, 64, 2, true) &&
+       make_map3(&m_sgu.m[kX2x128], xs, 64, cap, hk, 128, cap * 128, 64, 128, 2, true) &&
+       make_map3(&m_sd.m[kX2x64], hbuf, 64, cap, ik, 128, cap * 128, 64, 64, 2, true) &&
+       make_map3(&m_sd.m[kX2x128], hbuf, 64, cap, ik, 128, cap * 128, 64, 128, 2, true);
+  if (ok && L > 0) {
+    // wide LoRA A boxes: rb rank rows (gate and up for A_gu) of two K chunks.  The
+    // chunked views are exact only when K is a multiple of 64 (else the last
+    // chunk of the last row would run past the tensor), so otherwise none.
+    for (int j = 0; ok && j < 3; ++j) {
+      const uint32_t rb = 16u << j;
+      if ((int)rb > R) continue;
+      if (H % 64 == 0) {
+        const uint64_t d[4] = {64, (uint64_t)R, (uint64_t)L * E * 2, (uint64_t)H / 64};
+        const uint64_t st[3] = {(uint64_t)H * 2, (uint64_t)R * H * 2, 128};
+        const uint32_t b[4] = {64, rb, 2, 2};
+        ok = make_map4(&m_sgu.m[kAW16 + j], lora_a_gu, d, st, b);
+        aw_gu |= 1 << j;
+      }
+      if (ok && I % 64 == 0) {
+        ok = make_map3(&m_sd.m[kAW16 + j], lora_a_down, 64, (uint64_t)L * E * R, (uint64_t)I / 64, (uint64_t)I * 2,
+                       128, 64, rb, 2, true);
+        aw_d |= 1 << j;
+      }
+    }
   }
   if (ok && L > 0) {
     // LoRA A_gu as [(l, e, gate|up)][rank][k]: a box {64, rb, 2} holds rb gate and rb up rank rows
@@ -1307,7 +1390,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                              zgu, stream)) != MLR_OK)
       return rc;
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu; q.a3_mask = a3_gu; q.rmask = rm_sgu;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_gu; q.abox_mask = abox_gu; q.a3_mask = a3_gu; q.aw_mask = aw_gu;
+    q.rmask = rm_sgu;
     if ((rc = launch_gemm<kShrinkGU>(m_sgu, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 2, stream);
@@ -1323,7 +1407,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                              scalings, zd, stream)) != MLR_OK)
       return rc;
     Params q = p;
-    q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d; q.rmask = rm_sd;
+    q.n_tiles = counts + 1; q.nblk = f.mtiles_d; q.abox_mask = abox_d; q.aw_mask = aw_d; q.rmask = rm_sd;
     if ((rc = launch_gemm<kShrinkD>(m_sd, q, f.max_shrink, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 4, stream);
