@@ -47,15 +47,21 @@ constexpr int kBlock = 16;        // internal align block = MMA N granularity
 constexpr int kTileRows = 256;    // max sorted rows per tile (MMA N)
 constexpr int kInlinePieces = 30;  // LoRA pieces stored inside a base-tile record
 constexpr int kEpiWarp0 = 5;
-constexpr int kThreads = 288;     // 9 warps (warps 1-3 idle)
+constexpr int kMaxThreads = 416;  // up to 13 warps (warps 1-3 idle)
 constexpr int kGatherThreads = 256;
 constexpr int kPlanThreads = 1024;
 constexpr int kShrinkRows = 128;  // max sorted rows per shrink tile
 constexpr int kGemvRows = 4;      // buckets with at most this many pairs take the CUDA-core shrink
 constexpr int kGemvThreads = 256;
-constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging: 32 rows of bf16 h, or 16 rows of fp32
+constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging per epilogue half: 32 rows of bf16 h, or 16 rows of fp32
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
+
+// Epilogue warps: gate_up drains its single (not double-buffered) accumulator
+// with two warps per TMEM lane quarter, each taking alternate 32-column
+// chunks; the others use one warp per quarter.
+template <int KIND> constexpr int kEpiWarps = KIND == kGateUp ? 8 : 4;
+template <int KIND> constexpr int kThreadsOf = (kEpiWarp0 + kEpiWarps<KIND>) * 32;
 
 template <int KIND> struct Cfg;
 // The shrinks stage two 64-wide K chunks per ring slot (LoRA A in [0, 32 KB),
@@ -160,7 +166,7 @@ struct __align__(16) Ctl {
   uint64_t acc_empty[2];
   uint32_t tmem;
   int abort;
-  int epi_go;
+  int epi_go[2];  // per item parity: one epilogue half may run one item ahead of the other
   int tok[kTileRows];
   float w[kTileRows];
 };
@@ -168,7 +174,7 @@ struct __align__(16) Ctl {
 template <int KIND>
 constexpr int smem_bytes() {
   static_assert(Cfg<KIND>::kStages <= 8, "ring barriers");
-  return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + kEpiBytes + (int)sizeof(Ctl) + 1024;
+  return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) + 1024;
 }
 
 // SiLU(v) = v / (1 + e^-v) with CUDA's fast exponential and fast division
@@ -275,7 +281,7 @@ struct ExpandCursor {
 };
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   using CF = Cfg<KIND>;
   constexpr int S = CF::kStages;
@@ -289,7 +295,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + S * SB;
-  Ctl& c = *reinterpret_cast<Ctl*>(epi + kEpiBytes);
+  constexpr int kHalves = kEpiWarps<KIND> / 4;  // epilogue warps per TMEM lane quarter
+  Ctl& c = *reinterpret_cast<Ctl*>(epi + kHalves * kEpiBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, 64);  // 64-wide K chunks
   const int nks = kShrink ? (nk + 1) / 2 : nk;  // main steps (a shrink step covers two chunks)
@@ -301,7 +308,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.acc_full[b], 1);
-      mbar_init(&c.acc_empty[b], 128);
+      mbar_init(&c.acc_empty[b], 32 * kEpiWarps<KIND>);
     }
     c.abort = 0;
     fence_mbar_init();
@@ -511,7 +518,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     // ================================ epilogue =================================
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int m = quarter * 32 + lane;
-    const int et = tid - kEpiWarp0 * 32;  // 0..127
+    const int eh = (warp - kEpiWarp0) >> 2;             // epilogue half (gate_up: 0 or 1)
+    const int et = (tid - kEpiWarp0 * 32) & 127;         // 0..127 within the half
+    const int ebar = 1 + eh;                             // the half's named barrier (2 halves: 1, 2)
+    uint8_t* epih = epi + eh * kEpiBytes;                // the half's staging buffer
     int il = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++il) {
       const Item it = load_item<KIND>(p, item);
@@ -526,19 +536,20 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       }
       // one thread waits for the accumulator; the decision is shared through
       // shared memory so that all 128 epilogue threads take the same branch
-      if (et == 0) {
+      if (et == 0 && eh == 0) {
         const bool got = mbar_wait(&c.acc_full[b], (il / CF::kAccBufs) & 1, abort);
-        c.epi_go = (got && !*abort) ? 1 : 0;
+        c.epi_go[il & 1] = (got && !*abort) ? 1 : 0;
       }
-      named_bar_sync(1, 128);  // also publishes tok/w
+      if (kHalves == 1) named_bar_sync(1, 128);  // also publishes tok/w
+      else named_bar_sync(3, 32 * kEpiWarps<KIND>);
       tc_fence_after();
-      if (!c.epi_go) break;
+      if (!c.epi_go[il & 1]) break;
       const uint32_t tl = tmem + b * CF::kAccCols + ((uint32_t)(quarter * 32) << 16);
       if (KIND == kGateUp) {
-        uint16_t* hs = reinterpret_cast<uint16_t*>(epi);
+        uint16_t* hs = reinterpret_cast<uint16_t*>(epih);
         constexpr int kHs = 128 + 8;
         const int i0 = it.mb * 128;
-        for (int c0 = 0; c0 < it.nrows; c0 += 32) {
+        for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
           const int ncol = min(32, it.nrows - c0);  // 32 or 16
           if (ncol == 32) {
             float gv[32], uv[32];
@@ -553,7 +564,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(ebar, 128);
           const int icap = (int)round_up(p.I, 64);
           for (int q = et; q < ncol * 16; q += 128) {
             const int n = q >> 4, ch = q & 15;
@@ -566,10 +577,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + c0 + n) * 64 + (i & 63)) = v;
             }
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(ebar, 128);
         }
       } else if (KIND == kDown) {
-        float* ds = reinterpret_cast<float*>(epi);
+        float* ds = reinterpret_cast<float*>(epih);
         constexpr int kDs = 128 + 4;
         const int h0 = it.mb * 128;
         for (int c0 = 0; c0 < it.nrows; c0 += 16) {
@@ -577,7 +588,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           tmem_ld16(tl + c0, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) ds[j * kDs + m] = v[j];
-          named_bar_sync(1, 128);
+          named_bar_sync(ebar, 128);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int q = et + 128 * k;
@@ -589,7 +600,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               red_add_v4(p.yacc + (int64_t)t * p.H + h0 + quad * 4, w * v4.x, w * v4.y, w * v4.z, w * v4.w);
             }
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(ebar, 128);
         }
       } else {
         const int r = it.r, r16 = it.r16;
@@ -617,7 +628,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
       }
       tc_fence_before();
-      named_bar_sync(1, 128);  // tok/w and the staging chunk are free for the next item
+      named_bar_sync(ebar, 128);  // tok/w and the staging chunk are free for the next item
       mbar_arrive(&c.acc_empty[b]);
     }
   }
@@ -1148,7 +1159,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   if (max_items <= 0) return MLR_OK;
   if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
   const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-  moe_gemm_kernel<KIND><<<grid, kThreads, smem, stream>>>(maps, p);
+  moe_gemm_kernel<KIND><<<grid, kThreadsOf<KIND>, smem, stream>>>(maps, p);
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;
