@@ -5,14 +5,16 @@
 // with their routing weights).
 //
 // Launch sequence (one stream, no host synchronisation):
-//   align (block 16)  -> pairs sorted into (expert, adapter) buckets
-//   plan              -> tiles of <= 256 consecutive sorted rows of one expert
-//                        (with the adapter buckets they meet) for the base GEMMs,
-//                        and of one (expert, adapter) bucket for the shrinks
-//   gather_x          x_sorted[row] = x[token of the row's pair] (zeros on pads)
-//   shrink_gu         z_gu[row] = s_l * A_gu[l,e] x_t          (gate and up)
-//   gate_up           h[row]    = SiLU(W_g x + B_g z_g) * (W_u x + B_u z_u)
-//   shrink_d          z_d[row]  = s_l * A_d[l,e] h[row]
+//   align + plan      pairs sorted stably into (expert, adapter) buckets, in a
+//                     dense order (no padding); base tiles (16-aligned, <= 256
+//                     rows of one expert, with the LoRA pieces they meet) and
+//                     shrink tiles (one bucket's z region); one launch up to
+//                     16384 pairs, else counts -> plan -> dense scatter
+//   gather_x          x_sorted[u] = x[token of the u-th pair]; y_acc = 0
+//   shrink_gu         z_gu[bucket region] = s_l * A_gu[l,e] x_sorted   (gate, up)
+//                     (buckets of <= 4 pairs on CUDA cores when buckets are small)
+//   gate_up           h[u] = SiLU(W_g x + B_g z_g) * (W_u x + B_u z_u)
+//   shrink_d          z_d[bucket region] = s_l * A_d[l,e] h
 //   down              y_acc[t] += w * (W_d h + B_d z_d)
 //   convert           y = bf16(y_acc)
 //
@@ -29,12 +31,13 @@
 //              too few bytes per request; one copy into sorted order first lets
 //              every operand load be a large tiled box.)
 //   warp 4     TMEM allocation and the single-thread MMA issue (tcgen05.mma)
-//   warps 5-8  epilogue: TMEM -> registers -> global, overlapping the next
+//   warps 5-   epilogue: TMEM -> registers -> global, overlapping the next
 //              item's main loop (double-buffered accumulators where TMEM allows)
 // Because a tile's rows are sorted by adapter, each adapter owns a contiguous
 // column range of the accumulator: the LoRA expand is issued as extra MMAs on
-// that range (N = the bucket's rows) into the same TMEM accumulator as the base
-// GEMM, before the epilogue reads it.
+// that range, rounded out to 16 columns (the z rows outside the bucket are
+// zero), into the same TMEM accumulator as the base GEMM, before the epilogue
+// reads it.
 #include <cudaTypedefs.h>
 
 #include "mlr_align.cuh"
