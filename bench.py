@@ -132,6 +132,21 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
 
 
+def reduce_max(value, dist, device):
+    """The largest of a per-rank float over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rate(units_per_rank, world, ms_per_step_max):
+    """Whole-job throughput: every rank processes units_per_rank per step, timed by the slowest."""
+    return world * units_per_rank / (ms_per_step_max * 1e-3)
+
+
 def layer_work(cfg, batch, mapping):
     """Algorithmic FLOPs and bytes of the layer and of each stage (from the routing)."""
     import torch
@@ -316,12 +331,7 @@ def run_ours(args, rank, world, dist):
     n_st, n_calls = ctypes.c_int32(0), ctypes.c_int32(0)
     lib.moe_lora_profile_end(stage_ms, 16, ctypes.byref(n_st), ctypes.byref(n_calls))
     n_launch = lib.moe_lora_launch_count() - n_launch0
-    ms = e0.elapsed_time(e1)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = reduce_max(e0.elapsed_time(e1), dist, dev)
     stages = {lib.moe_lora_profile_stage_name(i).decode(): stage_ms[i] / max(1, n_calls.value)
               for i in range(n_st.value)}
 
@@ -356,11 +366,7 @@ def run_ours(args, rank, world, dist):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(f0.elapsed_time(f1) / e2e_steps, dist, dev)
 
     # check the status of the gated call only now (it synchronised long ago)
     if int(status.item()) != 0:
@@ -381,7 +387,7 @@ def run_ours(args, rank, world, dist):
 
     peaks, peak_src = load_peaks()
     ms_step = ms_max / args.steps
-    value = world * T / (ms_step * 1e-3)
+    value = weak_scaling_rate(T, world, ms_step)
     dom = max((s for s in st_work if s in stages), key=lambda s: stages[s])
     dom_ms = stages[dom]
     rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, "bf16_tflops_sustained")
@@ -404,11 +410,12 @@ def run_ours(args, rank, world, dist):
             "config": {"workload": cfg.name, "tokens": T, "hidden": H, "intermediate": I, "experts": E,
                        "topk": K, "loras": L, "max_rank": R, "seed": args.seed,
                        "parallelism": f"dp{world} (replicas)" if world > 1 else "single GPU",
-                       "l2": "no flush: each step streams ~1.7 GB of weights (> 129 MB L2)"},
+                       "l2": f"no flush: each step streams {byts / 1e9:.2f} GB of algorithmic bytes "
+                             f"(> 129 MB L2)"},
             "roofline": rf, "layer_roofline": layer,
             "stages_ms": {k: round(v, 4) for k, v in stages.items()},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+            "e2e": {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": int(n_launch), "clocks": clk.summary()}

@@ -163,6 +163,31 @@ def test_small_bucket_sizes(cuda_device):
     assert within(y, r) <= 0 and within(y0, r0) <= 0
 
 
+def test_empty_batch(cuda_device):
+    # T = 0: nothing to do, no launch, an empty y
+    c = custom_case(cuda_device, T=8, K=2, E=4, H=128, I=128, L=2, R=16, ranks=[16, 8],
+                    seg_lens=[8], adapters=[0])
+    empty = dict(x=c.x[:0], topk_ids=c.b.topk_ids[:0], topk_weights=c.b.topk_weights[:0],
+                 token_lora_mapping=torch.zeros(0, dtype=torch.int32, device=cuda_device),
+                 lora_ranks=c.b.lora_ranks, scalings=c.scal)
+    empty.update({k: getattr(c.w, k) for k in WKEYS})
+    y = mlr.fused_moe_lora_forward(**empty)
+    assert tuple(y.shape) == (0, 128)
+
+
+@pytest.mark.parametrize("what", ["expert", "adapter"])
+def test_out_of_range_ids_raise(cuda_device, what):
+    c = custom_case(cuda_device, T=40, K=2, E=4, H=128, I=128, L=2, R=16, ranks=[16, 8],
+                    seg_lens=[20, 20], adapters=[0, 1])
+    ids, mapping = c.b.topk_ids.clone(), torch.from_numpy(np.ascontiguousarray(c.mapping)).to(cuda_device)
+    if what == "expert":
+        ids[3, 1] = 4   # E = 4
+    else:
+        mapping[5] = 2  # L = 2
+    with pytest.raises(mlr.MoeLoraError, match="id out of range"):
+        c.gpu(mapping=mapping.cpu().numpy(), topk_ids=ids)
+
+
 def test_single_expert_top1(cuda_device):
     c = custom_case(cuda_device, T=40, K=1, E=1, H=128, I=128, L=2, R=16, ranks=[16, 8],
                     seg_lens=[25, 15], adapters=[1, 0], lora_std="fan_in")
