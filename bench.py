@@ -243,7 +243,8 @@ def run_reference(args, rank, world):
     cfg, b, w, x = make_inputs(args.config, dev, args.seed)
     st, mp, _ = oracle.batch_info(b.seg_indptr.numpy(), b.weight_indices.numpy(), b.lora_ranks.numpy(),
                                   cfg.num_tokens)
-    per_step_target = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    # each step a bounded sample: the whole run takes about 90 s of oracle time
+    per_step_target = max(0.25, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target, max_tokens=args.ref_tokens)
     rates, ns, secs = [], 0, 0.0
