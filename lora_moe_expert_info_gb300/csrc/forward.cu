@@ -56,14 +56,15 @@ constexpr int kPlanThreads = 1024;
 constexpr int kShrinkRows = 128;  // max sorted rows per shrink tile
 constexpr int kGemvRows = 4;      // buckets with at most this many pairs take the CUDA-core shrink
 constexpr int kGemvThreads = 256;
-constexpr int kEpiBytes = 32 * (128 + 8) * 2;  // staging per epilogue half: 32 rows of bf16 h, or 16 rows of fp32
+constexpr int kEpiBytes = 32 * (128 + 8) * 2;
+constexpr uint64_t kCopyGraceNs = 1000000;  // after an abort: time for issued TMA copies to land  // staging per epilogue half: 32 rows of bf16 h, or 16 rows of fp32
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 
-// Epilogue warps: gate_up drains its single (not double-buffered) accumulator
-// with two warps per TMEM lane quarter, each taking alternate 32-column
-// chunks; the others use one warp per quarter.
-template <int KIND> constexpr int kEpiWarps = KIND == kGateUp ? 8 : 4;
+// Epilogue warps: the base GEMMs drain their accumulators with two warps per
+// TMEM lane quarter, each taking alternate 32-column chunks; the shrinks use
+// one warp per quarter.
+template <int KIND> constexpr int kEpiWarps = (KIND == kGateUp || KIND == kDown) ? 8 : 4;
 template <int KIND> constexpr int kThreadsOf = (kEpiWarp0 + kEpiWarps<KIND>) * 32;
 
 template <int KIND> struct Cfg;
@@ -72,7 +73,13 @@ template <int KIND> struct Cfg;
 template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
 template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512; };
 template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
-template <> struct Cfg<kDown>     { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256; };
+// down runs on CTA pairs: a stage holds this CTA's 128 weight rows [0, 16 KB)
+// and its half of the tile's rows [16 KB, 32 KB).
+template <> struct Cfg<kDown>     { static constexpr int kStages = 6, kStageBytes = 32 * 1024, kAccBufs = 2, kAccCols = 256; };
+
+// GEMM kinds that run on CTA pairs (cluster of two, M = 256 tensor-core MMAs):
+// each CTA loads half of every row tile, so the row bytes per SM drop by half.
+template <int KIND> constexpr bool kPairOf = KIND == kDown;
 
 // Tensor maps of one GEMM kind, by slot.
 //   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
@@ -97,7 +104,8 @@ enum MapSlot {
   kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
   kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
   kX2x64 = 9, kX2x128 = 10, kAW16 = 11, kAW32 = 12, kAW64 = 13,  // shrinks: two-chunk boxes
-  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14, kNumMaps = 15
+  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14, kNumMaps = 15,
+  kRh32 = 9, kRh96 = 14  // pair kinds: half-tile row boxes of 32 / 96 rows (64 / 128 use kRows / kRows128)
 };
 struct Maps {
   CUtensorMap m[kNumMaps];
@@ -167,11 +175,12 @@ struct __align__(16) Ctl {
   uint64_t empty[8];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t drain;  // pairs: the leader's last commit, waited for before the teardown
   uint32_t tmem;
   int abort;
   int epi_go[2];  // per item parity: one epilogue half may run one item ahead of the other
-  int tok[kTileRows];
-  float w[kTileRows];
+  int tok[2][kTileRows];  // down: token and top-k weight of each tile column, by item parity
+  float w[2][kTileRows];
 };
 
 template <int KIND>
@@ -260,6 +269,30 @@ __device__ __forceinline__ Item load_item_warp(const Params& p, int item, TileRe
 // exist and suffice, else zrows.
 __device__ __forceinline__ int z_box_rows(const Params& p, int nj) { return (nj <= 64 && p.zshort) ? 64 : p.zrows; }
 
+// CTA pairs: rows of this CTA's half of an N-row tile (N a multiple of 16), as
+// one box of 32 / 64 / 96 / 128 rows; z rows of half an nj-column piece as one
+// box of 64 or 128 rows.
+__device__ __forceinline__ int pair_row_box(int nrows) {
+  const int h = nrows >> 1;
+  return h <= 32 ? 32 : h <= 64 ? 64 : h <= 96 ? 96 : 128;
+}
+__device__ __forceinline__ int pair_row_slot(int hh) {
+  return hh == 32 ? kRh32 : hh == 64 ? kRows : hh == 96 ? kRh96 : kRows128;
+}
+__device__ __forceinline__ int pair_z_rows(int nj) { return (nj >> 1) <= 64 ? 64 : 128; }
+
+template <bool PAIR>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (PAIR) mma_bf16_pair(d, a, b, idesc, acc);
+  else mma_bf16(d, a, b, idesc, acc);
+}
+// Commit to `bar`; for a pair, to the barrier at the same offset in both CTAs.
+template <bool PAIR>
+__device__ __forceinline__ void mma_commit_to(uint64_t* bar) {
+  if (PAIR) mma_commit_pair(bar, 3);
+  else mma_commit(bar);
+}
+
 // Bytes between the LoRA A tiles of a shrink stage's two K chunks: the packed
 // gate+up (or down) rank rows of the wide / a3 boxes, else a full 128-row M block.
 template <int KIND>
@@ -292,8 +325,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr bool kShrink = (KIND == kShrinkGU || KIND == kShrinkD);
   constexpr int kGates = (KIND == kGateUp) ? 2 : 1;
 
+  constexpr bool kPair = kPairOf<KIND>;
   const int n_items = *p.n_tiles * p.nblk;
-  if ((int)blockIdx.x >= n_items) return;
+  // work unit: a CTA, or for pairs a cluster (both CTAs take the same items and
+  // leave together)
+  const int unit = kPair ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int n_units = kPair ? (int)num_clusters_x() : (int)gridDim.x;
+  if (unit >= n_items) return;
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -311,17 +350,25 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.acc_full[b], 1);
-      mbar_init(&c.acc_empty[b], 32 * kEpiWarps<KIND>);
+      // pairs: one arrival per epilogue half of each CTA, on the leader's barrier
+      mbar_init(&c.acc_empty[b], kPair ? 2 * (kEpiWarps<KIND> / 4) : 32 * kEpiWarps<KIND>);
     }
+    mbar_init(&c.drain, 1);
     c.abort = 0;
     fence_mbar_init();
   }
   if (warp == 4) {
-    tmem_alloc(&c.tmem, 512);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&c.tmem, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c.tmem, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (kPair) cluster_sync_all();  // the peer's copies and commits may target this CTA's barriers from here on
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem;
   volatile int* abort = &c.abort;
@@ -330,7 +377,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     // ================================ producer =================================
     int gs = 0;  // global step counter of this CTA (ring position)
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    for (int item = unit; item < n_items && ok; item += n_units) {
       const Item it = load_item_warp<KIND>(p, item, &c.rec_p, lane);
       const int nsteps = nks + it.nexp;
       ExpandCursor cur;
@@ -426,11 +473,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               }
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
-            } else {  // kDown
-              mbar_arrive_expect_tx(&c.full[st], 16384 + rbytes);
-              tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
-              for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+            } else {  // kDown, on a CTA pair: this CTA's 128 weight rows and half of the tile's rows
+              static_assert(!(KIND == kDown) || kPair, "down runs on CTA pairs");
+              const int hh = pair_row_box(it.nrows);
+              if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
+              const uint32_t fb = cluster_addr(&c.full[st], 0);
+              tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * p.H + it.mb * 256 + (int)rank * 128);
+              tma_load_2d_pair(sbuf + 16384, &maps.m[pair_row_slot(hh)], fb, 0,
+                               kb * p.cap + it.row0 + (int)rank * (it.nrows >> 1));
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the piece (B operand)
@@ -439,9 +489,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int g = cur.g, kg = cur.kg;
             cur.next(pr16, kGates);
             const int nch = min(8, (pr16 - kg * 64) / 8);  // rank chunks of 8 (even)
-            const int zh = z_box_rows(p, pc.x >> 16);
-            mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zh * 16));
-            const int m0 = it.mb * 128;
+            // pairs: this CTA's 128 rows of LoRA B and half of the piece's z rows
+            const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
+            const int zoff = kPair ? (int)rank * ((pc.x >> 16) >> 1) : 0;
+            if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zh * 16));
+            else if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
+            const uint32_t fb = kPair ? cluster_addr(&c.full[st], 0) : 0u;
+            const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128;
             const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
                                              : (pl * p.E + it.e) * p.H + m0;
             const int zc0 = ((KIND == kGateUp ? g * p.R16 : 0) + kg * 64) >> 3;
@@ -449,8 +503,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
               const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
               const int zs = zh == 64 ? (nc == 8 ? kZ8s : (nc == 4 ? kZ4s : kZ2s)) : (nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2));
-              tma_load_3d(sbuf + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
-              tma_load_3d(sbuf + 16384 + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
+              if (kPair) {
+                tma_load_3d_pair(sbuf + ch * 2048, &maps.m[bs], fb, 0, brow, kg * 8 + ch);
+                tma_load_3d_pair(sbuf + 16384 + ch * zh * 16, &maps.m[zs], fb, 0, zrow + zoff, zc0 + ch);
+              } else {
+                tma_load_3d(sbuf + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
+                tma_load_3d(sbuf + 16384 + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
+              }
               ch += nc;
             }
           }
@@ -461,7 +520,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     // ================== MMA (the warp loads items, one thread issues) ==================
     int gs = 0, il = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++il) {
+    // pairs: the leader issues every MMA; the peer's MMA warp only allocates TMEM
+    for (int item = unit; item < n_items && ok && rank == 0; item += n_units, ++il) {
       const Item it = load_item_warp<KIND>(p, item, &c.rec_m, lane);
       if (lane == 0) {
         const int b = il % CF::kAccBufs;
@@ -476,14 +536,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           tc_fence_after();
           const uint32_t sb = smem_u32(smem + st * SB);
           if (s < nks) {
-            const uint32_t idesc = idesc_bf16_f32(128, it.nrows);
+            const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, it.nrows);
             if (KIND == kGateUp) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t a = (s > 0 || kk > 0) ? 1u : 0u;
                 const uint64_t bx = sdesc_sw128(sb + 32768 + kk * 32);
-                mma_bf16(acc, sdesc_sw128(sb + kk * 32), bx, idesc, a);
-                mma_bf16(acc + 256, sdesc_sw128(sb + 16384 + kk * 32), bx, idesc, a);
+                mma_issue<kPair>(acc, sdesc_sw128(sb + kk * 32), bx, idesc, a);
+                mma_issue<kPair>(acc + 256, sdesc_sw128(sb + 16384 + kk * 32), bx, idesc, a);
               }
             } else if (kShrink) {
               const int ast = shrink_a_stride<KIND>(it), xst = (it.nrows <= 64 ? 64 : 128) * 128;
@@ -491,12 +551,12 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               for (int kc = 0; kc < 2; ++kc)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_bf16(acc, sdesc_sw128(sb + kc * ast + kk * 32), sdesc_sw128(sb + 32768 + kc * xst + kk * 32),
+                  mma_issue<kPair>(acc, sdesc_sw128(sb + kc * ast + kk * 32), sdesc_sw128(sb + 32768 + kc * xst + kk * 32),
                            idesc, (s > 0 || kc > 0 || kk > 0) ? 1u : 0u);
             } else {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(acc, sdesc_sw128(sb + kk * 32), sdesc_sw128(sb + 16384 + kk * 32), idesc,
+                mma_issue<kPair>(acc, sdesc_sw128(sb + kk * 32), sdesc_sw128(sb + 16384 + kk * 32), idesc,
                          (s > 0 || kk > 0) ? 1u : 0u);
             }
           } else {
@@ -504,18 +564,24 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int g = cur.g, kg = cur.kg;
             cur.next(pc.z, kGates);
             const int nch = min(8, (pc.z - kg * 64) / 8);
-            const int zh = z_box_rows(p, pc.x >> 16);
+            const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
             const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + (pc.x & 0xffff);
-            const uint32_t idesc = idesc_bf16_f32(128, pc.x >> 16);
+            const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, pc.x >> 16);
             for (int k16 = 0; k16 < nch / 2; ++k16)
-              mma_bf16(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
+              mma_issue<kPair>(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
                        sdesc_noswz(sb + 16384 + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
           }
-          mma_commit(&c.empty[st]);
+          mma_commit_to<kPair>(&c.empty[st]);
         }
-        if (ok) mma_commit(&c.acc_full[b]);
+        if (ok) mma_commit_to<kPair>(&c.acc_full[b]);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (kPair && rank == 0 && lane == 0) {
+      // the pair's MMAs read both CTAs' shared memory and write both TMEMs:
+      // all of them complete before either CTA tears down
+      mma_commit_pair(&c.drain, 1);
+      if (!mbar_wait_for(&c.drain, 0, kWaitLimitNs)) *abort = 1;
     }
   } else if (warp >= kEpiWarp0) {
     // ================================ epilogue =================================
@@ -526,16 +592,17 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     const int ebar = 1 + eh;                             // the half's named barrier (2 halves: 1, 2)
     uint8_t* epih = epi + eh * kEpiBytes;                // the half's staging buffer
     int il = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++il) {
+    for (int item = unit; item < n_items; item += n_units, ++il) {
       const Item it = load_item<KIND>(p, item);
       const int b = il % CF::kAccBufs;
       if (KIND == kDown) {
-        for (int n = et; n < kTileRows; n += 128) {
-          const int pr = (n >= it.lo && n < it.hi) ? p.usorted[it.row0 + n] : (int)p.P;
-          const bool real = pr >= 0 && pr < p.P;
-          c.tok[n] = real ? pr / p.K : -1;
-          c.w[n] = real ? p.topk_weights[pr] : 0.f;
-        }
+        // by item parity: the other half may still read the previous item's
+        static_assert(KIND != kDown || kHalves * 128 == kTileRows, "one column per epilogue thread");
+        const int n = et + 128 * eh;
+        const int pr = (n >= it.lo && n < it.hi) ? p.usorted[it.row0 + n] : (int)p.P;
+        const bool real = pr >= 0 && pr < p.P;
+        c.tok[il & 1][n] = real ? pr / p.K : -1;
+        c.w[il & 1][n] = real ? p.topk_weights[pr] : 0.f;
       }
       // one thread waits for the accumulator; the decision is shared through
       // shared memory so that all 128 epilogue threads take the same branch
@@ -583,27 +650,47 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           named_bar_sync(ebar, 128);
         }
       } else if (KIND == kDown) {
-        float* ds = reinterpret_cast<float*>(epih);
-        constexpr int kDs = 128 + 4;
-        const int h0 = it.mb * 128;
-        for (int c0 = 0; c0 < it.nrows; c0 += 16) {
-          float v[16];
-          tmem_ld16(tl + c0, v);
+        // Each warp owns 32 rows of y (its TMEM lane quarter) and transposes
+        // 16 columns at a time through its own 2 KB of shared memory, so that a
+        // lane then holds 4 consecutive rows of one token: one 16-byte vector
+        // reduction into y_acc.  Only the warp synchronises.
+        static_assert(KIND != kDown || kEpiWarps<KIND> * 2048 <= kHalves * kEpiBytes, "per-warp staging");
+        const int hq = (kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128) + quarter * 32;
+        const int* tk = c.tok[il & 1];
+        const float* wk = c.w[il & 1];
+        float* wb = reinterpret_cast<float*>(epi) + (warp - kEpiWarp0) * 512;  // [16 columns][32 rows]
+        const int q4 = (lane & 7) * 4;   // this lane's 4 rows of y within the warp's 32
+        const bool hv = hq + q4 < p.H;   // H is a multiple of 8: all 4 rows or none
+        for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
+          const int nc = min(32, it.nrows - c0);  // 32 or 16
+          float v[32];
+          if (nc == 32) {
+            tmem_ld32(tl + c0, v);
+          } else {
+            float v16[16];
+            tmem_ld16(tl + c0, v16);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ds[j * kDs + m] = v[j];
-          named_bar_sync(ebar, 128);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int q = et + 128 * k;
-            const int n = q >> 5, quad = q & 31;
-            const int t = c.tok[c0 + n];
-            if (t >= 0 && h0 + quad * 4 < p.H) {
-              const float4 v4 = *reinterpret_cast<const float4*>(ds + n * kDs + quad * 4);
-              const float w = c.w[c0 + n];
-              red_add_v4(p.yacc + (int64_t)t * p.H + h0 + quad * 4, w * v4.x, w * v4.y, w * v4.z, w * v4.w);
-            }
+            for (int j = 0; j < 16; ++j) v[j] = v16[j];
           }
-          named_bar_sync(ebar, 128);
+#pragma unroll
+          for (int g = 0; g < 32; g += 16) {
+            if (g >= nc) break;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) wb[j * 32 + lane] = v[g + j];
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int j = k * 4 + (lane >> 3);  // column of this lane's reduction
+              const int n = c0 + g + j;
+              const int t = tk[n];
+              if (hv && t >= 0) {
+                const float4 x = *reinterpret_cast<const float4*>(wb + j * 32 + q4);
+                const float w = wk[n];
+                red_add_v4(p.yacc + (int64_t)t * p.H + hq + q4, w * x.x, w * x.y, w * x.z, w * x.w);
+              }
+            }
+            __syncwarp();
+          }
         }
       } else {
         const int r = it.r, r16 = it.r16;
@@ -632,13 +719,19 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       }
       tc_fence_before();
       named_bar_sync(ebar, 128);  // tok/w and the staging chunk are free for the next item
-      mbar_arrive(&c.acc_empty[b]);
+      if (!kPair) mbar_arrive(&c.acc_empty[b]);
+      else if (et == 0) mbar_arrive_cluster(cluster_addr(&c.acc_empty[b], 0));  // the leader's barrier
     }
   }
   if (tid == 0 && *abort) set_status(p.status, MLR_STATUS_TIMEOUT);
+  if (*abort) sleep_for_ns(kCopyGraceNs);  // copies already issued land before the teardown
   tc_fence_before();
-  __syncthreads();
-  if (warp == 4) tmem_dealloc(tmem, 512);
+  if (kPair) cluster_sync_all();  // neither CTA of a pair leaves while the other may still reach it
+  else __syncthreads();
+  if (warp == 4) {
+    if (kPair) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
+  }
 }
 
 // Block-wide exclusive scan of per-thread counts; returns this thread's offset.
@@ -1081,6 +1174,16 @@ bool make_row_maps(Maps& m, const void* base, uint64_t rows, int* mask) {
   return true;
 }
 
+// Half-tile row maps of the pair kinds: 32-, 96- and 128-row boxes (the
+// 64-row box is kRows) over a chunk-major buffer of `rows` >= 128 rows.
+bool make_pair_row_maps(Maps& m, const void* base, uint64_t rows) {
+  const int slot[3] = {kRh32, kRh96, kRows128};
+  const uint32_t height[3] = {32, 96, 128};
+  for (int j = 0; j < 3; ++j)
+    if (rows < height[j] || !make_map(&m.m[slot[j]], base, 64, rows, 64, height[j], true)) return false;
+  return true;
+}
+
 constexpr int kMaxForwardBuckets = 16384;  // E * (L + 1): the plan keeps two scans of it in shared memory
 
 struct FwdLayout {
@@ -1161,9 +1264,36 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   const int64_t max_items = max_tiles * p.nblk;
   if (max_items <= 0) return MLR_OK;
   if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
-  const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-  moe_gemm_kernel<KIND><<<grid, kThreadsOf<KIND>, smem, stream>>>(maps, p);
-  MLR_CHECK_LAUNCH();
+  if (kPairOf<KIND>) {
+    // clusters of two CTAs, as many as can be resident at once (a persistent
+    // grid with one pair more than fits would run that pair after the others)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreadsOf<KIND>);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int resident = 0;
+    if (resident == 0) {
+      cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND>, &cfg) != cudaSuccess || n <= 0)
+        return MLR_ERR_CUDA;
+      resident = n;
+    }
+    const int64_t pairs = max_items < resident ? max_items : resident;
+    cfg.gridDim = dim3(2 * (unsigned)pairs);
+    if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
+  } else {
+    const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
+    moe_gemm_kernel<KIND><<<grid, kThreadsOf<KIND>, smem, stream>>>(maps, p);
+    MLR_CHECK_LAUNCH();
+  }
   note_launch();
   return MLR_OK;
 }
@@ -1265,7 +1395,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
             make_map(&m_dn.m[kW], w_down, I, (uint64_t)E * H, 64, 128, true) &&
             make_map(&m_dn.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
             make_row_maps(m_gu, xs, hk * cap, &rm_gu) && make_row_maps(m_sgu, xs, hk * cap, &rm_sgu) &&
-            make_row_maps(m_sd, hbuf, ik * cap, &rm_sd) && make_row_maps(m_dn, hbuf, ik * cap, &rm_dn);
+            make_row_maps(m_sd, hbuf, ik * cap, &rm_sd) && make_pair_row_maps(m_dn, hbuf, ik * cap);
   rm_sgu &= 1;  // shrink tiles hold at most 128 rows
   rm_sd &= 1;
   if (ok && I >= 128) {
@@ -1325,7 +1455,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                      8, 128, nc[j]) &&
            // chunk-major z: [column/8][zcap][8]
            make_map3(&m_gu.m[zslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
-           make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
+           // down (CTA pairs): half a piece's z rows, 128-row boxes
+           make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, 128, nc[j]) &&
            make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]) &&
            make_map3(&m_dn.m[zsslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
     }
@@ -1427,7 +1558,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   prof_mark(prof, 4, stream);
   {
     Params q = p;
-    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 128); q.rmask = rm_dn;
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 256); q.rmask = rm_dn;  // a pair covers 256 rows of H
     if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);
