@@ -616,9 +616,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       if (!c.epi_go[il & 1]) break;
       const uint32_t tl = tmem + b * CF::kAccCols + ((uint32_t)(quarter * 32) << 16);
       if (KIND == kGateUp) {
-        uint16_t* hs = reinterpret_cast<uint16_t*>(epih);
-        constexpr int kHs = 128 + 8;
-        const int i0 = it.mb * 128;
+        // Each warp owns 32 rows of h (its TMEM lane quarter; they lie in one
+        // 64-wide chunk of h) and stages 32 columns of them through its own
+        // 2 KB of shared memory, then stores 64 contiguous bytes per column.
+        // Only the warp synchronises.
+        static_assert(KIND != kGateUp || kEpiWarps<KIND> * 2048 <= kHalves * kEpiBytes, "per-warp staging");
+        uint16_t* ws = reinterpret_cast<uint16_t*>(epi) + (warp - kEpiWarp0) * 1024;  // [32 columns][32 rows]
+        const int iw = it.mb * 128 + quarter * 32;  // first row of h of this warp
+        const bool chunk_ok = iw < (int)round_up(p.I, 64);
         for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
           const int ncol = min(32, it.nrows - c0);  // 32 or 16
           if (ncol == 32) {
@@ -626,28 +631,28 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             tmem_ld32(tl + c0, gv);
             tmem_ld32(tl + 256 + c0, uv);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+            for (int j = 0; j < 32; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           } else {
             float gv[16], uv[16];
             tmem_ld16(tl + c0, gv);
             tmem_ld16(tl + 256 + c0, uv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) hs[j * kHs + m] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+            for (int j = 0; j < 16; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           }
-          named_bar_sync(ebar, 128);
-          const int icap = (int)round_up(p.I, 64);
-          for (int q = et; q < ncol * 16; q += 128) {
-            const int n = q >> 4, ch = q & 15;
-            const int i = i0 + ch * 8;
+          __syncwarp();
+          // h is chunk-major: [I/64][cap][64]; rows past I are stored as zeros.
+          // Only this expert's columns are stored (the others belong to other tiles).
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int q = lane + 32 * k;
+            const int n = q >> 2, i = iw + (q & 3) * 8;
             const int col = c0 + n;
-            // h is chunk-major: [I/64][cap][64]; the tail past I is zero.  Only
-            // this expert's columns are stored (the others belong to other tiles).
-            if (i < icap && col >= it.lo && col < it.hi) {
-              const uint4 v = i < p.I ? *reinterpret_cast<const uint4*>(hs + n * kHs + ch * 8) : make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + c0 + n) * 64 + (i & 63)) = v;
+            if (n < ncol && chunk_ok && col >= it.lo && col < it.hi) {
+              const uint4 v = i < p.I ? *reinterpret_cast<const uint4*>(ws + n * 32 + (q & 3) * 8) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + col) * 64 + (i & 63)) = v;
             }
           }
-          named_bar_sync(ebar, 128);
+          __syncwarp();
         }
       } else if (KIND == kDown) {
         // Each warp owns 32 rows of y (its TMEM lane quarter) and transposes
