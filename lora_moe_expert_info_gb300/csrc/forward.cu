@@ -189,10 +189,17 @@ constexpr int smem_bytes() {
   return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) + 1024;
 }
 
-// SiLU(v) = v / (1 + e^-v) with CUDA's fast exponential and fast division
-// (a few ulp of fp32; the result is rounded to bf16 right after).  For
-// v << 0 the denominator overflows and the quotient is 0, the correct limit.
-__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+// SiLU(v) = v * sigmoid(v), with sigmoid(v) = (1 + tanh(v / 2)) / 2: one
+// hardware tanh (tanh.approx.f32, about 2^-11 relative error) and two FMAs,
+// half the special-function work of an exponential plus a division.  The
+// result is rounded to bf16 right after.  tanh saturates to -1 for v << 0, so
+// the product goes to 0, the correct limit.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float silu_f(float v) { return v * fmaf(0.5f, tanh_approx(0.5f * v), 0.5f); }
 
 // One work item: tile rows, weight block, adapter (shrinks: with its rank).
 struct Item {
