@@ -257,3 +257,38 @@ def test_deepseek_prefill_sampled(cuda_device):
     toks = np.concatenate([[0, c.cfg.num_tokens - 1], toks])
     assert within(y[toks], c.ref(tokens=toks)) <= 0
     assert np.isfinite(y).all()
+
+
+_FRESH_SCRIPT = r"""
+import sys, json, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import lora_moe_expert_info_gb300 as mlr
+from lora_moe_expert_info_gb300 import workloads
+cfg = workloads.CONFIGS["decode"]
+dev = torch.device("cuda", 0)
+b = workloads.make_batch(cfg, dev, 0)
+w = workloads.make_weights(cfg, b.lora_ranks, dev, 0)
+x = workloads.make_x(cfg, dev, 0)
+en, mp = mlr.moe_lora_batch_info(b.seg_indptr, b.weight_indices, b.lora_ranks, cfg.num_tokens)
+y = mlr.fused_moe_lora_forward(x, b.topk_ids, b.topk_weights, mp, b.lora_ranks, b.scalings,
+                               **{k: getattr(w, k) for k in sys.argv[2].split(",")})
+torch.cuda.synchronize()
+np.save(sys.argv[3], y.float().cpu().numpy())
+"""
+
+
+def test_first_forward_in_fresh_process(cuda_device, tmp_path):
+    """The first forward of a new process, where the caching allocator places the
+    tensors afresh (other allocations around them differ from an in-process
+    run), completes and matches the oracle on the decode workload."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = tmp_path / "y.npy"
+    r = subprocess.run([sys.executable, "-c", _FRESH_SCRIPT, root, ",".join(WKEYS), str(out)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    c = workload_case("decode", cuda_device)  # same seeded device generators as the child
+    y = np.load(out)
+    assert within(y, c.ref()) <= 0
