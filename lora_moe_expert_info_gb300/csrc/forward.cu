@@ -152,6 +152,7 @@ struct Params {
   int a3_mask;    // gate_up shrink: bit j set if the gate+up LoRA A map with (16 << j)-row boxes exists
   int aw_mask;    // shrinks: bit j set if the wide LoRA A map with (16 << j)-row boxes exists
   int rmask;      // bit 0 / 1 / 2 set if the 128- / 256- / 192-row maps of the row operand exist
+  int ykeep;      // down: 1 if y_acc fits in half of L2 (its reductions are then marked evict-last)
   int w3;         // gate_up: 1 if the gate+up weight map exists
   int64_t P;
   const float* topk_weights;
@@ -672,6 +673,11 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const float* wk = c.w[il & 1];
         float* wb = reinterpret_cast<float*>(epi) + (warp - kEpiWarp0) * 512;  // [16 columns][32 rows]
         const int q4 = (lane & 7) * 4;   // this lane's 4 rows of y within the warp's 32
+        // y_acc rows receive a token's top-k contributions spread over the whole
+        // launch; where y_acc fits in half of L2, keep it there against the
+        // streamed weights
+        const uint64_t ypol = l2_evict_last_policy();
+        const bool ykeep = p.ykeep != 0;
         const bool hv = hq + q4 < p.H;   // H is a multiple of 8: all 4 rows or none
         for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
           const int nc = min(32, it.nrows - c0);  // 32 or 16
@@ -698,7 +704,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               if (hv && t >= 0) {
                 const float4 x = *reinterpret_cast<const float4*>(wb + j * 32 + q4);
                 const float w = wk[n];
-                red_add_v4(p.yacc + (int64_t)t * p.H + hq + q4, w * x.x, w * x.y, w * x.z, w * x.w);
+                float* ya = p.yacc + (int64_t)t * p.H + hq + q4;
+                if (ykeep) red_add_v4_hint(ya, w * x.x, w * x.y, w * x.z, w * x.w, ypol);
+                else red_add_v4(ya, w * x.x, w * x.y, w * x.z, w * x.w);
               }
             }
             __syncwarp();
@@ -1571,6 +1579,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   {
     Params q = p;
     q.n_tiles = counts; q.nblk = (int)ceil_div(H, 256); q.rmask = rm_dn;  // a pair covers 256 rows of H
+    q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, stream)) != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);

@@ -283,6 +283,19 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+// L2 policy for data that is reused across the whole launch (evicted last).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// Vector fp32 reduction into global memory with an L2 cache policy.
+__device__ __forceinline__ void red_add_v4_hint(float* addr, float a, float b, float c, float d, uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d), "l"(pol)
+               : "memory");
+}
+
 // Scalar fp32 reduction into global memory.
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
