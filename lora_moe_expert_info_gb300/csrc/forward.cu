@@ -802,7 +802,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
                            int E, int C, int R, uint32_t* __restrict__ ustart_out,
                            TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                            ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                           int32_t* __restrict__ counts, int32_t* status, int gemv_rows) {
+                           int32_t* __restrict__ counts, int32_t* status, int gemv_rows, int by_span) {
   const int NB = E * C;
   int bad = 0;
   // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
@@ -844,14 +844,52 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       }
     }
     int total_t, total_p;
-    int toff = block_offsets(my_t, &total_t);
+    int toff_seq = block_offsets(my_t, &total_t);  // expert order
     int poff = block_offsets(my_p, &total_p);
+    // With by_span, experts are placed in order of decreasing span (64 classes
+    // of 16 rows), each expert's tiles in consecutive slots: the static
+    // round-robin of items over the CTAs then hands out the largest experts
+    // first, while the tiles of one expert still run side by side and share
+    // its weights in L2.  The order inside a class follows the shared-memory
+    // atomics; no result depends on which CTA runs an item.  Without by_span
+    // the experts keep their order (block_offsets above).
+    __shared__ int cls_base[64], cls_fill[64];
+    auto span_class = [](int span) { return 63 - min(63, span >> 4); };
+    if (by_span) {  // uniform over the block
+      if (threadIdx.x < 64) {
+        cls_base[threadIdx.x] = 0;
+        cls_fill[threadIdx.x] = 0;
+      }
+      __syncthreads();
+      for (int e = e0; e < e1; ++e) {
+        const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
+        if (ue1 == ue0) continue;
+        const int span = ceil16(ue1) - floor16(ue0), ts = tile_rows(span);
+        atomicAdd(&cls_base[span_class(span)], (span + ts - 1) / ts);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int run = 0;
+        for (int k = 0; k < 64; ++k) {
+          const int n = cls_base[k];
+          cls_base[k] = run;
+          run += n;
+        }
+      }
+      __syncthreads();
+    }
     for (int e = e0; e < e1; ++e) {
       const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
       if (ue1 == ue0) continue;
       // nt tiles of equal size (a multiple of 16) over [floor16(first row), ceil16(end))
       const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
       const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      int toff = toff_seq;
+      toff_seq += nt;
+      if (by_span) {
+        const int cls = span_class(span);
+        toff = cls_base[cls] + atomicAdd(&cls_fill[cls], nt);
+      }
       for (int k = 0; k < nt; ++k) {
         const int row0 = r0 + k * ts;
         const int N = min(ts, r0 + span - row0);
@@ -921,7 +959,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
             int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
             ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status,
-            int gemv_rows) {
+            int gemv_rows, int by_span) {
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -930,7 +968,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
   __syncthreads();
   align_block_scan(us, NB);
   plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts,
-             status, gemv_rows);
+             status, gemv_rows, by_span);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
@@ -943,7 +981,7 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
                   int32_t* __restrict__ usorted, uint32_t* __restrict__ ustart,
                   TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                   ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                  int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows) {
+                  int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows, int by_span) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
@@ -951,7 +989,7 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
   align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, nullptr, nullptr, nullptr, nullptr, nullptr, P,
               status, usorted);
   plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
-             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows);
+             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows, by_span);
 }
 
 // Dense x_sorted: row u < n = ustart[NB] (the valid pairs) is x[usorted[u] / K]
@@ -1488,6 +1526,9 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   // the CUDA-core shrink pays off when buckets average a few pairs (decode)
   const int64_t nb_nonempty = f.al.P < f.al.NB ? f.al.P : f.al.NB;
   const int gemv_rows = (L > 0 && f.al.P < 8 * nb_nonempty) ? kGemvRows : 0;
+  // largest experts first when experts average more than 32 rows (several
+  // tiles of differing sizes); small batches keep the cheaper plain order
+  const int by_span = f.al.P > 32 * (int64_t)E ? 1 : 0;
   const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
   if (align_block_ok(f.al)) {
     // one launch: the dense align and the tile plan (timed as the align stage)
@@ -1499,7 +1540,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows);
+                                                       gemv_rows, by_span);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
@@ -1513,7 +1554,8 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
-                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows);
+                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows,
+                                                  by_span);
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, topk_ids, token_lora_mapping, K, E, L, aws, ustart, usorted, stream)) !=
