@@ -1296,10 +1296,18 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   return f;
 }
 
+// The current device, or -1 when it cannot be read or is beyond the 64
+// devices the per-device caches below hold.
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  return dev;
+}
+
 int sm_count() {
   static int n[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  const int dev = current_device();
+  if (dev < 0) return 148;
   if (n[dev] == 0) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
@@ -1312,12 +1320,14 @@ int sm_count() {
 template <int KIND>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
   const int smem = smem_bytes<KIND>();
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory opt-in and the resident-cluster count are per device
+  const int dev = current_device();
+  static bool configured[64] = {};
+  if (dev < 0 || !configured[dev]) {
     if (cudaFuncSetAttribute(moe_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MLR_ERR_CUDA;
-    configured = true;
+    if (dev >= 0) configured[dev] = true;
   }
   const int64_t max_items = max_tiles * p.nblk;
   if (max_items <= 0) return MLR_OK;
@@ -1336,13 +1346,15 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    static int resident = 0;
+    static int resident_of[64] = {};
+    int resident = dev >= 0 ? resident_of[dev] : 0;
     if (resident == 0) {
       cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND>, &cfg) != cudaSuccess || n <= 0)
         return MLR_ERR_CUDA;
       resident = n;
+      if (dev >= 0) resident_of[dev] = n;
     }
     const int64_t pairs = max_items < resident ? max_items : resident;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
@@ -1364,12 +1376,13 @@ int launch_gemv(const ShrinkRec* tiles, const int32_t* n_tiles, int64_t max_tile
                 uint16_t* z, cudaStream_t stream) {
   if (max_tiles <= 0) return MLR_OK;
   const int smem = kGemvRows * (int)round_up(Kd, 64) * 2;
-  static int configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
+  const int dev = current_device();
+  static int configured[64] = {};  // largest opt-in so far, per device
+  if (smem > 48 * 1024 && (dev < 0 || smem > configured[dev])) {
     if (cudaFuncSetAttribute(shrink_gemv_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MLR_ERR_CUDA;
-    configured = smem;
+    if (dev >= 0) configured[dev] = smem;
   }
   const int64_t units = max_tiles * ((NG * R + 2 * kGemvThreads / 32 - 1) / (2 * kGemvThreads / 32));
   const int64_t grid = units < 6 * (int64_t)sm_count() ? units : 6 * (int64_t)sm_count();
