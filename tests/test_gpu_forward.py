@@ -292,3 +292,29 @@ def test_first_forward_in_fresh_process(cuda_device, tmp_path):
     c = workload_case("decode", cuda_device)  # same seeded device generators as the child
     y = np.load(out)
     assert within(y, c.ref()) <= 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes(cuda_device, seed):
+    """Seeded random layer shapes within the API's limits, every output against
+    the oracle: H and I any multiple of 8 (so the second CTA of a down pair may
+    hold rows past H, fully or partly), ranks of any size up to R, empty and
+    adapter-less segments, and batches on both sides of the 32-rows-per-expert
+    threshold that switches the tile order."""
+    g = np.random.default_rng(1000 + seed)
+    E = int(g.integers(1, 13))
+    K = int(g.integers(1, min(4, E) + 1))
+    H = 8 * int(g.integers(16, 65))    # 128 .. 512
+    I = 8 * int(g.integers(8, 49))     # 64 .. 384
+    L = int(g.integers(0, 6))
+    R = int(g.choice([16, 32, 64])) if L > 0 else 0
+    ranks = [int(g.integers(0, R + 1)) for _ in range(L)]
+    T = int(g.integers(1, 400))
+    nseg = int(g.integers(1, 6))
+    cuts = np.sort(g.choice(np.arange(0, T + 1), size=nseg - 1, replace=True)) if nseg > 1 else np.array([], int)
+    lens = np.diff(np.concatenate([[0], cuts, [T]])).astype(int).tolist()
+    adapters = [int(g.integers(-1, L)) if L > 0 else -1 for _ in lens]
+    c = custom_case(cuda_device, T=T, K=K, E=E, H=H, I=I, L=L, R=R, ranks=ranks, seg_lens=lens,
+                    adapters=adapters, seed=seed, lora_std="fan_in" if L > 0 else None,
+                    expert_bias=float(g.choice([0.0, 1.0])))
+    assert within(c.gpu(), c.ref()) <= 0, (T, K, E, H, I, L, R, ranks, lens, adapters)
