@@ -67,6 +67,9 @@ def _load():
                                            vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                            i64, i64, i64, i64, i64, i64, i64,
                                            vp, i64, vp, ctypes.c_int]
+            lib.oracle_lora_linear.restype = ctypes.c_int
+            lib.oracle_lora_linear.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                               i64, i64, i64, i64, i64, i64, vp, vp, i64, vp, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -186,5 +189,43 @@ def forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
         lora_ranks.ctypes.data, scalings.ctypes.data,
         ops[0][0], ops[1][0], ops[2][0], ops[3][0], ops[4][0], ops[5][0], wdt,
         T, K, E, H, I, L, R, tok_ptr, n_out, y.ctypes.data, int(threads))
+    del xk, tok
+    return int(st), y
+
+
+def lora_linear(x, token_lora_mapping, lora_ranks, scalings, w, lora_a, lora_b, slice_offsets,
+                tokens=None, threads: int = 0):
+    """Dense projection with per-segment LoRA and split B.  Returns (status, y)
+    with y float64 [len(tokens) or T, D_out].
+
+    Shapes: x [T, D_in]; w [D_out, D_in]; lora_a [L, S, R, D_in] (part s has its
+    own A); lora_b [L, D_out, R] (rows slice_offsets[s] .. slice_offsets[s+1]
+    multiply part s's z); slice_offsets: S + 1 increasing ints from 0 to D_out.
+    """
+    x_np = np.asarray(x)
+    T, D_in = x_np.shape
+    mapping = _i32(token_lora_mapping)
+    lora_ranks = _i32(lora_ranks)
+    scalings = np.ascontiguousarray(np.asarray(scalings, dtype=np.float32))
+    D_out, D_in2 = np.asarray(w).shape
+    L, S, R, D_in3 = np.asarray(lora_a).shape
+    assert D_in2 == D_in and D_in3 == D_in and np.asarray(lora_b).shape == (L, D_out, R)
+    offs = np.ascontiguousarray(np.asarray(slice_offsets, dtype=np.int64))
+    assert offs.shape == (S + 1,)
+    xp, xdt, xk = _operand(x_np)
+    ops = [_operand(a) for a in (w, lora_a, lora_b)]
+    wdt = ops[0][1]
+    if any(o[1] != wdt for o in ops):
+        raise TypeError("weight operands must share one dtype")
+    if tokens is None:
+        tok, n_out, tok_ptr = None, T, None
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        n_out, tok_ptr = tok.shape[0], tok.ctypes.data
+    y = np.zeros((n_out, D_out), dtype=np.float64)
+    st = _load().oracle_lora_linear(
+        xp, xdt, mapping.ctypes.data, lora_ranks.ctypes.data, scalings.ctypes.data,
+        ops[0][0], ops[1][0], ops[2][0], wdt, T, D_in, D_out, L, R, S, offs.ctypes.data,
+        tok_ptr, n_out, y.ctypes.data, int(threads))
     del xk, tok
     return int(st), y

@@ -14,6 +14,10 @@
  *                                          (.) ((W_up + a/r B_u A_u)x)],
  *             the align kernel that orders tokens by LoRA adapter and expert
  *             id, and the 4-D adapter stack [num_loras, num_experts, rank, dim].
+ *   [PR22323] "LoRA quantisation info and DeepSeek-V3 MLA fused projection"
+ *             page, section 实现拆解 items 2-3: ReplicatedLinearWithLoRA applies
+ *             LoRA to the fused q_a_proj + kv_a_proj_with_mqa projection, its B
+ *             split into two parts applied by two segment GEMMs.
  *   [PR24160] "shared MoE LoRA batch info" page, sections 实现拆解 and
  *             关键源码片段 (MoELoRABatchInfo dataclass; test_moe_lora_info.py):
  *             token_lora_mapping = repeat_interleave(weight_indices, seg_lens),
@@ -334,6 +338,98 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
       }
     }
     free(xv); free(a); free(zg); free(zu); free(zd);
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* dense projection with per-segment LoRA and split B  ([PR22323] 实现拆解   */
+/* items 2-3: ReplicatedLinearWithLoRA for the fused q_a_proj +              */
+/* kv_a_proj_with_mqa projection, its LoRA B split into two parts applied by */
+/* two segment GEMMs, and normalize_fused_qkv_a_proj fusing the two adapter  */
+/* entries into one)                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The projection's output rows are split into S parts by slice_offsets[0..S]
+ * (0 = slice_offsets[0] < ... < slice_offsets[S] = D_out).  Part s has its own
+ * LoRA A (rank rows of A_s) and takes rows slice_offsets[s] .. slice_offsets[s+1]
+ * of the stacked B.  For token t with adapter l (used iff l >= 0 and r_l > 0):
+ *   y[t][o] = sum_i W[o][i] x[t][i] + s_l * sum_{q < r_l} B[l][o][q] * z_s[q],
+ *   z_s[q]  = sum_i A[l][s][q][i] x[t][i],   s = the part that holds row o.
+ * Layouts (row-major): x [T, D_in]; w [D_out, D_in]; lora_a [L, S, R, D_in];
+ * lora_b [L, D_out, R]; y [n_out, D_out] double, row j for token tokens[j]
+ * (or j if tokens == NULL).
+ */
+int oracle_lora_linear(const void* x, int x_dtype, const int32_t* token_lora_mapping,
+                       const int32_t* lora_ranks, const float* scalings, const void* w,
+                       const void* lora_a, const void* lora_b, int w_dtype, int64_t T,
+                       int64_t D_in, int64_t D_out, int64_t L, int64_t R, int64_t S,
+                       const int64_t* slice_offsets, const int64_t* tokens, int64_t n_out,
+                       double* y, int num_threads) {
+  if (T < 0 || D_in < 1 || D_out < 1 || L < 0 || R < 0 || S < 1 || n_out < 0) return ORC_INVALID;
+  if (slice_offsets[0] != 0 || slice_offsets[S] != D_out) return ORC_INVALID;
+  for (int64_t s = 0; s < S; ++s)
+    if (slice_offsets[s + 1] <= slice_offsets[s]) return ORC_INVALID;
+  for (int64_t l = 0; l < L; ++l)
+    if (lora_ranks[l] < 0 || lora_ranks[l] > R) return ORC_INVALID;
+  for (int64_t j = 0; j < n_out; ++j) {
+    const int64_t t = tokens ? tokens[j] : j;
+    if (t < 0 || t >= T) return ORC_INVALID;
+    if (token_lora_mapping[t] < -1 || token_lora_mapping[t] >= L) return ORC_INDEX;
+  }
+  int status = ORC_OK;
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+  (void)num_threads;
+#endif
+
+#pragma omp parallel
+  {
+    double* xv = (double*)malloc(sizeof(double) * (size_t)D_in);
+    double* z = (double*)malloc(sizeof(double) * (size_t)(S * (R > 0 ? R : 1)));
+    const int ok = xv && z;
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_out; ++j) {
+      if (!ok) {
+#pragma omp atomic write
+        status = ORC_NOMEM;
+        continue;
+      }
+      const int64_t t = tokens ? tokens[j] : j;
+      double* yrow = y + j * D_out;
+      for (int64_t i = 0; i < D_in; ++i) xv[i] = ld(x, x_dtype, t * D_in + i);
+      const int32_t l = token_lora_mapping[t];
+      const int used = (l >= 0) && (lora_ranks[l] > 0);
+      const int64_t r = used ? lora_ranks[l] : 0;
+      const double sc = used ? (double)scalings[l] : 0.0;
+
+      /* shrink of every part: z_s = A_s x (first r rows only) */
+      for (int64_t s = 0; s < S; ++s)
+        for (int64_t q = 0; q < r; ++q) {
+          const int64_t a = ((l * S + s) * R + q) * D_in;
+          double acc = 0.0;
+          for (int64_t i = 0; i < D_in; ++i) acc += ld(lora_a, w_dtype, a + i) * xv[i];
+          z[s * R + q] = acc;
+        }
+
+      /* base row plus the expand of the part that holds the row */
+      int64_t s = 0;
+      for (int64_t o = 0; o < D_out; ++o) {
+        while (o >= slice_offsets[s + 1]) ++s;
+        double acc = 0.0;
+        for (int64_t i = 0; i < D_in; ++i) acc += ld(w, w_dtype, o * D_in + i) * xv[i];
+        if (r > 0) {
+          double d = 0.0;
+          for (int64_t q = 0; q < r; ++q) d += ld(lora_b, w_dtype, (l * D_out + o) * R + q) * z[s * R + q];
+          acc += sc * d;
+        }
+        yrow[o] = acc;
+      }
+    }
+    free(xv);
+    free(z);
   }
   return status;
 }
