@@ -195,6 +195,48 @@ int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const flo
                            int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
                            size_t ws_bytes, int32_t* d_status, void* stream);
 
+/* Scratch bytes lora_linear_forward needs for these sizes (0 on bad sizes). */
+size_t lora_linear_workspace_bytes(int32_t num_tokens, int32_t in_features, int32_t out_features,
+                                   int32_t num_loras, int32_t max_rank, int32_t num_slices);
+
+/*
+ * lora_linear_forward -- a dense projection with per-segment LoRA and a split B.
+ * Source: sglang PR #22323 page (LoRA quantisation info and the DeepSeek-V3 MLA
+ * fused projection), section 实现拆解 items 2-3: ReplicatedLinearWithLoRA applies
+ * LoRA to the fused q_a_proj + kv_a_proj_with_mqa projection, whose output rows
+ * hold two parts of unequal width; the LoRA B is split into the two parts and
+ * each part is applied by its own segment GEMM to its own LoRA A's shrink.
+ *
+ * The output rows are split into S parts at slice_offsets; for token t with
+ * adapter l = token_lora_mapping[t] (used iff l >= 0 and r_l > 0) and row o in
+ * part s:
+ *   y[t][o] = sum_i w[o][i] x[t][i] + s_l * sum_{q < r_l} lora_b[l][o][q] * z_s[q],
+ *   z_s[q]  = sum_i lora_a[l][s][q][i] x[t][i].
+ *
+ *   x             bf16 [T, D_in]
+ *   w             bf16 [D_out, D_in]
+ *   token_lora_mapping int32 [T] in [-1, L) (from moe_lora_batch_info)
+ *   lora_ranks    int32 [L] in [0, R];  scalings float [L] = alpha_l / r_l
+ *   lora_a        bf16 [L, S, R, D_in]   part s's A
+ *   lora_b        bf16 [L, D_out, R]     rows of part s multiply part s's z
+ *   slice_offsets HOST int32 [S + 1]: 0 = offsets[0] < ... < offsets[S] = D_out
+ *   y             bf16 [T, D_out] out
+ * Requirements: S = 1 or 2; with S = 2 the second part starts on a multiple of
+ * 256 rows (the MLA projection: 1536 + 576); D_in, D_out multiples of 8 and
+ * >= 128; R a multiple of 16 in [16, 256] when L > 0; L + 1 <= 16384; every base
+ * pointer 16-byte aligned.  Bad offsets return MLR_ERR_INVALID, other sizes
+ * outside these MLR_ERR_UNSUPPORTED (and lora_linear_workspace_bytes 0).
+ * Accumulation is fp32 and the LoRA intermediate z is rounded to bf16.  The
+ * profile stages (see below) of this call are "align_plan", "gather",
+ * "shrink_gate_up" (the shrink), "down" (the projection) and "convert".
+ */
+int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const int32_t* token_lora_mapping,
+                        const int32_t* lora_ranks, const float* scalings, const mlr_bf16* lora_a,
+                        const mlr_bf16* lora_b, const int32_t* slice_offsets, int32_t num_tokens,
+                        int32_t in_features, int32_t out_features, int32_t num_loras, int32_t max_rank,
+                        int32_t num_slices, mlr_bf16* y, void* workspace, size_t ws_bytes,
+                        int32_t* d_status, void* stream);
+
 /*
  * Observability.  The pages describe no tracing; these calls exist so that a
  * caller can attribute the forward's GPU time to its stages without a profiler.

@@ -93,6 +93,11 @@ def library() -> ctypes.CDLL:
                 lib.fused_moe_lora_workspace_bytes.argtypes = [i32] * 7
                 lib.fused_moe_lora_forward.restype = ctypes.c_int
                 lib.fused_moe_lora_forward.argtypes = [vp] * 12 + [i32] * 7 + [vp, vp, sz, vp, vp]
+            if hasattr(lib, "lora_linear_forward"):
+                lib.lora_linear_workspace_bytes.restype = sz
+                lib.lora_linear_workspace_bytes.argtypes = [i32] * 6
+                lib.lora_linear_forward.restype = ctypes.c_int
+                lib.lora_linear_forward.argtypes = [vp] * 8 + [i32] * 6 + [vp, vp, sz, vp, vp]
             _lib = lib
     return _lib
 
@@ -288,4 +293,54 @@ def fused_moe_lora_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_r
     _check_host(code, "fused_moe_lora_forward")
     if check:
         _check_device(status, "fused_moe_lora_forward")
+    return y
+
+
+def lora_linear_forward(x, w, token_lora_mapping, lora_ranks, scalings, lora_a, lora_b, slice_offsets,
+                        y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None, check: bool = True,
+                        status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dense projection with per-segment LoRA and split B; returns y bf16 [T, D_out].
+
+    Shapes: x [T, D_in]; w [D_out, D_in]; token_lora_mapping [T]; lora_ranks,
+    scalings [L]; lora_a [L, S, R, D_in] (part s's A); lora_b [L, D_out, R];
+    slice_offsets: S + 1 ints (host), 0 = offsets[0] < ... < offsets[S] = D_out.
+    """
+    lib = library()
+    if not hasattr(lib, "lora_linear_forward"):
+        raise RuntimeError("library built without lora_linear_forward")
+    dev = x.device
+    bf = torch.bfloat16
+    _req(x, "x", bf, dev)
+    _req(w, "w", bf, dev)
+    _req(token_lora_mapping, "token_lora_mapping", torch.int32, dev)
+    _req(lora_ranks, "lora_ranks", torch.int32, dev)
+    _req(scalings, "scalings", torch.float32, dev)
+    _req(lora_a, "lora_a", bf, dev)
+    _req(lora_b, "lora_b", bf, dev)
+    T, D_in = x.shape
+    D_out = w.shape[0]
+    L, S, R, _ = lora_a.shape
+    offs = (ctypes.c_int32 * (S + 1))(*[int(v) for v in slice_offsets])
+    if (len(slice_offsets) != S + 1 or tuple(w.shape) != (D_out, D_in) or tuple(lora_a.shape) != (L, S, R, D_in)
+            or tuple(lora_b.shape) != (L, D_out, R) or token_lora_mapping.numel() < T
+            or lora_ranks.numel() != L or scalings.numel() != L):
+        raise ValueError("lora_linear_forward: inconsistent shapes")
+    if y is None:
+        y = torch.empty(T, D_out, dtype=bf, device=dev)
+    _req(y, "y", bf, dev)
+    wsb = int(lib.lora_linear_workspace_bytes(T, D_in, D_out, L, R, S))
+    if wsb == 0 and T > 0:
+        raise ValueError("lora_linear_forward: unsupported sizes")
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    if check and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = lib.lora_linear_forward(
+        _ptr(x), _ptr(w), _ptr(token_lora_mapping), _ptr(lora_ranks), _ptr(scalings), _ptr(lora_a),
+        _ptr(lora_b), ctypes.cast(offs, ctypes.c_void_p), T, D_in, D_out, L, R, S, _ptr(y), _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream))
+    _check_host(code, "lora_linear_forward")
+    if check:
+        _check_device(status, "lora_linear_forward")
     return y

@@ -153,6 +153,7 @@ struct Params {
   int aw_mask;    // shrinks: bit j set if the wide LoRA A map with (16 << j)-row boxes exists
   int rmask;      // bit 0 / 1 / 2 set if the 128- / 256- / 192-row maps of the row operand exist
   int ykeep;      // down: 1 if y_acc fits in half of L2 (its reductions are then marked evict-last)
+  int zslice_blk; // down: 256-row blocks from this index on read the second rank slice of z (split B)
   int w3;         // gate_up: 1 if the gate+up weight map exists
   int64_t P;
   const float* topk_weights;
@@ -506,7 +507,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128;
             const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
                                              : (pl * p.E + it.e) * p.H + m0;
-            const int zc0 = ((KIND == kGateUp ? g * p.R16 : 0) + kg * 64) >> 3;
+            // z columns of this step: gate_up's gate / up half, or (down with a
+            // split B) the rank slice of the output block's part
+            const int zslice = (KIND == kDown && it.mb >= p.zslice_blk) ? p.R16 : 0;
+            const int zc0 = ((KIND == kGateUp ? g * p.R16 : zslice) + kg * 64) >> 3;
             for (int ch = 0; ch < nch;) {
               const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
               const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
@@ -610,7 +614,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const int pr = (n >= it.lo && n < it.hi) ? p.usorted[it.row0 + n] : (int)p.P;
         const bool real = pr >= 0 && pr < p.P;
         c.tok[il & 1][n] = real ? pr / p.K : -1;
-        c.w[il & 1][n] = real ? p.topk_weights[pr] : 0.f;
+        c.w[il & 1][n] = real ? (p.topk_weights ? p.topk_weights[pr] : 1.f) : 0.f;  // none: weight 1
       }
       // one thread waits for the accumulator; the decision is shared through
       // shared memory so that all 128 epilogue threads take the same branch
@@ -1242,6 +1246,86 @@ bool make_pair_row_maps(Maps& m, const void* base, uint64_t rows) {
   return true;
 }
 
+// Maps of the gate_up-shape shrink (two rank blocks per adapter): the row
+// operand `rows` (chunk-major [ceil(Kd/64)][cap][64]) and LoRA A as
+// [L, E, 2, R, Kd].  Returns the masks of the optional views it made.
+bool make_shrink2_maps(Maps& m, const void* rows, uint64_t cap, int Kd, const void* lora_a, int L, int E, int R,
+                       int* abox, int* a3, int* aw, int* rmask) {
+  const uint64_t kc = (uint64_t)ceil_div(Kd, 64);
+  *abox = *a3 = *aw = *rmask = 0;
+  bool ok = make_map(&m.m[kRows], rows, 64, kc * cap, 64, 64, true) && make_row_maps(m, rows, kc * cap, rmask) &&
+            // x rows as [chunk][row][64]: a box of 64 or 128 rows covers two K chunks
+            make_map3(&m.m[kX2x64], rows, 64, cap, kc, 128, cap * 128, 64, 64, 2, true) &&
+            make_map3(&m.m[kX2x128], rows, 64, cap, kc, 128, cap * 128, 64, 128, 2, true);
+  *rmask &= 1;  // shrink tiles hold at most 128 rows
+  if (!ok || L == 0) return ok;
+  for (int j = 0; ok && j < 3; ++j) {
+    const uint32_t rb = 16u << j;
+    if ((int)rb > R) continue;
+    // wide boxes: rb gate and rb up rank rows of two K chunks; exact only when
+    // Kd is a multiple of 64 (else the last chunk of the last row would run past
+    // the tensor)
+    if (Kd % 64 == 0) {
+      const uint64_t d[4] = {64, (uint64_t)R, (uint64_t)L * E * 2, (uint64_t)Kd / 64};
+      const uint64_t st[3] = {(uint64_t)Kd * 2, (uint64_t)R * Kd * 2, 128};
+      const uint32_t b[4] = {64, rb, 2, 2};
+      ok = make_map4(&m.m[kAW16 + j], lora_a, d, st, b);
+      *aw |= 1 << j;
+    }
+    // LoRA A as [(l, e, gate|up)][rank][k]: a box {64, rb, 2} holds rb gate and rb up rank rows
+    ok = ok && make_map3(&m.m[kA3x16 + j], lora_a, Kd, R, (uint64_t)L * E * 2, (uint64_t)Kd * 2,
+                         (uint64_t)R * Kd * 2, 64, rb, 2, true);
+    *a3 |= 1 << j;
+  }
+  return ok && make_abox_maps(m, lora_a, Kd, (uint64_t)L * E * 2 * R, abox);
+}
+
+// Maps of the down-shape shrink (one rank block per adapter): the row operand
+// and LoRA A as [L, E, R, Kd].
+bool make_shrink1_maps(Maps& m, const void* rows, uint64_t cap, int Kd, const void* lora_a, int L, int E, int R,
+                       int* abox, int* aw, int* rmask) {
+  const uint64_t kc = (uint64_t)ceil_div(Kd, 64);
+  *abox = *aw = *rmask = 0;
+  bool ok = make_map(&m.m[kRows], rows, 64, kc * cap, 64, 64, true) && make_row_maps(m, rows, kc * cap, rmask) &&
+            make_map3(&m.m[kX2x64], rows, 64, cap, kc, 128, cap * 128, 64, 64, 2, true) &&
+            make_map3(&m.m[kX2x128], rows, 64, cap, kc, 128, cap * 128, 64, 128, 2, true);
+  *rmask &= 1;
+  if (!ok || L == 0) return ok;
+  for (int j = 0; ok && j < 3; ++j) {
+    const uint32_t rb = 16u << j;
+    if ((int)rb > R || Kd % 64 != 0) continue;
+    ok = make_map3(&m.m[kAW16 + j], lora_a, 64, (uint64_t)L * E * R, (uint64_t)Kd / 64, (uint64_t)Kd * 2, 128, 64,
+                   rb, 2, true);
+    *aw |= 1 << j;
+  }
+  return ok && make_abox_maps(m, lora_a, Kd, (uint64_t)L * E * R, abox);
+}
+
+// Maps of the down-shape GEMM on CTA pairs: weights as [E * M rows][Kd], the
+// row operand (chunk-major, half-tile boxes of 32 / 64 / 96 / 128 rows), LoRA
+// B as [L, E, M, R] in rank chunks of 8, and z (chunk-major
+// [zchunks][zcap][8]) in half-piece boxes.
+bool make_down_maps(Maps& m, const void* w, int M, int Kd, int E, const void* rows, uint64_t cap,
+                    const void* lora_b, int L, int R, const void* z, uint64_t zcap, int zchunks) {
+  const uint64_t kc = (uint64_t)ceil_div(Kd, 64);
+  bool ok = make_map(&m.m[kW], w, Kd, (uint64_t)E * M, 64, 128, true) &&
+            make_map(&m.m[kRows], rows, 64, kc * cap, 64, 64, true) && make_pair_row_maps(m, rows, kc * cap);
+  if (!ok || L == 0) return ok;
+  const int nc[3] = {8, 4, 2};
+  const int bslot[3] = {kB8, kB4, kB2}, zslot[3] = {kZ8, kZ4, kZ2}, zsslot[3] = {kZ8s, kZ4s, kZ2s};
+  for (int j = 0; ok && j < 3; ++j) {
+    if (nc[j] > R / 8) continue;  // a box may not span more rank chunks than exist
+    ok = make_map3(&m.m[bslot[j]], lora_b, 8, (uint64_t)L * E * M, (uint64_t)R / 8, (uint64_t)R * 2, 16, 8, 128,
+                   nc[j]) &&
+         make_map3(&m.m[zslot[j]], z, 8, zcap, (uint64_t)zchunks, 16, zcap * 16, 8, 128, nc[j]) &&
+         make_map3(&m.m[zsslot[j]], z, 8, zcap, (uint64_t)zchunks, 16, zcap * 16, 8, 64, nc[j]);
+  }
+  return ok;
+}
+
+// Bit 0 / 1: the 8- / 4-chunk LoRA B and z views exist (they need R / 8 chunks).
+int b_view_mask(int R) { return (R / 8 >= 8 ? 1 : 0) | (R / 8 >= 4 ? 2 : 0); }
+
 constexpr int kMaxForwardBuckets = 16384;  // E * (L + 1): the plan keeps two scans of it in shared memory
 
 struct FwdLayout {
@@ -1454,82 +1538,34 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
 
   // tensor maps
   Maps m_sgu{}, m_gu{}, m_sd{}, m_dn{};
-  int abox_gu = 0, abox_d = 0, bmask = 0, a3_gu = 0, w3 = 0, aw_gu = 0, aw_d = 0;
+  int abox_gu = 0, abox_d = 0, a3_gu = 0, w3 = 0, aw_gu = 0, aw_d = 0;
   int rm_sgu = 0, rm_gu = 0, rm_sd = 0, rm_dn = 0;
+  const int bmask = L > 0 ? b_view_mask(R) : 0;
   const uint64_t cap = (uint64_t)f.cap, zcap = (uint64_t)f.zcap;
-  const uint64_t hk = (uint64_t)ceil_div(H, 64), ik = (uint64_t)ceil_div(I, 64);
+  const uint64_t hk = (uint64_t)ceil_div(H, 64);
   const uint32_t zrows = (uint32_t)(f.zcap < 256 ? f.zcap : 256);
   bool ok = make_map(&m_gu.m[kW], w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
-            make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
-            make_map(&m_sgu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
-            make_map(&m_sd.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
-            make_map(&m_dn.m[kW], w_down, I, (uint64_t)E * H, 64, 128, true) &&
-            make_map(&m_dn.m[kRows], hbuf, 64, ik * cap, 64, 64, true) &&
-            make_row_maps(m_gu, xs, hk * cap, &rm_gu) && make_row_maps(m_sgu, xs, hk * cap, &rm_sgu) &&
-            make_row_maps(m_sd, hbuf, ik * cap, &rm_sd) && make_pair_row_maps(m_dn, hbuf, ik * cap);
-  rm_sgu &= 1;  // shrink tiles hold at most 128 rows
-  rm_sd &= 1;
+            make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) && make_row_maps(m_gu, xs, hk * cap, &rm_gu) &&
+            make_shrink2_maps(m_sgu, xs, cap, H, lora_a_gu, L, E, R, &abox_gu, &a3_gu, &aw_gu, &rm_sgu) &&
+            make_shrink1_maps(m_sd, hbuf, cap, I, lora_a_down, L, E, R, &abox_d, &aw_d, &rm_sd) &&
+            make_down_maps(m_dn, w_down, H, I, E, hbuf, cap, lora_b_down, L, R, zd, zcap, f.R16 / 8);
   if (ok && I >= 128) {
     // W_gate_up as [(e, gate|up)][row][k]: a box {64, 128, 2} is a 128-row block of gate and of up
     ok = make_map3(&m_gu.m[kW3], w_gate_up, H, I, (uint64_t)E * 2, (uint64_t)H * 2, (uint64_t)I * H * 2, 64, 128, 2,
                    true);
     w3 = 1;
   }
-  // shrinks: x_sorted / h as [chunk][row][64]; a box of 64 or 128 rows covers two K chunks
-  ok = ok && make_map3(&m_sgu.m[kX2x64], xs, 64, cap, hk, 128, cap * 128, 64, 64, 2, true) &&
-       make_map3(&m_sgu.m[kX2x128], xs, 64, cap, hk, 128, cap * 128, 64, 128, 2, true) &&
-       make_map3(&m_sd.m[kX2x64], hbuf, 64, cap, ik, 128, cap * 128, 64, 64, 2, true) &&
-       make_map3(&m_sd.m[kX2x128], hbuf, 64, cap, ik, 128, cap * 128, 64, 128, 2, true);
   if (ok && L > 0) {
-    // wide LoRA A boxes: rb rank rows (gate and up for A_gu) of two K chunks.  The
-    // chunked views are exact only when K is a multiple of 64 (else the last
-    // chunk of the last row would run past the tensor), so otherwise none.
-    for (int j = 0; ok && j < 3; ++j) {
-      const uint32_t rb = 16u << j;
-      if ((int)rb > R) continue;
-      if (H % 64 == 0) {
-        const uint64_t d[4] = {64, (uint64_t)R, (uint64_t)L * E * 2, (uint64_t)H / 64};
-        const uint64_t st[3] = {(uint64_t)H * 2, (uint64_t)R * H * 2, 128};
-        const uint32_t b[4] = {64, rb, 2, 2};
-        ok = make_map4(&m_sgu.m[kAW16 + j], lora_a_gu, d, st, b);
-        aw_gu |= 1 << j;
-      }
-      if (ok && I % 64 == 0) {
-        ok = make_map3(&m_sd.m[kAW16 + j], lora_a_down, 64, (uint64_t)L * E * R, (uint64_t)I / 64, (uint64_t)I * 2,
-                       128, 64, rb, 2, true);
-        aw_d |= 1 << j;
-      }
-    }
-  }
-  if (ok && L > 0) {
-    // LoRA A_gu as [(l, e, gate|up)][rank][k]: a box {64, rb, 2} holds rb gate and rb up rank rows
-    for (int j = 0; ok && j < 3; ++j) {
-      const int rb = 16 << j;
-      if (rb > R) continue;
-      ok = make_map3(&m_sgu.m[kA3x16 + j], lora_a_gu, H, R, (uint64_t)L * E * 2, (uint64_t)H * 2,
-                     (uint64_t)R * H * 2, 64, rb, 2, true);
-      a3_gu |= 1 << j;
-    }
-  }
-  if (ok && L > 0) {
-    ok = make_abox_maps(m_sgu, lora_a_gu, H, (uint64_t)L * E * 2 * R, &abox_gu) &&
-         make_abox_maps(m_sd, lora_a_down, I, (uint64_t)L * E * R, &abox_d);
+    // gate_up expand: LoRA B stacks as [rank chunk][row][8] (each row's ranks are
+    // contiguous) and chunk-major z [column/8][zcap][8]
     const int nc[3] = {8, 4, 2};
     const int bslot[3] = {kB8, kB4, kB2}, zslot[3] = {kZ8, kZ4, kZ2}, zsslot[3] = {kZ8s, kZ4s, kZ2s};
     for (int j = 0; ok && j < 3; ++j) {
       if (nc[j] > R / 8) continue;  // a box may not span more rank chunks than exist
-      if (j < 2) bmask |= 1 << j;
-      // LoRA B stacks as [rank chunk][row][8]: each row's ranks are contiguous
       ok = make_map3(&m_gu.m[bslot[j]], lora_b_gu, 8, (uint64_t)L * E * 2 * I, (uint64_t)R / 8, (uint64_t)R * 2, 16,
                      8, 128, nc[j]) &&
-           make_map3(&m_dn.m[bslot[j]], lora_b_down, 8, (uint64_t)L * E * H, (uint64_t)R / 8, (uint64_t)R * 2, 16,
-                     8, 128, nc[j]) &&
-           // chunk-major z: [column/8][zcap][8]
            make_map3(&m_gu.m[zslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
-           // down (CTA pairs): half a piece's z rows, 128-row boxes
-           make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, 128, nc[j]) &&
-           make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]) &&
-           make_map3(&m_dn.m[zsslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
+           make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
     }
   }
   if (!ok) return MLR_ERR_CUDA;
@@ -1602,6 +1638,7 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   p.pieces = pieces;
   p.shrink_tiles = shrink_tiles;
   p.zgu = zgu; p.h = hbuf; p.zd = zd; p.yacc = yacc;
+  p.zslice_blk = INT32_MAX;
   p.status = d_status;
 
   if (L > 0) {
@@ -1639,6 +1676,191 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * H;
+  convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
+  MLR_CHECK_LAUNCH();
+  note_launch();
+  prof_mark(prof, 6, stream);
+  return MLR_OK;
+}
+
+// ------------------------------------------------------------------------
+// Dense projection with per-segment LoRA and split B (the MLA fused
+// q_a_proj + kv_a_proj projection): the same machinery as one expert with
+// top-1 routing.  Tokens are ordered by adapter, gathered, shrunk per adapter
+// bucket (one or two rank blocks), then one GEMM on CTA pairs computes
+// W x + s B z per output block, reading the rank block of the block's part.
+// ------------------------------------------------------------------------
+namespace mlr {
+namespace {
+
+// Workspace of the projection: the forward's layout for one expert, top-1,
+// with the wider of D_in / D_out as its hidden size (x_sorted and y_acc) and
+// the smallest intermediate size.
+FwdLayout lin_layout(int32_t T, int32_t D_in, int32_t D_out, int32_t L, int32_t R, int32_t S) {
+  FwdLayout f{};
+  f.ok = false;
+  if (T < 0 || D_in < 128 || D_out < 128 || D_in % 8 || D_out % 8 || (S != 1 && S != 2)) return f;
+  return fwd_layout(T, 1, 1, D_in > D_out ? D_in : D_out, 64, L, R);
+}
+
+}  // namespace
+}  // namespace mlr
+
+extern "C" size_t lora_linear_workspace_bytes(int32_t num_tokens, int32_t in_features, int32_t out_features,
+                                              int32_t num_loras, int32_t max_rank, int32_t num_slices) {
+  const mlr::FwdLayout f = mlr::lin_layout(num_tokens, in_features, out_features, num_loras, max_rank, num_slices);
+  return f.ok ? (size_t)f.total : 0;
+}
+
+extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const int32_t* token_lora_mapping,
+                                   const int32_t* lora_ranks, const float* scalings, const mlr_bf16* lora_a,
+                                   const mlr_bf16* lora_b, const int32_t* slice_offsets, int32_t T, int32_t D_in,
+                                   int32_t D_out, int32_t L, int32_t R, int32_t S, mlr_bf16* y, void* workspace,
+                                   size_t ws_bytes, int32_t* d_status, void* stream_) {
+  using namespace mlr;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (slice_offsets == nullptr || (S != 1 && S != 2)) return MLR_ERR_INVALID;
+  // parts: 0 = offsets[0] < offsets[1] < ... = D_out; the second part starts on
+  // a 256-row block (one output block of a CTA pair)
+  if (slice_offsets[0] != 0 || slice_offsets[S] != D_out) return MLR_ERR_INVALID;
+  if (S == 2 && (slice_offsets[1] <= 0 || slice_offsets[1] >= D_out || slice_offsets[1] % 256 != 0))
+    return MLR_ERR_INVALID;
+  const FwdLayout f = lin_layout(T, D_in, D_out, L, R, S);
+  if (!f.ok) {
+    if (T < 0 || L < 0 || R < 0) return MLR_ERR_INVALID;
+    return MLR_ERR_UNSUPPORTED;
+  }
+  if (T == 0) return MLR_OK;
+  const void* need[] = {x, w, token_lora_mapping, y};
+  for (const void* q : need)
+    if (q == nullptr) return MLR_ERR_INVALID;
+  if (L > 0 && (lora_ranks == nullptr || scalings == nullptr || lora_a == nullptr || lora_b == nullptr))
+    return MLR_ERR_INVALID;
+  const void* aligned[] = {x, w, lora_a, lora_b, y};
+  for (const void* q : aligned)
+    if ((reinterpret_cast<uintptr_t>(q) & 15) != 0) return MLR_ERR_INVALID;
+  if (workspace == nullptr || ws_bytes < (size_t)f.total) return MLR_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLR_ERR_INVALID;
+
+  char* ws = static_cast<char*>(workspace);
+  char* aws = ws + f.o_align;
+  TileRec* base_tiles = reinterpret_cast<TileRec*>(ws + f.o_base);
+  ShrinkRec* shrink_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_shrink);
+  ShrinkRec* gemv_tiles = reinterpret_cast<ShrinkRec*>(ws + f.o_gemv);
+  int4* pieces = reinterpret_cast<int4*>(ws + f.o_pieces);
+  uint32_t* ustart = reinterpret_cast<uint32_t*>(ws + f.o_ustart);
+  int32_t* usorted = reinterpret_cast<int32_t*>(ws + f.o_usorted);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + f.o_counts);
+  uint16_t* z = reinterpret_cast<uint16_t*>(ws + (S == 2 ? f.o_zgu : f.o_zd));
+  float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
+  const uint32_t* btotal = reinterpret_cast<const uint32_t*>(aws + f.al.btotal_off);
+
+  // tensor maps: the shrink (two rank blocks = the gate_up-shape shrink with
+  // the parts as gate and up; one block = the down-shape shrink) and the
+  // projection on CTA pairs
+  Maps m_s{}, m_p{};
+  int abox = 0, a3 = 0, aw = 0, rm = 0;
+  const uint64_t cap = (uint64_t)f.cap, zcap = (uint64_t)f.zcap;
+  bool ok = S == 2 ? make_shrink2_maps(m_s, xs, cap, D_in, lora_a, L, 1, R, &abox, &a3, &aw, &rm)
+                   : make_shrink1_maps(m_s, xs, cap, D_in, lora_a, L, 1, R, &abox, &aw, &rm);
+  ok = ok && make_down_maps(m_p, w, D_out, D_in, 1, xs, cap, lora_b, L, R, z, zcap, S * f.R16 / 8);
+  if (!ok) return MLR_ERR_CUDA;
+
+  const int prof = prof_call_begin(stream);
+  int rc = MLR_OK;
+  const int64_t nb_nonempty = f.al.P < f.al.NB ? f.al.P : f.al.NB;
+  const int gemv_rows = (L > 0 && f.al.P < 8 * nb_nonempty) ? kGemvRows : 0;
+  const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
+  int32_t* zeros_ids = reinterpret_cast<int32_t*>(ws + f.o_h);  // expert id 0 of every token
+  if (cudaMemsetAsync(zeros_ids, 0, (size_t)T * 4, stream) != cudaSuccess) return MLR_ERR_CUDA;
+  if (align_block_ok(f.al)) {
+    const size_t zs_off = align_block_smem(f.al), sm = zs_off + scan_bytes;
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+      return MLR_ERR_CUDA;
+    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(zeros_ids, token_lora_mapping, (int)f.al.P, 1, 1, L, R,
+                                                       lora_ranks, usorted, ustart, base_tiles, pieces,
+                                                       shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
+                                                       gemv_rows, 0);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+  } else {
+    if ((rc = align_dense_count(f.al, zeros_ids, token_lora_mapping, 1, 1, L, aws, d_status, stream)) != MLR_OK)
+      return rc;
+    const size_t sm = 2 * scan_bytes;
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+      return MLR_ERR_CUDA;
+    plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, 1, f.C, R, ustart, base_tiles, pieces,
+                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows, 0);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+    if ((rc = align_dense_scatter(f.al, zeros_ids, token_lora_mapping, 1, 1, L, aws, ustart, usorted, stream)) !=
+        MLR_OK)
+      return rc;
+  }
+  prof_mark(prof, 0, stream);
+  {
+    const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
+    const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
+    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, 1, D_in, f.cap, xs, yacc,
+                                                         (int64_t)T * D_out / 4);
+    MLR_CHECK_LAUNCH();
+    note_launch();
+  }
+  prof_mark(prof, 1, stream);
+
+  Params p{};
+  p.T = T; p.K = 1; p.E = 1; p.L = L; p.R = R; p.R16 = f.R16; p.C = f.C;
+  p.cap = (int)f.cap;
+  p.zcap = (int)f.zcap;
+  p.zrows = (int)(f.zcap < 256 ? f.zcap : 256);
+  p.zshort = p.zrows >= 64 ? 1 : 0;
+  p.bmask = L > 0 ? b_view_mask(R) : 0;
+  p.P = T;
+  p.topk_weights = nullptr;  // weight 1 for every token
+  p.lora_ranks = lora_ranks;
+  p.scalings = scalings;
+  p.usorted = usorted;
+  p.base_tiles = base_tiles;
+  p.pieces = pieces;
+  p.shrink_tiles = shrink_tiles;
+  p.yacc = yacc;
+  p.status = d_status;
+  p.zslice_blk = S == 2 ? slice_offsets[1] / 256 : INT32_MAX;
+  if (L > 0) {
+    Params q = p;
+    q.n_tiles = counts + 1; q.abox_mask = abox; q.aw_mask = aw; q.rmask = rm;
+    if (S == 2) {
+      // the parts' A blocks stand where gate_up's gate and up blocks stand
+      q.H = D_in; q.nblk = f.mtiles_gu; q.a3_mask = a3; q.zgu = z;
+      if (gemv_rows > 0 &&
+          (rc = launch_gemv<2>(gemv_tiles, counts + 2, f.max_gemv, lora_a, xs, D_in, f, 1, R, lora_ranks,
+                               scalings, z, stream)) != MLR_OK)
+        return rc;
+      if ((rc = launch_gemm<kShrinkGU>(m_s, q, f.max_shrink, stream)) != MLR_OK) return rc;
+    } else {
+      q.I = D_in; q.nblk = f.mtiles_d; q.zd = z;
+      if (gemv_rows > 0 &&
+          (rc = launch_gemv<1>(gemv_tiles, counts + 2, f.max_gemv, lora_a, xs, D_in, f, 1, R, lora_ranks,
+                               scalings, z, stream)) != MLR_OK)
+        return rc;
+      if ((rc = launch_gemm<kShrinkD>(m_s, q, f.max_shrink, stream)) != MLR_OK) return rc;
+    }
+  }
+  prof_mark(prof, 2, stream);
+  prof_mark(prof, 3, stream);
+  prof_mark(prof, 4, stream);
+  {
+    Params q = p;
+    q.H = D_out; q.I = D_in;  // output rows and K of the down-shape GEMM
+    q.n_tiles = counts; q.nblk = (int)ceil_div(D_out, 256);
+    q.ykeep = (int64_t)T * D_out * 4 <= ((int64_t)64 << 20) ? 1 : 0;
+    if ((rc = launch_gemm<kDown>(m_p, q, f.max_base, stream)) != MLR_OK) return rc;
+  }
+  prof_mark(prof, 5, stream);
+  const int64_t n = (int64_t)T * D_out;
   convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
   MLR_CHECK_LAUNCH();
   note_launch();

@@ -99,6 +99,29 @@ def test_forward_host_checks(lib):
     assert f(*args) == mlr.MLR_ERR_UNSUPPORTED
 
 
+def test_linear_host_checks(lib):
+    ws = lib.lora_linear_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(8192, 7168, 2112, 4, 64, 2) > 0           # the MLA fused projection
+    assert ws(64, 120, 256, 2, 16, 1) == 0              # D_in below 128
+    assert ws(64, 256, 256, 2, 24, 1) == 0              # R not a multiple of 16
+    assert ws(64, 256, 256, 2, 16, 3) == 0              # more than two parts
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the calls return before any launch
+    f = lib.lora_linear_forward
+    f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int32] * 6 + [ctypes.c_void_p, ctypes.c_void_p,
+                                                               ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+
+    def call(offsets, D_out=512, S=2):
+        offs = (ctypes.c_int32 * len(offsets))(*offsets)
+        return f(fake, fake, fake, fake, fake, fake, fake, ctypes.cast(offs, ctypes.c_void_p), 64, 256, D_out, 2, 16,
+                 S, fake, fake, ctypes.c_size_t(1 << 30), None, None)
+
+    assert call([0, 200, 512]) == mlr.MLR_ERR_INVALID   # second part not on a 256-row block
+    assert call([0, 256, 500]) == mlr.MLR_ERR_INVALID   # last offset is not D_out
+    assert call([0, 512, 512]) == mlr.MLR_ERR_INVALID   # empty second part
+    assert call([0, 512], S=1, D_out=510) == mlr.MLR_ERR_INVALID
+
+
 def test_status_strings(lib):
     assert b"under-covers" in lib.moe_lora_status_string(mlr.MLR_ERR_UNDERCOVERED)
     assert lib.moe_lora_status_string(0) == b"ok"
