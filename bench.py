@@ -423,6 +423,238 @@ def run_ours(args, rank, world, dist):
     return line
 
 
+# --------------------------------------- dense projection with split-B LoRA --
+# The MLA fused q_a_proj + kv_a_proj projection of a DeepSeek-V3-like prefill
+# batch: hidden 7168 -> 1536 + 576 output rows in two parts, 4 adapter slots.
+LINEAR_CONFIGS = {
+    "mla_fused_proj": {"tokens": 8192, "in": 7168, "offsets": (0, 1536, 2112), "loras": 4, "max_rank": 64,
+                       "ranks": (16, 32, 64, 64), "segments": 8},
+}
+LINEAR_METRIC = "MLA fused-projection LoRA tokens/s and % of roofline (bf16, 1×GB300)"
+
+
+def make_linear_inputs(cfg, device, seed):
+    import torch
+    g = torch.Generator(device=device).manual_seed(seed)
+    gc = torch.Generator().manual_seed(seed)
+    T, D_in, offs, L, R = cfg["tokens"], cfg["in"], cfg["offsets"], cfg["loras"], cfg["max_rank"]
+    D_out, S = offs[-1], len(offs) - 1
+    bf = torch.bfloat16
+    x = torch.randn(T, D_in, generator=g, device=device, dtype=bf)
+    w = torch.randn(D_out, D_in, generator=g, device=device, dtype=bf).mul_(D_in ** -0.5)
+    a = torch.randn(L, S, R, D_in, generator=g, device=device, dtype=bf).mul_(D_in ** -0.5)
+    b = torch.randn(L, D_out, R, generator=g, device=device, dtype=bf).mul_(R ** -0.5)
+    ranks = torch.tensor(cfg["ranks"], dtype=torch.int32, device=device)
+    scal = torch.full((L,), 2.0, dtype=torch.float32, device=device)
+    seg = T // cfg["segments"]
+    adapters = torch.randint(0, L, (cfg["segments"],), generator=gc)
+    mapping = adapters.repeat_interleave(seg).to(torch.int32).to(device)
+    return x, w, a, b, ranks, scal, mapping, list(offs)
+
+
+def linear_work(cfg, ranks_np, mapping_np):
+    """(flops, algorithmic bytes) of one projection call: base GEMM, shrink and
+    expand per token, the weights, every used adapter's factors, x and y."""
+    import numpy as np
+    T, D_in, offs, R = cfg["tokens"], cfg["in"], cfg["offsets"], cfg["max_rank"]
+    D_out, S = offs[-1], len(offs) - 1
+    r_tok = np.where(mapping_np >= 0, ranks_np[np.clip(mapping_np, 0, None)], 0).astype(np.float64)
+    flops = 2.0 * T * D_out * D_in + float((2.0 * S * D_in + 2.0 * D_out) * r_tok.sum())
+    used = np.unique(mapping_np[mapping_np >= 0])
+    lora_bytes = float(sum((S * D_in + D_out) * int(ranks_np[l]) * 2 for l in used))
+    byts = 2.0 * D_out * D_in + lora_bytes + 2.0 * T * D_in + 2.0 * T * D_out + 4.0 * T
+    return flops, byts
+
+
+def linear_oracle_rate(x, w, a, b, ranks, scal, mapping_np, offs, target_s, seed=0, max_tokens=None):
+    import numpy as np
+    import torch
+
+    import oracle
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    xb, wb, ab, bb = bits(x), bits(w), bits(a), bits(b)
+    rk, sc = ranks.cpu().numpy(), scal.cpu().numpy()
+    T = x.shape[0]
+    rng = np.random.default_rng(seed)
+    n0 = min(T, 8)
+    t0 = time.perf_counter()
+    oracle.lora_linear(xb, mapping_np, rk, sc, wb, ab, bb, offs, tokens=rng.choice(T, n0, replace=False))
+    per_tok = (time.perf_counter() - t0) / n0
+    n = int(max(n0, min(T, target_s / max(per_tok, 1e-9))))
+    if max_tokens:
+        n = min(n, max_tokens)
+    toks = np.sort(rng.choice(T, n, replace=False))
+    t0 = time.perf_counter()
+    st, _ = oracle.lora_linear(xb, mapping_np, rk, sc, wb, ab, bb, offs, tokens=toks)
+    secs = time.perf_counter() - t0
+    assert st == 0
+    return n / secs, n, secs, oracle.max_threads()
+
+
+def linear_config_entry(cfg, args, world):
+    return {"workload": args.config, "tokens": cfg["tokens"], "in_features": cfg["in"],
+            "out_parts": list(cfg["offsets"]), "loras": cfg["loras"], "max_rank": cfg["max_rank"],
+            "seed": args.seed, "parallelism": f"dp{world} (replicas)" if world > 1 else "single GPU"}
+
+
+def run_linear_reference(args, rank, world):
+    """The oracle's dense projection as it stands, timed on host cores (rank 0 only)."""
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    cfg = LINEAR_CONFIGS[args.config]
+    x, w, a, b, ranks, scal, mapping, offs = make_linear_inputs(cfg, "cpu", args.seed)
+    mp = mapping.numpy()
+    per_step_target = max(0.25, 90.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        linear_oracle_rate(x, w, a, b, ranks, scal, mp, offs, per_step_target, seed=1000 + i, max_tokens=args.ref_tokens)
+    ns, secs, thr = 0, 0.0, 1
+    for i in range(args.steps):
+        r, n, s_, thr = linear_oracle_rate(x, w, a, b, ranks, scal, mp, offs, per_step_target, seed=i,
+                                           max_tokens=args.ref_tokens)
+        ns += n
+        secs += s_
+    value = ns / secs
+    return {"impl": "reference", "metric": LINEAR_METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": linear_config_entry(cfg, args, world),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{ns} tokens over {args.steps} steps (seeded samples of the "
+                                       f"{cfg['tokens']}-token batch), fp64 C oracle, OpenMP over tokens"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_linear(args, rank, world, dist):
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import lora_moe_expert_info_gb300 as mlr
+    import oracle
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = mlr.library()
+    cfg = LINEAR_CONFIGS[args.config]
+    x, w, a, b, ranks, scal, mapping, offs = make_linear_inputs(cfg, dev, args.seed + rank)
+    T, D_in, D_out, L, R, S = cfg["tokens"], cfg["in"], offs[-1], cfg["loras"], cfg["max_rank"], len(offs) - 1
+    y = torch.empty(T, D_out, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(int(lib.lora_linear_workspace_bytes(T, D_in, D_out, L, R, S)), dtype=torch.uint8, device=dev)
+
+    def step():
+        mlr.lora_linear_forward(x, w, mapping, ranks, scal, a, b, offs, y=y, workspace=ws, check=False)
+
+    # correctness gate before timing: status word and a sampled oracle check
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    mlr.lora_linear_forward(x, w, mapping, ranks, scal, a, b, offs, y=y, workspace=ws, status=status)
+    mp_np = mapping.cpu().numpy()
+    toks = np.sort(np.random.default_rng(7).choice(T, 16, replace=False))
+    bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    st, yref = oracle.lora_linear(bits(x), mp_np, ranks.cpu().numpy(), scal.cpu().numpy(), bits(w), bits(a),
+                                  bits(b), offs, tokens=toks)
+    yg = y.float().cpu().numpy()[toks]
+    if st != 0 or (np.abs(yg - yref) - (2e-2 + 2e-2 * np.abs(yref))).max() > 0:
+        raise RuntimeError("projection differs from the oracle on the sampled tokens")
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    if dist is not None:
+        dist.barrier()
+    n_launch0 = lib.moe_lora_launch_count()
+    lib.moe_lora_profile_begin(min(args.steps, 4096))
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    stage_ms = (ctypes.c_double * 16)()
+    n_st, n_calls = ctypes.c_int32(0), ctypes.c_int32(0)
+    lib.moe_lora_profile_end(stage_ms, 16, ctypes.byref(n_st), ctypes.byref(n_calls))
+    n_launch = lib.moe_lora_launch_count() - n_launch0
+    ms_max = reduce_max(e0.elapsed_time(e1), dist, dev)
+    stages = {lib.moe_lora_profile_stage_name(i).decode(): stage_ms[i] / max(1, n_calls.value)
+              for i in range(n_st.value)}
+
+    # end to end through the public API from pinned host buffers
+    host_in = {"x": x.cpu().pin_memory(), "mapping": mapping.cpu().pin_memory(),
+               "ranks": ranks.cpu().pin_memory(), "scal": scal.cpu().pin_memory()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    y_host = torch.empty(T, D_out, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        mlr.lora_linear_forward(dev_in["x"], w, dev_in["mapping"], dev_in["ranks"], dev_in["scal"], a, b, offs,
+                                y=y, workspace=ws, check=False)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 200))
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(f0.elapsed_time(f1) / e2e_steps, dist, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"projection reported device status {int(status.item())}")
+    if rank != 0:
+        return None
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        oracle.build()
+        rate, n, secs, thr = linear_oracle_rate(x, w, a, b, ranks, scal, mp_np, offs, args.cpu_seconds)
+        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": f"{n} seeded tokens of the {T}-token batch ({secs:.1f} s), fp64 C oracle, "
+                         f"OpenMP over tokens"}
+    peaks, peak_src = load_peaks()
+    ms_step = ms_max / args.steps
+    flops, byts = linear_work(cfg, ranks.cpu().numpy(), mp_np)
+    # the projection GEMM (profile stage "down") carries the base GEMM and the expand
+    proj_ms = stages.get("down", ms_step)
+    r_tok = np.where(mp_np >= 0, ranks.cpu().numpy()[np.clip(mp_np, 0, None)], 0).astype(np.float64)
+    proj_flops = 2.0 * T * D_out * D_in + float(2.0 * D_out * r_tok.sum())
+    proj_bytes = 2.0 * D_out * D_in + 2.0 * T * D_in + 4.0 * T * D_out
+    rf = roofline_entry(proj_flops, proj_bytes, proj_ms, peaks, "bf16_tflops_sustained")
+    rf.update({"kernel": "moe_gemm_kernel<3>", "stage": "down (the projection GEMM)",
+               "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+               "traffic": recorded_traffic("down", args.config), "algorithmic_bytes": int(proj_bytes),
+               "algorithmic_flops": int(proj_flops), "launch_ms": round(proj_ms, 4)})
+    layer = roofline_entry(flops, byts, ms_step, peaks, "bf16_tflops_sustained")
+    layer.update({"algorithmic_bytes": int(byts), "algorithmic_flops": int(flops)})
+    return {"metric": LINEAR_METRIC, "value": round(weak_scaling_rate(T, world, ms_step), 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": linear_config_entry(cfg, args, world),
+            "roofline": rf, "layer_roofline": layer,
+            "stages_ms": {k: round(v, 4) for k, v in stages.items() if v > 0},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": int(n_launch), "clocks": clk.summary()}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,10 +679,11 @@ def main(argv=None):
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl")
         dist = tdist
+    linear = args.config in LINEAR_CONFIGS
     if args.impl == "reference":
-        line = run_reference(args, rank, world)
+        line = run_linear_reference(args, rank, world) if linear else run_reference(args, rank, world)
     else:
-        line = run_ours(args, rank, world, dist)
+        line = run_linear(args, rank, world, dist) if linear else run_ours(args, rank, world, dist)
     if line is not None and rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -48,6 +48,8 @@ namespace {
 
 constexpr int kBlock = 16;        // internal align block = MMA N granularity
 constexpr int kTileRows = 256;    // max sorted rows per tile (MMA N)
+constexpr int kPlanBigTiles = 8;   // experts with at least this many tiles are planned by the whole block
+constexpr int kPlanBigQueue = 64;  // ... up to this many such experts (the rest by their owner thread)
 constexpr int kInlinePieces = 30;  // LoRA pieces stored inside a base-tile record
 constexpr int kEpiWarp0 = 5;
 constexpr int kMaxThreads = 416;  // up to 13 warps (warps 1-3 idle)
@@ -809,6 +811,10 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
                            int32_t* __restrict__ counts, int32_t* status, int gemv_rows, int by_span) {
   const int NB = E * C;
   int bad = 0;
+  // experts with many tiles, planned by the whole block at the end
+  __shared__ int big_n;
+  __shared__ int4 big_q[kPlanBigQueue];
+  if (threadIdx.x == 0) big_n = 0;
   // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
   for (int b = threadIdx.x; b < NB; b += kPlanThreads) {
     ustart_out[b] = us[b];
@@ -829,6 +835,31 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
     if (cl == 0) return 0;
     const int r = lora_ranks[cl - 1];
     return (r > 0 && r <= R) ? (r + 15) & ~15 : 0;
+  };
+  // tile k of expert e (tiles of ts rows from r0 over span rows) at slot
+  // `slot`, its pieces at pieces[poff ..]; returns the number of pieces
+  auto write_tile = [&](int e, int k, int slot, int poff, int r0, int span, int ts) -> int {
+    const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
+    const int row0 = r0 + k * ts;
+    const int N = min(ts, r0 + span - row0);
+    TileRec& rec = base_tiles[slot];
+    int np = 0, nexp_gu = 0, nexp_d = 0;
+    for (int b = e * C + 1; b < (e + 1) * C; ++b) {
+      const int r16 = rank16(b);
+      if (r16 == 0 || us[b + 1] == us[b]) continue;
+      const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
+      const int a0 = max(z0, row0), a1 = min(z1, row0 + N);
+      if (a1 <= a0) continue;
+      const int4 pc = make_int4((a0 - row0) | ((a1 - a0) << 16), b % C - 1, r16, (int)zs[b] + (a0 - z0));
+      pieces[poff + np] = pc;
+      if (np < kInlinePieces) rec.pc[np] = pc;
+      ++np;
+      nexp_gu += 2 * ((r16 + 63) >> 6);
+      nexp_d += (r16 + 63) >> 6;
+    }
+    rec.head = make_int4(e, row0, N, poff);
+    rec.info = make_int4(max(ue0, row0) - row0, min(ue1, row0 + N) - row0, np, nexp_gu | (nexp_d << 16));
+    return np;
   };
   // ---- base tiles: per expert, equal tiles of <= 256 rows from floor16(first row) ----
   {
@@ -894,28 +925,20 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
         const int cls = span_class(span);
         toff = cls_base[cls] + atomicAdd(&cls_fill[cls], nt);
       }
-      for (int k = 0; k < nt; ++k) {
-        const int row0 = r0 + k * ts;
-        const int N = min(ts, r0 + span - row0);
-        TileRec& rec = base_tiles[toff++];
-        int np = 0, nexp_gu = 0, nexp_d = 0;
-        for (int b = e * C + 1; b < (e + 1) * C; ++b) {
-          const int r16 = rank16(b);
-          if (r16 == 0 || us[b + 1] == us[b]) continue;
-          const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
-          const int a0 = max(z0, row0), a1 = min(z1, row0 + N);
-          if (a1 <= a0) continue;
-          const int4 pc = make_int4((a0 - row0) | ((a1 - a0) << 16), b % C - 1, r16, (int)zs[b] + (a0 - z0));
-          pieces[poff + np] = pc;
-          if (np < kInlinePieces) rec.pc[np] = pc;
-          ++np;
-          nexp_gu += 2 * ((r16 + 63) >> 6);
-          nexp_d += (r16 + 63) >> 6;
+      if (nt >= kPlanBigTiles) {
+        // many tiles: queued for the whole block (below); its pieces start at poff
+        const int q = atomicAdd(&big_n, 1);
+        if (q < kPlanBigQueue) {
+          big_q[q] = make_int4(e, toff, poff, 0);
+          for (int b = e * C + 1; b < (e + 1) * C; ++b) {
+            if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+            const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
+            poff += (z1 - 1 - r0) / ts - (z0 - r0) / ts + 1;  // tiles it meets
+          }
+          continue;
         }
-        rec.head = make_int4(e, row0, N, poff);
-        rec.info = make_int4(max(ue0, row0) - row0, min(ue1, row0 + N) - row0, np, nexp_gu | (nexp_d << 16));
-        poff += np;
       }
+      for (int k = 0; k < nt; ++k) poff += write_tile(e, k, toff + k, poff, r0, span, ts);
     }
     if (threadIdx.x == 0) counts[0] = total_t;
   }
@@ -951,6 +974,30 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
     if (threadIdx.x == 0) {
       counts[1] = total;
       counts[2] = total_g;
+    }
+  }
+  {
+    // Experts with many tiles: every thread takes tiles of the queued experts.
+    // Tile k's pieces start after the pieces of tiles 0..k-1, which is, for
+    // each LoRA bucket of the expert (a contiguous run of tiles), the number
+    // of its tiles before k.
+    const int nbig = min(big_n, kPlanBigQueue);
+    for (int qi = 0; qi < nbig; ++qi) {
+      const int4 bq = big_q[qi];
+      const int e = bq.x;
+      const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
+      const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
+      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      for (int k = threadIdx.x; k < nt; k += kPlanThreads) {
+        int pk = bq.z;
+        for (int b = e * C + 1; b < (e + 1) * C; ++b) {
+          if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+          const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
+          const int t0 = (z0 - r0) / ts, t1 = (z1 - 1 - r0) / ts;
+          pk += max(0, min(t1, k - 1) - t0 + 1);
+        }
+        write_tile(e, k, bq.y + k, pk, r0, span, ts);
+      }
     }
   }
   if (bad) set_status(status, MLR_STATUS_RANK);

@@ -136,6 +136,89 @@ static __device__ __forceinline__ AlignBlockSmem align_block_carve(unsigned char
   return m;
 }
 
+// Dense order for batches with few buckets (<= kAlignFewBuckets, e.g. one
+// expert: a dense projection with per-segment adapters).  Thread t owns the
+// contiguous pairs [t * ipt, (t + 1) * ipt); per bucket, a block-wide exclusive
+// scan of the per-thread counts gives each thread the place of its first pair
+// of that bucket, so pairs land in increasing index inside every bucket
+// (stable) without any per-pair search.  On return cnt[b] is the first dense
+// row of bucket b and cnt[NB] the number of valid pairs, as after align_block.
+constexpr int kAlignFewBuckets = 16;
+static __device__ __noinline__ void align_block_few(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
+                                       int P, int topk, int E, int L, uint32_t* cnt, int32_t* d_status,
+                                       int32_t* __restrict__ dense_out) {
+  __shared__ uint32_t wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = L + 1, NB = E * C;
+  const int ipt = (P + kAlignBlockThreads - 1) / kAlignBlockThreads;  // <= kAlignBlockMaxItems
+  const int j0 = tid * ipt;
+  uint8_t key[kAlignBlockMaxItems];
+  int bad = 0;
+#pragma unroll
+  for (int i = 0; i < kAlignBlockMaxItems; ++i) {
+    key[i] = 0xFF;
+    const int j = j0 + i;
+    if (i < ipt && j < P) {
+      const int e = __ldg(topk_ids + j);
+      const int l = __ldg(mapping + j / topk);
+      if (e < 0 || e >= E || l < -1 || l >= L) bad |= MLR_STATUS_INDEX;
+      else key[i] = (uint8_t)(e * C + l + 1);
+    }
+  }
+  if (bad) set_status(d_status, bad);
+  uint32_t off[kAlignFewBuckets];
+#pragma unroll
+  for (int b = 0; b < kAlignFewBuckets; ++b) {
+    off[b] = 0;
+    if (b >= NB) continue;  // uniform over the block
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < kAlignBlockMaxItems; ++i) mine += key[i] == b ? 1u : 0u;
+    uint32_t inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t w = wsum[lane];  // kAlignBlockThreads / 32 == 32 warps
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      wsum[lane] = w;
+      if (lane == 31) cnt[b] = w;  // bucket size
+    }
+    __syncthreads();
+    off[b] = inc - mine + (warp > 0 ? wsum[warp - 1] : 0u);
+    __syncthreads();  // wsum is reused by the next bucket
+  }
+  if (tid == 0) {
+    uint32_t run = 0;
+    for (int b = 0; b < NB; ++b) {
+      const uint32_t n = cnt[b];
+      cnt[b] = run;
+      run += n;
+    }
+    cnt[NB] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kAlignBlockMaxItems; ++i) {
+    const int b = key[i];
+    if (b == 0xFF) continue;
+    uint32_t o = 0;
+#pragma unroll
+    for (int q = 0; q < kAlignFewBuckets; ++q)
+      if (q == b) o = off[q]++;
+    dense_out[cnt[b] + o] = j0 + i;
+  }
+  __syncthreads();
+}
+
 static __device__ void align_block(const int32_t* __restrict__ topk_ids,
                                    const int32_t* __restrict__ mapping, int P, int topk, int E,
                                    int L, int block_size, const AlignBlockSmem& sm,
@@ -150,6 +233,10 @@ static __device__ void align_block(const int32_t* __restrict__ topk_ids,
   uint16_t* order = sm.order;
   const int tid = threadIdx.x;
   const int C = L + 1, NB = E * C;
+  if (dense_out != nullptr && NB <= kAlignFewBuckets) {
+    align_block_few(topk_ids, mapping, P, topk, E, L, cnt, d_status, dense_out);
+    return;
+  }
   for (int b = tid; b <= NB; b += kAlignBlockThreads) cnt[b] = 0u;
   const int rounds = (P + kAlignBlockThreads - 1) / kAlignBlockThreads;
   // Keys of pairs j = it * 1024 + tid; the token j / topk is advanced per round
