@@ -59,3 +59,12 @@ def test_reference_arm_nonzero_rank_exits_quietly():
                         "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_linear_stage_names():
+    stages = {"align_plan": 0.05, "gather": 0.04, "shrink_gate_up": 0.03, "gate_up": 0.002,
+              "shrink_down": 0.001, "down": 0.16, "convert": 0.02}
+    out = bench.linear_stage_times(stages)
+    assert out == {"align_plan": 0.05, "gather": 0.04, "shrink": 0.03, "projection_gemm": 0.16,
+                   "convert": 0.02, "marker_gaps": 0.003}
+    assert abs(sum(out.values()) - sum(stages.values())) < 1e-9
