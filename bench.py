@@ -50,10 +50,12 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the translation unit that holds the GEMM kernels (forward.cu and
+    the headers); a recorded DRAM capture applies only while it is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lora_moe_expert_info_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name == "forward.cu" or name.endswith(".cuh"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -72,6 +74,149 @@ def recorded_traffic(stage: str, workload: str):
                 r.get("source_hash") == kernel_source_hash():
             return r.get("dram_bytes_per_launch")
     return None
+
+
+def stage_profile(lib, step, n_calls):
+    """Average ms per stage over n_calls untimed steps, every stage marked."""
+    import torch
+    lib.moe_lora_profile_stages(all_stages(lib))
+    lib.moe_lora_profile_begin(n_calls)
+    for _ in range(n_calls):
+        step()
+    torch.cuda.synchronize()
+    return read_stage_profile(lib)
+
+
+def read_stage_profile(lib):
+    """End the library's recording; average ms per stage over the recorded calls."""
+    import ctypes
+    stage_ms = (ctypes.c_double * 16)()
+    n_st, n_calls = ctypes.c_int32(0), ctypes.c_int32(0)
+    lib.moe_lora_profile_end(stage_ms, 16, ctypes.byref(n_st), ctypes.byref(n_calls))
+    return {lib.moe_lora_profile_stage_name(i).decode(): stage_ms[i] / max(1, n_calls.value)
+            for i in range(n_st.value)}
+
+
+def all_stages(lib):
+    n = 0
+    while lib.moe_lora_profile_stage_name(n) is not None:
+        n += 1
+    return (1 << n) - 1
+
+
+def stage_index(lib, name):
+    i = 0
+    while True:
+        n = lib.moe_lora_profile_stage_name(i)
+        if n is None:
+            raise KeyError(name)
+        if n.decode() == name:
+            return i
+        i += 1
+
+
+def timed_region(lib, args, step, stream, dist, local, dom):
+    """The timed steps: barrier and synchronise on both sides, CUDA events on the
+    launching stream, clocks sampled throughout.  Only the two events that bound
+    stage `dom` are recorded inside the forward, so its launch time is measured
+    live at the cost of two events per step instead of eight.
+
+    Returns (ms over all steps, dom's average ms, kernels launched, clock sampler).
+    """
+    import torch
+    lib.moe_lora_profile_stages(1 << stage_index(lib, dom))
+    if dist is not None:
+        dist.barrier()
+    n_launch0 = lib.moe_lora_launch_count()
+    lib.moe_lora_profile_begin(min(args.steps, 4096))
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    live = read_stage_profile(lib)
+    lib.moe_lora_profile_stages(all_stages(lib))
+    n_launch = lib.moe_lora_launch_count() - n_launch0
+    return e0.elapsed_time(e1), live[dom], n_launch, clk
+
+
+def pipelined_e2e(n_steps, upload, compute, download, stream):
+    """Milliseconds per step with two steps in flight, as a serving loop runs.
+
+    Step i uploads its inputs into buffer slot i % 2 on an upload stream, runs on
+    `stream` (the library's launch stream), and its result is read back on a
+    download stream.  Slot reuse is ordered by events: step i's upload waits for
+    step i - 2's compute (which read the slot's inputs), and its compute waits
+    for step i - 2's download (which read the slot's result).  So step i + 1's
+    upload and step i - 1's download overlap step i's compute, while every step
+    still copies its own inputs in and its own result out.  Timed from the
+    first upload to the last download with CUDA events.
+    """
+    import torch
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    f0.record(s_in)
+    for i in range(n_steps):
+        sl = i % 2
+        if i >= 2:
+            s_in.wait_event(done[sl])
+        with torch.cuda.stream(s_in):
+            upload(sl)
+        ready[sl].record(s_in)
+        stream.wait_event(ready[sl])
+        if i >= 2:
+            stream.wait_event(read[sl])
+        with torch.cuda.stream(stream):
+            compute(sl)
+        done[sl].record(stream)
+        s_out.wait_event(done[sl])
+        with torch.cuda.stream(s_out):
+            download(sl)
+        read[sl].record(s_out)
+    f1.record(s_out)  # every earlier step precedes the last download
+    torch.cuda.synchronize()
+    return f0.elapsed_time(f1) / n_steps
+
+
+def measure_e2e(args, upload, compute, download, stream, dist, dev):
+    """End-to-end ms per step: two steps in flight (the reported figure), and
+    one step at a time on one stream (reported beside it).  Max over ranks."""
+    import torch
+    n = max(3, min(args.steps, 200))
+
+    def serial_step():
+        with torch.cuda.stream(stream):
+            upload(0)
+            compute(0)
+            download(0)
+
+    for _ in range(3):
+        serial_step()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n):
+        serial_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    serial = f0.elapsed_time(f1) / n
+    pipelined_e2e(4, upload, compute, download, stream)  # warm-up of the streams and events
+    piped = pipelined_e2e(n, upload, compute, download, stream)
+    return reduce_max(piped, dist, dev), reduce_max(serial, dist, dev)
 
 
 class ClockSampler:
@@ -310,64 +455,40 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    if dist is not None:
-        dist.barrier()
-    n_launch0 = lib.moe_lora_launch_count()
-    lib.moe_lora_profile_begin(min(args.steps, 4096))
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-    import ctypes
-    stage_ms = (ctypes.c_double * 16)()
-    n_st, n_calls = ctypes.c_int32(0), ctypes.c_int32(0)
-    lib.moe_lora_profile_end(stage_ms, 16, ctypes.byref(n_st), ctypes.byref(n_calls))
-    n_launch = lib.moe_lora_launch_count() - n_launch0
-    ms_max = reduce_max(e0.elapsed_time(e1), dist, dev)
-    stages = {lib.moe_lora_profile_stage_name(i).decode(): stage_ms[i] / max(1, n_calls.value)
-              for i in range(n_st.value)}
+    # per-stage breakdown from untimed steps; the dominant GEMM stage is then
+    # timed live inside the timed region
+    stages = stage_profile(lib, step, max(3, min(args.steps, 50)))
+    dom = max((s for s in STAGE_KERNELS if s in stages), key=lambda s: stages[s])
+    ms_total, dom_ms, n_launch, clk = timed_region(lib, args, step, stream, dist, local, dom)
+    ms_max = reduce_max(ms_total, dist, dev)
 
     # end to end through the public API from pinned host buffers
     host_in = {"x": x.cpu().pin_memory(), "topk_ids": b.topk_ids.cpu().pin_memory(),
                "topk_weights": b.topk_weights.cpu().pin_memory(), "seg_indptr": b.seg_indptr.cpu().pin_memory(),
                "weight_indices": b.weight_indices.cpu().pin_memory(),
                "lora_ranks": b.lora_ranks.cpu().pin_memory(), "scalings": b.scalings.cpu().pin_memory()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    y_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+    y_dev = [y, torch.empty_like(y)]
+    y_host = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = y_host.numel() * y_host.element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
 
-    def e2e_step():
+    def upload(sl):
         for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        mlr.moe_lora_batch_info(dev_in["seg_indptr"], dev_in["weight_indices"], dev_in["lora_ranks"], T,
-                                max_len, adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
-        mlr.fused_moe_lora_forward(dev_in["x"], dev_in["topk_ids"], dev_in["topk_weights"], mapping,
-                                   dev_in["lora_ranks"], dev_in["scalings"], **wk, y=y, workspace=ws,
-                                   check=False)
-        y_host.copy_(y, non_blocking=True)
+            dev_in[sl][k].copy_(v, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 200))
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(f0.elapsed_time(f1) / e2e_steps, dist, dev)
+    def compute(sl):
+        d = dev_in[sl]
+        mlr.moe_lora_batch_info(d["seg_indptr"], d["weight_indices"], d["lora_ranks"], T,
+                                max_len, adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
+        mlr.fused_moe_lora_forward(d["x"], d["topk_ids"], d["topk_weights"], mapping,
+                                   d["lora_ranks"], d["scalings"], **wk, y=y_dev[sl], workspace=ws,
+                                   check=False)
+
+    def download(sl):
+        y_host[sl].copy_(y_dev[sl], non_blocking=True)
+
+    e2e_ms, e2e_serial_ms = measure_e2e(args, upload, compute, download, stream, dist, dev)
 
     # check the status of the gated call only now (it synchronised long ago)
     if int(status.item()) != 0:
@@ -389,8 +510,6 @@ def run_ours(args, rank, world, dist):
     peaks, peak_src = load_peaks()
     ms_step = ms_max / args.steps
     value = weak_scaling_rate(T, world, ms_step)
-    dom = max((s for s in st_work if s in stages), key=lambda s: stages[s])
-    dom_ms = stages[dom]
     rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, "bf16_tflops_sustained")
     rf["kernel"] = STAGE_KERNELS.get(dom, dom)
     rf["stage"] = dom
@@ -418,7 +537,8 @@ def run_ours(args, rank, world, dist):
             "cpu_baseline": cpu,
             "e2e": {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4), "steps_in_flight": 2,
+                    "serial_ms_per_step": round(e2e_serial_ms, 4)},
             "gpu_launches": int(n_launch), "clocks": clk.summary()}
     return line
 
@@ -563,58 +683,34 @@ def run_linear(args, rank, world, dist):
         step()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    if dist is not None:
-        dist.barrier()
-    n_launch0 = lib.moe_lora_launch_count()
-    lib.moe_lora_profile_begin(min(args.steps, 4096))
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-    stage_ms = (ctypes.c_double * 16)()
-    n_st, n_calls = ctypes.c_int32(0), ctypes.c_int32(0)
-    lib.moe_lora_profile_end(stage_ms, 16, ctypes.byref(n_st), ctypes.byref(n_calls))
-    n_launch = lib.moe_lora_launch_count() - n_launch0
-    ms_max = reduce_max(e0.elapsed_time(e1), dist, dev)
-    stages = {lib.moe_lora_profile_stage_name(i).decode(): stage_ms[i] / max(1, n_calls.value)
-              for i in range(n_st.value)}
+    # per-stage breakdown from untimed steps; the projection GEMM (profile stage
+    # "down") is timed live inside the timed region
+    stages = stage_profile(lib, step, max(3, min(args.steps, 50)))
+    ms_total, proj_ms, n_launch, clk = timed_region(lib, args, step, stream, dist, local, "down")
+    ms_max = reduce_max(ms_total, dist, dev)
 
     # end to end through the public API from pinned host buffers
     host_in = {"x": x.cpu().pin_memory(), "mapping": mapping.cpu().pin_memory(),
                "ranks": ranks.cpu().pin_memory(), "scal": scal.cpu().pin_memory()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    y_host = torch.empty(T, D_out, dtype=torch.bfloat16).pin_memory()
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+    y_dev = [y, torch.empty_like(y)]
+    y_host = [torch.empty(T, D_out, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = y_host.numel() * y_host.element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
 
-    def e2e_step():
+    def upload(sl):
         for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        mlr.lora_linear_forward(dev_in["x"], w, dev_in["mapping"], dev_in["ranks"], dev_in["scal"], a, b, offs,
-                                y=y, workspace=ws, check=False)
-        y_host.copy_(y, non_blocking=True)
+            dev_in[sl][k].copy_(v, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 200))
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(f0.elapsed_time(f1) / e2e_steps, dist, dev)
+    def compute(sl):
+        d = dev_in[sl]
+        mlr.lora_linear_forward(d["x"], w, d["mapping"], d["ranks"], d["scal"], a, b, offs,
+                                y=y_dev[sl], workspace=ws, check=False)
+
+    def download(sl):
+        y_host[sl].copy_(y_dev[sl], non_blocking=True)
+
+    e2e_ms, e2e_serial_ms = measure_e2e(args, upload, compute, download, stream, dist, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"projection reported device status {int(status.item())}")
     if rank != 0:
@@ -631,7 +727,6 @@ def run_linear(args, rank, world, dist):
     ms_step = ms_max / args.steps
     flops, byts = linear_work(cfg, ranks.cpu().numpy(), mp_np)
     # the projection GEMM (profile stage "down") carries the base GEMM and the expand
-    proj_ms = stages.get("down", ms_step)
     r_tok = np.where(mp_np >= 0, ranks.cpu().numpy()[np.clip(mp_np, 0, None)], 0).astype(np.float64)
     proj_flops = 2.0 * T * D_out * D_in + float(2.0 * D_out * r_tok.sum())
     proj_bytes = 2.0 * D_out * D_in + 2.0 * T * D_in + 4.0 * T * D_out
@@ -651,7 +746,8 @@ def run_linear(args, rank, world, dist):
             "cpu_baseline": cpu,
             "e2e": {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4), "steps_in_flight": 2,
+                    "serial_ms_per_step": round(e2e_serial_ms, 4)},
             "gpu_launches": int(n_launch), "clocks": clk.summary()}
 
 

@@ -248,12 +248,18 @@ int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const int32_t* tok
  *   recorded events complete, writes the summed milliseconds of each stage over
  *   the recorded calls into stage_ms[0..min(max_stages, *n_stages)), the number of
  *   recorded calls into *n_calls (host pointers), and stops recording.
+ * moe_lora_profile_stages(mask): stages that later moe_lora_profile_begin
+ *   calls time (bit i = stage i; all stages by default).  Only the events that
+ *   bound a selected stage are recorded, so timing one stage adds two events
+ *   per call instead of eight; unselected stages report 0 ms.  Returns
+ *   MLR_ERR_INVALID for an empty mask or bits past the last stage.
  * moe_lora_profile_stage_name(i): "align_plan" (the (expert, adapter) align in
  *   dense order and the tile plan), "gather" (x copied into sorted row order; zeroes the fp32
  *   accumulator), "shrink_gate_up", "gate_up", "shrink_down", "down", "convert"
  *   (static storage; NULL past the last stage).
  * moe_lora_launch_count(): kernels this library has launched in this process.
  */
+int moe_lora_profile_stages(uint32_t mask);
 int moe_lora_profile_begin(int32_t max_calls);
 int moe_lora_profile_end(double* stage_ms, int32_t max_stages, int32_t* n_stages, int32_t* n_calls);
 const char* moe_lora_profile_stage_name(int32_t stage);

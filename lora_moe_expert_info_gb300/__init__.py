@@ -79,6 +79,8 @@ def library() -> ctypes.CDLL:
             lib.moe_lora_align.restype = ctypes.c_int
             lib.moe_lora_align.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, i64,
                                            vp, sz, vp, vp]
+            lib.moe_lora_profile_stages.restype = ctypes.c_int
+            lib.moe_lora_profile_stages.argtypes = [ctypes.c_uint32]
             lib.moe_lora_profile_begin.restype = ctypes.c_int
             lib.moe_lora_profile_begin.argtypes = [i32]
             lib.moe_lora_profile_end.restype = ctypes.c_int

@@ -13,6 +13,15 @@ std::mutex g_mu;
 bool g_on = false;
 int g_max_calls = 0, g_calls = 0;
 std::vector<cudaEvent_t> g_events;  // [max_calls][kProfStages + 1]
+constexpr uint32_t kAllStages = (1u << kProfStages) - 1;
+uint32_t g_select = kAllStages;  // stages that the next begin() times
+uint32_t g_mask = kAllStages;    // stages timed by the current recording
+
+// Boundary b (0 = call start, b = s + 1 after stage s) is recorded when a
+// selected stage starts or ends there.
+bool boundary_needed(int b) {
+  return ((b < kProfStages && ((g_mask >> b) & 1)) || (b > 0 && ((g_mask >> (b - 1)) & 1)));
+}
 
 const char* kStageNames[kProfStages] = {"align_plan", "gather", "shrink_gate_up", "gate_up",
                                         "shrink_down", "down", "convert"};
@@ -25,12 +34,12 @@ int prof_call_begin(cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_on || g_calls >= g_max_calls) return -1;
   const int slot = g_calls++;
-  cudaEventRecord(g_events[(size_t)slot * (kProfStages + 1)], stream);
+  if (boundary_needed(0)) cudaEventRecord(g_events[(size_t)slot * (kProfStages + 1)], stream);
   return slot;
 }
 
 void prof_mark(int slot, int stage, cudaStream_t stream) {
-  if (slot < 0) return;
+  if (slot < 0 || !boundary_needed(stage + 1)) return;
   cudaEventRecord(g_events[(size_t)slot * (kProfStages + 1) + stage + 1], stream);
 }
 
@@ -48,7 +57,16 @@ extern "C" int moe_lora_profile_begin(int32_t max_calls) {
   }
   g_max_calls = max_calls;
   g_calls = 0;
+  g_mask = g_select;
   g_on = true;
+  return MLR_OK;
+}
+
+extern "C" int moe_lora_profile_stages(uint32_t mask) {
+  using namespace mlr;
+  if (mask == 0 || (mask & ~kAllStages) != 0) return MLR_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_select = mask;
   return MLR_OK;
 }
 
@@ -61,10 +79,14 @@ extern "C" int moe_lora_profile_end(double* stage_ms, int32_t max_stages, int32_
   if (n_calls) *n_calls = g_calls;
   if (stage_ms == nullptr) return MLR_OK;
   for (int s = 0; s < max_stages && s < kProfStages; ++s) stage_ms[s] = 0.0;
+  int last = 0;  // the last boundary recorded in every call
+  for (int b = 0; b <= kProfStages; ++b)
+    if (boundary_needed(b)) last = b;
   for (int c = 0; c < g_calls; ++c) {
     cudaEvent_t* ev = &g_events[(size_t)c * (kProfStages + 1)];
-    if (cudaEventSynchronize(ev[kProfStages]) != cudaSuccess) return MLR_ERR_CUDA;
+    if (cudaEventSynchronize(ev[last]) != cudaSuccess) return MLR_ERR_CUDA;
     for (int s = 0; s < max_stages && s < kProfStages; ++s) {
+      if (((g_mask >> s) & 1) == 0) continue;
       float ms = 0.f;
       if (cudaEventElapsedTime(&ms, ev[s], ev[s + 1]) != cudaSuccess) return MLR_ERR_CUDA;
       stage_ms[s] += ms;

@@ -125,3 +125,15 @@ def test_linear_host_checks(lib):
 def test_status_strings(lib):
     assert b"under-covers" in lib.moe_lora_status_string(mlr.MLR_ERR_UNDERCOVERED)
     assert lib.moe_lora_status_string(0) == b"ok"
+
+
+def test_profile_stage_selection_checks(lib):
+    # host-side only: selecting stages records nothing until a forward runs
+    assert lib.moe_lora_profile_stages(0) == mlr.MLR_ERR_INVALID
+    assert lib.moe_lora_profile_stages(1 << 7) == mlr.MLR_ERR_INVALID
+    n = 0
+    while lib.moe_lora_profile_stage_name(n) is not None:
+        n += 1
+    assert n == 7
+    assert lib.moe_lora_profile_stages(1 << 3) == 0
+    assert lib.moe_lora_profile_stages((1 << n) - 1) == 0  # back to every stage
