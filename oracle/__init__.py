@@ -67,6 +67,13 @@ def _load():
                                            vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                            i64, i64, i64, i64, i64, i64, i64,
                                            vp, i64, vp, ctypes.c_int]
+            lib.oracle_forward_fp8.restype = ctypes.c_int
+            lib.oracle_forward_fp8.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
+                                               vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                               i64, i64, i64, i64, i64, i64, i64,
+                                               vp, i64, vp, ctypes.c_int]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint32]
             lib.oracle_lora_linear.restype = ctypes.c_int
             lib.oracle_lora_linear.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                                i64, i64, i64, i64, i64, i64, vp, vp, i64, vp, ctypes.c_int]
@@ -188,6 +195,62 @@ def forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
         xp, xdt, topk_ids.ctypes.data, topk_weights.ctypes.data, mapping.ctypes.data,
         lora_ranks.ctypes.data, scalings.ctypes.data,
         ops[0][0], ops[1][0], ops[2][0], ops[3][0], ops[4][0], ops[5][0], wdt,
+        T, K, E, H, I, L, R, tok_ptr, n_out, y.ctypes.data, int(threads))
+    del xk, tok
+    return int(st), y
+
+
+def e4m3_value(code: int) -> float:
+    """The value of an FP8 E4M3 code (0..255)."""
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                w_gate_up_q, w_gate_up_scale, w_down_q, w_down_scale,
+                lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens=None, threads: int = 0):
+    """The layer with FP8 E4M3 base experts.  Returns (status, y) with y float64.
+
+    w_gate_up_q [E,2I,H] and w_down_q [E,H,I] are uint8 E4M3 codes;
+    w_gate_up_scale [E,ceil(2I/128),ceil(H/128)] and w_down_scale
+    [E,ceil(H/128),ceil(I/128)] float32 scales of their 128 x 128 blocks.  The
+    other operands are as in forward() (LoRA operands share one dtype).
+    """
+    x_np = np.asarray(x)
+    T, H = x_np.shape
+    topk_ids = _i32(topk_ids)
+    K = topk_ids.shape[1]
+    topk_weights = np.ascontiguousarray(np.asarray(topk_weights, dtype=np.float32))
+    mapping = _i32(token_lora_mapping)
+    lora_ranks = _i32(lora_ranks)
+    scalings = np.ascontiguousarray(np.asarray(scalings, dtype=np.float32))
+    wq = np.ascontiguousarray(np.asarray(w_gate_up_q, dtype=np.uint8))
+    dq = np.ascontiguousarray(np.asarray(w_down_q, dtype=np.uint8))
+    E, I2, H2 = wq.shape
+    I = I2 // 2
+    L, _, _, R, _ = np.asarray(lora_a_gu).shape
+    assert H2 == H and dq.shape == (E, H, I)
+    ws = np.ascontiguousarray(np.asarray(w_gate_up_scale, dtype=np.float32))
+    ds = np.ascontiguousarray(np.asarray(w_down_scale, dtype=np.float32))
+    assert ws.shape == (E, (2 * I + 127) // 128, (H + 127) // 128)
+    assert ds.shape == (E, (H + 127) // 128, (I + 127) // 128)
+    assert np.asarray(lora_b_gu).shape == (L, E, 2, I, R)
+    assert np.asarray(lora_a_down).shape == (L, E, R, I)
+    assert np.asarray(lora_b_down).shape == (L, E, H, R)
+    xp, xdt, xk = _operand(x_np)
+    ops = [_operand(a) for a in (lora_a_gu, lora_b_gu, lora_a_down, lora_b_down)]
+    ldt = ops[0][1]
+    if any(o[1] != ldt for o in ops):
+        raise TypeError("LoRA operands must share one dtype")
+    if tokens is None:
+        tok, n_out, tok_ptr = None, T, None
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        n_out, tok_ptr = tok.shape[0], tok.ctypes.data
+    y = np.zeros((n_out, H), dtype=np.float64)
+    st = _load().oracle_forward_fp8(
+        xp, xdt, topk_ids.ctypes.data, topk_weights.ctypes.data, mapping.ctypes.data,
+        lora_ranks.ctypes.data, scalings.ctypes.data, wq.ctypes.data, ws.ctypes.data,
+        dq.ctypes.data, ds.ctypes.data, ops[0][0], ops[1][0], ops[2][0], ops[3][0], ldt,
         T, K, E, H, I, L, R, tok_ptr, n_out, y.ctypes.data, int(threads))
     del xk, tok
     return int(st), y

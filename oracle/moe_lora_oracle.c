@@ -17,7 +17,10 @@
  *   [PR22323] "LoRA quantisation info and DeepSeek-V3 MLA fused projection"
  *             page, section 实现拆解 items 2-3: ReplicatedLinearWithLoRA applies
  *             LoRA to the fused q_a_proj + kv_a_proj_with_mqa projection, its B
- *             split into two parts applied by two segment GEMMs.
+ *             split into two parts applied by two segment GEMMs.  Its 功能与动机
+ *             section and 实现拆解 item 1: quantised MoE experts (FP8,
+ *             block-wise INT8, WNA16) hand their scales to the LoRA MoE layer,
+ *             which then runs with quantised base weights.
  *   [PR24160] "shared MoE LoRA batch info" page, sections 实现拆解 and
  *             关键源码片段 (MoELoRABatchInfo dataclass; test_moe_lora_info.py):
  *             token_lora_mapping = repeat_interleave(weight_indices, seg_lens),
@@ -38,12 +41,22 @@
  *   - the top-k weight multiplies the whole expert output, LoRA delta
  *     included; an adapter contributes iff its id is >= 0 and its rank > 0;
  *     only the first rank columns/rows of the zero-padded stacks are read.
+ *   - quantised experts (the pages name the methods, not their formats): FP8
+ *     E4M3 expert weights, each 128 x 128 block (rows x columns of W_gate_up
+ *     [E, 2I, H] and W_down [E, H, I]) with one float scale, the weight being
+ *     code value x scale (the DeepSeek-V3 checkpoint layout, inverse scales
+ *     [E, ceil(rows/128), ceil(cols/128)]).  Activations, LoRA A and B stay
+ *     bf16; only the base weights are quantised.
  *
  * Parity pins (see tests/test_oracle_*.py): the worked mapping example of
  * [PR24160]; torch.repeat_interleave on random segments; brute-force sorted()
  * for align; a dense SwiGLU MLP via torch for one expert; dense-materialised
  * W + s*B*A against the factored form; base identity for B = 0, adapter -1
- * and rank 0; linearity and permutation invariances of the top-k combine.
+ * and rank 0; linearity and permutation invariances of the top-k combine;
+ * for FP8 experts, the E4M3 decoder against the format's defining values and
+ * torch's float8_e4m3fn for all 256 codes, and the layer against the fp64
+ * forward on weights dequantised with numpy (unit and power-of-two block
+ * scales, ragged and gate/up-shared blocks).
  */
 #include <math.h>
 #include <stdint.h>
@@ -209,6 +222,43 @@ static double ld(const void* base, int dtype, int64_t idx) {
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /*
+ * FP8 E4M3 (the OCP 8-bit floating-point format's E4M3 encoding, as used for
+ * DeepSeek-V3's FP8 weights): sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits.  Exponent field 0 holds subnormals 0.m x 2^-6; there are no
+ * infinities, and exponent and mantissa fields both all ones is NaN.  Largest
+ * finite value 1.75 x 2^8 = 448.
+ */
+double oracle_e4m3_value(uint32_t code) {
+  const int sign = (int)((code >> 7) & 1u), ef = (int)((code >> 3) & 15u), mf = (int)(code & 7u);
+  double v;
+  if (ef == 15 && mf == 7) return NAN;
+  if (ef == 0) v = ldexp((double)mf / 8.0, -6);
+  else v = ldexp(1.0 + (double)mf / 8.0, ef - 7);
+  return sign ? -v : v;
+}
+
+/*
+ * A base expert weight [E, rows, cols]: dtype 0 bf16 bits, 1 double, or 2 FP8
+ * E4M3 codes whose value is code x scale[e][row / 128][col / 128].
+ */
+typedef struct {
+  const void* p;
+  int dtype;
+  const float* scale;
+  int64_t rows, cols;
+} WeightView;
+
+static double ld_w(const WeightView* v, int64_t e, int64_t row, int64_t col) {
+  const int64_t idx = (e * v->rows + row) * v->cols + col;
+  if (v->dtype == 2) {
+    const int64_t rb = (v->rows + 127) / 128, cb = (v->cols + 127) / 128;
+    const double sc = (double)v->scale[(e * rb + row / 128) * cb + col / 128];
+    return oracle_e4m3_value(((const uint8_t*)v->p)[idx]) * sc;
+  }
+  return ld(v->p, v->dtype, idx);
+}
+
+/*
  * Layouts (row-major):
  *   x           [T, H]
  *   topk_ids    [T, K] int32, topk_weights [T, K] float
@@ -221,14 +271,14 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
  *   lora_b_down [L, E, H, R]
  *   y           [n_out, H] double, row j for token tokens[j] (or j if tokens == NULL)
  */
-int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
-                   const float* topk_weights, const int32_t* token_lora_mapping,
-                   const int32_t* lora_ranks, const float* scalings,
-                   const void* w_gate_up, const void* w_down, const void* lora_a_gu,
-                   const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
-                   int w_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
-                   int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
-                   int num_threads) {
+static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
+                        const float* topk_weights, const int32_t* token_lora_mapping,
+                        const int32_t* lora_ranks, const float* scalings,
+                        const WeightView* wgu, const WeightView* wdn, const void* lora_a_gu,
+                        const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                        int w_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                        int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                        int num_threads) {
   if (T < 0 || K < 1 || E < 1 || H < 1 || I < 1 || L < 0 || R < 0 || n_out < 0)
     return ORC_INVALID;
   for (int64_t l = 0; l < L; ++l)
@@ -292,12 +342,10 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
 
           /* gate and up projections, each with its own LoRA delta; SiLU(g) * u */
           for (int64_t i = 0; i < I; ++i) {
-            const int64_t wg = (e * 2 * I + i) * H;
-            const int64_t wu = (e * 2 * I + I + i) * H;
             double g = 0.0, u = 0.0;
             for (int64_t h = 0; h < H; ++h) {
-              g += ld(w_gate_up, w_dtype, wg + h) * xv[h];
-              u += ld(w_gate_up, w_dtype, wu + h) * xv[h];
+              g += ld_w(wgu, e, i, h) * xv[h];
+              u += ld_w(wgu, e, I + i, h) * xv[h];
             }
             if (r > 0) {
               const int64_t bg = (((l * E + e) * 2 + 0) * I + i) * R;
@@ -323,9 +371,8 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
 
           /* down projection with its LoRA delta, weighted into y */
           for (int64_t h = 0; h < H; ++h) {
-            const int64_t wd = (e * H + h) * I;
             double d = 0.0;
-            for (int64_t i = 0; i < I; ++i) d += ld(w_down, w_dtype, wd + i) * a[i];
+            for (int64_t i = 0; i < I; ++i) d += ld_w(wdn, e, h, i) * a[i];
             if (r > 0) {
               const int64_t bd = ((l * E + e) * H + h) * R;
               double dd = 0.0;
@@ -340,6 +387,48 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
     free(xv); free(a); free(zg); free(zu); free(zd);
   }
   return status;
+}
+
+int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
+                   const float* topk_weights, const int32_t* token_lora_mapping,
+                   const int32_t* lora_ranks, const float* scalings,
+                   const void* w_gate_up, const void* w_down, const void* lora_a_gu,
+                   const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                   int w_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                   int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                   int num_threads) {
+  if (w_dtype != 0 && w_dtype != 1) return ORC_INVALID;
+  const WeightView wgu = {w_gate_up, w_dtype, NULL, 2 * I, H};
+  const WeightView wdn = {w_down, w_dtype, NULL, H, I};
+  return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
+                      &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, w_dtype, T, K, E, H, I, L, R,
+                      tokens, n_out, y, num_threads);
+}
+
+/*
+ * The same layer with FP8 E4M3 base experts ([PR22323] 功能与动机 and 实现拆解
+ * item 1: LoRA on quantised MoE models).  w_gate_up_q [E, 2I, H] and
+ * w_down_q [E, H, I] hold E4M3 codes; w_gate_up_scale [E, ceil(2I/128),
+ * ceil(H/128)] and w_down_scale [E, ceil(H/128), ceil(I/128)] the float scale
+ * of each 128 x 128 block.  LoRA operands are bf16 bits or double (lora_dtype).
+ */
+int oracle_forward_fp8(const void* x, int x_dtype, const int32_t* topk_ids,
+                       const float* topk_weights, const int32_t* token_lora_mapping,
+                       const int32_t* lora_ranks, const float* scalings,
+                       const uint8_t* w_gate_up_q, const float* w_gate_up_scale,
+                       const uint8_t* w_down_q, const float* w_down_scale, const void* lora_a_gu,
+                       const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                       int lora_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                       int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                       int num_threads) {
+  if (lora_dtype != 0 && lora_dtype != 1) return ORC_INVALID;
+  if (w_gate_up_q == NULL || w_gate_up_scale == NULL || w_down_q == NULL || w_down_scale == NULL)
+    return ORC_INVALID;
+  const WeightView wgu = {w_gate_up_q, 2, w_gate_up_scale, 2 * I, H};
+  const WeightView wdn = {w_down_q, 2, w_down_scale, H, I};
+  return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
+                      &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
+                      R, tokens, n_out, y, num_threads);
 }
 
 /* ------------------------------------------------------------------------ */
