@@ -292,8 +292,12 @@ def weak_scaling_rate(units_per_rank, world, ms_per_step_max):
     return world * units_per_rank / (ms_per_step_max * 1e-3)
 
 
-def layer_work(cfg, batch, mapping):
-    """Algorithmic FLOPs and bytes of the layer and of each stage (from the routing)."""
+def layer_work(cfg, batch, mapping, fp8=False):
+    """Algorithmic FLOPs and bytes of the layer and of each stage (from the routing).
+
+    fp8: the base expert weights are one byte each plus a float32 scale per
+    128 x 128 block; LoRA operands and activations stay bf16.
+    """
     import torch
     T, K, E, H, I, L = cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.hidden, cfg.intermediate, cfg.num_loras
     ids = batch.topk_ids.long().cpu()
@@ -309,14 +313,21 @@ def layer_work(cfg, batch, mapping):
     keys = torch.unique(pair_l[sel] * E + ids.reshape(-1)[sel])
     sum_r_le = float(ranks[keys // E].sum()) if keys.numel() else 0.0
     W = 2  # bf16 bytes
+    nb = lambda n: (n + 127) // 128  # noqa: E731
+    # base expert bytes per touched expert: gate_up and down matrices
+    if fp8:
+        wgu = 2 * H * I + 4 * nb(2 * I) * nb(H)
+        wdn = H * I + 4 * nb(H) * nb(I)
+    else:
+        wgu, wdn = 2 * H * I * W, H * I * W
     st = {
         "shrink_gate_up": (4 * H * sum_r_pairs, 2 * H * sum_r_le * W + T * H * W),
-        "gate_up": (4 * H * I * P + 4 * I * sum_r_pairs, 2 * H * I * W * touched_e + 2 * I * sum_r_le * W + T * H * W),
+        "gate_up": (4 * H * I * P + 4 * I * sum_r_pairs, wgu * touched_e + 2 * I * sum_r_le * W + T * H * W),
         "shrink_down": (2 * I * sum_r_pairs, I * sum_r_le * W),
-        "down": (2 * H * I * P + 2 * H * sum_r_pairs, H * I * W * touched_e + H * sum_r_le * W + T * H * W + P * 4),
+        "down": (2 * H * I * P + 2 * H * sum_r_pairs, wdn * touched_e + H * sum_r_le * W + T * H * W + P * 4),
     }
     flops = 6 * H * I * P + 6 * (H + I) * sum_r_pairs
-    byts = 3 * H * I * W * touched_e + (3 * H + 3 * I) * sum_r_le * W + 2 * T * H * W + P * 8 + T * 4
+    byts = (wgu + wdn) * touched_e + (3 * H + 3 * I) * sum_r_le * W + 2 * T * H * W + P * 8 + T * 4
     return flops, byts, st
 
 
@@ -334,24 +345,34 @@ def roofline_entry(flops, byts, ms, peaks, peak_kind):
 
 
 # ------------------------------------------------------------ the two arms --
-def make_inputs(cfg_name, device, seed):
+def make_inputs(cfg_name, device, seed, fp8=False):
+    """Batch, bf16 weights and x; with fp8 also FP8 experts (else None)."""
     from lora_moe_expert_info_gb300 import workloads
     cfg = workloads.CONFIGS[cfg_name]
     b = workloads.make_batch(cfg, device=device, seed=seed)
     w = workloads.make_weights(cfg, b.lora_ranks, device=device, seed=seed)
     x = workloads.make_x(cfg, device=device, seed=seed)
-    return cfg, b, w, x
+    q = workloads.make_fp8_experts(cfg, device=device, seed=seed) if fp8 else None
+    return cfg, b, w, x, q
 
 
-def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None, seed=0):
-    """Oracle tokens/s on a bounded seeded token sample; returns (rate, n_tokens, secs, threads)."""
+def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None, seed=0, q=None):
+    """Oracle tokens/s on a bounded seeded token sample; returns (rate, n_tokens, secs, threads).
+    With q (FP8 experts) the oracle's FP8 forward runs."""
     import numpy as np
     import torch
 
     import oracle
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    host = [bits(getattr(w, k)) for k in ("w_gate_up", "w_down", "lora_a_gu", "lora_b_gu",
-                                          "lora_a_down", "lora_b_down")]
+    if q is None:
+        fwd = oracle.forward
+        host = [bits(getattr(w, k)) for k in ("w_gate_up", "w_down", "lora_a_gu", "lora_b_gu",
+                                              "lora_a_down", "lora_b_down")]
+    else:
+        fwd = oracle.forward_fp8
+        host = [q.w_gate_up_q.cpu().numpy(), q.w_gate_up_scale.cpu().numpy(), q.w_down_q.cpu().numpy(),
+                q.w_down_scale.cpu().numpy()] + [bits(getattr(w, k)) for k in ("lora_a_gu", "lora_b_gu",
+                                                                               "lora_a_down", "lora_b_down")]
     xb = bits(x)
     ids = b.topk_ids.cpu().numpy()
     wts = b.topk_weights.cpu().numpy()
@@ -362,14 +383,14 @@ def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None,
     # calibrate on a few tokens, then size the sample to ~target_s of CPU work
     n0 = min(T, 8)
     t0 = time.perf_counter()
-    oracle.forward(xb, ids, wts, mapping_np, ranks, scal, *host, tokens=rng.choice(T, n0, replace=False))
+    fwd(xb, ids, wts, mapping_np, ranks, scal, *host, tokens=rng.choice(T, n0, replace=False))
     per_tok = (time.perf_counter() - t0) / n0
     n = int(max(n0, min(T, target_s / max(per_tok, 1e-9))))
     if max_tokens:
         n = min(n, max_tokens)
     toks = np.sort(rng.choice(T, n, replace=False))
     t0 = time.perf_counter()
-    st, _ = oracle.forward(xb, ids, wts, mapping_np, ranks, scal, *host, tokens=toks)
+    st, _ = fwd(xb, ids, wts, mapping_np, ranks, scal, *host, tokens=toks)
     secs = time.perf_counter() - t0
     assert st == 0
     return n / secs, n, secs, oracle.max_threads()
@@ -385,18 +406,19 @@ def run_reference(args, rank, world):
         return None
     oracle.build()
     dev = "cpu"
-    cfg, b, w, x = make_inputs(args.config, dev, args.seed)
+    fp8 = args.weights == "fp8"
+    cfg, b, w, x, q = make_inputs(args.config, dev, args.seed, fp8)
     st, mp, _ = oracle.batch_info(b.seg_indptr.numpy(), b.weight_indices.numpy(), b.lora_ranks.numpy(),
                                   cfg.num_tokens)
     # each step a bounded sample: the whole run takes about 90 s of oracle time
     per_step_target = max(0.25, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target, max_tokens=args.ref_tokens)
+        oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target, max_tokens=args.ref_tokens, q=q)
     rates, ns, secs = [], 0, 0.0
     thr = 1
     for i in range(args.steps):
         r, n, s, thr = oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target,
-                                          max_tokens=args.ref_tokens, seed=i)
+                                          max_tokens=args.ref_tokens, seed=i, q=q)
         rates.append(r)
         ns += n
         secs += s
@@ -407,7 +429,8 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "tokens": cfg.num_tokens, "hidden": cfg.hidden,
                        "intermediate": cfg.intermediate, "experts": cfg.num_experts, "topk": cfg.topk,
-                       "loras": cfg.num_loras, "max_rank": cfg.max_rank, "seed": args.seed},
+                       "loras": cfg.num_loras, "max_rank": cfg.max_rank, "seed": args.seed,
+                       "weights": WEIGHT_LABEL[args.weights]},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                              "sample": f"{ns} tokens over {args.steps} steps (seeded samples of the "
                                        f"{cfg.num_tokens}-token batch), fp64 C oracle, OpenMP over tokens"},
@@ -427,7 +450,8 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lib = mlr.library()
-    cfg, b, w, x = make_inputs(args.config, dev, args.seed + rank)
+    fp8 = args.weights == "fp8"
+    cfg, b, w, x, q = make_inputs(args.config, dev, args.seed + rank, fp8)
     T, K, E, H, I, L, R = (cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.hidden, cfg.intermediate,
                            cfg.num_loras, cfg.max_rank)
     max_len = int(b.seg_lens.max())
@@ -435,21 +459,27 @@ def run_ours(args, rank, world, dist):
     mapping = torch.empty(T, dtype=torch.int32, device=dev)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mlr.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R), dtype=torch.uint8, device=dev)
-    wk = {k: getattr(w, k) for k in ("w_gate_up", "w_down", "lora_a_gu", "lora_b_gu", "lora_a_down",
-                                     "lora_b_down")}
+    lk = {k: getattr(w, k) for k in ("lora_a_gu", "lora_b_gu", "lora_a_down", "lora_b_down")}
+    if fp8:
+        forward = mlr.fused_moe_lora_forward_fp8
+        wk = dict(w_gate_up_q=q.w_gate_up_q, w_gate_up_scale=q.w_gate_up_scale, w_down_q=q.w_down_q,
+                  w_down_scale=q.w_down_scale, **lk)
+    else:
+        forward = mlr.fused_moe_lora_forward
+        wk = dict(w_gate_up=w.w_gate_up, w_down=w.w_down, **lk)
 
     def step():
         mlr.moe_lora_batch_info(b.seg_indptr, b.weight_indices, b.lora_ranks, T, max_len,
                                 adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
-        mlr.fused_moe_lora_forward(x, b.topk_ids, b.topk_weights, mapping, b.lora_ranks, b.scalings,
-                                   **wk, y=y, workspace=ws, check=False)
+        forward(x, b.topk_ids, b.topk_weights, mapping, b.lora_ranks, b.scalings, **wk, y=y, workspace=ws,
+                check=False)
 
-    # correctness gate before timing: status word and a sampled oracle check
+    # correctness gate before timing: the status word of a checked call
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     mlr.moe_lora_batch_info(b.seg_indptr, b.weight_indices, b.lora_ranks, T, max_len,
                             adapter_enabled=enabled, token_lora_mapping=mapping)
-    mlr.fused_moe_lora_forward(x, b.topk_ids, b.topk_weights, mapping, b.lora_ranks, b.scalings, **wk,
-                               y=y, workspace=ws, status=status)
+    forward(x, b.topk_ids, b.topk_weights, mapping, b.lora_ranks, b.scalings, **wk, y=y, workspace=ws,
+            status=status)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -481,9 +511,8 @@ def run_ours(args, rank, world, dist):
         d = dev_in[sl]
         mlr.moe_lora_batch_info(d["seg_indptr"], d["weight_indices"], d["lora_ranks"], T,
                                 max_len, adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
-        mlr.fused_moe_lora_forward(d["x"], d["topk_ids"], d["topk_weights"], mapping,
-                                   d["lora_ranks"], d["scalings"], **wk, y=y_dev[sl], workspace=ws,
-                                   check=False)
+        forward(d["x"], d["topk_ids"], d["topk_weights"], mapping, d["lora_ranks"], d["scalings"], **wk,
+                y=y_dev[sl], workspace=ws, check=False)
 
     def download(sl):
         y_host[sl].copy_(y_dev[sl], non_blocking=True)
@@ -498,11 +527,11 @@ def run_ours(args, rank, world, dist):
 
     # sampled correctness against the oracle and the CPU baseline
     mp_np = mapping.cpu().numpy()
-    flops, byts, st_work = layer_work(cfg, b, mapping)
+    flops, byts, st_work = layer_work(cfg, b, mapping, fp8)
     cpu = None
     if not args.no_cpu_baseline:
         oracle.build()
-        rate, n, secs, thr = oracle_sample_rate(cfg, b, w, x, mp_np, target_s=args.cpu_seconds)
+        rate, n, secs, thr = oracle_sample_rate(cfg, b, w, x, mp_np, target_s=args.cpu_seconds, q=q)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                "sample": f"{n} seeded tokens of the {T}-token batch ({secs:.1f} s), fp64 C oracle, "
                          f"OpenMP over tokens"}
@@ -514,7 +543,7 @@ def run_ours(args, rank, world, dist):
     rf["kernel"] = STAGE_KERNELS.get(dom, dom)
     rf["stage"] = dom
     rf["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    tr = recorded_traffic(dom, cfg.name)
+    tr = recorded_traffic(dom, cfg.name + ("_fp8" if fp8 else ""))
     rf["traffic"] = tr
     rf["algorithmic_bytes"] = int(st_work[dom][1])
     rf["algorithmic_flops"] = int(st_work[dom][0])
@@ -529,6 +558,7 @@ def run_ours(args, rank, world, dist):
             "data": "synthetic",
             "config": {"workload": cfg.name, "tokens": T, "hidden": H, "intermediate": I, "experts": E,
                        "topk": K, "loras": L, "max_rank": R, "seed": args.seed,
+                       "weights": WEIGHT_LABEL[args.weights],
                        "parallelism": f"dp{world} (replicas)" if world > 1 else "single GPU",
                        "l2": f"no flush: each step streams {byts / 1e9:.2f} GB of algorithmic bytes "
                              f"(> 129 MB L2)"},
@@ -550,6 +580,7 @@ LINEAR_CONFIGS = {
     "mla_fused_proj": {"tokens": 8192, "in": 7168, "offsets": (0, 1536, 2112), "loras": 4, "max_rank": 64,
                        "ranks": (16, 32, 64, 64), "segments": 8},
 }
+WEIGHT_LABEL = {"bf16": "bf16", "fp8": "fp8 e4m3, fp32 scale per 128x128 block (bf16 LoRA)"}
 LINEAR_METRIC = "MLA fused-projection LoRA tokens/s and % of roofline (bf16, 1×GB300)"
 
 
@@ -773,11 +804,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen_moe_prefill")
+    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                    help="base expert weights of the MoE workloads: bf16, or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
+    if args.config in LINEAR_CONFIGS and args.weights != "bf16":
+        ap.error("--weights applies to the MoE workloads only")
     if args.warmup < 3:
         args.warmup = 3
 

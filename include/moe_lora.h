@@ -195,6 +195,36 @@ int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const flo
                            int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
                            size_t ws_bytes, int32_t* d_status, void* stream);
 
+/*
+ * fused_moe_lora_forward_fp8 -- the same layer with FP8 base experts (sglang
+ * PR #22323 page, 功能与动机 and 实现拆解 item 1: quantised MoE methods hand
+ * their scales to the LoRA MoE layer, which then runs on quantised experts).
+ *
+ * The pages name the methods, not a format.  Here: w_gate_up_q [E, 2I, H]
+ * and w_down_q [E, H, I] hold FP8 E4M3 codes (one byte each, same row order as
+ * the bf16 weights).  w_gate_up_scale [E, ceil(2I/128), ceil(H/128)] and
+ * w_down_scale [E, ceil(H/128), ceil(I/128)] are float32 scales.  Weight
+ * (e, row, col) = value of its code x scale[e][row / 128][col / 128]: the
+ * DeepSeek-V3 block-FP8 layout (128 x 128 blocks, inverse scales).  x, the
+ * LoRA stacks and y stay bf16; only the base weights are quantised.  All
+ * other arguments, the workspace (fused_moe_lora_workspace_bytes) and the
+ * status behaviour are those of fused_moe_lora_forward.  Additional limits:
+ * hidden and intermediate multiples of 16; the scale arrays non-null and
+ * 4-byte aligned (else MLR_ERR_INVALID; sizes MLR_ERR_UNSUPPORTED).  Each
+ * weight is dequantised to bf16 on chip (one rounding of code x scale), so
+ * y matches the exact dequantised layer within the bf16 forward's tolerance.
+ */
+int fused_moe_lora_forward_fp8(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                               const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                               const float* scalings, const uint8_t* w_gate_up_q,
+                               const float* w_gate_up_scale, const uint8_t* w_down_q,
+                               const float* w_down_scale, const mlr_bf16* lora_a_gu,
+                               const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                               const mlr_bf16* lora_b_down, int32_t num_tokens, int32_t topk,
+                               int32_t num_experts, int32_t hidden, int32_t intermediate,
+                               int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
+                               size_t ws_bytes, int32_t* d_status, void* stream);
+
 /* Scratch bytes lora_linear_forward needs for these sizes (0 on bad sizes). */
 size_t lora_linear_workspace_bytes(int32_t num_tokens, int32_t in_features, int32_t out_features,
                                    int32_t num_loras, int32_t max_rank, int32_t num_slices);

@@ -95,6 +95,8 @@ def library() -> ctypes.CDLL:
                 lib.fused_moe_lora_workspace_bytes.argtypes = [i32] * 7
                 lib.fused_moe_lora_forward.restype = ctypes.c_int
                 lib.fused_moe_lora_forward.argtypes = [vp] * 12 + [i32] * 7 + [vp, vp, sz, vp, vp]
+                lib.fused_moe_lora_forward_fp8.restype = ctypes.c_int
+                lib.fused_moe_lora_forward_fp8.argtypes = [vp] * 14 + [i32] * 7 + [vp, vp, sz, vp, vp]
             if hasattr(lib, "lora_linear_forward"):
                 lib.lora_linear_workspace_bytes.restype = sz
                 lib.lora_linear_workspace_bytes.argtypes = [i32] * 6
@@ -295,6 +297,81 @@ def fused_moe_lora_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_r
     _check_host(code, "fused_moe_lora_forward")
     if check:
         _check_device(status, "fused_moe_lora_forward")
+    return y
+
+
+def _codes(t: torch.Tensor, name: str, dev) -> torch.Tensor:
+    """FP8 E4M3 weights as their byte codes (uint8 or float8_e4m3fn tensors)."""
+    if hasattr(torch, "float8_e4m3fn") and t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    _req(t, name, torch.uint8, dev)
+    return t
+
+
+def fused_moe_lora_forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                               w_gate_up_q, w_gate_up_scale, w_down_q, w_down_scale,
+                               lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
+                               y: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None,
+                               check: bool = True, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The layer with FP8 E4M3 base experts and 128 x 128 block scales.
+
+    w_gate_up_q [E,2I,H] and w_down_q [E,H,I]: uint8 (or float8_e4m3fn) codes;
+    w_gate_up_scale [E,ceil(2I/128),ceil(H/128)] and w_down_scale
+    [E,ceil(H/128),ceil(I/128)]: float32, weight = code value x block scale.
+    Everything else as in fused_moe_lora_forward.
+    """
+    lib = library()
+    if not hasattr(lib, "fused_moe_lora_forward_fp8"):
+        raise RuntimeError("library built without fused_moe_lora_forward_fp8")
+    dev = x.device
+    bf = torch.bfloat16
+    _req(x, "x", bf, dev)
+    _req(topk_ids, "topk_ids", torch.int32, dev)
+    _req(topk_weights, "topk_weights", torch.float32, dev)
+    _req(token_lora_mapping, "token_lora_mapping", torch.int32, dev)
+    _req(lora_ranks, "lora_ranks", torch.int32, dev)
+    _req(scalings, "scalings", torch.float32, dev)
+    wq = _codes(w_gate_up_q, "w_gate_up_q", dev)
+    dq = _codes(w_down_q, "w_down_q", dev)
+    _req(w_gate_up_scale, "w_gate_up_scale", torch.float32, dev)
+    _req(w_down_scale, "w_down_scale", torch.float32, dev)
+    for t, n in ((lora_a_gu, "lora_a_gu"), (lora_b_gu, "lora_b_gu"), (lora_a_down, "lora_a_down"),
+                 (lora_b_down, "lora_b_down")):
+        _req(t, n, bf, dev)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    E, I2, H2 = wq.shape
+    I = I2 // 2
+    L, _, _, R, _ = lora_a_gu.shape
+    cb = lambda n: (n + 127) // 128  # noqa: E731
+    if (H2 != H or tuple(dq.shape) != (E, H, I)
+            or tuple(w_gate_up_scale.shape) != (E, cb(2 * I), cb(H))
+            or tuple(w_down_scale.shape) != (E, cb(H), cb(I))
+            or tuple(lora_a_gu.shape) != (L, E, 2, R, H)
+            or tuple(lora_b_gu.shape) != (L, E, 2, I, R) or tuple(lora_a_down.shape) != (L, E, R, I)
+            or tuple(lora_b_down.shape) != (L, E, H, R) or tuple(topk_ids.shape) != (T, K)
+            or tuple(topk_weights.shape) != (T, K) or token_lora_mapping.numel() < T
+            or lora_ranks.numel() != L or scalings.numel() != L):
+        raise ValueError("fused_moe_lora_forward_fp8: inconsistent shapes")
+    if y is None:
+        y = torch.empty(T, H, dtype=bf, device=dev)
+    _req(y, "y", bf, dev)
+    wsb = int(lib.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R))
+    if wsb == 0 and T > 0:
+        raise ValueError("fused_moe_lora_forward_fp8: unsupported sizes")
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    if check and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = lib.fused_moe_lora_forward_fp8(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(token_lora_mapping), _ptr(lora_ranks),
+        _ptr(scalings), _ptr(wq), _ptr(w_gate_up_scale), _ptr(dq), _ptr(w_down_scale), _ptr(lora_a_gu),
+        _ptr(lora_b_gu), _ptr(lora_a_down), _ptr(lora_b_down), T, K, E, H, I, L, R, _ptr(y),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check_host(code, "fused_moe_lora_forward_fp8")
+    if check:
+        _check_device(status, "fused_moe_lora_forward_fp8")
     return y
 
 

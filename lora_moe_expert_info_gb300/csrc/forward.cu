@@ -68,6 +68,10 @@ enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 // one warp per quarter.
 template <int KIND> constexpr int kEpiWarps = (KIND == kGateUp || KIND == kDown) ? 8 : 4;
 template <int KIND> constexpr int kThreadsOf = (kEpiWarp0 + kEpiWarps<KIND>) * 32;
+// FP8-weight kernels add three converter warps after the epilogue (16 warps,
+// 512 threads): with warps 1-3 they are the six converter warps.
+constexpr int kCvWarps = 6;
+template <int KIND, bool Q> constexpr int kLaunchThreads = kThreadsOf<KIND> + (Q ? 96 : 0);
 
 template <int KIND> struct Cfg;
 // The shrinks stage two 64-wide K chunks per ring slot (LoRA A in [0, 32 KB),
@@ -157,6 +161,8 @@ struct Params {
   int ykeep;      // down: 1 if y_acc fits in half of L2 (its reductions are then marked evict-last)
   int zslice_blk; // down: 256-row blocks from this index on read the second rank slice of z (split B)
   int w3;         // gate_up: 1 if the gate+up weight map exists
+  int wsr, wsc;   // FP8 weights: 128-row and 128-column scale blocks per expert matrix
+  const float* wscale;  // FP8 weights: [E][wsr][wsc] block scales (weight = code x scale)
   int64_t P;
   const float* topk_weights;
   const int32_t* lora_ranks;
@@ -177,6 +183,7 @@ struct __align__(16) Ctl {
   TileRec rec_p, rec_m;  // the current base tile of the producer / MMA warp
   uint64_t full[8];   // one per ring stage (at most 8)
   uint64_t empty[8];
+  uint64_t raw_full[8];  // FP8 weights: the stage's raw weight tile has landed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;  // pairs: the leader's last commit, waited for before the teardown
@@ -327,9 +334,15 @@ struct ExpandCursor {
   }
 };
 
-template <int KIND>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+// Q (gate_up and down only): the expert weights are FP8 E4M3 with 128 x 128
+// block scales.  The producer loads the raw codes of a K step into the upper
+// half of the stage's weight area; warps 1-3 convert them in place into the
+// bf16 tile the MMAs read (code x scale, 128-byte swizzle), so the MMAs, the
+// LoRA expand and the epilogue are those of the bf16 kernel.
+template <int KIND, bool Q = false>
+__global__ void __launch_bounds__(Q ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
+  static_assert(!Q || KIND == kGateUp || KIND == kDown, "FP8 weights: the base GEMMs only");
   using CF = Cfg<KIND>;
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
@@ -356,8 +369,11 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&c.full[s], 1);
+      // FP8: the producer's arrival plus one per converter warp (on a pair,
+      // both CTAs' converter warps arrive on the leader's barrier)
+      mbar_init(&c.full[s], Q ? 1 + (kPair ? 2 : 1) * kCvWarps : 1);
       mbar_init(&c.empty[s], 1);
+      if (Q) mbar_init(&c.raw_full[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.acc_full[b], 1);
@@ -474,27 +490,43 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               // B operand: rows of x_sorted (gate_up shrink) or h (down shrink), both chunks
               tma_load_3d(sbuf + 32768, &maps.m[xh == 64 ? kX2x64 : kX2x128], &c.full[st], 0, it.row0, c0);
             } else if (KIND == kGateUp) {
-              mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
               const int i0 = it.mb * 128;
-              if (p.w3) {
-                tma_load_3d(sbuf, &maps.m[kW3], &c.full[st], kb * 64, i0, it.e * 2);
+              if (Q) {
+                // raw codes of the gate and up blocks: [gate|up][128 rows][64 bytes]
+                mbar_arrive_expect_tx(&c.raw_full[st], 16384);
+                tma_load_3d(sbuf + 16384, &maps.m[kW], &c.raw_full[st], kb * 64, i0, it.e * 2);
+                mbar_arrive_expect_tx(&c.full[st], rbytes);
               } else {
-                tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
-                tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+                mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
+                if (p.w3) {
+                  tma_load_3d(sbuf, &maps.m[kW3], &c.full[st], kb * 64, i0, it.e * 2);
+                } else {
+                  tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
+                  tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+                }
               }
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else {  // kDown, on a CTA pair: this CTA's 128 weight rows and half of the tile's rows
               static_assert(!(KIND == kDown) || kPair, "down runs on CTA pairs");
               const int hh = pair_row_box(it.nrows);
-              if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
               const uint32_t fb = cluster_addr(&c.full[st], 0);
-              tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * p.H + it.mb * 256 + (int)rank * 128);
+              if (Q) {
+                // this CTA's 128 raw weight rows of 64 bytes, on its own barrier
+                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * hh * 128);
+                mbar_arrive_expect_tx(&c.raw_full[st], 8192);
+                tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * 64, it.mb * 256 + (int)rank * 128,
+                            it.e);
+              } else {
+                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
+                tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * p.H + it.mb * 256 + (int)rank * 128);
+              }
               tma_load_2d_pair(sbuf + 16384, &maps.m[pair_row_slot(hh)], fb, 0,
                                kb * p.cap + it.row0 + (int)rank * (it.nrows >> 1));
             }
           } else {
             // expand step: LoRA B chunk (A operand) + z rows of the piece (B operand)
+            if (Q) mbar_arrive(&c.raw_full[st]);  // no raw weights: the converters only pass
             const int4 pc = it.piece(cur.b);  // {j0 | nj << 16, l, r16, zrow}
             const int pl = pc.y, pr16 = pc.z, zrow = pc.w;
             const int g = cur.g, kg = cur.kg;
@@ -529,6 +561,86 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           }
         }
       }
+    }
+  } else if (Q && (warp < 4 || warp >= kThreadsOf<KIND> / 32)) {
+    // ================ converters (FP8 weights): raw codes -> bf16 tile ================
+    // Warps 1-3 and the three warps after the epilogue.  The raw codes sit in
+    // the upper half of the stage's weight area, which the bf16 tile also
+    // covers, so every thread first holds its raw chunks in registers and the
+    // group meets once (a barrier that also votes on giving up) before anyone
+    // writes; then each warp converts its chunks and arrives on its own.  A
+    // chunk's block scale is fetched before its raw tile is waited for.
+    constexpr int kCv = kCvWarps * 32;
+    constexpr int kRawOff = KIND == kGateUp ? 16384 : 8192;  // raw codes within the stage
+    constexpr int kChunks = KIND == kGateUp ? 1024 : 512;     // 16-byte raw chunks per K step
+    constexpr int kPer = (kChunks + kCv - 1) / kCv;
+    const int ct = warp < 4 ? tid - 32 : 96 + tid - kThreadsOf<KIND>;
+    int gs = 0;
+    for (int item = unit; item < n_items; item += n_units) {
+      const Item it = load_item<KIND>(p, item);
+      const int nsteps = nks + it.nexp;
+      bool stop = false;
+      for (int s = 0; s < nsteps; ++s, ++gs) {
+        const int st = gs % S, round = gs / S;
+        const uint32_t sb = smem_u32(smem + st * SB);
+        float scv[kPer];
+        if (s < nks) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const int q = ct + kCv * j;
+            // gate_up: q = (g, r, c4) of [gate|up][128 rows][4 chunks]; down: (r, c4)
+            const int g = KIND == kGateUp ? (q >> 9) & 1 : 0;
+            const int r = (q >> 2) & 127;
+            scv[j] = 0.f;
+            if (q < kChunks) {
+              if (KIND == kGateUp) {
+                const int row = it.mb * 128 + r;  // row of the gate or up matrix
+                if (row < p.I)
+                  scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + (g * p.I + row) / 128) * p.wsc + (s >> 1));
+              } else {
+                const int row = it.mb * 256 + (int)rank * 128 + r;  // row of W_down (an H index)
+                if (row < p.H) scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + row / 128) * p.wsc + (s >> 1));
+              }
+            }
+          }
+        }
+        const bool w_ok = mbar_wait(&c.raw_full[st], round & 1, abort);
+        uint4 raw[kPer];
+        if (s < nks) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const int q = ct + kCv * j;
+            if (q < kChunks) raw[j] = lds128(sb + kRawOff + q * 16);  // (unused if the wait failed)
+          }
+        }
+        // every raw chunk is in registers, and every thread takes the same decision
+        if (named_bar_any(4, kCv, !w_ok)) {
+          stop = true;
+          break;
+        }
+        if (s < nks) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const int q = ct + kCv * j;
+            if (q >= kChunks) continue;
+            const int g = KIND == kGateUp ? q >> 9 : 0;
+            const int r = (q >> 2) & 127, c4 = q & 3;
+            const float sc = scv[j];
+            const uint2 a = e4m3x4_scaled_bf16(raw[j].x, sc), b = e4m3x4_scaled_bf16(raw[j].y, sc);
+            const uint2 d = e4m3x4_scaled_bf16(raw[j].z, sc), e = e4m3x4_scaled_bf16(raw[j].w, sc);
+            const uint32_t rowa = sb + g * 16384 + r * 128;
+            sts128(rowa + (((2 * c4) ^ (r & 7)) * 16), make_uint4(a.x, a.y, b.x, b.y));
+            sts128(rowa + (((2 * c4 + 1) ^ (r & 7)) * 16), make_uint4(d.x, d.y, e.x, e.y));
+          }
+          fence_proxy_async_smem();  // the tile is read next by the tensor cores
+        }
+        __syncwarp();  // this warp's chunks are written
+        if (lane == 0) {
+          if (kPair) mbar_arrive_cluster(cluster_addr(&c.full[st], 0));  // the leader's barrier
+          else mbar_arrive(&c.full[st]);
+        }
+      }
+      if (stop) break;
     }
   } else if (warp == 4) {
     // ================== MMA (the warp loads items, one thread issues) ==================
@@ -1448,14 +1560,14 @@ int sm_count() {
 }
 
 // Persistent launch: one CTA per SM (or fewer when there are fewer items).
-template <int KIND>
+template <int KIND, bool Q = false>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
   const int smem = smem_bytes<KIND>();
   // the shared-memory opt-in and the resident-cluster count are per device
   const int dev = current_device();
   static bool configured[64] = {};
   if (dev < 0 || !configured[dev]) {
-    if (cudaFuncSetAttribute(moe_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(moe_gemm_kernel<KIND, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MLR_ERR_CUDA;
     if (dev >= 0) configured[dev] = true;
@@ -1472,7 +1584,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreadsOf<KIND>);
+    cfg.blockDim = dim3(kLaunchThreads<KIND, Q>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1482,17 +1594,17 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     if (resident == 0) {
       cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND>, &cfg) != cudaSuccess || n <= 0)
+      if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND, Q>, &cfg) != cudaSuccess || n <= 0)
         return MLR_ERR_CUDA;
       resident = n;
       if (dev >= 0) resident_of[dev] = n;
     }
     const int64_t pairs = max_items < resident ? max_items : resident;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
-    if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND, Q>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
   } else {
     const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-    moe_gemm_kernel<KIND><<<grid, kThreadsOf<KIND>, smem, stream>>>(maps, p);
+    moe_gemm_kernel<KIND, Q><<<grid, kLaunchThreads<KIND, Q>, smem, stream>>>(maps, p);
     MLR_CHECK_LAUNCH();
   }
   note_launch();
@@ -1536,26 +1648,48 @@ extern "C" size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t top
   return f.ok ? (size_t)f.total : 0;
 }
 
-extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
-                                      const int32_t* token_lora_mapping, const int32_t* lora_ranks,
-                                      const float* scalings, const mlr_bf16* w_gate_up,
-                                      const mlr_bf16* w_down, const mlr_bf16* lora_a_gu,
-                                      const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
-                                      const mlr_bf16* lora_b_down, int32_t T, int32_t K, int32_t E,
-                                      int32_t H, int32_t I, int32_t L, int32_t R, mlr_bf16* y,
-                                      void* workspace, size_t ws_bytes, int32_t* d_status,
-                                      void* stream_) {
-  using namespace mlr;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+namespace mlr {
+namespace {
+
+// 3-D uint8 view {d0, d1, d2} with byte strides s1 (dim 1) and s2 (dim 2), no
+// swizzle (FP8 weight codes, read by the converters as plain rows).
+bool make_map3_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                  uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The layer.  fp8: w_gate_up / w_down hold E4M3 codes with block scales
+// s_gu [E][ceil(2I/128)][ceil(H/128)] and s_d [E][ceil(H/128)][ceil(I/128)];
+// otherwise they are bf16 and the scales are unused.
+int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                const int32_t* token_lora_mapping, const int32_t* lora_ranks, const float* scalings,
+                const void* w_gate_up, const void* w_down, const float* s_gu, const float* s_d, bool fp8,
+                const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                const mlr_bf16* lora_b_down, int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L,
+                int32_t R, mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                cudaStream_t stream) {
   const FwdLayout f = fwd_layout(T, K, E, H, I, L, R);
   if (!f.ok) {
     if (T < 0 || K < 1 || E < 1 || L < 0 || R < 0) return MLR_ERR_INVALID;
     return MLR_ERR_UNSUPPORTED;
   }
+  // FP8 codes are one byte: the TMA row strides (H and I bytes) must be 16-byte multiples
+  if (fp8 && (H % 16 != 0 || I % 16 != 0)) return MLR_ERR_UNSUPPORTED;
   if (T == 0) return MLR_OK;
   const void* need[] = {x, topk_ids, topk_weights, token_lora_mapping, w_gate_up, w_down, y};
   for (const void* q : need)
     if (q == nullptr) return MLR_ERR_INVALID;
+  if (fp8 && (s_gu == nullptr || s_d == nullptr || (reinterpret_cast<uintptr_t>(s_gu) & 3) != 0 ||
+              (reinterpret_cast<uintptr_t>(s_d) & 3) != 0))
+    return MLR_ERR_INVALID;
   if (L > 0) {
     const void* lo[] = {lora_ranks, scalings, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down};
     for (const void* q : lo)
@@ -1596,11 +1730,17 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
             make_shrink2_maps(m_sgu, xs, cap, H, lora_a_gu, L, E, R, &abox_gu, &a3_gu, &aw_gu, &rm_sgu) &&
             make_shrink1_maps(m_sd, hbuf, cap, I, lora_a_down, L, E, R, &abox_d, &aw_d, &rm_sd) &&
             make_down_maps(m_dn, w_down, H, I, E, hbuf, cap, lora_b_down, L, R, zd, zcap, f.R16 / 8);
-  if (ok && I >= 128) {
+  if (ok && I >= 128 && !fp8) {
     // W_gate_up as [(e, gate|up)][row][k]: a box {64, 128, 2} is a 128-row block of gate and of up
     ok = make_map3(&m_gu.m[kW3], w_gate_up, H, I, (uint64_t)E * 2, (uint64_t)H * 2, (uint64_t)I * H * 2, 64, 128, 2,
                    true);
     w3 = 1;
+  }
+  if (ok && fp8) {
+    // codes: W_gate_up as [(e, gate|up)][I rows][H bytes], a box of 64 bytes x 128 rows of gate and
+    // of up; W_down as [e][H rows][I bytes], a box of 64 bytes x 128 rows.  Rows past I (or H) read 0.
+    ok = make_map3_u8(&m_gu.m[kW], w_gate_up, H, I, (uint64_t)E * 2, H, (uint64_t)I * H, 64, 128, 2) &&
+         make_map3_u8(&m_dn.m[kW], w_down, I, H, E, I, (uint64_t)H * I, 64, 128, 1);
   }
   if (ok && L > 0) {
     // gate_up expand: LoRA B stacks as [rank chunk][row][8] (each row's ranks are
@@ -1702,7 +1842,10 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   {
     Params q = p;
     q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128); q.rmask = rm_gu; q.w3 = w3;
-    if ((rc = launch_gemm<kGateUp>(m_gu, q, f.max_base, stream)) != MLR_OK) return rc;
+    q.wscale = s_gu; q.wsr = (int)ceil_div(2 * I, 128); q.wsc = (int)ceil_div(H, 128);
+    rc = fp8 ? launch_gemm<kGateUp, true>(m_gu, q, f.max_base, stream)
+             : launch_gemm<kGateUp>(m_gu, q, f.max_base, stream);
+    if (rc != MLR_OK) return rc;
   }
   prof_mark(prof, 3, stream);
   if (L > 0) {
@@ -1719,7 +1862,10 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
     Params q = p;
     q.n_tiles = counts; q.nblk = (int)ceil_div(H, 256); q.rmask = rm_dn;  // a pair covers 256 rows of H
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
-    if ((rc = launch_gemm<kDown>(m_dn, q, f.max_base, stream)) != MLR_OK) return rc;
+    q.wscale = s_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
+    rc = fp8 ? launch_gemm<kDown, true>(m_dn, q, f.max_base, stream)
+             : launch_gemm<kDown>(m_dn, q, f.max_base, stream);
+    if (rc != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * H;
@@ -1728,6 +1874,39 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
   note_launch();
   prof_mark(prof, 6, stream);
   return MLR_OK;
+}
+
+}  // namespace
+}  // namespace mlr
+
+extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                                      const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                                      const float* scalings, const mlr_bf16* w_gate_up,
+                                      const mlr_bf16* w_down, const mlr_bf16* lora_a_gu,
+                                      const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                                      const mlr_bf16* lora_b_down, int32_t T, int32_t K, int32_t E,
+                                      int32_t H, int32_t I, int32_t L, int32_t R, mlr_bf16* y,
+                                      void* workspace, size_t ws_bytes, int32_t* d_status,
+                                      void* stream_) {
+  return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up, w_down,
+                          nullptr, nullptr, false, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I,
+                          L, R, y, workspace, ws_bytes, d_status, static_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int fused_moe_lora_forward_fp8(const mlr_bf16* x, const int32_t* topk_ids,
+                                          const float* topk_weights, const int32_t* token_lora_mapping,
+                                          const int32_t* lora_ranks, const float* scalings,
+                                          const uint8_t* w_gate_up_q, const float* w_gate_up_scale,
+                                          const uint8_t* w_down_q, const float* w_down_scale,
+                                          const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu,
+                                          const mlr_bf16* lora_a_down, const mlr_bf16* lora_b_down, int32_t T,
+                                          int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R,
+                                          mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                          void* stream_) {
+  return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up_q,
+                          w_down_q, w_gate_up_scale, w_down_scale, true, lora_a_gu, lora_b_gu, lora_a_down,
+                          lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes, d_status,
+                          static_cast<cudaStream_t>(stream_));
 }
 
 // ------------------------------------------------------------------------

@@ -276,6 +276,69 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Barrier over `count` threads that also ORs `pred` over them: every
+// participant gets the same answer (a uniform exit decision).
+__device__ __forceinline__ bool named_bar_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// 16-byte shared-memory load / store at a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tensor-core operands written by threads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four FP8 E4M3 codes (byte j of w is element j) times `sc`, rounded to bf16:
+// element 2i in the low half of word i of the result.  E4M3 values convert to
+// f16 exactly; the product is formed in fp32.
+__device__ __forceinline__ uint2 e4m3x4_scaled_bf16(uint32_t w, float sc) {
+  uint2 o;
+  asm("{\n\t"
+      ".reg .b16 l16, h16;\n\t"
+      ".reg .b32 p01, p23;\n\t"
+      ".reg .f16 a0, a1, a2, a3;\n\t"
+      ".reg .f32 f0, f1, f2, f3;\n\t"
+      "mov.b32 {l16, h16}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p01, l16;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p23, h16;\n\t"
+      "mov.b32 {a0, a1}, p01;\n\t"
+      "mov.b32 {a2, a3}, p23;\n\t"
+      "cvt.f32.f16 f0, a0;\n\t"
+      "cvt.f32.f16 f1, a1;\n\t"
+      "cvt.f32.f16 f2, a2;\n\t"
+      "cvt.f32.f16 f3, a3;\n\t"
+      "mul.rn.f32 f0, f0, %3;\n\t"
+      "mul.rn.f32 f1, f1, %3;\n\t"
+      "mul.rn.f32 f2, f2, %3;\n\t"
+      "mul.rn.f32 f3, f3, %3;\n\t"
+      "cvt.rn.bf16x2.f32 %0, f1, f0;\n\t"
+      "cvt.rn.bf16x2.f32 %1, f3, f2;\n\t"
+      "}"
+      : "=r"(o.x), "=r"(o.y)
+      : "r"(w), "f"(sc));
+  return o;
+}
+
 // Vector fp32 reduction into global memory (16-byte aligned address).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),

@@ -227,6 +227,42 @@ def make_weights(cfg: LayerConfig, ranks: torch.Tensor, device="cpu", seed: int 
     return LayerWeights(w_gate_up, w_down, a_gu, b_gu, a_d, b_d)
 
 
+@dataclasses.dataclass
+class Fp8Experts:
+    w_gate_up_q: torch.Tensor      # uint8 [E, 2I, H], FP8 E4M3 codes
+    w_gate_up_scale: torch.Tensor  # float32 [E, ceil(2I/128), ceil(H/128)]
+    w_down_q: torch.Tensor         # uint8 [E, H, I]
+    w_down_scale: torch.Tensor     # float32 [E, ceil(H/128), ceil(I/128)]
+
+
+def make_fp8_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> Fp8Experts:
+    """FP8 E4M3 expert weights with one float32 scale per 128 x 128 block.
+
+    Codes are N(0, 32^2) samples cast to E4M3 (torch's float8_e4m3fn); each
+    block's scale is U(0.75, 1.25) / (32 sqrt(fan_in)), so code x scale has
+    about the bf16 weights' N(0, 1/fan_in) spread and the scales are not
+    powers of two.
+    """
+    E, H, I = cfg.num_experts, cfg.hidden, cfg.intermediate
+    g = _gen(device, seed + 5)
+    nb = lambda n: (n + 127) // 128  # noqa: E731
+
+    def mat(rows, cols, fan_in):
+        z = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(32.0)
+        codes = z.to(torch.float8_e4m3fn).view(torch.uint8)
+        u = torch.rand((nb(rows), nb(cols)), generator=g, device=device, dtype=torch.float32)
+        return codes, (u * 0.5 + 0.75) / (32.0 * math.sqrt(fan_in))
+
+    wq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
+    ws = torch.empty(E, nb(2 * I), nb(H), dtype=torch.float32, device=device)
+    dq = torch.empty(E, H, I, dtype=torch.uint8, device=device)
+    ds = torch.empty(E, nb(H), nb(I), dtype=torch.float32, device=device)
+    for e in range(E):  # per expert keeps temporaries small at large sizes
+        wq[e], ws[e] = mat(2 * I, H, H)
+        dq[e], ds[e] = mat(H, I, I)
+    return Fp8Experts(wq, ws, dq, ds)
+
+
 def make_x(cfg: LayerConfig, device="cpu", seed: int = 0) -> torch.Tensor:
     g = _gen(device, seed + 3)
     return torch.randn(cfg.num_tokens, cfg.hidden, generator=g, device=device,

@@ -137,3 +137,17 @@ def test_profile_stage_selection_checks(lib):
     assert n == 7
     assert lib.moe_lora_profile_stages(1 << 3) == 0
     assert lib.moe_lora_profile_stages((1 << n) - 1) == 0  # back to every stage
+
+
+def test_fp8_forward_host_checks(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the calls return before any launch
+    f = lib.fused_moe_lora_forward_fp8
+    big = ctypes.c_size_t(1 << 30)
+    # hidden 136: a multiple of 8 (fine for bf16) but not of 16 (FP8 rows are bytes)
+    assert f(*([fake] * 14 + [64, 2, 8, 136, 512, 4, 16, fake, fake, big, None, None])) == mlr.MLR_ERR_UNSUPPORTED
+    assert f(*([fake] * 14 + [64, 2, 8, 256, 520, 4, 16, fake, fake, big, None, None])) == mlr.MLR_ERR_UNSUPPORTED
+    # a missing scale array
+    args = [fake] * 7 + [None] + [fake] * 6 + [64, 2, 8, 256, 512, 4, 16, fake, fake, big, None, None]
+    assert f(*args) == mlr.MLR_ERR_INVALID
+    args = [fake] * 9 + [None] + [fake] * 4 + [64, 2, 8, 256, 512, 4, 16, fake, fake, big, None, None]
+    assert f(*args) == mlr.MLR_ERR_INVALID
