@@ -85,7 +85,16 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 6, kStageByte
 
 // GEMM kinds that run on CTA pairs (cluster of two, M = 256 tensor-core MMAs):
 // each CTA loads half of every row tile, so the row bytes per SM drop by half.
-template <int KIND> constexpr bool kPairOf = KIND == kDown;
+// The FP8-weight down GEMM runs on single CTAs: a pair would need a
+// cluster-scope release from the peer's converters at every K step.
+template <int KIND, bool Q = false> constexpr bool kPairOf = KIND == kDown && !Q;
+
+// Ring of a GEMM: the FP8 down GEMM on a single CTA stages its 128 weight rows
+// [0, 16 KB) and all of the tile's rows [16 KB, 48 KB).
+template <int KIND, bool Q> struct CfgOf : Cfg<KIND> {};
+template <> struct CfgOf<kDown, true> {
+  static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256;
+};
 
 // Tensor maps of one GEMM kind, by slot.
 //   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
@@ -194,10 +203,11 @@ struct __align__(16) Ctl {
   float w[2][kTileRows];
 };
 
-template <int KIND>
+template <int KIND, bool Q = false>
 constexpr int smem_bytes() {
-  static_assert(Cfg<KIND>::kStages <= 8, "ring barriers");
-  return Cfg<KIND>::kStages * Cfg<KIND>::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) + 1024;
+  using CF = CfgOf<KIND, Q>;
+  static_assert(CF::kStages <= 8, "ring barriers");
+  return CF::kStages * CF::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) + 1024;
 }
 
 // SiLU(v) = v * sigmoid(v), with sigmoid(v) = (1 + tanh(v / 2)) / 2: one
@@ -343,13 +353,13 @@ template <int KIND, bool Q = false>
 __global__ void __launch_bounds__(Q ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   static_assert(!Q || KIND == kGateUp || KIND == kDown, "FP8 weights: the base GEMMs only");
-  using CF = Cfg<KIND>;
+  using CF = CfgOf<KIND, Q>;
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
   constexpr bool kShrink = (KIND == kShrinkGU || KIND == kShrinkD);
   constexpr int kGates = (KIND == kGateUp) ? 2 : 1;
 
-  constexpr bool kPair = kPairOf<KIND>;
+  constexpr bool kPair = kPairOf<KIND, Q>;
   const int n_items = *p.n_tiles * p.nblk;
   // work unit: a CTA, or for pairs a cluster (both CTAs take the same items and
   // leave together)
@@ -507,20 +517,20 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               }
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+            } else if (!kPair) {
+              // kDown with FP8 weights, on a single CTA: raw codes of 128 weight rows
+              // on their own barrier, then all of the tile's rows
+              static_assert(KIND != kDown || kPair || Q, "bf16 down runs on CTA pairs");
+              mbar_arrive_expect_tx(&c.raw_full[st], 8192);
+              tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * 64, it.mb * 128, it.e);
+              mbar_arrive_expect_tx(&c.full[st], rbytes);
+              for (int q = 0; q < rbox; ++q)
+                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else {  // kDown, on a CTA pair: this CTA's 128 weight rows and half of the tile's rows
-              static_assert(!(KIND == kDown) || kPair, "down runs on CTA pairs");
               const int hh = pair_row_box(it.nrows);
+              if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
               const uint32_t fb = cluster_addr(&c.full[st], 0);
-              if (Q) {
-                // this CTA's 128 raw weight rows of 64 bytes, on its own barrier
-                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * hh * 128);
-                mbar_arrive_expect_tx(&c.raw_full[st], 8192);
-                tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * 64, it.mb * 256 + (int)rank * 128,
-                            it.e);
-              } else {
-                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
-                tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * p.H + it.mb * 256 + (int)rank * 128);
-              }
+              tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * p.H + it.mb * 256 + (int)rank * 128);
               tma_load_2d_pair(sbuf + 16384, &maps.m[pair_row_slot(hh)], fb, 0,
                                kb * p.cap + it.row0 + (int)rank * (it.nrows >> 1));
             }
@@ -598,7 +608,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 if (row < p.I)
                   scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + (g * p.I + row) / 128) * p.wsc + (s >> 1));
               } else {
-                const int row = it.mb * 256 + (int)rank * 128 + r;  // row of W_down (an H index)
+                const int row = it.mb * 128 + r;  // row of W_down (an H index; single-CTA 128-row blocks)
                 if (row < p.H) scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + row / 128) * p.wsc + (s >> 1));
               }
             }
@@ -1562,7 +1572,7 @@ int sm_count() {
 // Persistent launch: one CTA per SM (or fewer when there are fewer items).
 template <int KIND, bool Q = false>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
-  const int smem = smem_bytes<KIND>();
+  const int smem = smem_bytes<KIND, Q>();
   // the shared-memory opt-in and the resident-cluster count are per device
   const int dev = current_device();
   static bool configured[64] = {};
@@ -1575,7 +1585,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   const int64_t max_items = max_tiles * p.nblk;
   if (max_items <= 0) return MLR_OK;
   if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
-  if (kPairOf<KIND>) {
+  if (kPairOf<KIND, Q>) {
     // clusters of two CTAs, as many as can be resident at once (a persistent
     // grid with one pair more than fits would run that pair after the others)
     cudaLaunchAttribute attr[1];
@@ -1740,7 +1750,16 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     // codes: W_gate_up as [(e, gate|up)][I rows][H bytes], a box of 64 bytes x 128 rows of gate and
     // of up; W_down as [e][H rows][I bytes], a box of 64 bytes x 128 rows.  Rows past I (or H) read 0.
     ok = make_map3_u8(&m_gu.m[kW], w_gate_up, H, I, (uint64_t)E * 2, H, (uint64_t)I * H, 64, 128, 2) &&
-         make_map3_u8(&m_dn.m[kW], w_down, I, H, E, I, (uint64_t)H * I, 64, 128, 1);
+         make_map3_u8(&m_dn.m[kW], w_down, I, H, E, I, (uint64_t)H * I, 64, 128, 1) &&
+         // the FP8 down GEMM runs on single CTAs: whole-tile row boxes over h, and
+         // z boxes of zrows rows (a CTA loads a piece's z rows whole)
+         make_row_maps(m_dn, hbuf, (uint64_t)ceil_div(I, 64) * cap, &rm_dn);
+    const int nc[3] = {8, 4, 2};
+    const int zslot[3] = {kZ8, kZ4, kZ2};
+    for (int j = 0; ok && L > 0 && j < 3; ++j) {
+      if (nc[j] > R / 8) continue;
+      ok = make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]);
+    }
   }
   if (ok && L > 0) {
     // gate_up expand: LoRA B stacks as [rank chunk][row][8] (each row's ranks are
@@ -1860,7 +1879,8 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   prof_mark(prof, 4, stream);
   {
     Params q = p;
-    q.n_tiles = counts; q.nblk = (int)ceil_div(H, 256); q.rmask = rm_dn;  // a pair covers 256 rows of H
+    // a pair covers 256 rows of H, a single CTA (FP8 weights) 128
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, fp8 ? 128 : 256); q.rmask = rm_dn;
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     q.wscale = s_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
     rc = fp8 ? launch_gemm<kDown, true>(m_dn, q, f.max_base, stream)
