@@ -68,3 +68,24 @@ def test_linear_stage_names():
     assert out == {"align_plan": 0.05, "gather": 0.04, "shrink": 0.03, "projection_gemm": 0.16,
                    "convert": 0.02, "marker_gaps": 0.003}
     assert abs(sum(out.values()) - sum(stages.values())) < 1e-9
+
+
+def test_layer_work_fp8_weights_are_one_byte_plus_block_scales():
+    import math
+
+    from lora_moe_expert_info_gb300 import workloads
+    cfg = workloads.CONFIGS["tiny"]
+    b = workloads.make_batch(cfg, device="cpu", seed=0)
+    # any mapping with valid adapters serves the byte count
+    mapping = torch.zeros(cfg.num_tokens, dtype=torch.int32)
+    f16, b16, s16 = bench.layer_work(cfg, b, mapping)
+    f8, b8, s8 = bench.layer_work(cfg, b, mapping, fp8=True)
+    assert f16 == f8 and {k: v[0] for k, v in s16.items()} == {k: v[0] for k, v in s8.items()}
+    H, I = cfg.hidden, cfg.intermediate
+    touched = torch.unique(b.topk_ids).numel()
+    nb = lambda n: math.ceil(n / 128)  # noqa: E731
+    per_expert_bf16 = 3 * H * I * 2
+    per_expert_fp8 = 3 * H * I + 4 * (nb(2 * I) * nb(H) + nb(H) * nb(I))
+    assert b16 - b8 == touched * (per_expert_bf16 - per_expert_fp8)
+    # the shrinks do not read base weights
+    assert s16["shrink_gate_up"] == s8["shrink_gate_up"] and s16["shrink_down"] == s8["shrink_down"]
