@@ -268,6 +268,28 @@ int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const int32_t* tok
                         int32_t* d_status, void* stream);
 
 /*
+ * lora_tp_qkv_b_rows -- the rows of a fused q/k/v projection's LoRA B (and of
+ * its base weight) that tensor-parallel rank tp_rank holds (sglang PR #24420
+ * page, 关键源码片段: mem_pool.py _column_parallel_lora_b_per_rank_dim and
+ * layers.py slice_lora_b_weights).  B is stacked along its output rows as q
+ * (num_heads * head_dim rows), then k and v (num_kv_heads * head_dim rows
+ * each).  While tp_size <= num_kv_heads a rank takes an even 1/tp_size of each
+ * block.  Beyond that, each KV head is replicated over tp_size / num_kv_heads
+ * ranks, and a rank takes its 1/tp_size of q plus one whole head of k and of v
+ * (the head of index tp_rank / replicas).
+ *
+ * Host only: no device memory, no stream.  ranges (host int32[6]) receives
+ * [q_begin, q_end, k_begin, k_end, v_begin, v_end) as rows of the full B;
+ * *per_rank_rows (nullable) = (q_end - q_begin) + (k_end - k_begin) +
+ * (v_end - v_begin).  The rank's projection is lora_linear_forward on those
+ * rows of W and B (one part).  Returns MLR_ERR_INVALID on a null ranges,
+ * non-positive sizes, a rank outside [0, tp_size), num_heads not divisible by
+ * tp_size, or tp_size and num_kv_heads neither dividing the other.
+ */
+int lora_tp_qkv_b_rows(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t tp_size,
+                       int32_t tp_rank, int32_t* ranges, int32_t* per_rank_rows);
+
+/*
  * Observability.  The pages describe no tracing; these calls exist so that a
  * caller can attribute the forward's GPU time to its stages without a profiler.
  *

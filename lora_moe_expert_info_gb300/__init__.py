@@ -25,9 +25,9 @@ import torch
 from . import _build
 
 __all__ = ["moe_lora_batch_info", "moe_lora_align", "moe_lora_align_capacity",
-           "moe_lora_align_workspace_bytes", "fused_moe_lora_forward",
-           "fused_moe_lora_workspace_bytes", "library", "library_path", "MoeLoraError",
-           "STATUS_BITS"]
+           "moe_lora_align_workspace_bytes", "fused_moe_lora_forward", "fused_moe_lora_forward_fp8",
+           "fused_moe_lora_workspace_bytes", "lora_linear_forward", "lora_tp_qkv_b_rows", "tp_take_rows",
+           "library", "library_path", "MoeLoraError", "STATUS_BITS"]
 
 MLR_OK = 0
 MLR_ERR_INVALID = -1
@@ -102,6 +102,9 @@ def library() -> ctypes.CDLL:
                 lib.lora_linear_workspace_bytes.argtypes = [i32] * 6
                 lib.lora_linear_forward.restype = ctypes.c_int
                 lib.lora_linear_forward.argtypes = [vp] * 8 + [i32] * 6 + [vp, vp, sz, vp, vp]
+            if hasattr(lib, "lora_tp_qkv_b_rows"):
+                lib.lora_tp_qkv_b_rows.restype = ctypes.c_int
+                lib.lora_tp_qkv_b_rows.argtypes = [i32] * 5 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = lib
     return _lib
 
@@ -423,3 +426,22 @@ def lora_linear_forward(x, w, token_lora_mapping, lora_ranks, scalings, lora_a, 
     if check:
         _check_device(status, "lora_linear_forward")
     return y
+
+
+def lora_tp_qkv_b_rows(num_heads: int, num_kv_heads: int, head_dim: int, tp_size: int, tp_rank: int):
+    """Rows of a fused q/k/v projection's LoRA B (and base weight) that one
+    tensor-parallel rank holds, with KV heads replicated when tp_size exceeds
+    num_kv_heads.  Returns ([(q0, q1), (k0, k1), (v0, v1)], per_rank_rows)."""
+    lib = library()
+    r = (ctypes.c_int32 * 6)()
+    n = ctypes.c_int32(0)
+    code = lib.lora_tp_qkv_b_rows(num_heads, num_kv_heads, head_dim, tp_size, tp_rank, r, ctypes.byref(n))
+    _check_host(code, "lora_tp_qkv_b_rows")
+    return [(r[0], r[1]), (r[2], r[3]), (r[4], r[5])], int(n.value)
+
+
+def tp_take_rows(t: torch.Tensor, ranges, dim: int = 0) -> torch.Tensor:
+    """A rank's shard of an output-row-stacked tensor: the given row ranges of
+    dimension `dim`, concatenated (load-time layout step, as for the rank's
+    copy of W or LoRA B; the per-token path runs in lora_linear_forward)."""
+    return torch.cat([t.narrow(dim, a, b - a) for a, b in ranges], dim=dim).contiguous()

@@ -292,3 +292,45 @@ def lora_linear(x, token_lora_mapping, lora_ranks, scalings, w, lora_a, lora_b, 
         tok_ptr, n_out, y.ctypes.data, int(threads))
     del xk, tok
     return int(st), y
+
+
+def tp_qkv_b_rows(num_heads: int, num_kv_heads: int, head_dim: int, tp_size: int, tp_rank: int):
+    """Rows of a fused q/k/v LoRA B held by one tensor-parallel rank, or None.
+
+    [PR24420] page ("qkv_proj LoRA B sizing under KV-head replication"),
+    关键源码片段, restated in two steps as the page gives them:
+      1. the per-rank B output size (mem_pool.py): an even split of
+         q + 2 kv rows, unless tp_size exceeds the KV heads; then 1/tp of q
+         plus one whole head (head_dim rows) of k and of v;
+      2. the rows taken (layers.py slice_lora_b_weights): q rows
+         [q_shard * rank, +q_shard); k and v rows of KV shard rank // replicas
+         (replicas = tp_size / num_kv_heads when the heads are replicated, else
+         1), offset by the full q size and, for v, the full k size.
+    Returns ([(q0, q1), (k0, k1), (v0, v1)], per_rank_rows).
+    """
+    if min(num_heads, num_kv_heads, head_dim, tp_size) < 1 or not 0 <= tp_rank < tp_size:
+        return None
+    if num_heads % tp_size:
+        return None
+    q_size = num_heads * head_dim
+    k_size = num_kv_heads * head_dim  # the k block of B, as the checkpoint stores it
+    replicated = tp_size > num_kv_heads
+    if replicated and tp_size % num_kv_heads:
+        return None
+    if not replicated and num_kv_heads % tp_size:
+        return None
+    # step 1: the per-rank size
+    if not replicated:
+        per_rank = (q_size + 2 * k_size) // tp_size
+    else:
+        per_rank = q_size // tp_size + 2 * head_dim
+    # step 2: the slices
+    replicas = tp_size // num_kv_heads if replicated else 1
+    q_shard = q_size // tp_size
+    kv_shard = head_dim if replicated else k_size // tp_size
+    kv_id = tp_rank // replicas
+    q = (q_shard * tp_rank, q_shard * (tp_rank + 1))
+    k = (q_size + kv_shard * kv_id, q_size + kv_shard * (kv_id + 1))
+    v = (q_size + k_size + kv_shard * kv_id, q_size + k_size + kv_shard * (kv_id + 1))
+    assert per_rank == sum(b - a for a, b in (q, k, v))
+    return [q, k, v], per_rank
