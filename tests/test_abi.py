@@ -151,3 +151,32 @@ def test_fp8_forward_host_checks(lib):
     assert f(*args) == mlr.MLR_ERR_INVALID
     args = [fake] * 9 + [None] + [fake] * 4 + [64, 2, 8, 256, 512, 4, 16, fake, fake, big, None, None]
     assert f(*args) == mlr.MLR_ERR_INVALID
+
+
+def test_fp8_binding_rejects_bad_inputs_before_any_call():
+    # CPU tensors: every case must fail in the binding's checks, never reach the library
+    import pytest
+    import torch
+    T, K, E, H, I, L, R = 8, 2, 3, 128, 64, 2, 16
+    bf = torch.bfloat16
+    x = torch.zeros(T, H, dtype=bf)
+    ids = torch.zeros(T, K, dtype=torch.int32)
+    wts = torch.zeros(T, K, dtype=torch.float32)
+    mp = torch.zeros(T, dtype=torch.int32)
+    ranks = torch.zeros(L, dtype=torch.int32)
+    scal = torch.zeros(L, dtype=torch.float32)
+    wq = torch.zeros(E, 2 * I, H, dtype=torch.uint8)
+    ws = torch.zeros(E, 1, 1, dtype=torch.float32)
+    dq = torch.zeros(E, H, I, dtype=torch.uint8)
+    ds = torch.zeros(E, 1, 1, dtype=torch.float32)
+    lo = dict(lora_a_gu=torch.zeros(L, E, 2, R, H, dtype=bf), lora_b_gu=torch.zeros(L, E, 2, I, R, dtype=bf),
+              lora_a_down=torch.zeros(L, E, R, I, dtype=bf), lora_b_down=torch.zeros(L, E, H, R, dtype=bf))
+    f = mlr.fused_moe_lora_forward_fp8
+    with pytest.raises(ValueError):   # scale of W_gate_up has the wrong number of row blocks
+        f(x, ids, wts, mp, ranks, scal, wq, torch.zeros(E, 2, 1), dq, ds, **lo)
+    with pytest.raises(ValueError):   # W_down codes of the wrong shape
+        f(x, ids, wts, mp, ranks, scal, wq, ws, torch.zeros(E, I, H, dtype=torch.uint8), ds, **lo)
+    with pytest.raises(TypeError):    # codes must be bytes
+        f(x, ids, wts, mp, ranks, scal, wq.to(bf), ws, dq, ds, **lo)
+    with pytest.raises(TypeError):    # scales must be float32
+        f(x, ids, wts, mp, ranks, scal, wq, ws.double(), dq, ds, **lo)

@@ -113,3 +113,12 @@ def test_rank_projection_is_a_column_block_of_the_full_one(tp):
         st, yr = oracle.lora_linear(x, mapping, ranks, scal, w[rows], a, b[:, rows], [0, n])
         assert st == oracle.OK
         np.testing.assert_allclose(yr, y[:, rows], rtol=1e-12, atol=1e-12)
+
+
+def test_take_rows_helper_matches_index_selection():
+    import torch
+    ranges, n = mlr.lora_tp_qkv_b_rows(8, 2, 16, 4, 3)
+    b = torch.arange(3 * 192 * 4, dtype=torch.float32).reshape(3, 192, 4)
+    rows = rows_of(ranges)
+    assert torch.equal(mlr.tp_take_rows(b, ranges, dim=1), b[:, rows])
+    assert mlr.tp_take_rows(b[0], ranges, dim=0).shape == (n, 4)
