@@ -4,11 +4,15 @@
 One step = one batch through the whole hot path: moe_lora_batch_info (once per
 batch) and fused_moe_lora_forward (align, LoRA shrinks, gate_up GEMM with the
 fused LoRA expand and SiLU*up, down GEMM with the fused LoRA expand and the
-top-k combine).  Inputs are seeded synthetic tensors resident in HBM; the
-workload is the Qwen-MoE-like prefill (4096 tokens, hidden 2048, intermediate
-768, 128 experts top-8, 8 LoRA slots ranks {8,16,32,64}).  Each step streams
-~1.7 GB of expert and adapter weights, far more than the 129 MB L2, so no
-explicit L2 flush is done between steps.
+top-k combine).  Inputs are seeded synthetic tensors resident in HBM.  The
+headline workload is the DeepSeek-V3-like prefill (8192 tokens, hidden 7168,
+intermediate 2048, 256 experts top-8, 4 LoRA slots ranks {16,32,64,64}, 22.5 GB
+of bf16 expert weights), the largest of the layer's workloads.  Each step
+streams far more than the 129 MB L2, so no explicit L2 flush is done between
+steps.  The Qwen-MoE-like prefill, decode and the metadata-only stress batch
+(batch_info + align on 1,048,576 tokens, inputs rotated over four copies so
+that they do not sit in L2) are measured in the same run, each with its own
+roofline fractions, under "workloads".
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded token sample of the same workload instead.
@@ -33,6 +37,13 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-LoRA layer tokens/s and % of roofline (bf16, 1×GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Tensor peak for the fractions: the burst figure.  Every timed region here is
+# at most a few seconds of back-to-back steps, and the burst peak is the
+# stricter (larger) denominator.
+PEAK_KIND = "bf16_tflops"
+DEFAULT_EXTRAS = "qwen_moe_prefill,decode,metadata_stress"
+COMBINE_NAME = {False: "atomic (fp32 reductions)", True: "deterministic (per-pair rows, summed in k order)"}
+METADATA_METRIC = "MoE-LoRA metadata (batch_info + align) tokens/s and % of HBM roofline (int32, 1×GB300)"
 STAGE_KERNELS = {"gate_up": "moe_gemm_kernel<1>", "down": "moe_gemm_kernel<3>",
                  "shrink_gate_up": "moe_gemm_kernel<0>", "shrink_down": "moe_gemm_kernel<2>"}
 
@@ -439,19 +450,18 @@ def run_reference(args, rank, world):
     return line
 
 
-def run_ours(args, rank, world, dist):
-    import numpy as np
+def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
+    """One MoE workload: the timed steps, the live-timed dominant stage, the
+    stage breakdown, and optionally the end-to-end loop and the oracle's rate.
+    Returns the workload's entry (rank 0) or None (other ranks)."""
     import torch
 
     import lora_moe_expert_info_gb300 as mlr
-    import oracle
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    lib = mlr.library()
     fp8 = args.weights == "fp8"
-    cfg, b, w, x, q = make_inputs(args.config, dev, args.seed + rank, fp8)
+    cfg, b, w, x, q = make_inputs(name, dev, args.seed + rank, fp8)
     T, K, E, H, I, L, R = (cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.hidden, cfg.intermediate,
                            cfg.num_loras, cfg.max_rank)
     max_len = int(b.seg_lens.max())
@@ -491,45 +501,73 @@ def run_ours(args, rank, world, dist):
     dom = max((s for s in STAGE_KERNELS if s in stages), key=lambda s: stages[s])
     ms_total, dom_ms, n_launch, clk = timed_region(lib, args, step, stream, dist, local, dom)
     ms_max = reduce_max(ms_total, dist, dev)
+    # the other top-k combine, timed the same way (events around the steps)
+    mode = mlr.deterministic()
+    mlr.set_deterministic(not mode)
+    try:
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        alt_ms = reduce_max(a0.elapsed_time(a1), dist, dev) / args.steps
+    finally:
+        mlr.set_deterministic(mode)
+    combine = {"mode": COMBINE_NAME[mode], "alternative": {"mode": COMBINE_NAME[not mode],
+                                                           "ms_per_step": round(alt_ms, 4)}}
 
-    # end to end through the public API from pinned host buffers
-    host_in = {"x": x.cpu().pin_memory(), "topk_ids": b.topk_ids.cpu().pin_memory(),
-               "topk_weights": b.topk_weights.cpu().pin_memory(), "seg_indptr": b.seg_indptr.cpu().pin_memory(),
-               "weight_indices": b.weight_indices.cpu().pin_memory(),
-               "lora_ranks": b.lora_ranks.cpu().pin_memory(), "scalings": b.scalings.cpu().pin_memory()}
-    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
-    y_dev = [y, torch.empty_like(y)]
-    y_host = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = y_host[0].numel() * y_host[0].element_size()
+    e2e = None
+    if with_e2e:
+        # end to end through the public API from pinned host buffers
+        host_in = {"x": x.cpu().pin_memory(), "topk_ids": b.topk_ids.cpu().pin_memory(),
+                   "topk_weights": b.topk_weights.cpu().pin_memory(),
+                   "seg_indptr": b.seg_indptr.cpu().pin_memory(),
+                   "weight_indices": b.weight_indices.cpu().pin_memory(),
+                   "lora_ranks": b.lora_ranks.cpu().pin_memory(), "scalings": b.scalings.cpu().pin_memory()}
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+        y_dev = [y, torch.empty_like(y)]
+        y_host = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = y_host[0].numel() * y_host[0].element_size()
 
-    def upload(sl):
-        for k, v in host_in.items():
-            dev_in[sl][k].copy_(v, non_blocking=True)
+        def upload(sl):
+            for k, v in host_in.items():
+                dev_in[sl][k].copy_(v, non_blocking=True)
 
-    def compute(sl):
-        d = dev_in[sl]
-        mlr.moe_lora_batch_info(d["seg_indptr"], d["weight_indices"], d["lora_ranks"], T,
-                                max_len, adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
-        forward(d["x"], d["topk_ids"], d["topk_weights"], mapping, d["lora_ranks"], d["scalings"], **wk,
-                y=y_dev[sl], workspace=ws, check=False)
+        def compute(sl):
+            d = dev_in[sl]
+            mlr.moe_lora_batch_info(d["seg_indptr"], d["weight_indices"], d["lora_ranks"], T,
+                                    max_len, adapter_enabled=enabled, token_lora_mapping=mapping, check=False)
+            forward(d["x"], d["topk_ids"], d["topk_weights"], mapping, d["lora_ranks"], d["scalings"], **wk,
+                    y=y_dev[sl], workspace=ws, check=False)
 
-    def download(sl):
-        y_host[sl].copy_(y_dev[sl], non_blocking=True)
+        def download(sl):
+            y_host[sl].copy_(y_dev[sl], non_blocking=True)
 
-    e2e_ms, e2e_serial_ms = measure_e2e(args, upload, compute, download, stream, dist, dev)
+        e2e_ms, e2e_serial_ms = measure_e2e(args, upload, compute, download, stream, dist, dev)
+        e2e = {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_ms, 4), "steps_in_flight": 2,
+               "serial_ms_per_step": round(e2e_serial_ms, 4)}
 
     # check the status of the gated call only now (it synchronised long ago)
     if int(status.item()) != 0:
-        raise RuntimeError(f"forward reported device status {int(status.item())}")
+        raise RuntimeError(f"{name}: forward reported device status {int(status.item())}")
     if rank != 0:
         return None
 
-    # sampled correctness against the oracle and the CPU baseline
     mp_np = mapping.cpu().numpy()
     flops, byts, st_work = layer_work(cfg, b, mapping, fp8)
     cpu = None
-    if not args.no_cpu_baseline:
+    if with_cpu:
+        import oracle
         oracle.build()
         rate, n, secs, thr = oracle_sample_rate(cfg, b, w, x, mp_np, target_s=args.cpu_seconds, q=q)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
@@ -538,38 +576,195 @@ def run_ours(args, rank, world, dist):
 
     peaks, peak_src = load_peaks()
     ms_step = ms_max / args.steps
-    value = weak_scaling_rate(T, world, ms_step)
-    rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, "bf16_tflops_sustained")
+    rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, PEAK_KIND)
     rf["kernel"] = STAGE_KERNELS.get(dom, dom)
     rf["stage"] = dom
-    rf["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    tr = recorded_traffic(dom, cfg.name + ("_fp8" if fp8 else ""))
-    rf["traffic"] = tr
+    rf["peak_source"] = peak_label(peak_src)
+    rf["traffic"] = recorded_traffic(dom, cfg.name + ("_fp8" if fp8 else ""))
     rf["algorithmic_bytes"] = int(st_work[dom][1])
     rf["algorithmic_flops"] = int(st_work[dom][0])
     rf["launch_ms"] = round(dom_ms, 4)
-    layer = roofline_entry(flops, byts, ms_step, peaks, "bf16_tflops_sustained")
-    layer["tensor_frac"] = round(flops / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+    layer = layer_fractions(flops, byts, ms_step, peaks)
+    entry = {"value": round(weak_scaling_rate(T, world, ms_step), 1), "unit": "tokens/s",
+             "ms_per_step": round(ms_step, 4),
+             "config": {"workload": cfg.name, "tokens": T, "hidden": H, "intermediate": I, "experts": E,
+                        "topk": K, "loras": L, "max_rank": R, "seed": args.seed,
+                        "weights": WEIGHT_LABEL[args.weights],
+                        "l2": f"no flush: each step streams {byts / 1e9:.2f} GB of algorithmic bytes "
+                              f"(> 129 MB L2)"},
+             "roofline": rf, "layer_roofline": layer,
+             "stages_ms": {k: round(v, 4) for k, v in stages.items()},
+             "combine": combine,
+             "gpu_launches": int(n_launch), "clocks": clk.summary()}
+    if cpu is not None:
+        entry["cpu_baseline"] = cpu
+    if e2e is not None:
+        entry["e2e"] = e2e
+    return entry
+
+
+def layer_fractions(flops, byts, ms_step, peaks):
+    """The layer's roofline entry with both fractions: HBM (bytes) and the
+    dense bf16 tensor peak (FLOPs), the latter being the prefill bar."""
+    layer = roofline_entry(flops, byts, ms_step, peaks, PEAK_KIND)
+    s = ms_step * 1e-3
+    layer["hbm_frac"] = round(byts / s / 1e9 / peaks["hbm_gbs"], 4)
+    layer["tensor_frac"] = round(flops / s / 1e12 / peaks[PEAK_KIND], 4)
+    layer["roofline_ms"] = round(1e3 * max(byts / (peaks["hbm_gbs"] * 1e9),
+                                           flops / (peaks[PEAK_KIND] * 1e12)), 4)
     layer["algorithmic_bytes"] = int(byts)
     layer["algorithmic_flops"] = int(flops)
-    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+    return layer
+
+
+def peak_label(src):
+    return f"{src} {PEAK_KIND} (MEASURED_PEAKS.json)" if src == "measured" else f"fallback {PEAK_KIND}"
+
+
+def metadata_bytes(bs, L, T, P, npad, block_size):
+    """Algorithmic bytes of the metadata calls: batch_info reads seg_indptr,
+    weight_indices and lora_ranks and writes the mapping and the enabled mask;
+    align reads topk_ids and the mapping and writes the padded sorted ids, the
+    two block label arrays and the padded count."""
+    bi = 4 * (2 * bs + 1 + 2 * L + T)
+    al = 4 * (P + T) + 4 * (npad + 2 * (npad // block_size) + 1)
+    return bi, al
+
+
+def measure_metadata(args, rank, world, dist, n_copies=4):
+    """The metadata-only stress workload: moe_lora_batch_info + moe_lora_align
+    on 1,048,576 tokens.  Its inputs and outputs (about 80 MB per step) would
+    sit in the 129 MB L2, so every step uses the next of n_copies copies of
+    them (rotated, about 320 MB in all)."""
+    import torch
+
+    import lora_moe_expert_info_gb300 as mlr
+    from lora_moe_expert_info_gb300 import workloads
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    cfg = workloads.CONFIGS["metadata_stress"]
+    T, K, E, L, bsz = cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.num_loras, cfg.block_size
+    b = workloads.make_batch(cfg, device=dev, seed=args.seed + rank)
+    bs = b.weight_indices.numel()
+    P = T * K
+    cap = mlr.moe_lora_align_capacity(T, K, E, L, bsz)
+    nblk = cap // bsz
+    ws = torch.empty(max(256, mlr.moe_lora_align_workspace_bytes(T, K, E, L, bsz)), dtype=torch.uint8,
+                     device=dev)
+    copies = []
+    for _ in range(n_copies):
+        copies.append({
+            "indptr": b.seg_indptr.clone(), "wi": b.weight_indices.clone(), "ranks": b.lora_ranks.clone(),
+            "ids": b.topk_ids.clone(), "mapping": torch.empty(T, dtype=torch.int32, device=dev),
+            "enabled": torch.empty(L, dtype=torch.int32, device=dev),
+            "out": (torch.empty(cap, dtype=torch.int32, device=dev),
+                    torch.empty(nblk, dtype=torch.int32, device=dev),
+                    torch.empty(nblk, dtype=torch.int32, device=dev),
+                    torch.empty(1, dtype=torch.int32, device=dev))})
+
+    def batch_info(c):
+        mlr.moe_lora_batch_info(c["indptr"], c["wi"], c["ranks"], T, 0, adapter_enabled=c["enabled"],
+                                token_lora_mapping=c["mapping"], check=False)
+
+    def align(c):
+        mlr.moe_lora_align(c["ids"], c["mapping"], E, L, bsz, out=c["out"], workspace=ws, check=False)
+
+    # checked calls first (status words), then warm-up
+    for c in copies:
+        mlr.moe_lora_batch_info(c["indptr"], c["wi"], c["ranks"], T, 0, adapter_enabled=c["enabled"],
+                                token_lora_mapping=c["mapping"])
+        mlr.moe_lora_align(c["ids"], c["mapping"], E, L, bsz, out=c["out"], workspace=ws)
+    npad = int(copies[0]["out"][3].item())
+    stream = torch.cuda.current_stream()
+    n = max(4 * n_copies, args.steps)
+
+    def timed(fn):
+        for i in range(max(3, args.warmup)):
+            fn(copies[i % n_copies])
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(copies[i % n_copies])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return reduce_max(e0.elapsed_time(e1) / n, dist, dev)
+
+    with ClockSampler(local) as clk:
+        ms_bi = timed(batch_info)
+        ms_al = timed(align)
+        l0 = mlr.library().moe_lora_launch_count()
+        ms_step = timed(lambda c: (batch_info(c), align(c)))
+        launches_per_step = (mlr.library().moe_lora_launch_count() - l0) // (n + max(3, args.warmup))
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    bi_bytes, al_bytes = metadata_bytes(bs, L, T, P, npad, bsz)
+
+    def rl(byts, ms):
+        ach = byts / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(byts),
+                "launch_ms": round(ms, 5), "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)"}
+
+    return {"value": round(weak_scaling_rate(T, world, ms_step), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms_step, 5),
+            "config": {"workload": cfg.name, "tokens": T, "segments": bs, "experts": E, "topk": K, "loras": L,
+                       "block_size": bsz, "pairs": P, "num_tokens_post_pad": npad, "seed": args.seed,
+                       "l2": f"{n_copies} rotated copies of every input and output "
+                             f"({n_copies * (bi_bytes + al_bytes) / 1e6:.0f} MB > 129 MB L2)"},
+            "roofline": dict(rl(bi_bytes + al_bytes, ms_step), kernel="batch_info + align (one step)"),
+            "calls": {"moe_lora_batch_info": rl(bi_bytes, ms_bi), "moe_lora_align": rl(al_bytes, ms_al)},
+            "gpu_launches_per_step": int(launches_per_step), "clocks": clk.summary()}
+
+
+def run_ours(args, rank, world, dist):
+    """The headline workload (its JSON line), with the other workloads of the
+    same north-star table measured in the same run under "workloads"."""
+    import torch
+
+    import lora_moe_expert_info_gb300 as mlr
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(torch.device("cuda", local))
+    lib = mlr.library()
+    mlr.set_deterministic(args.combine == "deterministic")
+    if args.config == "metadata_stress":
+        head = measure_metadata(args, rank, world, dist)
+        if rank != 0:
+            return None
+        return {"metric": METADATA_METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+                "data": "synthetic", "config": head["config"], "roofline": head["roofline"],
+                "calls": head["calls"], "cpu_baseline": None, "e2e": None,
+                "gpu_launches": head["gpu_launches_per_step"] * max(4 * 4, args.steps),
+                "clocks": head["clocks"]}
+    head = measure_moe(args.config, args, rank, world, dist, lib, with_e2e=True,
+                       with_cpu=not args.no_cpu_baseline)
+    extras = {}
+    for name in [n for n in args.extras.split(",") if n and n != args.config]:
+        torch.cuda.empty_cache()
+        if name == "metadata_stress":
+            extras[name] = measure_metadata(args, rank, world, dist)
+        else:
+            extras[name] = measure_moe(name, args, rank, world, dist, lib, with_e2e=False, with_cpu=False)
+    if rank != 0:
+        return None
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": cfg.name, "tokens": T, "hidden": H, "intermediate": I, "experts": E,
-                       "topk": K, "loras": L, "max_rank": R, "seed": args.seed,
-                       "weights": WEIGHT_LABEL[args.weights],
-                       "parallelism": f"dp{world} (replicas)" if world > 1 else "single GPU",
-                       "l2": f"no flush: each step streams {byts / 1e9:.2f} GB of algorithmic bytes "
-                             f"(> 129 MB L2)"},
-            "roofline": rf, "layer_roofline": layer,
-            "stages_ms": {k: round(v, 4) for k, v in stages.items()},
-            "cpu_baseline": cpu,
-            "e2e": {"value": round(weak_scaling_rate(T, world, e2e_ms), 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 4), "steps_in_flight": 2,
-                    "serial_ms_per_step": round(e2e_serial_ms, 4)},
-            "gpu_launches": int(n_launch), "clocks": clk.summary()}
+            "config": dict(head["config"],
+                           parallelism=f"dp{world} (replicas)" if world > 1 else "single GPU"),
+            "roofline": head["roofline"], "layer_roofline": head["layer_roofline"],
+            "stages_ms": head["stages_ms"], "combine": head["combine"], "cpu_baseline": head.get("cpu_baseline"),
+            "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
+    if extras:
+        line["workloads"] = extras
     return line
 
 
@@ -761,12 +956,12 @@ def run_linear(args, rank, world, dist):
     r_tok = np.where(mp_np >= 0, ranks.cpu().numpy()[np.clip(mp_np, 0, None)], 0).astype(np.float64)
     proj_flops = 2.0 * T * D_out * D_in + float(2.0 * D_out * r_tok.sum())
     proj_bytes = 2.0 * D_out * D_in + 2.0 * T * D_in + 4.0 * T * D_out
-    rf = roofline_entry(proj_flops, proj_bytes, proj_ms, peaks, "bf16_tflops_sustained")
+    rf = roofline_entry(proj_flops, proj_bytes, proj_ms, peaks, PEAK_KIND)
     rf.update({"kernel": "moe_gemm_kernel<3>", "stage": "down (the projection GEMM)",
-               "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+               "peak_source": peak_label(peak_src),
                "traffic": recorded_traffic("down", args.config), "algorithmic_bytes": int(proj_bytes),
                "algorithmic_flops": int(proj_flops), "launch_ms": round(proj_ms, 4)})
-    layer = roofline_entry(flops, byts, ms_step, peaks, "bf16_tflops_sustained")
+    layer = layer_fractions(flops, byts, ms_step, peaks)
     layer.update({"algorithmic_bytes": int(byts), "algorithmic_flops": int(flops)})
     return {"metric": LINEAR_METRIC, "value": round(weak_scaling_rate(T, world, ms_step), 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -803,9 +998,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="qwen_moe_prefill")
+    ap.add_argument("--config", default="deepseek_v3_prefill",
+                    help="headline workload (default: the DeepSeek-V3-like prefill, the largest that fits one GPU)")
+    ap.add_argument("--extras", default=DEFAULT_EXTRAS,
+                    help="comma-separated workloads measured after the headline and reported under "
+                         "'workloads' ('' for none)")
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="base expert weights of the MoE workloads: bf16, or FP8 E4M3 with 128x128 block scales")
+    ap.add_argument("--combine", choices=["atomic", "deterministic"], default="deterministic",
+                    help="top-k combine of the MoE forward (the other one is timed beside it)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=None)

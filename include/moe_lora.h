@@ -143,7 +143,9 @@ int moe_lora_align(const int32_t* topk_ids, const int32_t* token_lora_mapping,
  * a workspace there.  The call allocates nothing.
  * The first call on a device looks up the array's address on that device (the
  * current device, which must be the stream's); make that first call before
- * any stream capture.  All calls share the one array, so calls whose work may
+ * any stream capture.  The address is cached per device ordinal for the life of
+ * the process: it assumes the device's primary context, so do not use this
+ * call after cudaDeviceReset or under another driver-API context.  All calls share the one array, so calls whose work may
  * overlap on the GPU (different streams, or different host threads) race and
  * corrupt each other's results; calls ordered on one stream are safe, and no
  * clearing is needed between them.
@@ -183,7 +185,10 @@ size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t 
  * H >= 128, I >= 64, R a multiple of 16 in [16, 256] when L > 0,
  * E * (L + 1) <= 16384, every base pointer 16-byte aligned.  Sizes outside
  * these return MLR_ERR_UNSUPPORTED (and fused_moe_lora_workspace_bytes 0).
- * The top-k combine uses fp32 atomics, so y may differ in the last bits between runs.
+ * The top-k combine is set process-wide by moe_lora_set_deterministic (below):
+ * fp32 atomic reductions, whose order (and so y's last bits) may differ
+ * between runs, or per-pair rows summed in increasing k, bit-identical between
+ * runs.
  */
 int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
                            const int32_t* token_lora_mapping, const int32_t* lora_ranks,
@@ -311,6 +316,92 @@ int lora_tp_qkv_b_rows(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim
  *   (static storage; NULL past the last stage).
  * moe_lora_launch_count(): kernels this library has launched in this process.
  */
+/*
+ * Expert parallelism (the multi-GPU form of the layer that the pages point to
+ * in other PRs: the DeepEP dispatch among the sglang PR #22323 page's related
+ * PRs, 关联脉络, and the TP/EP question of the sglang PR #14105 page's review,
+ * 评论区精华).  The E experts are split over n_ranks ranks in equal contiguous
+ * ranges: rank d owns experts [d*E/n_ranks, (d+1)*E/n_ranks).  One step on
+ * every rank:
+ *   1. moe_lora_ep_dispatch packs this rank's (token, slot) pairs by owner;
+ *   2. the caller exchanges the packed rows with an all-to-all (send_counts
+ *      rows to each rank; NCCL, or any transport: the library moves no data
+ *      between GPUs);
+ *   3. each owner runs fused_moe_lora_forward on the rows it received with
+ *      top-1 routing (topk_ids = the received expert ids, topk_weights = the
+ *      received weights, token_lora_mapping = the received adapters) over its
+ *      own experts' weights and LoRA stacks [L, E/n_ranks, ...]: each output
+ *      row is w * (expert output);
+ *   4. the caller returns those rows with the reverse all-to-all, so this rank
+ *      holds them in its send order;
+ *   5. moe_lora_ep_combine sums each token's rows.
+ *
+ * moe_lora_ep_workspace_bytes(T, K, n_ranks): scratch of the dispatch (0 on
+ *   bad sizes).  Limits: 1 <= n_ranks <= 64, T*K < 2^31.
+ *
+ * moe_lora_ep_dispatch: pair p = t*K + k with expert e in [0, E) goes to rank
+ *   e / (E/n_ranks); the send order lists rank 0's pairs first, each rank's in
+ *   increasing p.  Outputs (device, caller-owned, T*K rows of capacity):
+ *     send_x      bf16 [T*K, H]: x row of the pair's token
+ *     send_expert int32 [T*K]:   e - (first expert of the destination)
+ *     send_weight float [T*K]:   topk_weights[p]
+ *     send_lora   int32 [T*K]:   token_lora_mapping[t]
+ *     send_counts int32 [n_ranks]: rows for each rank (rows [sum of earlier
+ *                 counts, + count) of the send buffers)
+ *     pair_pos    int32 [T*K]:   row of pair p in the send order, -1 if dropped
+ *   A pair whose expert id is outside [0, E) is dropped and sets
+ *   MLR_STATUS_INDEX.  Requirements: E a multiple of n_ranks, H a multiple of
+ *   8, x and send_x 16-byte aligned; else MLR_ERR_INVALID (n_ranks above 64:
+ *   MLR_ERR_UNSUPPORTED).
+ *
+ * moe_lora_ep_combine: y[t] = sum over k in increasing order of
+ *   rows[pair_pos[t*K + k]] (skipping -1), in fp32, rounded to bf16: y is
+ *   bit-identical between runs.  rows: bf16 [>= valid pairs, H], 16-byte
+ *   aligned; y: bf16 [T, H].
+ */
+size_t moe_lora_ep_workspace_bytes(int32_t num_tokens, int32_t topk, int32_t n_ranks);
+int moe_lora_ep_dispatch(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                         const int32_t* token_lora_mapping, int32_t num_tokens, int32_t topk, int32_t hidden,
+                         int32_t num_experts, int32_t n_ranks, mlr_bf16* send_x, int32_t* send_expert,
+                         float* send_weight, int32_t* send_lora, int32_t* send_counts, int32_t* pair_pos,
+                         void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
+int moe_lora_ep_combine(const mlr_bf16* rows, const int32_t* pair_pos, int32_t num_tokens, int32_t topk,
+                        int32_t hidden, mlr_bf16* y, void* stream);
+
+/*
+ * Failure detection.  The pages describe none; every pipeline wait of the GEMM
+ * kernels (a stage of operands to land, an accumulator to fill or drain) gives
+ * up after a limit instead of spinning forever, sets MLR_STATUS_TIMEOUT in
+ * d_status, and every role of the kernel then leaves, frees its TMEM and
+ * returns, so the CUDA context stays usable.  Results of that call are invalid.
+ *
+ * moe_lora_set_wait_limit_ns(ns): the limit for launches enqueued from now on,
+ *   process-wide (default 2 s; 0 is taken as 1 ns, so a wait that is not
+ *   already satisfied gives up at once).  Returns MLR_ERR_INVALID above 60 s.
+ *   Teardown waits (in-flight copies and MMAs before TMEM is freed) keep their
+ *   own fixed 2 s limit.
+ * moe_lora_wait_limit_ns(): the current limit.
+ */
+int moe_lora_set_wait_limit_ns(uint64_t ns);
+uint64_t moe_lora_wait_limit_ns(void);
+
+/*
+ * The top-k combine of fused_moe_lora_forward(_fp8) (the weighted sum over a
+ * token's K experts, named by the layer formula's sum over top-k; the pages
+ * leave its order open).  Process-wide, for calls enqueued from now on;
+ * deterministic (1) by default.
+ *   on = 0: the down GEMM adds w * d into an fp32 accumulator with atomic
+ *           reductions, in whatever order the pairs finish; y may differ in
+ *           its last bits between runs.
+ *   on = 1: the down GEMM writes w * d of each pair, rounded to bf16, into a
+ *           row of its own (inside the workspace, no extra bytes), and a
+ *           combine kernel sums a token's K rows in increasing k in fp32:
+ *           y is bit-identical between runs.
+ * Returns MLR_ERR_INVALID for other values.  moe_lora_deterministic() reads it.
+ */
+int moe_lora_set_deterministic(int32_t on);
+int32_t moe_lora_deterministic(void);
+
 int moe_lora_profile_stages(uint32_t mask);
 int moe_lora_profile_begin(int32_t max_calls);
 int moe_lora_profile_end(double* stage_ms, int32_t max_stages, int32_t* n_stages, int32_t* n_calls);

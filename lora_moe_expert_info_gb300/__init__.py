@@ -16,6 +16,8 @@ no fallback path.
 from __future__ import annotations
 
 import ctypes
+import functools
+import inspect
 import os
 import threading
 from typing import Optional, Tuple
@@ -27,7 +29,7 @@ from . import _build
 __all__ = ["moe_lora_batch_info", "moe_lora_align", "moe_lora_align_capacity",
            "moe_lora_align_workspace_bytes", "fused_moe_lora_forward", "fused_moe_lora_forward_fp8",
            "fused_moe_lora_workspace_bytes", "lora_linear_forward", "lora_tp_qkv_b_rows", "tp_take_rows",
-           "library", "library_path", "MoeLoraError", "STATUS_BITS"]
+           "set_wait_limit_ns", "wait_limit_ns", "set_deterministic", "deterministic", "library", "library_path", "MoeLoraError", "STATUS_BITS"]
 
 MLR_OK = 0
 MLR_ERR_INVALID = -1
@@ -90,6 +92,14 @@ def library() -> ctypes.CDLL:
             lib.moe_lora_profile_stage_name.argtypes = [i32]
             lib.moe_lora_launch_count.restype = ctypes.c_uint64
             lib.moe_lora_launch_count.argtypes = []
+            lib.moe_lora_set_wait_limit_ns.restype = ctypes.c_int
+            lib.moe_lora_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.moe_lora_wait_limit_ns.restype = ctypes.c_uint64
+            lib.moe_lora_wait_limit_ns.argtypes = []
+            lib.moe_lora_set_deterministic.restype = ctypes.c_int
+            lib.moe_lora_set_deterministic.argtypes = [i32]
+            lib.moe_lora_deterministic.restype = i32
+            lib.moe_lora_deterministic.argtypes = []
             if hasattr(lib, "fused_moe_lora_forward"):
                 lib.fused_moe_lora_workspace_bytes.restype = sz
                 lib.fused_moe_lora_workspace_bytes.argtypes = [i32] * 7
@@ -107,6 +117,46 @@ def library() -> ctypes.CDLL:
                 lib.lora_tp_qkv_b_rows.argtypes = [i32] * 5 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
             _lib = lib
     return _lib
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Give-up limit of the GEMM kernels' pipeline waits for later launches
+    (process-wide; default 2 s).  A wait that runs out sets the device status
+    bit "device wait timed out" and the kernel returns early."""
+    _check_host(library().moe_lora_set_wait_limit_ns(int(ns)), "moe_lora_set_wait_limit_ns")
+
+
+def wait_limit_ns() -> int:
+    return int(library().moe_lora_wait_limit_ns())
+
+
+def set_deterministic(on: bool) -> None:
+    """Top-k combine of the MoE forward for later calls (process-wide): False =
+    fp32 atomic reductions (order-dependent last bits), True = per-pair rows
+    summed in increasing k (bit-identical between runs)."""
+    _check_host(library().moe_lora_set_deterministic(1 if on else 0), "moe_lora_set_deterministic")
+
+
+def deterministic() -> bool:
+    return bool(library().moe_lora_deterministic())
+
+
+def _on_stream(fn):
+    """Runs a wrapper with its `stream` argument as torch's current stream, so
+    that the outputs, workspace and status word it allocates (and zeroes) are
+    ordered on the stream the kernels are enqueued on, the caching allocator
+    records them there, and the status read synchronises that stream."""
+    sig = inspect.signature(fn)
+
+    @functools.wraps(fn)
+    def run(*args, **kw):
+        bound = sig.bind(*args, **kw)
+        s = bound.arguments.get("stream")
+        if s is None:
+            return fn(*args, **kw)
+        with torch.cuda.stream(s):
+            return fn(*args, **kw)
+    return run
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -152,6 +202,7 @@ def _req(t: torch.Tensor, name: str, dtype, dev):
         raise ValueError(f"{name} must be contiguous")
 
 
+@_on_stream
 def moe_lora_batch_info(seg_indptr: torch.Tensor, weight_indices: torch.Tensor,
                         lora_ranks: torch.Tensor, num_tokens: int, max_len: int = 0,
                         adapter_enabled: Optional[torch.Tensor] = None,
@@ -200,6 +251,7 @@ def moe_lora_align_workspace_bytes(num_tokens, topk, num_experts, num_loras, blo
                                                         block_size))
 
 
+@_on_stream
 def moe_lora_align(topk_ids: torch.Tensor, token_lora_mapping: torch.Tensor, num_experts: int,
                    num_loras: int, block_size: int, out=None, workspace=None, stream=None,
                    check: bool = True):
@@ -245,6 +297,7 @@ def fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R) -> int:
     return int(library().fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R))
 
 
+@_on_stream
 def fused_moe_lora_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
                            w_gate_up, w_down, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
                            y: Optional[torch.Tensor] = None,
@@ -311,6 +364,7 @@ def _codes(t: torch.Tensor, name: str, dev) -> torch.Tensor:
     return t
 
 
+@_on_stream
 def fused_moe_lora_forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
                                w_gate_up_q, w_gate_up_scale, w_down_q, w_down_scale,
                                lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
@@ -378,6 +432,7 @@ def fused_moe_lora_forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lo
     return y
 
 
+@_on_stream
 def lora_linear_forward(x, w, token_lora_mapping, lora_ranks, scalings, lora_a, lora_b, slice_offsets,
                         y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                         stream=None, check: bool = True,

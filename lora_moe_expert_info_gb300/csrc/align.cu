@@ -2,16 +2,17 @@
 // stable, each bucket padded to block_size (sglang PR #14105 page, 实现拆解:
 // moe_lora_align_block_size "sorts tokens by LoRA adapter and expert id").
 //
-// key(p) = e * (L+1) + (lora + 1); NB = E * (L+1) buckets.  Up to 32768 pairs
-// and 8192 buckets, one block does everything in shared memory (align_block).
+// key(p) = e * (L+1) + (lora + 1); NB = E * (L+1) buckets.  Up to
+// kAlignBlockMaxPairs (16384) pairs and kAlignBlockMaxBuckets (8192) buckets,
+// one block does everything in shared memory (align_block).
 // Otherwise pairs are split into G contiguous chunks of up to 32768 pairs and
 // four launches follow:
 //   1. count    : per chunk, a shared-memory histogram over NB buckets
 //                 -> cnt[g][b]
 //   2. colscan  : per bucket, exclusive prefix over chunks (in place) and the
-//                 bucket total
-//   3. bktscan  : one block, exclusive scan of the padded totals -> bucket
-//                 starts and num_tokens_post_pad
+//                 bucket total (32 buckets x 32 chunk segments per block)
+//   3. bktscan  : one block, exclusive scan of the padded totals in shared
+//                 memory -> bucket starts and num_tokens_post_pad
 //   4. scatter  : per chunk, stable local ranks and the final placement
 //                 (plus the pad sentinels and the per-block expert/adapter ids)
 // Stability inside a chunk: pairs are visited in rounds of 1024 consecutive
@@ -26,7 +27,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kMaxItems = 32;                         // pairs per thread per chunk
 constexpr int kMaxChunk = kThreads * kMaxItems;       // 32768 (fits uint16 indices)
-constexpr int kColThreads = 256;
+constexpr int kColWarps = 32;  // chunk segments per bucket in the column scan
+constexpr int kColThreads = 32 * kColWarps;
 
 __global__ void __launch_bounds__(kThreads)
 align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
@@ -39,83 +41,76 @@ align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
   const int64_t p0 = (int64_t)blockIdx.x * chunk;
   const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
   int bad = 0;
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const int key = align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
-    if (key >= 0) atomicAdd(&hist[key], 1u);
+  // every key of this thread first (all loads in flight), then the counts
+  int key[kMaxItems];
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it) {
+    const int j = it * kThreads + threadIdx.x;
+    key[it] = j < n ? align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad) : -1;
   }
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it)
+    if (key[it] >= 0) atomicAdd(&hist[key[it]], 1u);
   if (bad) set_status(d_status, bad);
   __syncthreads();
   uint32_t* row = cnt + (int64_t)blockIdx.x * NB;
   for (int b = threadIdx.x; b < NB; b += blockDim.x) row[b] = hist[b];
 }
 
+// Per bucket, the exclusive prefix of its counts over the chunks, in place,
+// and its total.  A block takes 32 buckets (one per lane) and splits the G
+// chunks over its 32 warps: each thread sums its segment (loads in flight
+// together), the 32 segment sums of a bucket are scanned in shared memory,
+// then each thread rewrites its segment.
 __global__ void __launch_bounds__(kColThreads)
 align_colscan_kernel(uint32_t* __restrict__ cnt, int G, int NB, uint32_t* __restrict__ btotal) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= NB) return;
-  uint32_t run = 0;
-  int g = 0;
-  // 16 loads in flight per round trip to L2
-  for (; g + 16 <= G; g += 16) {
-    uint32_t c[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) c[q] = cnt[(int64_t)(g + q) * NB + b];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      cnt[(int64_t)(g + q) * NB + b] = run;
-      run += c[q];
+  __shared__ uint32_t part[kColWarps][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int b = blockIdx.x * 32 + lane;
+  const int seg = (G + kColWarps - 1) / kColWarps;
+  const int g0 = min(G, w * seg), g1 = min(G, g0 + seg);
+  uint32_t local = 0;
+  if (b < NB) {
+#pragma unroll 8
+    for (int g = g0; g < g1; ++g) local += cnt[(int64_t)g * NB + b];
+  }
+  part[w][lane] = local;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t run = 0;
+    for (int q = 0; q < kColWarps; ++q) {
+      const uint32_t v = part[q][lane];
+      part[q][lane] = run;
+      run += v;
+    }
+    if (b < NB) btotal[b] = run;
+  }
+  __syncthreads();
+  uint32_t run = part[w][lane];
+  if (b < NB) {
+    for (int g = g0; g < g1; ++g) {
+      const uint32_t c = cnt[(int64_t)g * NB + b];
+      cnt[(int64_t)g * NB + b] = run;
+      run += c;
     }
   }
-  for (; g < G; ++g) {
-    const uint32_t c = cnt[(int64_t)g * NB + b];
-    cnt[(int64_t)g * NB + b] = run;
-    run += c;
-  }
-  btotal[b] = run;
 }
 
+// One block: the padded bucket totals are loaded (coalesced) into shared
+// memory, scanned there, and written out as the padded bucket starts.
+// Dynamic shared memory: (NB + 1) uint32.
 __global__ void __launch_bounds__(kThreads)
 align_bucketscan_kernel(const uint32_t* __restrict__ btotal, int NB, int block_size,
                         uint32_t* __restrict__ bstart, int32_t* __restrict__ num_post_pad,
                         int64_t capacity, int32_t* d_status) {
-  // bstart[0..NB] holds padded totals, then is scanned in place.
+  extern __shared__ uint32_t sb[];
   for (int b = threadIdx.x; b < NB; b += blockDim.x)
-    bstart[b] = (btotal[b] + block_size - 1) / block_size * block_size;
+    sb[b] = (btotal[b] + block_size - 1) / block_size * block_size;
   __syncthreads();
-  // per-thread contiguous ranges read global memory; fine for one block
-  __shared__ uint32_t warp_tot[32];
-  const int per = (NB + blockDim.x - 1) / blockDim.x;
-  const int b0 = min(NB, (int)threadIdx.x * per), b1 = min(NB, b0 + per);
-  uint32_t local = 0;
-  for (int b = b0; b < b1; ++b) local += bstart[b];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t inc = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    uint32_t w = lane < nw ? warp_tot[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += v;
-    }
-    if (lane < nw) warp_tot[lane] = w;
-  }
-  __syncthreads();
-  uint32_t run = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0u);
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t c = bstart[b];
-    bstart[b] = run;
-    run += c;
-  }
-  if (threadIdx.x == blockDim.x - 1) {
-    bstart[NB] = run;
+  align_block_scan(sb, NB);  // sb[NB] = total
+  for (int b = threadIdx.x; b <= NB; b += blockDim.x) bstart[b] = sb[b];
+  if (threadIdx.x == 0) {
+    const uint32_t run = sb[NB];
     *num_post_pad = (int32_t)run;
     if ((int64_t)run > capacity) set_status(d_status, MLR_STATUS_CAPACITY);
   }
@@ -140,18 +135,21 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
   const int64_t p0 = (int64_t)blockIdx.x * chunk;
   const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
   const int rounds = (n + kThreads - 1) / kThreads;
-  // (key << 16) | slot per pair; key < 40960 and slot < 32768 both fit 16 bits
+  // (key << 16) | slot per pair; key < 40960 and slot < 32768 both fit 16 bits.
+  // Every key of this thread is loaded first (all loads in flight), then the
+  // counting rounds run on shared memory only.
   uint32_t ks[kMaxItems];
   int bad = 0;
 #pragma unroll
   for (int it = 0; it < kMaxItems; ++it) {
+    const int j = it * kThreads + threadIdx.x;
+    const int key = j < n ? align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad) : -1;
+    ks[it] = key >= 0 ? (uint32_t)key : 0xFFFFFFFFu;
+  }
+#pragma unroll
+  for (int it = 0; it < kMaxItems; ++it) {
     if (it < rounds) {
-      const int j = it * kThreads + threadIdx.x;
-      ks[it] = 0xFFFFFFFFu;
-      if (j < n) {
-        const int key = align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad);
-        if (key >= 0) ks[it] = ((uint32_t)key << 16) | atomicAdd(&off[key], 1u);
-      }
+      if (ks[it] != 0xFFFFFFFFu) ks[it] = (ks[it] << 16) | atomicAdd(&off[ks[it]], 1u);
       __syncthreads();  // rounds are ordered: a bucket's slots follow round order
     }
   }
@@ -287,12 +285,16 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
     MLR_CHECK_LAUNCH();
     note_launch();
   }
-  align_colscan_kernel<<<(int)ceil_div(pl.NB, kColThreads), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB,
-                                                                                     btotal);
+  align_colscan_kernel<<<(int)ceil_div(pl.NB, 32), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
   MLR_CHECK_LAUNCH();
   note_launch();
-  align_bucketscan_kernel<<<1, kThreads, 0, stream>>>(btotal, pl.NB, block_size, bstart, num_post_pad,
-                                                      capacity, d_status);
+  const size_t sm_scan = (size_t)(pl.NB + 1) * 4;
+  if (sm_scan > 48 * 1024 &&
+      cudaFuncSetAttribute(align_bucketscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan) !=
+          cudaSuccess)
+    return MLR_ERR_CUDA;
+  align_bucketscan_kernel<<<1, kThreads, sm_scan, stream>>>(btotal, pl.NB, block_size, bstart, num_post_pad,
+                                                            capacity, d_status);
   MLR_CHECK_LAUNCH();
   note_launch();
   if (pl.G > 0) {
@@ -321,7 +323,7 @@ int align_dense_count(const AlignPlan& pl, const int32_t* topk_ids, const int32_
     MLR_CHECK_LAUNCH();
     note_launch();
   }
-  align_colscan_kernel<<<(int)ceil_div(pl.NB, kColThreads), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
+  align_colscan_kernel<<<(int)ceil_div(pl.NB, 32), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;

@@ -35,6 +35,11 @@ namespace {
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the lookup may load this library's module onto that device).
+// The cache is keyed by device ordinal: it assumes the device's primary
+// context (the one the CUDA runtime uses) for the life of the process.  After
+// cudaDeviceReset, or under another driver-API context made current, the
+// cached address would be stale, so callers doing either must not use this
+// entry point afterwards.
 int scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

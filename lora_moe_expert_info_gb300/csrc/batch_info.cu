@@ -3,8 +3,9 @@
 // items 1-3 and the MoELoRABatchInfo dataclass in 关键源码片段).
 //
 // One launch.  Blocks 0..nt-1 each own a tile of 1024 consecutive tokens: the
-// block finds the first and last request segment of its tile with two binary
-// searches, stages that run of seg_indptr / weight_indices in shared memory and
+// block finds the first and last request segment of its tile with a
+// block-cooperative 256-way search, stages that run of seg_indptr /
+// weight_indices in shared memory and
 // every thread resolves 4 consecutive tokens there (one 16-byte store).  The
 // last block validates seg_indptr, the max_len hint and the adapter ids, and
 // writes all num_loras entries of adapter_enabled from a shared bit set.
@@ -18,6 +19,39 @@ constexpr int kTokPerThread = 4;
 constexpr int kTile = kThreads * kTokPerThread;
 constexpr int kStaged = 2048;               // segments staged per tile
 constexpr int kMaxLoras = 65536;            // adapter_enabled bit set: 8 KB
+
+// Block-wide search for the segments of two tokens ta <= tb: the largest i in
+// [0, bs - 1] with indptr[i] <= t, for t = ta and t = tb (indptr assumed
+// non-decreasing; any result stays in [0, bs - 1] otherwise).  Each round the
+// block samples kThreads evenly spaced entries of the remaining range and
+// counts those <= t, which narrows the range kThreads-fold: two or three
+// rounds of one load per thread instead of a serial binary search of
+// log2(bs) dependent loads.  All threads of the block call it.
+__device__ __forceinline__ void block_seg_search2(const int32_t* __restrict__ indptr, int bs, int ta, int tb,
+                                                  int* ra, int* rb) {
+  int a0 = 0, b0 = bs - 1, a1 = 0, b1 = bs - 1;  // inclusive ranges of the two answers
+  while (true) {
+    const int na = b0 - a0 + 1, nb = b1 - a1 + 1;
+    if (na <= 1 && nb <= 1) break;
+    const int sa = (na + kThreads - 1) / kThreads, sb = (nb + kThreads - 1) / kThreads;  // strides
+    const int ca = a0 + (int)threadIdx.x * sa, cb = a1 + (int)threadIdx.x * sb;
+    const bool pa = na > 1 && ca <= b0 && __ldg(indptr + ca) <= ta;
+    const bool pb = nb > 1 && cb <= b1 && __ldg(indptr + cb) <= tb;
+    const int ka = __syncthreads_count(pa), kb = __syncthreads_count(pb);
+    if (na > 1) {
+      const int lo = a0 + (max(ka, 1) - 1) * sa;  // the answer lies in [lo, lo + sa - 1]
+      a0 = lo;
+      b0 = min(b0, lo + sa - 1);
+    }
+    if (nb > 1) {
+      const int lo = a1 + (max(kb, 1) - 1) * sb;
+      a1 = lo;
+      b1 = min(b1, lo + sb - 1);
+    }
+  }
+  *ra = a0;
+  *rb = a1;
+}
 
 // largest i in [lo, hi] with indptr[i] <= t  (indptr assumed non-decreasing)
 __device__ __forceinline__ int seg_search(const int32_t* __restrict__ indptr, int lo, int hi, int t) {
@@ -36,7 +70,6 @@ batch_info_kernel(const int32_t* __restrict__ seg_indptr, const int32_t* __restr
   __shared__ int32_t s_ptr[kStaged + 1];
   __shared__ int32_t s_wi[kStaged];
   __shared__ uint32_t s_bits[kMaxLoras / 32];
-  __shared__ int s_lo, s_n;
   __shared__ int s_bad;
 
   const int ntile = (int)ceil_div(num_tokens, kTile);
@@ -70,14 +103,9 @@ batch_info_kernel(const int32_t* __restrict__ seg_indptr, const int32_t* __restr
   // ---- token tile ----
   const int t0 = blockIdx.x * kTile;
   const int t_last = min(num_tokens, t0 + kTile) - 1;
-  if (threadIdx.x == 0) {
-    const int lo = seg_search(seg_indptr, 0, bs - 1, t0);
-    const int hi = seg_search(seg_indptr, 0, bs - 1, t_last);
-    s_lo = lo;
-    s_n = hi - lo + 1;
-  }
-  __syncthreads();
-  const int lo = s_lo, n = s_n;
+  int lo, hi;
+  block_seg_search2(seg_indptr, bs, t0, t_last, &lo, &hi);
+  const int n = hi - lo + 1;
   const bool staged = (n >= 1 && n <= kStaged);
   if (staged) {
     for (int j = threadIdx.x; j <= n; j += blockDim.x) s_ptr[j] = seg_indptr[lo + j];
@@ -89,10 +117,10 @@ batch_info_kernel(const int32_t* __restrict__ seg_indptr, const int32_t* __restr
   if (t >= num_tokens) return;
   int v[kTokPerThread];
   if (staged) {
-    int j = 0, hi = n - 1;
-    while (j < hi) {  // largest j with s_ptr[j] <= t
-      const int mid = (j + hi + 1) >> 1;
-      if (s_ptr[mid] <= t) j = mid; else hi = mid - 1;
+    int j = 0, jh = n - 1;
+    while (j < jh) {  // largest j with s_ptr[j] <= t
+      const int mid = (j + jh + 1) >> 1;
+      if (s_ptr[mid] <= t) j = mid; else jh = mid - 1;
     }
 #pragma unroll
     for (int q = 0; q < kTokPerThread; ++q) {

@@ -173,6 +173,7 @@ struct Params {
   int wsr, wsc;   // FP8 weights: 128-row and 128-column scale blocks per expert matrix
   const float* wscale;  // FP8 weights: [E][wsr][wsc] block scales (weight = code x scale)
   int64_t P;
+  uint64_t wait_ns;  // give-up limit of the pipeline waits
   const float* topk_weights;
   const int32_t* lora_ranks;
   const float* scalings;
@@ -185,6 +186,7 @@ struct Params {
   uint16_t* h;    // [I/64][cap][64]
   uint16_t* zd;   // [R16/8][zcap][8]
   float* yacc;    // [T, H]
+  uint16_t* dpair;  // down, deterministic combine: bf16 w * d of every pair, [P][H] (else null)
   int32_t* status;
 };
 
@@ -421,7 +423,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       for (int s = 0; s < nsteps; ++s, ++gs) {
         const int st = gs % S, round = gs / S;
         uint8_t* sbuf = smem + st * SB;
-        const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort);
+        const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort, p.wait_ns);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         const bool main_step = s < nks;
         // the row tile of x_sorted / h: one 64/128/192/256-row box where the
@@ -614,7 +616,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
           }
         }
-        const bool w_ok = mbar_wait(&c.raw_full[st], round & 1, abort);
+        const bool w_ok = mbar_wait(&c.raw_full[st], round & 1, abort, p.wait_ns);
         uint4 raw[kPer];
         if (s < nks) {
 #pragma unroll
@@ -661,14 +663,14 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       const Item it = load_item_warp<KIND>(p, item, &c.rec_m, lane);
       if (lane == 0) {
         const int b = il % CF::kAccBufs;
-        if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort)) ok = false;
+        if (!mbar_wait(&c.acc_empty[b], ((il / CF::kAccBufs) & 1) ^ 1, abort, p.wait_ns)) ok = false;
         tc_fence_after();
         const uint32_t acc = tmem + b * CF::kAccCols;
         const int nsteps = ok ? nks + it.nexp : 0;
         ExpandCursor cur;
         for (int s = 0; s < nsteps; ++s, ++gs) {
           const int st = gs % S, round = gs / S;
-          if (!mbar_wait(&c.full[st], round & 1, abort)) { ok = false; break; }
+          if (!mbar_wait(&c.full[st], round & 1, abort, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sb = smem_u32(smem + st * SB);
           if (s < nks) {
@@ -726,7 +728,6 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     const int eh = (warp - kEpiWarp0) >> 2;             // epilogue half (gate_up: 0 or 1)
     const int et = (tid - kEpiWarp0 * 32) & 127;         // 0..127 within the half
     const int ebar = 1 + eh;                             // the half's named barrier (2 halves: 1, 2)
-    uint8_t* epih = epi + eh * kEpiBytes;                // the half's staging buffer
     int il = 0;
     for (int item = unit; item < n_items; item += n_units, ++il) {
       const Item it = load_item<KIND>(p, item);
@@ -737,13 +738,15 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const int n = et + 128 * eh;
         const int pr = (n >= it.lo && n < it.hi) ? p.usorted[it.row0 + n] : (int)p.P;
         const bool real = pr >= 0 && pr < p.P;
-        c.tok[il & 1][n] = real ? pr / p.K : -1;
+        // the token (fp32 reductions into y_acc) or, for the deterministic
+        // combine, the pair (its own row of dpair)
+        c.tok[il & 1][n] = real ? (p.dpair ? pr : pr / p.K) : -1;
         c.w[il & 1][n] = real ? (p.topk_weights ? p.topk_weights[pr] : 1.f) : 0.f;  // none: weight 1
       }
       // one thread waits for the accumulator; the decision is shared through
       // shared memory so that all 128 epilogue threads take the same branch
       if (et == 0 && eh == 0) {
-        const bool got = mbar_wait(&c.acc_full[b], (il / CF::kAccBufs) & 1, abort);
+        const bool got = mbar_wait(&c.acc_full[b], (il / CF::kAccBufs) & 1, abort, p.wait_ns);
         c.epi_go[il & 1] = (got && !*abort) ? 1 : 0;
       }
       if (kHalves == 1) named_bar_sync(1, 128);  // also publishes tok/w
@@ -824,6 +827,30 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) wb[j * 32 + lane] = v[g + j];
             __syncwarp();
+            if (p.dpair) {
+              // deterministic combine: a lane holds 8 consecutive rows of one
+              // pair and stores w * d as bf16 into the pair's own row (16 B)
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int j = k * 8 + (lane >> 2);
+                const int n = c0 + g + j;
+                const int pr = tk[n];
+                const int q8 = (lane & 3) * 8;
+                if (hq + q8 < p.H && pr >= 0) {  // H is a multiple of 8: all 8 rows or none
+                  const float4 a = *reinterpret_cast<const float4*>(wb + j * 32 + q8);
+                  const float4 d = *reinterpret_cast<const float4*>(wb + j * 32 + q8 + 4);
+                  const float w = wk[n];
+                  uint4 o;
+                  o.x = (uint32_t)f32_to_bf16_bits(w * a.x) | ((uint32_t)f32_to_bf16_bits(w * a.y) << 16);
+                  o.y = (uint32_t)f32_to_bf16_bits(w * a.z) | ((uint32_t)f32_to_bf16_bits(w * a.w) << 16);
+                  o.z = (uint32_t)f32_to_bf16_bits(w * d.x) | ((uint32_t)f32_to_bf16_bits(w * d.y) << 16);
+                  o.w = (uint32_t)f32_to_bf16_bits(w * d.z) | ((uint32_t)f32_to_bf16_bits(w * d.w) << 16);
+                  *reinterpret_cast<uint4*>(p.dpair + (int64_t)pr * p.H + hq + q8) = o;
+                }
+              }
+              __syncwarp();
+              continue;
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int j = k * 4 + (lane >> 3);  // column of this lane's reduction
@@ -1306,6 +1333,41 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
   }
 }
 
+// Deterministic top-k combine: y[t] = sum over k, in increasing k, of the
+// pair rows dpair[t*K + k] (bf16 w * d written by the down GEMM), in fp32.
+// Pairs the align dropped (expert or adapter id out of range) never received
+// a row and add nothing.  One thread per 8 consecutive columns of a token.
+__global__ void combine_kernel(const uint16_t* __restrict__ dpair, const int32_t* __restrict__ topk_ids,
+                               const int32_t* __restrict__ mapping, int64_t T, int K, int H, int E, int L,
+                               uint16_t* __restrict__ y) {
+  const int g8 = H / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * g8) return;
+  const int64_t t = i / g8;
+  const int c = (int)(i - t * g8) * 8;
+  const int l = __ldg(mapping + t);
+  const bool lora_ok = l >= -1 && l < L;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int k = 0; k < K; ++k) {
+    const int64_t pr = t * K + k;
+    const int e = __ldg(topk_ids + pr);
+    if (!lora_ok || e < 0 || e >= E) continue;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(dpair + pr * H + c));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] += __uint_as_float(wv[q] << 16);
+      acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
+    }
+  }
+  uint4 o;
+  o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
+  o.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
+  o.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
+  o.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
+  *reinterpret_cast<uint4*>(y + t * H + c) = o;
+}
+
 __global__ void convert_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, int64_t n) {
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 4 <= n) {
@@ -1776,6 +1838,10 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   }
   if (!ok) return MLR_ERR_CUDA;
 
+  // deterministic combine: the down GEMM writes each pair's weighted row into
+  // the x_sorted region (dead after gate_up: P rows of H <= its cap rows of
+  // round_up(H, 64)) and a combine kernel sums a token's rows in k order
+  const bool det = combine_deterministic();
   const int prof = prof_call_begin(stream);
   int rc = MLR_OK;
   // the CUDA-core shrink pays off when buckets average a few pairs (decode)
@@ -1822,7 +1888,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
     gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, yacc,
-                                                         (int64_t)T * H / 4);
+                                                         det ? 0 : (int64_t)T * H / 4);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -1836,6 +1902,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   p.zshort = zrows >= 64 ? 1 : 0;  // zcap >= 256, so the 64-row maps always exist
   p.bmask = bmask;
   p.P = (int64_t)T * K;
+  p.wait_ns = wait_limit_ns();
   p.topk_weights = topk_weights;
   p.lora_ranks = lora_ranks;
   p.scalings = scalings;
@@ -1882,6 +1949,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     // a pair covers 256 rows of H, a single CTA (FP8 weights) 128
     q.n_tiles = counts; q.nblk = (int)ceil_div(H, fp8 ? 128 : 256); q.rmask = rm_dn;
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
+    q.dpair = det ? xs : nullptr;
     q.wscale = s_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
     rc = fp8 ? launch_gemm<kDown, true>(m_dn, q, f.max_base, stream)
              : launch_gemm<kDown>(m_dn, q, f.max_base, stream);
@@ -1889,7 +1957,11 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * H;
-  convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
+  if (det)
+    combine_kernel<<<(unsigned)ceil_div(n / 8, 256), 256, 0, stream>>>(xs, topk_ids, token_lora_mapping, T, K, H, E,
+                                                                        L, y);
+  else
+    convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
   MLR_CHECK_LAUNCH();
   note_launch();
   prof_mark(prof, 6, stream);
@@ -2065,6 +2137,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
   p.zshort = p.zrows >= 64 ? 1 : 0;
   p.bmask = L > 0 ? b_view_mask(R) : 0;
   p.P = T;
+  p.wait_ns = wait_limit_ns();
   p.topk_weights = nullptr;  // weight 1 for every token
   p.lora_ranks = lora_ranks;
   p.scalings = scalings;

@@ -20,7 +20,10 @@
 
 namespace mlr {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+// A pipeline wait gives up after this long by default (the limit is a run-time
+// setting, moe_lora_set_wait_limit_ns); teardown waits always use it.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;  // largest settable limit: 60 s
 
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -65,14 +68,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up when
-// *abort is set by another role or after kWaitLimitNs (then sets *abort).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// *abort is set by another role or after limit_ns (then sets *abort).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }

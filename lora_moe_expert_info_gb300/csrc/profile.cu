@@ -9,6 +9,8 @@ namespace mlr {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_ns{kWaitLimitNs};
+std::atomic<int> g_deterministic{1};  // measured no slower than the atomic combine
 std::mutex g_mu;
 bool g_on = false;
 int g_max_calls = 0, g_calls = 0;
@@ -29,6 +31,10 @@ const char* kStageNames[kProfStages] = {"align_plan", "gather", "shrink_gate_up"
 }  // namespace
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
+bool combine_deterministic() { return g_deterministic.load(std::memory_order_relaxed) != 0; }
 
 int prof_call_begin(cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -100,3 +106,19 @@ extern "C" const char* moe_lora_profile_stage_name(int32_t stage) {
 }
 
 extern "C" uint64_t moe_lora_launch_count(void) { return mlr::g_launches.load(); }
+
+extern "C" int moe_lora_set_wait_limit_ns(uint64_t ns) {
+  if (ns > mlr::kMaxWaitLimitNs) return MLR_ERR_INVALID;
+  mlr::g_wait_ns.store(ns == 0 ? 1 : ns, std::memory_order_relaxed);
+  return MLR_OK;
+}
+
+extern "C" uint64_t moe_lora_wait_limit_ns(void) { return mlr::wait_limit_ns(); }
+
+extern "C" int moe_lora_set_deterministic(int32_t on) {
+  if (on != 0 && on != 1) return MLR_ERR_INVALID;
+  mlr::g_deterministic.store(on, std::memory_order_relaxed);
+  return MLR_OK;
+}
+
+extern "C" int32_t moe_lora_deterministic(void) { return mlr::combine_deterministic() ? 1 : 0; }

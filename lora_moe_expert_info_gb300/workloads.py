@@ -55,6 +55,14 @@ CONFIGS = {
         "deepseek_v3_prefill", 7168, 2048, 256, 8, 4, 64, 16, 8192,
         "DeepSeek-V3-like prefill: hidden 7168, intermediate 2048, 256 experts top-8, 4 slots ranks "
         "{16,32,64,64} alpha=2r, 8192 tokens in 8 segments of 1024, router bias N(0,0.5)"),
+    # One eighth of the DeepSeek-V3-like prefill (32 experts, 1024 tokens; the
+    # same shapes, ranks, routing bias and about 256 pairs per expert): a
+    # 2.8 GB case for counter captures whose per-expert traffic scales to the
+    # full batch.
+    "deepseek_v3_slice": LayerConfig(
+        "deepseek_v3_slice", 7168, 2048, 32, 8, 4, 64, 16, 1024,
+        "one eighth of the DeepSeek-V3-like prefill: hidden 7168, intermediate 2048, 32 experts top-8, "
+        "4 slots ranks {16,32,64,64} alpha=2r, 1024 tokens in 8 segments of 128, router bias N(0,0.5)"),
     "metadata_stress": LayerConfig(
         "metadata_stress", 0, 0, 256, 8, 64, 64, 64, 1048576,
         "metadata stress: 1,048,576 tokens in 4096 segments (geometric lens, mean 256), 64 slots "
@@ -138,7 +146,7 @@ def _ranks_and_scalings(cfg: LayerConfig, g: torch.Generator):
     elif cfg.name == "decode":
         ranks = [[0, 8, 16, 32][l % 4] for l in range(L)]
         scal = [0.0 if r == 0 else 2.0 for r in ranks]
-    elif cfg.name == "deepseek_v3_prefill":
+    elif cfg.name in ("deepseek_v3_prefill", "deepseek_v3_slice"):
         ranks = [16, 32, 64, 64]
         scal = [2.0] * L
     elif cfg.name == "metadata_stress":
@@ -166,8 +174,8 @@ def _segments(cfg: LayerConfig, g: torch.Generator):
         adapters = torch.randint(0, L, (256,), generator=g).int()
         none = torch.rand(256, generator=g) < 0.1
         adapters[none] = -1
-    elif cfg.name == "deepseek_v3_prefill":
-        lens = torch.full((8,), 1024, dtype=torch.int32)
+    elif cfg.name in ("deepseek_v3_prefill", "deepseek_v3_slice"):
+        lens = torch.full((8,), T // 8, dtype=torch.int32)
         adapters = torch.randint(0, L, (8,), generator=g).int()
     elif cfg.name == "metadata_stress":
         u = torch.rand(4096, generator=g, dtype=torch.float64).clamp_min(1e-12)
@@ -186,7 +194,7 @@ def make_batch(cfg: LayerConfig, device="cpu", seed: int = 0) -> Batch:
     lens, adapters = _segments(cfg, gc)
     ranks, scal = _ranks_and_scalings(cfg, gc)
     gd = _gen(device, seed + 1)
-    bias = 0.5 if cfg.name in ("deepseek_v3_prefill",) else 0.0
+    bias = 0.5 if cfg.name in ("deepseek_v3_prefill", "deepseek_v3_slice") else 0.0
     ids, wts = route(cfg.num_tokens, cfg.num_experts, cfg.topk, gd, device, expert_bias_std=bias)
     return Batch(lens.to(device), _indptr(lens).to(device), adapters.to(device),
                  ranks.to(device), scal.to(device), ids, wts)

@@ -163,6 +163,35 @@ def test_small_bucket_sizes(cuda_device):
     assert within(y, r) <= 0 and within(y0, r0) <= 0
 
 
+def _fill_rank_padding(w, ranks, value):
+    """Writes `value` into every stack entry past slot l's rank r_l (the rank
+    padding the header allows to hold any finite value)."""
+    for l, r in enumerate(int(v) for v in ranks):
+        w.lora_a_gu[l, :, :, r:, :] = value
+        w.lora_b_gu[l, :, :, :, r:] = value
+        w.lora_a_down[l, :, r:, :] = value
+        w.lora_b_down[l, :, :, r:] = value
+
+
+@pytest.mark.parametrize("small_buckets", [False, True])
+def test_finite_nonzero_rank_padding_is_ignored(cuda_device, small_buckets):
+    # ranks 12, 0, 24, 5 under R = 32: the padding past each rank (and the whole
+    # stack of the rank-0 slot) holds 1000.0; y must still equal the oracle's,
+    # which reads only the first r_l ranks.  small_buckets: one pair per bucket,
+    # so the CUDA-core shrink runs instead of the tensor-core one.
+    if small_buckets:
+        c = custom_case(cuda_device, T=24, K=1, E=24, H=128, I=128, L=4, R=32, ranks=[12, 0, 24, 5],
+                        seg_lens=[6, 6, 6, 6], adapters=[0, 1, 2, 3], lora_std="fan_in", seed=4)
+        c.b.topk_ids.copy_(torch.arange(24, dtype=torch.int32, device=cuda_device).view(24, 1))
+    else:
+        c = custom_case(cuda_device, T=180, K=2, E=4, H=192, I=128, L=4, R=32, ranks=[12, 0, 24, 5],
+                        seg_lens=[40, 50, 60, 30], adapters=[0, 1, 2, 3], lora_std="fan_in", seed=2)
+    r = c.ref()
+    _fill_rank_padding(c.w, c.b.lora_ranks.cpu(), 1000.0)
+    assert np.array_equal(c.ref(), r)  # the oracle never reads the padding
+    assert within(c.gpu(), r) <= 0
+
+
 def test_empty_batch(cuda_device):
     # T = 0: nothing to do, no launch, an empty y
     c = custom_case(cuda_device, T=8, K=2, E=4, H=128, I=128, L=2, R=16, ranks=[16, 8],

@@ -5,10 +5,12 @@ own every byte through their own pools, latency-critical paths where
 cudaMalloc/cudaFree could synchronise the device, layers given no allocator).
 The no-allocation entry point keeps its scratch in a fixed array inside the
 library.  These tests call it through the C ABI and check that its results
-equal the workspace-taking moe_lora_align bit for bit on two calls in a row
-(the second call reuses the shared scratch the first one left behind), and
-that sizes beyond the fixed scratch are refused.  The file is named to be
-collected last and needs no state from other tests.
+equal, bit for bit, both the workspace-taking moe_lora_align and the CPU oracle
+on calls in a row (each later call reuses the shared scratch the one before it
+left behind, on the single-block path and on the four-launch chunked path with
+differently shaped count matrices), and that sizes beyond the fixed scratch are
+refused.  The file is named to be collected last and needs no state from other
+tests.
 """
 import ctypes
 
@@ -17,6 +19,7 @@ import pytest
 import torch
 
 import lora_moe_expert_info_gb300 as mlr
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -66,6 +69,12 @@ def _check_same_as_workspace_call(topk, mapping, E, L, bs):
     assert torch.equal(be[:npad // bs], rbe[:npad // bs])
     assert torch.equal(bl[:npad // bs], rbl[:npad // bs])
     assert torch.all(s[mlr.moe_lora_align_capacity(*topk.shape, E, L, bs):] == -7)  # never past capacity
+    # and the CPU oracle's canonical order
+    st, os_, obe, obl, on = oracle.align(topk.cpu().numpy(), mapping.cpu().numpy(), E, L, bs)
+    assert st == 0 and on == npad
+    assert np.array_equal(s[:npad].cpu().numpy(), os_)
+    assert np.array_equal(be[:npad // bs].cpu().numpy(), obe)
+    assert np.array_equal(bl[:npad // bs].cpu().numpy(), obl)
 
 
 def test_two_calls_in_a_row_match_workspace_align(cuda_device):
@@ -75,6 +84,18 @@ def test_two_calls_in_a_row_match_workspace_align(cuda_device):
     _check_same_as_workspace_call(t1, m1, 128, 8, 16)
     t2, m2 = _inputs(2, 256, 8, 128, 32, cuda_device)
     _check_same_as_workspace_call(t2, m2, 128, 32, 16)
+
+
+def test_chunked_calls_in_a_row_with_other_shapes(cuda_device):
+    # Both calls take the four-launch chunked path (more than 16384 pairs); the
+    # second has fewer chunks and another bucket count, so its count matrix
+    # overlaps the stale one of the first call with a different layout.
+    t1, m1 = _inputs(3, 4096, 8, 128, 8, cuda_device)     # 32768 pairs, 128 x 9 buckets
+    assert 4096 * 8 > 16384
+    _check_same_as_workspace_call(t1, m1, 128, 8, 16)
+    t2, m2 = _inputs(4, 3000, 6, 64, 4, cuda_device)      # 18000 pairs, 64 x 5 buckets
+    assert 3000 * 6 > 16384
+    _check_same_as_workspace_call(t2, m2, 64, 4, 32)
 
 
 def test_sizes_beyond_the_fixed_scratch_are_refused(cuda_device):
