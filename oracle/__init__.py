@@ -72,6 +72,13 @@ def _load():
                                                vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                                i64, i64, i64, i64, i64, i64, i64,
                                                vp, i64, vp, ctypes.c_int]
+            lib.oracle_forward_int8.restype = ctypes.c_int
+            lib.oracle_forward_int8.argtypes = lib.oracle_forward_fp8.argtypes
+            lib.oracle_forward_w4a16.restype = ctypes.c_int
+            lib.oracle_forward_w4a16.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                                 i64, i64, i64, i64, i64, i64, i64,
+                                                 vp, i64, vp, ctypes.c_int]
             lib.oracle_e4m3_value.restype = ctypes.c_double
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint32]
             lib.oracle_lora_linear.restype = ctypes.c_int
@@ -253,6 +260,97 @@ def forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scali
         dq.ctypes.data, ds.ctypes.data, ops[0][0], ops[1][0], ops[2][0], ops[3][0], ldt,
         T, K, E, H, I, L, R, tok_ptr, n_out, y.ctypes.data, int(threads))
     del xk, tok
+    return int(st), y
+
+
+def _quant_common(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                  lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens):
+    x_np = np.asarray(x)
+    T, H = x_np.shape
+    topk_ids = _i32(topk_ids)
+    c = dict(T=T, H=H, K=topk_ids.shape[1], topk_ids=topk_ids,
+             topk_weights=np.ascontiguousarray(np.asarray(topk_weights, dtype=np.float32)),
+             mapping=_i32(token_lora_mapping), lora_ranks=_i32(lora_ranks),
+             scalings=np.ascontiguousarray(np.asarray(scalings, dtype=np.float32)))
+    L, E, _, R, _ = np.asarray(lora_a_gu).shape
+    c.update(L=L, E=E, R=R)
+    c["x"] = _operand(x_np)
+    ops = [_operand(a) for a in (lora_a_gu, lora_b_gu, lora_a_down, lora_b_down)]
+    ldt = ops[0][1]
+    if any(o[1] != ldt for o in ops):
+        raise TypeError("LoRA operands must share one dtype")
+    c.update(ops=ops, ldt=ldt)
+    if tokens is None:
+        c.update(tok=None, n_out=T, tok_ptr=None)
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        c.update(tok=tok, n_out=tok.shape[0], tok_ptr=tok.ctypes.data)
+    return c
+
+
+def forward_int8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                 w_gate_up_q, w_gate_up_scale, w_down_q, w_down_scale,
+                 lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens=None, threads: int = 0):
+    """The layer with block-wise INT8 base experts.  Returns (status, y) float64.
+
+    w_gate_up_q [E,2I,H] and w_down_q [E,H,I] hold int8 codes (int8 or uint8
+    arrays of the two's-complement bytes); the scales are float32 per 128 x 128
+    block, laid out as in forward_fp8; weight = code x scale.
+    """
+    c = _quant_common(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                      lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens)
+    wq = np.ascontiguousarray(np.asarray(w_gate_up_q).view(np.uint8))
+    dq = np.ascontiguousarray(np.asarray(w_down_q).view(np.uint8))
+    T, H, K, E, L, R = c["T"], c["H"], c["K"], c["E"], c["L"], c["R"]
+    I = wq.shape[1] // 2
+    assert wq.shape == (E, 2 * I, H) and dq.shape == (E, H, I)
+    ws = np.ascontiguousarray(np.asarray(w_gate_up_scale, dtype=np.float32))
+    ds = np.ascontiguousarray(np.asarray(w_down_scale, dtype=np.float32))
+    assert ws.shape == (E, (2 * I + 127) // 128, (H + 127) // 128)
+    assert ds.shape == (E, (H + 127) // 128, (I + 127) // 128)
+    y = np.zeros((c["n_out"], H), dtype=np.float64)
+    ops = c["ops"]
+    st = _load().oracle_forward_int8(
+        c["x"][0], c["x"][1], c["topk_ids"].ctypes.data, c["topk_weights"].ctypes.data, c["mapping"].ctypes.data,
+        c["lora_ranks"].ctypes.data, c["scalings"].ctypes.data, wq.ctypes.data, ws.ctypes.data,
+        dq.ctypes.data, ds.ctypes.data, ops[0][0], ops[1][0], ops[2][0], ops[3][0], c["ldt"],
+        T, K, E, H, I, L, R, c["tok_ptr"], c["n_out"], y.ctypes.data, int(threads))
+    return int(st), y
+
+
+def forward_w4a16(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                  w_gate_up_q, w_gate_up_scale, w_gate_up_zero, w_down_q, w_down_scale, w_down_zero,
+                  lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens=None, threads: int = 0):
+    """The layer with 4-bit base experts and 16-bit activations.  Returns (status, y).
+
+    w_gate_up_q [E,2I,H/2] and w_down_q [E,H,I/2] are uint8 bytes each holding
+    two uint4 codes (the even column in the low nibble); w_*_scale float32 and
+    w_*_zero uint8 (0..15) are [E, rows, ceil(cols/128)]: one scale and zero
+    point per row and group of 128 columns; weight = (code - zero) x scale.
+    """
+    c = _quant_common(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                      lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens)
+    T, H, K, E, L, R = c["T"], c["H"], c["K"], c["E"], c["L"], c["R"]
+    wq = np.ascontiguousarray(np.asarray(w_gate_up_q, dtype=np.uint8))
+    dq = np.ascontiguousarray(np.asarray(w_down_q, dtype=np.uint8))
+    I = wq.shape[1] // 2
+    assert wq.shape == (E, 2 * I, H // 2) and dq.shape == (E, H, I // 2)
+    arrs = []
+    for a, dt, shp in ((w_gate_up_scale, np.float32, (E, 2 * I, (H + 127) // 128)),
+                       (w_gate_up_zero, np.uint8, (E, 2 * I, (H + 127) // 128)),
+                       (w_down_scale, np.float32, (E, H, (I + 127) // 128)),
+                       (w_down_zero, np.uint8, (E, H, (I + 127) // 128))):
+        a = np.ascontiguousarray(np.asarray(a, dtype=dt))
+        assert a.shape == shp
+        arrs.append(a)
+    y = np.zeros((c["n_out"], H), dtype=np.float64)
+    ops = c["ops"]
+    st = _load().oracle_forward_w4a16(
+        c["x"][0], c["x"][1], c["topk_ids"].ctypes.data, c["topk_weights"].ctypes.data, c["mapping"].ctypes.data,
+        c["lora_ranks"].ctypes.data, c["scalings"].ctypes.data, wq.ctypes.data, arrs[0].ctypes.data,
+        arrs[1].ctypes.data, dq.ctypes.data, arrs[2].ctypes.data, arrs[3].ctypes.data,
+        ops[0][0], ops[1][0], ops[2][0], ops[3][0], c["ldt"],
+        T, K, E, H, I, L, R, c["tok_ptr"], c["n_out"], y.ctypes.data, int(threads))
     return int(st), y
 
 

@@ -238,22 +238,37 @@ double oracle_e4m3_value(uint32_t code) {
 }
 
 /*
- * A base expert weight [E, rows, cols]: dtype 0 bf16 bits, 1 double, or 2 FP8
- * E4M3 codes whose value is code x scale[e][row / 128][col / 128].
+ * A base expert weight [E, rows, cols]: dtype 0 bf16 bits, 1 double,
+ *   2 FP8 E4M3 codes: value = code x scale[e][row / 128][col / 128];
+ *   3 INT8 codes (two's complement, -128..127): the same 128 x 128 block scales;
+ *   4 UINT4 codes, two per byte along a row (element 2j in the low nibble of
+ *     byte j, element 2j+1 in the high nibble), with a scale and a zero point
+ *     (0..15) per row and group of 128 columns:
+ *     value = (code - zero[e][row][col / 128]) x scale[e][row][col / 128].
  */
 typedef struct {
   const void* p;
   int dtype;
   const float* scale;
   int64_t rows, cols;
+  const uint8_t* zero;  /* dtype 4 only */
 } WeightView;
 
 static double ld_w(const WeightView* v, int64_t e, int64_t row, int64_t col) {
   const int64_t idx = (e * v->rows + row) * v->cols + col;
-  if (v->dtype == 2) {
+  if (v->dtype == 2 || v->dtype == 3) {
     const int64_t rb = (v->rows + 127) / 128, cb = (v->cols + 127) / 128;
     const double sc = (double)v->scale[(e * rb + row / 128) * cb + col / 128];
-    return oracle_e4m3_value(((const uint8_t*)v->p)[idx]) * sc;
+    const uint8_t code = ((const uint8_t*)v->p)[idx];
+    if (v->dtype == 2) return oracle_e4m3_value(code) * sc;
+    return (double)(code < 128 ? (int)code : (int)code - 256) * sc;
+  }
+  if (v->dtype == 4) {
+    const int64_t gpr = (v->cols + 127) / 128;  /* groups per row */
+    const uint8_t byte = ((const uint8_t*)v->p)[(e * v->rows + row) * (v->cols / 2) + col / 2];
+    const int code = (col % 2 == 0) ? (byte & 15) : (byte >> 4);
+    const int64_t g = (e * v->rows + row) * gpr + col / 128;
+    return (double)(code - (int)v->zero[g]) * (double)v->scale[g];
   }
   return ld(v->p, v->dtype, idx);
 }
@@ -398,8 +413,8 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
                    int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
                    int num_threads) {
   if (w_dtype != 0 && w_dtype != 1) return ORC_INVALID;
-  const WeightView wgu = {w_gate_up, w_dtype, NULL, 2 * I, H};
-  const WeightView wdn = {w_down, w_dtype, NULL, H, I};
+  const WeightView wgu = {w_gate_up, w_dtype, NULL, 2 * I, H, NULL};
+  const WeightView wdn = {w_down, w_dtype, NULL, H, I, NULL};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, w_dtype, T, K, E, H, I, L, R,
                       tokens, n_out, y, num_threads);
@@ -424,8 +439,61 @@ int oracle_forward_fp8(const void* x, int x_dtype, const int32_t* topk_ids,
   if (lora_dtype != 0 && lora_dtype != 1) return ORC_INVALID;
   if (w_gate_up_q == NULL || w_gate_up_scale == NULL || w_down_q == NULL || w_down_scale == NULL)
     return ORC_INVALID;
-  const WeightView wgu = {w_gate_up_q, 2, w_gate_up_scale, 2 * I, H};
-  const WeightView wdn = {w_down_q, 2, w_down_scale, H, I};
+  const WeightView wgu = {w_gate_up_q, 2, w_gate_up_scale, 2 * I, H, NULL};
+  const WeightView wdn = {w_down_q, 2, w_down_scale, H, I, NULL};
+  return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
+                      &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
+                      R, tokens, n_out, y, num_threads);
+}
+
+/*
+ * The same layer with block-wise INT8 base experts ([PR22323] 功能与动机 and
+ * 实现拆解 item 1 name the INT8 method, blockwise_int8): codes are signed
+ * 8-bit integers with the FP8 layer's layout and 128 x 128 block scales;
+ * weight = code x scale.
+ */
+int oracle_forward_int8(const void* x, int x_dtype, const int32_t* topk_ids,
+                        const float* topk_weights, const int32_t* token_lora_mapping,
+                        const int32_t* lora_ranks, const float* scalings,
+                        const uint8_t* w_gate_up_q, const float* w_gate_up_scale,
+                        const uint8_t* w_down_q, const float* w_down_scale, const void* lora_a_gu,
+                        const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                        int lora_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                        int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                        int num_threads) {
+  if (lora_dtype != 0 && lora_dtype != 1) return ORC_INVALID;
+  if (w_gate_up_q == NULL || w_gate_up_scale == NULL || w_down_q == NULL || w_down_scale == NULL)
+    return ORC_INVALID;
+  const WeightView wgu = {w_gate_up_q, 3, w_gate_up_scale, 2 * I, H, NULL};
+  const WeightView wdn = {w_down_q, 3, w_down_scale, H, I, NULL};
+  return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
+                      &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
+                      R, tokens, n_out, y, num_threads);
+}
+
+/*
+ * The same layer with 4-bit weights and 16-bit activations ([PR22323] names
+ * the WNA16 method): w_gate_up_q [E, 2I, H/2] and w_down_q [E, H, I/2] hold
+ * UINT4 codes two per byte (low nibble first); scale and zero
+ * [E, rows, ceil(cols/128)] give each row's groups of 128 input columns a
+ * float scale and a zero point; weight = (code - zero) x scale.  H and I even.
+ */
+int oracle_forward_w4a16(const void* x, int x_dtype, const int32_t* topk_ids,
+                         const float* topk_weights, const int32_t* token_lora_mapping,
+                         const int32_t* lora_ranks, const float* scalings,
+                         const uint8_t* w_gate_up_q, const float* w_gate_up_scale,
+                         const uint8_t* w_gate_up_zero, const uint8_t* w_down_q,
+                         const float* w_down_scale, const uint8_t* w_down_zero, const void* lora_a_gu,
+                         const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                         int lora_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                         int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                         int num_threads) {
+  if (lora_dtype != 0 && lora_dtype != 1) return ORC_INVALID;
+  if (w_gate_up_q == NULL || w_gate_up_scale == NULL || w_gate_up_zero == NULL || w_down_q == NULL ||
+      w_down_scale == NULL || w_down_zero == NULL || H % 2 != 0 || I % 2 != 0)
+    return ORC_INVALID;
+  const WeightView wgu = {w_gate_up_q, 4, w_gate_up_scale, 2 * I, H, w_gate_up_zero};
+  const WeightView wdn = {w_down_q, 4, w_down_scale, H, I, w_down_zero};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
                       R, tokens, n_out, y, num_threads);
