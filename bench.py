@@ -303,12 +303,15 @@ def weak_scaling_rate(units_per_rank, world, ms_per_step_max):
     return world * units_per_rank / (ms_per_step_max * 1e-3)
 
 
-def layer_work(cfg, batch, mapping, fp8=False):
+def layer_work(cfg, batch, mapping, fp8=False, fmt=None):
     """Algorithmic FLOPs and bytes of the layer and of each stage (from the routing).
 
-    fp8: the base expert weights are one byte each plus a float32 scale per
-    128 x 128 block; LoRA operands and activations stay bf16.
+    fmt (or fp8=True for "fp8"): the base expert weights' format.  "fp8" and
+    "int8": one byte per weight plus a float32 scale per 128 x 128 block;
+    "w4a16": half a byte per weight plus a float32 scale and a one-byte zero
+    point per row and 128-column group.  LoRA operands and activations stay bf16.
     """
+    fmt = fmt or ("fp8" if fp8 else "bf16")
     import torch
     T, K, E, H, I, L = cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.hidden, cfg.intermediate, cfg.num_loras
     ids = batch.topk_ids.long().cpu()
@@ -326,9 +329,12 @@ def layer_work(cfg, batch, mapping, fp8=False):
     W = 2  # bf16 bytes
     nb = lambda n: (n + 127) // 128  # noqa: E731
     # base expert bytes per touched expert: gate_up and down matrices
-    if fp8:
+    if fmt in ("fp8", "int8"):
         wgu = 2 * H * I + 4 * nb(2 * I) * nb(H)
         wdn = H * I + 4 * nb(H) * nb(I)
+    elif fmt == "w4a16":
+        wgu = H * I + 5 * 2 * I * nb(H)
+        wdn = H * I // 2 + 5 * H * nb(I)
     else:
         wgu, wdn = 2 * H * I * W, H * I * W
     st = {
@@ -356,34 +362,40 @@ def roofline_entry(flops, byts, ms, peaks, peak_kind):
 
 
 # ------------------------------------------------------------ the two arms --
-def make_inputs(cfg_name, device, seed, fp8=False):
-    """Batch, bf16 weights and x; with fp8 also FP8 experts (else None)."""
+def make_inputs(cfg_name, device, seed, fmt="bf16"):
+    """Batch, bf16 weights and x; for a quantised format also its experts (else None)."""
     from lora_moe_expert_info_gb300 import workloads
     cfg = workloads.CONFIGS[cfg_name]
     b = workloads.make_batch(cfg, device=device, seed=seed)
     w = workloads.make_weights(cfg, b.lora_ranks, device=device, seed=seed)
     x = workloads.make_x(cfg, device=device, seed=seed)
-    q = workloads.make_fp8_experts(cfg, device=device, seed=seed) if fp8 else None
+    make = {"fp8": workloads.make_fp8_experts, "int8": workloads.make_int8_experts,
+            "w4a16": workloads.make_w4a16_experts}.get(fmt)
+    q = make(cfg, device=device, seed=seed) if make else None
     return cfg, b, w, x, q
 
 
-def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None, seed=0, q=None):
+QUANT_KEYS = {"fp8": ("w_gate_up_q", "w_gate_up_scale", "w_down_q", "w_down_scale"),
+              "int8": ("w_gate_up_q", "w_gate_up_scale", "w_down_q", "w_down_scale"),
+              "w4a16": ("w_gate_up_q", "w_gate_up_scale", "w_gate_up_zero", "w_down_q", "w_down_scale",
+                        "w_down_zero")}
+
+
+def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None, seed=0, q=None, fmt="bf16"):
     """Oracle tokens/s on a bounded seeded token sample; returns (rate, n_tokens, secs, threads).
-    With q (FP8 experts) the oracle's FP8 forward runs."""
+    With q (quantised experts of format fmt) the oracle's matching forward runs."""
     import numpy as np
     import torch
 
     import oracle
     bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    lora = [bits(getattr(w, k)) for k in ("lora_a_gu", "lora_b_gu", "lora_a_down", "lora_b_down")]
     if q is None:
         fwd = oracle.forward
-        host = [bits(getattr(w, k)) for k in ("w_gate_up", "w_down", "lora_a_gu", "lora_b_gu",
-                                              "lora_a_down", "lora_b_down")]
+        host = [bits(w.w_gate_up), bits(w.w_down)] + lora
     else:
-        fwd = oracle.forward_fp8
-        host = [q.w_gate_up_q.cpu().numpy(), q.w_gate_up_scale.cpu().numpy(), q.w_down_q.cpu().numpy(),
-                q.w_down_scale.cpu().numpy()] + [bits(getattr(w, k)) for k in ("lora_a_gu", "lora_b_gu",
-                                                                               "lora_a_down", "lora_b_down")]
+        fwd = {"fp8": oracle.forward_fp8, "int8": oracle.forward_int8, "w4a16": oracle.forward_w4a16}[fmt]
+        host = [getattr(q, k).cpu().numpy() for k in QUANT_KEYS[fmt]] + lora
     xb = bits(x)
     ids = b.topk_ids.cpu().numpy()
     wts = b.topk_weights.cpu().numpy()
@@ -417,19 +429,19 @@ def run_reference(args, rank, world):
         return None
     oracle.build()
     dev = "cpu"
-    fp8 = args.weights == "fp8"
-    cfg, b, w, x, q = make_inputs(args.config, dev, args.seed, fp8)
+    fmt = args.weights
+    cfg, b, w, x, q = make_inputs(args.config, dev, args.seed, fmt)
     st, mp, _ = oracle.batch_info(b.seg_indptr.numpy(), b.weight_indices.numpy(), b.lora_ranks.numpy(),
                                   cfg.num_tokens)
     # each step a bounded sample: the whole run takes about 90 s of oracle time
     per_step_target = max(0.25, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target, max_tokens=args.ref_tokens, q=q)
+        oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target, max_tokens=args.ref_tokens, q=q, fmt=fmt)
     rates, ns, secs = [], 0, 0.0
     thr = 1
     for i in range(args.steps):
         r, n, s, thr = oracle_sample_rate(cfg, b, w, x, mp, target_s=per_step_target,
-                                          max_tokens=args.ref_tokens, seed=i, q=q)
+                                          max_tokens=args.ref_tokens, seed=i, q=q, fmt=fmt)
         rates.append(r)
         ns += n
         secs += s
@@ -460,8 +472,8 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
-    fp8 = args.weights == "fp8"
-    cfg, b, w, x, q = make_inputs(name, dev, args.seed + rank, fp8)
+    fmt = args.weights
+    cfg, b, w, x, q = make_inputs(name, dev, args.seed + rank, fmt)
     T, K, E, H, I, L, R = (cfg.num_tokens, cfg.topk, cfg.num_experts, cfg.hidden, cfg.intermediate,
                            cfg.num_loras, cfg.max_rank)
     max_len = int(b.seg_lens.max())
@@ -470,10 +482,10 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mlr.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R), dtype=torch.uint8, device=dev)
     lk = {k: getattr(w, k) for k in ("lora_a_gu", "lora_b_gu", "lora_a_down", "lora_b_down")}
-    if fp8:
-        forward = mlr.fused_moe_lora_forward_fp8
-        wk = dict(w_gate_up_q=q.w_gate_up_q, w_gate_up_scale=q.w_gate_up_scale, w_down_q=q.w_down_q,
-                  w_down_scale=q.w_down_scale, **lk)
+    if q is not None:
+        forward = {"fp8": mlr.fused_moe_lora_forward_fp8, "int8": mlr.fused_moe_lora_forward_int8,
+                   "w4a16": mlr.fused_moe_lora_forward_w4a16}[fmt]
+        wk = dict({k: getattr(q, k) for k in QUANT_KEYS[fmt]}, **lk)
     else:
         forward = mlr.fused_moe_lora_forward
         wk = dict(w_gate_up=w.w_gate_up, w_down=w.w_down, **lk)
@@ -564,12 +576,12 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
         return None
 
     mp_np = mapping.cpu().numpy()
-    flops, byts, st_work = layer_work(cfg, b, mapping, fp8)
+    flops, byts, st_work = layer_work(cfg, b, mapping, fmt=fmt)
     cpu = None
     if with_cpu:
         import oracle
         oracle.build()
-        rate, n, secs, thr = oracle_sample_rate(cfg, b, w, x, mp_np, target_s=args.cpu_seconds, q=q)
+        rate, n, secs, thr = oracle_sample_rate(cfg, b, w, x, mp_np, target_s=args.cpu_seconds, q=q, fmt=fmt)
         cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                "sample": f"{n} seeded tokens of the {T}-token batch ({secs:.1f} s), fp64 C oracle, "
                          f"OpenMP over tokens"}
@@ -580,7 +592,7 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
     rf["kernel"] = STAGE_KERNELS.get(dom, dom)
     rf["stage"] = dom
     rf["peak_source"] = peak_label(peak_src)
-    rf["traffic"] = recorded_traffic(dom, cfg.name + ("_fp8" if fp8 else ""))
+    rf["traffic"] = recorded_traffic(dom, cfg.name + ("" if fmt == "bf16" else "_" + fmt))
     rf["algorithmic_bytes"] = int(st_work[dom][1])
     rf["algorithmic_flops"] = int(st_work[dom][0])
     rf["launch_ms"] = round(dom_ms, 4)
@@ -662,12 +674,28 @@ def measure_metadata(args, rank, world, dist, n_copies=4):
                     torch.empty(nblk, dtype=torch.int32, device=dev),
                     torch.empty(1, dtype=torch.int32, device=dev))})
 
+    # The timed calls go straight through the C ABI with their pointer
+    # arguments prepared once, so that the host's per-call cost stays below the
+    # kernels' time (the checked wrapper calls above validated every buffer).
+    import ctypes
+    lib = mlr.library()
+    vp = ctypes.c_void_p
+    sp = vp(torch.cuda.current_stream().cuda_stream)
+    for c in copies:
+        o = c["out"]
+        c["bi_args"] = (vp(c["indptr"].data_ptr()), vp(c["wi"].data_ptr()), vp(c["ranks"].data_ptr()), bs, L, T, 0,
+                        vp(c["mapping"].data_ptr()), vp(c["enabled"].data_ptr()), None, sp)
+        c["al_args"] = (vp(c["ids"].data_ptr()), vp(c["mapping"].data_ptr()), T, K, E, L, bsz, vp(o[0].data_ptr()),
+                        vp(o[1].data_ptr()), vp(o[2].data_ptr()), vp(o[3].data_ptr()), cap, vp(ws.data_ptr()),
+                        ws.numel(), None, sp)
+
     def batch_info(c):
-        mlr.moe_lora_batch_info(c["indptr"], c["wi"], c["ranks"], T, 0, adapter_enabled=c["enabled"],
-                                token_lora_mapping=c["mapping"], check=False)
+        if lib.moe_lora_batch_info(*c["bi_args"]) != 0:
+            raise RuntimeError("moe_lora_batch_info failed")
 
     def align(c):
-        mlr.moe_lora_align(c["ids"], c["mapping"], E, L, bsz, out=c["out"], workspace=ws, check=False)
+        if lib.moe_lora_align(*c["al_args"]) != 0:
+            raise RuntimeError("moe_lora_align failed")
 
     # checked calls first (status words), then warm-up
     for c in copies:
@@ -775,7 +803,9 @@ LINEAR_CONFIGS = {
     "mla_fused_proj": {"tokens": 8192, "in": 7168, "offsets": (0, 1536, 2112), "loras": 4, "max_rank": 64,
                        "ranks": (16, 32, 64, 64), "segments": 8},
 }
-WEIGHT_LABEL = {"bf16": "bf16", "fp8": "fp8 e4m3, fp32 scale per 128x128 block (bf16 LoRA)"}
+WEIGHT_LABEL = {"bf16": "bf16", "fp8": "fp8 e4m3, fp32 scale per 128x128 block (bf16 LoRA)",
+                "int8": "int8, fp32 scale per 128x128 block (bf16 LoRA)",
+                "w4a16": "uint4 two per byte, fp32 scale and uint8 zero point per row and 128 columns (bf16 LoRA)"}
 LINEAR_METRIC = "MLA fused-projection LoRA tokens/s and % of roofline (bf16, 1×GB300)"
 
 
@@ -1003,7 +1033,7 @@ def main(argv=None):
     ap.add_argument("--extras", default=DEFAULT_EXTRAS,
                     help="comma-separated workloads measured after the headline and reported under "
                          "'workloads' ('' for none)")
-    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+    ap.add_argument("--weights", choices=["bf16", "fp8", "int8", "w4a16"], default="bf16",
                     help="base expert weights of the MoE workloads: bf16, or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--combine", choices=["atomic", "deterministic"], default="deterministic",
                     help="top-k combine of the MoE forward (the other one is timed beside it)")

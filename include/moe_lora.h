@@ -230,6 +230,51 @@ int fused_moe_lora_forward_fp8(const mlr_bf16* x, const int32_t* topk_ids, const
                                int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
                                size_t ws_bytes, int32_t* d_status, void* stream);
 
+/*
+ * fused_moe_lora_forward_int8 -- the same layer with block-wise INT8 base
+ * experts (sglang PR #22323 page, 功能与动机 and 实现拆解 item 1: the INT8
+ * method, blockwise_int8, among those that hand their scales to the LoRA MoE
+ * layer).  w_gate_up_q [E, 2I, H] and w_down_q [E, H, I] hold two's-complement
+ * int8 codes; the scale arrays and their 128 x 128 blocks are laid out as for
+ * fused_moe_lora_forward_fp8; weight = code x scale.  Everything else, the
+ * workspace and the limits are those of fused_moe_lora_forward_fp8.
+ */
+int fused_moe_lora_forward_int8(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                                const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                                const float* scalings, const int8_t* w_gate_up_q,
+                                const float* w_gate_up_scale, const int8_t* w_down_q,
+                                const float* w_down_scale, const mlr_bf16* lora_a_gu,
+                                const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                                const mlr_bf16* lora_b_down, int32_t num_tokens, int32_t topk,
+                                int32_t num_experts, int32_t hidden, int32_t intermediate,
+                                int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
+                                size_t ws_bytes, int32_t* d_status, void* stream);
+
+/*
+ * fused_moe_lora_forward_w4a16 -- the same layer with 4-bit base experts and
+ * bf16 activations (the page's WNA16 method).  The pages name the method only;
+ * the format here: w_gate_up_q [E, 2I, H/2] and w_down_q [E, H, I/2] hold two
+ * UINT4 codes per byte along a row (the even column in the low nibble);
+ * w_gate_up_scale (float) and w_gate_up_zero (uint8, 0..15) are
+ * [E, 2I, ceil(H/128)], w_down_scale and w_down_zero [E, H, ceil(I/128)]: one
+ * scale and zero point per row and group of 128 input columns;
+ * weight = (code - zero) x scale.  Additional limits: hidden and intermediate
+ * multiples of 32 (else MLR_ERR_UNSUPPORTED); scale arrays 4-byte aligned and
+ * every quantisation array non-null (else MLR_ERR_INVALID).  Everything else
+ * as fused_moe_lora_forward_fp8.
+ */
+int fused_moe_lora_forward_w4a16(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                                 const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                                 const float* scalings, const uint8_t* w_gate_up_q,
+                                 const float* w_gate_up_scale, const uint8_t* w_gate_up_zero,
+                                 const uint8_t* w_down_q, const float* w_down_scale,
+                                 const uint8_t* w_down_zero, const mlr_bf16* lora_a_gu,
+                                 const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                                 const mlr_bf16* lora_b_down, int32_t num_tokens, int32_t topk,
+                                 int32_t num_experts, int32_t hidden, int32_t intermediate,
+                                 int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
+                                 size_t ws_bytes, int32_t* d_status, void* stream);
+
 /* Scratch bytes lora_linear_forward needs for these sizes (0 on bad sizes). */
 size_t lora_linear_workspace_bytes(int32_t num_tokens, int32_t in_features, int32_t out_features,
                                    int32_t num_loras, int32_t max_rank, int32_t num_slices);

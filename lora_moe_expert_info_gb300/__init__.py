@@ -28,6 +28,7 @@ from . import _build
 
 __all__ = ["moe_lora_batch_info", "moe_lora_align", "moe_lora_align_capacity",
            "moe_lora_align_workspace_bytes", "fused_moe_lora_forward", "fused_moe_lora_forward_fp8",
+           "fused_moe_lora_forward_int8", "fused_moe_lora_forward_w4a16",
            "fused_moe_lora_workspace_bytes", "lora_linear_forward", "lora_tp_qkv_b_rows", "tp_take_rows",
            "set_wait_limit_ns", "wait_limit_ns", "set_deterministic", "deterministic", "library", "library_path", "MoeLoraError", "STATUS_BITS"]
 
@@ -107,6 +108,10 @@ def library() -> ctypes.CDLL:
                 lib.fused_moe_lora_forward.argtypes = [vp] * 12 + [i32] * 7 + [vp, vp, sz, vp, vp]
                 lib.fused_moe_lora_forward_fp8.restype = ctypes.c_int
                 lib.fused_moe_lora_forward_fp8.argtypes = [vp] * 14 + [i32] * 7 + [vp, vp, sz, vp, vp]
+                lib.fused_moe_lora_forward_int8.restype = ctypes.c_int
+                lib.fused_moe_lora_forward_int8.argtypes = [vp] * 14 + [i32] * 7 + [vp, vp, sz, vp, vp]
+                lib.fused_moe_lora_forward_w4a16.restype = ctypes.c_int
+                lib.fused_moe_lora_forward_w4a16.argtypes = [vp] * 16 + [i32] * 7 + [vp, vp, sz, vp, vp]
             if hasattr(lib, "lora_linear_forward"):
                 lib.lora_linear_workspace_bytes.restype = sz
                 lib.lora_linear_workspace_bytes.argtypes = [i32] * 6
@@ -430,6 +435,105 @@ def fused_moe_lora_forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lo
     if check:
         _check_device(status, "fused_moe_lora_forward_fp8")
     return y
+
+
+def _quant_forward(fn_name, x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, quant,
+                   lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, y, workspace, stream, check, status,
+                   I_of, code_shapes, side_shapes):
+    """Shared marshalling of the quantised-expert forwards: `quant` is the list of
+    (tensor, name, dtype) of the code / scale / zero arrays in C argument order;
+    code_shapes(E, I, H) and side_shapes(E, I, H) give their expected shapes."""
+    lib = library()
+    if not hasattr(lib, fn_name):
+        raise RuntimeError(f"library built without {fn_name}")
+    dev = x.device
+    bf = torch.bfloat16
+    _req(x, "x", bf, dev)
+    _req(topk_ids, "topk_ids", torch.int32, dev)
+    _req(topk_weights, "topk_weights", torch.float32, dev)
+    _req(token_lora_mapping, "token_lora_mapping", torch.int32, dev)
+    _req(lora_ranks, "lora_ranks", torch.int32, dev)
+    _req(scalings, "scalings", torch.float32, dev)
+    for t, n, dt in quant:
+        _req(t, n, dt, dev)
+    for t, n in ((lora_a_gu, "lora_a_gu"), (lora_b_gu, "lora_b_gu"), (lora_a_down, "lora_a_down"),
+                 (lora_b_down, "lora_b_down")):
+        _req(t, n, bf, dev)
+    T, H = x.shape
+    K = topk_ids.shape[1]
+    E = quant[0][0].shape[0]
+    I = I_of(quant[0][0])
+    L, _, _, R, _ = lora_a_gu.shape
+    expect = list(code_shapes(E, I, H)) + list(side_shapes(E, I, H))
+    if (any(tuple(t.shape) != shp for (t, _, _), shp in zip(quant, expect))
+            or tuple(lora_a_gu.shape) != (L, E, 2, R, H)
+            or tuple(lora_b_gu.shape) != (L, E, 2, I, R) or tuple(lora_a_down.shape) != (L, E, R, I)
+            or tuple(lora_b_down.shape) != (L, E, H, R) or tuple(topk_ids.shape) != (T, K)
+            or tuple(topk_weights.shape) != (T, K) or token_lora_mapping.numel() < T
+            or lora_ranks.numel() != L or scalings.numel() != L):
+        raise ValueError(f"{fn_name}: inconsistent shapes")
+    if y is None:
+        y = torch.empty(T, H, dtype=bf, device=dev)
+    _req(y, "y", bf, dev)
+    wsb = int(lib.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R))
+    if wsb == 0 and T > 0:
+        raise ValueError(f"{fn_name}: unsupported sizes")
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    if check and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = getattr(lib, fn_name)(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(token_lora_mapping), _ptr(lora_ranks),
+        _ptr(scalings), *[_ptr(t) for t, _, _ in quant], _ptr(lora_a_gu), _ptr(lora_b_gu), _ptr(lora_a_down),
+        _ptr(lora_b_down), T, K, E, H, I, L, R, _ptr(y), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream))
+    _check_host(code, fn_name)
+    if check:
+        _check_device(status, fn_name)
+    return y
+
+
+@_on_stream
+def fused_moe_lora_forward_int8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                                w_gate_up_q, w_gate_up_scale, w_down_q, w_down_scale,
+                                lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
+                                y: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None,
+                                check: bool = True, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The layer with block-wise INT8 base experts: w_gate_up_q [E,2I,H] and
+    w_down_q [E,H,I] int8 codes, scales laid out as for the FP8 layer
+    (float32 per 128 x 128 block); weight = code x scale."""
+    cb = lambda n: (n + 127) // 128  # noqa: E731
+    quant = [(w_gate_up_q, "w_gate_up_q", torch.int8), (w_gate_up_scale, "w_gate_up_scale", torch.float32),
+             (w_down_q, "w_down_q", torch.int8), (w_down_scale, "w_down_scale", torch.float32)]
+    return _quant_forward("fused_moe_lora_forward_int8", x, topk_ids, topk_weights, token_lora_mapping,
+                          lora_ranks, scalings, quant, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, y,
+                          workspace, stream, check, status, lambda w: w.shape[1] // 2,
+                          lambda E, I, H: [(E, 2 * I, H), (E, cb(2 * I), cb(H)), (E, H, I), (E, cb(H), cb(I))],
+                          lambda E, I, H: [])
+
+
+@_on_stream
+def fused_moe_lora_forward_w4a16(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                                 w_gate_up_q, w_gate_up_scale, w_gate_up_zero, w_down_q, w_down_scale,
+                                 w_down_zero, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
+                                 y: Optional[torch.Tensor] = None,
+                                 workspace: Optional[torch.Tensor] = None, stream=None,
+                                 check: bool = True, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The layer with 4-bit base experts: w_gate_up_q [E,2I,H/2] and w_down_q
+    [E,H,I/2] uint8 bytes of two uint4 codes (even column in the low nibble);
+    scales (float32) and zero points (uint8) [E, rows, ceil(cols/128)], one per
+    row and 128-column group; weight = (code - zero) x scale."""
+    cb = lambda n: (n + 127) // 128  # noqa: E731
+    quant = [(w_gate_up_q, "w_gate_up_q", torch.uint8), (w_gate_up_scale, "w_gate_up_scale", torch.float32),
+             (w_gate_up_zero, "w_gate_up_zero", torch.uint8), (w_down_q, "w_down_q", torch.uint8),
+             (w_down_scale, "w_down_scale", torch.float32), (w_down_zero, "w_down_zero", torch.uint8)]
+    return _quant_forward("fused_moe_lora_forward_w4a16", x, topk_ids, topk_weights, token_lora_mapping,
+                          lora_ranks, scalings, quant, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, y,
+                          workspace, stream, check, status, lambda w: w.shape[1] // 2,
+                          lambda E, I, H: [(E, 2 * I, H // 2), (E, 2 * I, cb(H)), (E, 2 * I, cb(H)),
+                                           (E, H, I // 2), (E, H, cb(I)), (E, H, cb(I))],
+                          lambda E, I, H: [])
 
 
 @_on_stream

@@ -15,6 +15,9 @@
 //                 memory -> bucket starts and num_tokens_post_pad
 //   4. scatter  : per chunk, stable local ranks and the final placement
 //                 (plus the pad sentinels and the per-block expert/adapter ids)
+// When two bucket arrays and a chunk fit in shared memory (NB up to about
+// 20000), the scatter scans the padded totals itself (launch 3 is skipped)
+// and keeps every bucket's global base in shared memory.
 // Stability inside a chunk: pairs are visited in rounds of 1024 consecutive
 // indices separated by barriers, so a bucket's slots follow round order; the
 // few same-round neighbours of a pair are re-ranked by index when it is placed.
@@ -27,10 +30,44 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kMaxItems = 32;                         // pairs per thread per chunk
 constexpr int kMaxChunk = kThreads * kMaxItems;       // 32768 (fits uint16 indices)
+constexpr int kLoadBatch = 8;                         // pairs whose loads a thread issues together
+constexpr size_t kSmemLimit = 227 * 1024;             // dynamic shared memory per block
+
+// The current device, or -1 (per-device caches of the launch set-up).
+int current_device_id() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  return dev;
+}
+
+// Keys of this thread's pairs j = (bt + i) * kThreads + tid, i < kLoadBatch, of
+// the chunk starting at pair p0 with n pairs (-1 past the end or for an id out
+// of range, which also flags `bad`).  All loads are issued before any is used.
+__device__ __forceinline__ void align_load_keys(const int32_t* __restrict__ topk_ids,
+                                                const int32_t* __restrict__ mapping, int64_t p0, int n, int bt,
+                                                int topk, int E, int C, int L, int (&key)[kLoadBatch], int& bad) {
+  int ev[kLoadBatch], lv[kLoadBatch];
+#pragma unroll
+  for (int i = 0; i < kLoadBatch; ++i) {
+    const int j = (bt + i) * kThreads + (int)threadIdx.x;
+    const int64_t p = p0 + (j < n ? j : 0);
+    ev[i] = __ldg(topk_ids + p);
+    lv[i] = __ldg(mapping + p / topk);
+  }
+#pragma unroll
+  for (int i = 0; i < kLoadBatch; ++i) {
+    const int j = (bt + i) * kThreads + (int)threadIdx.x;
+    key[i] = -1;
+    if (j < n) {
+      if (ev[i] < 0 || ev[i] >= E || lv[i] < -1 || lv[i] >= L) bad |= MLR_STATUS_INDEX;
+      else key[i] = ev[i] * C + lv[i] + 1;
+    }
+  }
+}
 constexpr int kColWarps = 32;  // chunk segments per bucket in the column scan
 constexpr int kColThreads = 32 * kColWarps;
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)  // two blocks per SM: 32 registers
 align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
                    int64_t P, int topk, int E, int L, int chunk, uint32_t* __restrict__ cnt,
                    int32_t* d_status) {
@@ -41,16 +78,16 @@ align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
   const int64_t p0 = (int64_t)blockIdx.x * chunk;
   const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
   int bad = 0;
-  // every key of this thread first (all loads in flight), then the counts
-  int key[kMaxItems];
+  // keys in batches of kLoadBatch pairs: the batch's loads are issued together
+  // (unconditionally, past-the-end lanes reading pair p0), then counted
 #pragma unroll
-  for (int it = 0; it < kMaxItems; ++it) {
-    const int j = it * kThreads + threadIdx.x;
-    key[it] = j < n ? align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad) : -1;
+  for (int bt = 0; bt < kMaxItems; bt += kLoadBatch) {
+    int key[kLoadBatch];
+    align_load_keys(topk_ids, mapping, p0, n, bt, topk, E, C, L, key, bad);
+#pragma unroll
+    for (int i = 0; i < kLoadBatch; ++i)
+      if (key[i] >= 0) atomicAdd(&hist[key[i]], 1u);
   }
-#pragma unroll
-  for (int it = 0; it < kMaxItems; ++it)
-    if (key[it] >= 0) atomicAdd(&hist[key[it]], 1u);
   if (bad) set_status(d_status, bad);
   __syncthreads();
   uint32_t* row = cnt + (int64_t)blockIdx.x * NB;
@@ -116,36 +153,54 @@ align_bucketscan_kernel(const uint32_t* __restrict__ btotal, int NB, int block_s
   }
 }
 
+// Per chunk: the stable placement of its pairs.  kBases: the global start of
+// every bucket (plus this chunk's earlier-chunk count) is built once in shared
+// memory -- for the padded align by scanning the padded bucket totals here
+// (which also writes num_tokens_post_pad, the pad sentinels and the block
+// labels of this block's share of the buckets: no separate bucket-scan
+// launch), for the dense order from dense_start -- so that placing a pair
+// reads no global memory.  Without kBases (bucket counts too large for two
+// bucket arrays in shared memory) the bases are read per pair from bstart and
+// the count matrix, and the pads and labels are written grid-wide.
+template <bool kBases>
 __global__ void __launch_bounds__(kThreads)
 align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
                      int64_t P, int topk, int E, int L, int chunk, int block_size,
                      const uint32_t* __restrict__ cnt, const uint32_t* __restrict__ btotal,
                      const uint32_t* __restrict__ bstart, int32_t* __restrict__ sorted_ids,
                      int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
-                     int64_t capacity, const uint32_t* __restrict__ dense_start) {
+                     int32_t* __restrict__ num_post_pad, int64_t capacity, int32_t* d_status,
+                     const uint32_t* __restrict__ dense_start) {
   // dense_start != nullptr: the dense order (no padding, no labels) for the
   // forward; sorted_ids then receives pair ids at dense_start[b] + rank.
   extern __shared__ uint32_t smem[];
   const int C = L + 1, NB = E * C;
+  const int nb4 = (int)round_up(NB + 1, 4);
   uint32_t* off = smem;                                             // [NB + 1]
-  uint16_t* stage = reinterpret_cast<uint16_t*>(smem + NB + 1);     // [chunk]
-  for (int b = threadIdx.x; b < NB; b += blockDim.x) off[b] = 0u;
+  uint32_t* gb = smem + nb4;                                        // [NB + 1] (kBases)
+  uint16_t* stage = reinterpret_cast<uint16_t*>(smem + (kBases ? 2 : 1) * nb4);  // [chunk]
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) {
+    off[b] = 0u;
+    if (kBases) gb[b] = dense_start ? dense_start[b] : (btotal[b] + block_size - 1) / block_size * block_size;
+  }
   __syncthreads();
 
   const int64_t p0 = (int64_t)blockIdx.x * chunk;
   const int n = (int)(P - p0 < chunk ? P - p0 : chunk);
   const int rounds = (n + kThreads - 1) / kThreads;
   // (key << 16) | slot per pair; key < 40960 and slot < 32768 both fit 16 bits.
-  // Every key of this thread is loaded first (all loads in flight), then the
-  // counting rounds run on shared memory only.
+  // The keys are loaded first (batches of loads in flight), then the counting
+  // rounds run on shared memory only.
   uint32_t ks[kMaxItems];
   int bad = 0;
 #pragma unroll
-  for (int it = 0; it < kMaxItems; ++it) {
-    const int j = it * kThreads + threadIdx.x;
-    const int key = j < n ? align_pair_key(topk_ids, mapping, p0 + j, topk, E, C, L, bad) : -1;
-    ks[it] = key >= 0 ? (uint32_t)key : 0xFFFFFFFFu;
+  for (int bt = 0; bt < kMaxItems; bt += kLoadBatch) {
+    int key[kLoadBatch];
+    align_load_keys(topk_ids, mapping, p0, n, bt, topk, E, C, L, key, bad);
+#pragma unroll
+    for (int i = 0; i < kLoadBatch; ++i) ks[bt + i] = key[i] >= 0 ? (uint32_t)key[i] : 0xFFFFFFFFu;
   }
+  (void)bad;  // the count kernel reports ids out of range
 #pragma unroll
   for (int it = 0; it < kMaxItems; ++it) {
     if (it < rounds) {
@@ -154,6 +209,36 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
     }
   }
   align_block_scan(off, NB);
+  const int lane = threadIdx.x & 31;
+  const int64_t cap64 = capacity < INT32_MAX ? capacity : INT32_MAX;
+  const int cap = (int)cap64, cap_blocks = (int)(cap64 / block_size);
+  if (kBases) {
+    if (!dense_start) {
+      align_block_scan(gb, NB);  // gb[b]: padded start of bucket b; gb[NB]: total
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *num_post_pad = (int32_t)gb[NB];
+        if ((int64_t)gb[NB] > capacity) set_status(d_status, MLR_STATUS_CAPACITY);
+      }
+      // pad sentinels and block labels of this block's share of the buckets:
+      // one warp per bucket, lanes writing consecutive entries
+      const int per = (NB + (int)gridDim.x - 1) / (int)gridDim.x;
+      const int b0 = min(NB, (int)blockIdx.x * per), b1 = min(NB, b0 + per);
+      for (int b = b0 + (threadIdx.x >> 5); b < b1; b += kThreads / 32) {
+        const int st = (int)gb[b], en = (int)gb[b + 1];
+        if (st == en) continue;
+        for (int q = st + (int)btotal[b] + lane; q < en && q < cap; q += 32) sorted_ids[q] = (int32_t)P;
+        const int expert = b / C, lora = b - expert * C - 1;
+        for (int blk = st / block_size + lane; blk < en / block_size && blk < cap_blocks; blk += 32) {
+          block_expert[blk] = expert;
+          block_lora[blk] = lora;
+        }
+      }
+      __syncthreads();
+    }
+    // plus the pairs of each bucket in earlier chunks (coalesced)
+    const uint32_t* crow = cnt + (int64_t)blockIdx.x * NB;
+    for (int b = threadIdx.x; b < NB; b += blockDim.x) gb[b] += crow[b];
+  }
 #pragma unroll
   for (int it = 0; it < kMaxItems; ++it)
     if (it < rounds && ks[it] != 0xFFFFFFFFu)
@@ -176,25 +261,23 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
       }
       const int round_start = m + 1;
       for (m = pos + 1; m < hi && (stage[m] >> 10) == (uint32_t)it; ++m) less += stage[m] < j;
-      const int64_t dst = (int64_t)(dense_start ? dense_start[k] : bstart[k]) + crow[k] + (round_start - lo) + less;
+      const int64_t base = kBases ? (int64_t)gb[k] : (int64_t)(dense_start ? dense_start[k] : bstart[k]) + crow[k];
+      const int64_t dst = base + (round_start - lo) + less;
       if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + j);
     }
   }
-  if (dense_start) return;
+  if (kBases || dense_start) return;
 
   // Pad sentinels and per-block labels: one warp per bucket over the whole
   // grid, lanes writing consecutive entries.  Padded positions are below
   // P + NB * block_size < 2^31 (align_plan checks the bound).
-  const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  const int64_t cap64 = capacity < INT32_MAX ? capacity : INT32_MAX;
-  const int cap = (int)cap64, cap_blocks = (int)(cap64 / block_size);
   for (int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < NB; b += nwarps) {
-    const int s = (int)bstart[b], e = (int)bstart[b + 1];
-    if (s == e) continue;
-    for (int q = s + (int)btotal[b] + lane; q < e && q < cap; q += 32) sorted_ids[q] = (int32_t)P;
+    const int st = (int)bstart[b], en = (int)bstart[b + 1];
+    if (st == en) continue;
+    for (int q = st + (int)btotal[b] + lane; q < en && q < cap; q += 32) sorted_ids[q] = (int32_t)P;
     const int expert = b / C, lora = b - expert * C - 1;
-    for (int blk = s / block_size + lane; blk < e / block_size && blk < cap_blocks; blk += 32) {
+    for (int blk = st / block_size + lane; blk < en / block_size && blk < cap_blocks; blk += 32) {
       block_expert[blk] = expert;
       block_lora[blk] = lora;
     }
@@ -243,8 +326,34 @@ AlignPlan align_plan(int32_t num_tokens, int32_t topk, int32_t num_experts, int3
 }
 
 size_t align_smem_count(const AlignPlan& pl) { return (size_t)pl.NB * 4; }
-size_t align_smem_scatter(const AlignPlan& pl) {
-  return (size_t)(pl.NB + 1) * 4 + round_up((int64_t)pl.chunk * 2, 16);
+// Dynamic shared memory of the scatter: one (or, with the bucket bases, two)
+// bucket arrays of round_up(NB + 1, 4) words and the chunk's uint16 stage.
+size_t align_smem_scatter(const AlignPlan& pl, bool bases) {
+  return (size_t)((bases ? 2 : 1) * round_up(pl.NB + 1, 4) * 4 + round_up((int64_t)pl.chunk * 2, 16));
+}
+bool align_bases_fit(const AlignPlan& pl) { return align_smem_scatter(pl, true) <= kSmemLimit; }
+
+template <bool kBases>
+int launch_scatter(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk, int E, int L,
+                   int block_size, const uint32_t* cnt, const uint32_t* btotal, const uint32_t* bstart,
+                   int32_t* sorted_ids, int32_t* block_expert, int32_t* block_lora, int32_t* num_post_pad,
+                   int64_t capacity, int32_t* d_status, const uint32_t* dense_start, cudaStream_t stream) {
+  const size_t sm = align_smem_scatter(pl, kBases);
+  const int dev = current_device_id();
+  static size_t configured[64] = {};  // largest opt-in so far, per device
+  if (sm > 48 * 1024 && (dev < 0 || sm > configured[dev])) {
+    if (cudaFuncSetAttribute(align_scatter_kernel<kBases>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+        cudaSuccess)
+      return MLR_ERR_CUDA;
+    if (dev >= 0) configured[dev] = sm;
+  }
+  align_scatter_kernel<kBases><<<pl.G, kThreads, sm, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk,
+                                                               block_size, cnt, btotal, bstart, sorted_ids,
+                                                               block_expert, block_lora, num_post_pad, capacity,
+                                                               d_status, dense_start);
+  MLR_CHECK_LAUNCH();
+  note_launch();
+  return MLR_OK;
 }
 
 int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* mapping, int topk,
@@ -268,12 +377,7 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
     note_launch();
     return MLR_OK;
   }
-  const size_t sm_count = align_smem_count(pl), sm_scatter = align_smem_scatter(pl);
-  if (sm_scatter > 48 * 1024) {
-    if (cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sm_scatter) != cudaSuccess)
-      return MLR_ERR_CUDA;
-  }
+  const size_t sm_count = align_smem_count(pl);
   if (sm_count > 48 * 1024) {
     if (cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm_count) != cudaSuccess)
@@ -288,6 +392,9 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
   align_colscan_kernel<<<(int)ceil_div(pl.NB, 32), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
   MLR_CHECK_LAUNCH();
   note_launch();
+  if (pl.G > 0 && align_bases_fit(pl))  // the scatter scans the bucket totals itself
+    return launch_scatter<true>(pl, topk_ids, mapping, topk, E, L, block_size, cnt, btotal, nullptr, sorted_ids,
+                                block_expert, block_lora, num_post_pad, capacity, d_status, nullptr, stream);
   const size_t sm_scan = (size_t)(pl.NB + 1) * 4;
   if (sm_scan > 48 * 1024 &&
       cudaFuncSetAttribute(align_bucketscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan) !=
@@ -297,13 +404,9 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
                                                             capacity, d_status);
   MLR_CHECK_LAUNCH();
   note_launch();
-  if (pl.G > 0) {
-    align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(
-        topk_ids, mapping, pl.P, topk, E, L, pl.chunk, block_size, cnt, btotal, bstart, sorted_ids,
-        block_expert, block_lora, capacity, nullptr);
-    MLR_CHECK_LAUNCH();
-    note_launch();
-  }
+  if (pl.G > 0)
+    return launch_scatter<false>(pl, topk_ids, mapping, topk, E, L, block_size, cnt, btotal, bstart, sorted_ids,
+                                 block_expert, block_lora, num_post_pad, capacity, d_status, nullptr, stream);
   return MLR_OK;
 }
 
@@ -335,17 +438,11 @@ int align_dense_scatter(const AlignPlan& pl, const int32_t* topk_ids, const int3
   if (pl.G == 0) return MLR_OK;
   const char* ws = static_cast<const char*>(workspace);
   const uint32_t* cnt = reinterpret_cast<const uint32_t*>(ws + pl.cnt_off);
-  const size_t sm_scatter = align_smem_scatter(pl);
-  if (sm_scatter > 48 * 1024 &&
-      cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scatter) !=
-          cudaSuccess)
-    return MLR_ERR_CUDA;
-  align_scatter_kernel<<<pl.G, kThreads, sm_scatter, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk, 1,
-                                                               cnt, nullptr, nullptr, dense_sorted, nullptr, nullptr,
-                                                               pl.P, dense_start);
-  MLR_CHECK_LAUNCH();
-  note_launch();
-  return MLR_OK;
+  if (align_bases_fit(pl))
+    return launch_scatter<true>(pl, topk_ids, mapping, topk, E, L, 1, cnt, nullptr, nullptr, dense_sorted, nullptr,
+                                nullptr, nullptr, pl.P, nullptr, dense_start, stream);
+  return launch_scatter<false>(pl, topk_ids, mapping, topk, E, L, 1, cnt, nullptr, nullptr, dense_sorted, nullptr,
+                               nullptr, nullptr, pl.P, nullptr, dense_start, stream);
 }
 
 }  // namespace mlr

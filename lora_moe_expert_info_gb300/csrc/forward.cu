@@ -62,6 +62,12 @@ constexpr int kEpiBytes = 32 * (128 + 8) * 2;
 constexpr uint64_t kCopyGraceNs = 1000000;  // after an abort: time for issued TMA copies to land  // staging per epilogue half: 32 rows of bf16 h, or 16 rows of fp32
 
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
+// Base expert weight formats: bf16, or codes that converter warps dequantise
+// on chip -- FP8 E4M3 and INT8 with 128 x 128 block scales, UINT4 (two per
+// byte) with a scale and zero point per row and 128-column group.
+enum QFmt : int { kQNone = 0, kQFp8 = 1, kQInt8 = 2, kQU4 = 3 };
+// Raw code bytes of one weight row per 64-wide K step.
+template <int QF> constexpr int kRawRowBytes = QF == kQU4 ? 32 : 64;
 
 // Epilogue warps: the base GEMMs drain their accumulators with two warps per
 // TMEM lane quarter, each taking alternate 32-column chunks; the shrinks use
@@ -171,7 +177,9 @@ struct Params {
   int zslice_blk; // down: 256-row blocks from this index on read the second rank slice of z (split B)
   int w3;         // gate_up: 1 if the gate+up weight map exists
   int wsr, wsc;   // FP8 weights: 128-row and 128-column scale blocks per expert matrix
-  const float* wscale;  // FP8 weights: [E][wsr][wsc] block scales (weight = code x scale)
+  const float* wscale;  // FP8 / INT8: [E][wsr][wsc] block scales (weight = code x scale);
+                        // UINT4: [E][rows][wsc] group scales
+  const uint8_t* wzero;   // UINT4: [E][rows][wsc] group zero points
   int64_t P;
   uint64_t wait_ns;  // give-up limit of the pipeline waits
   const float* topk_weights;
@@ -351,10 +359,11 @@ struct ExpandCursor {
 // half of the stage's weight area; warps 1-3 convert them in place into the
 // bf16 tile the MMAs read (code x scale, 128-byte swizzle), so the MMAs, the
 // LoRA expand and the epilogue are those of the bf16 kernel.
-template <int KIND, bool Q = false>
-__global__ void __launch_bounds__(Q ? 512 : kMaxThreads, 1)
+template <int KIND, int QF = kQNone>
+__global__ void __launch_bounds__(QF != kQNone ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
-  static_assert(!Q || KIND == kGateUp || KIND == kDown, "FP8 weights: the base GEMMs only");
+  constexpr bool Q = QF != kQNone;
+  static_assert(!Q || KIND == kGateUp || KIND == kDown, "quantised weights: the base GEMMs only");
   using CF = CfgOf<KIND, Q>;
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
@@ -504,9 +513,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             } else if (KIND == kGateUp) {
               const int i0 = it.mb * 128;
               if (Q) {
-                // raw codes of the gate and up blocks: [gate|up][128 rows][64 bytes]
-                mbar_arrive_expect_tx(&c.raw_full[st], 16384);
-                tma_load_3d(sbuf + 16384, &maps.m[kW], &c.raw_full[st], kb * 64, i0, it.e * 2);
+                // raw codes of the gate and up blocks: [gate|up][128 rows][row bytes]
+                mbar_arrive_expect_tx(&c.raw_full[st], 256 * kRawRowBytes<QF>);
+                tma_load_3d(sbuf + 16384, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, i0, it.e * 2);
                 mbar_arrive_expect_tx(&c.full[st], rbytes);
               } else {
                 mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
@@ -523,8 +532,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               // kDown with FP8 weights, on a single CTA: raw codes of 128 weight rows
               // on their own barrier, then all of the tile's rows
               static_assert(KIND != kDown || kPair || Q, "bf16 down runs on CTA pairs");
-              mbar_arrive_expect_tx(&c.raw_full[st], 8192);
-              tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * 64, it.mb * 128, it.e);
+              mbar_arrive_expect_tx(&c.raw_full[st], 128 * kRawRowBytes<QF>);
+              tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, it.mb * 128, it.e);
               mbar_arrive_expect_tx(&c.full[st], rbytes);
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
@@ -575,16 +584,17 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       }
     }
   } else if (Q && (warp < 4 || warp >= kThreadsOf<KIND> / 32)) {
-    // ================ converters (FP8 weights): raw codes -> bf16 tile ================
+    // ============ converters (quantised weights): raw codes -> bf16 tile ============
     // Warps 1-3 and the three warps after the epilogue.  The raw codes sit in
     // the upper half of the stage's weight area, which the bf16 tile also
     // covers, so every thread first holds its raw chunks in registers and the
     // group meets once (a barrier that also votes on giving up) before anyone
     // writes; then each warp converts its chunks and arrives on its own.  A
-    // chunk's block scale is fetched before its raw tile is waited for.
+    // chunk's scale (and zero point) is fetched before its raw tile is waited for.
     constexpr int kCv = kCvWarps * 32;
-    constexpr int kRawOff = KIND == kGateUp ? 16384 : 8192;  // raw codes within the stage
-    constexpr int kChunks = KIND == kGateUp ? 1024 : 512;     // 16-byte raw chunks per K step
+    constexpr int kRawOff = KIND == kGateUp ? 16384 : 8192;   // raw codes within the stage
+    constexpr int kCpr = kRawRowBytes<QF> / 16;                // 16-byte raw chunks per row
+    constexpr int kChunks = (KIND == kGateUp ? 256 : 128) * kCpr;  // raw chunks per K step
     constexpr int kPer = (kChunks + kCv - 1) / kCv;
     const int ct = warp < 4 ? tid - 32 : 96 + tid - kThreadsOf<KIND>;
     int gs = 0;
@@ -595,23 +605,27 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       for (int s = 0; s < nsteps; ++s, ++gs) {
         const int st = gs % S, round = gs / S;
         const uint32_t sb = smem_u32(smem + st * SB);
-        float scv[kPer];
+        float scv[kPer], zv[kPer];
         if (s < nks) {
 #pragma unroll
           for (int j = 0; j < kPer; ++j) {
-            const int q = ct + kCv * j;
-            // gate_up: q = (g, r, c4) of [gate|up][128 rows][4 chunks]; down: (r, c4)
-            const int g = KIND == kGateUp ? (q >> 9) & 1 : 0;
-            const int r = (q >> 2) & 127;
+            // chunk q = (row ri, chunk of the row); gate_up rows ri = (gate|up, r)
+            const int q = ct + kCv * j, ri = q / kCpr;
+            const int g = KIND == kGateUp ? (ri >> 7) & 1 : 0;
+            const int r = ri & 127;
+            const int row = it.mb * 128 + r;  // row of the gate or up matrix, or of W_down
             scv[j] = 0.f;
-            if (q < kChunks) {
-              if (KIND == kGateUp) {
-                const int row = it.mb * 128 + r;  // row of the gate or up matrix
-                if (row < p.I)
-                  scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + (g * p.I + row) / 128) * p.wsc + (s >> 1));
+            zv[j] = 0.f;
+            if (q < kChunks && row < (KIND == kGateUp ? p.I : p.H)) {
+              const int64_t wrow = KIND == kGateUp ? (int64_t)it.e * 2 * p.I + g * p.I + row
+                                                   : (int64_t)it.e * p.H + row;  // row of the stacked matrix
+              if (QF == kQU4) {
+                const int64_t gi = wrow * p.wsc + (s >> 1);  // this row's 128-column group
+                scv[j] = __ldg(p.wscale + gi);
+                zv[j] = (float)__ldg(p.wzero + gi);
               } else {
-                const int row = it.mb * 128 + r;  // row of W_down (an H index; single-CTA 128-row blocks)
-                if (row < p.H) scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + row / 128) * p.wsc + (s >> 1));
+                const int64_t rb = KIND == kGateUp ? (g * p.I + row) / 128 : row / 128;
+                scv[j] = __ldg(p.wscale + ((int64_t)it.e * p.wsr + rb) * p.wsc + (s >> 1));
               }
             }
           }
@@ -635,14 +649,34 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           for (int j = 0; j < kPer; ++j) {
             const int q = ct + kCv * j;
             if (q >= kChunks) continue;
-            const int g = KIND == kGateUp ? q >> 9 : 0;
-            const int r = (q >> 2) & 127, c4 = q & 3;
+            const int ri = q / kCpr, c = q % kCpr;
+            const int g = KIND == kGateUp ? ri >> 7 : 0;
+            const int r = ri & 127;
             const float sc = scv[j];
-            const uint2 a = e4m3x4_scaled_bf16(raw[j].x, sc), b = e4m3x4_scaled_bf16(raw[j].y, sc);
-            const uint2 d = e4m3x4_scaled_bf16(raw[j].z, sc), e = e4m3x4_scaled_bf16(raw[j].w, sc);
             const uint32_t rowa = sb + g * 16384 + r * 128;
-            sts128(rowa + (((2 * c4) ^ (r & 7)) * 16), make_uint4(a.x, a.y, b.x, b.y));
-            sts128(rowa + (((2 * c4 + 1) ^ (r & 7)) * 16), make_uint4(d.x, d.y, e.x, e.y));
+            if (QF == kQU4) {
+              // 32 codes: four words of eight, bf16 units 4c .. 4c + 3 of the row
+              const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                sts128(rowa + (((4 * c + v) ^ (r & 7)) * 16), u4x8_scaled_bf16(wv[v], zv[j], sc));
+            } else {
+              // 16 codes: bf16 units 2c, 2c + 1 of the row
+              uint2 a, b, d, e;
+              if (QF == kQFp8) {
+                a = e4m3x4_scaled_bf16(raw[j].x, sc);
+                b = e4m3x4_scaled_bf16(raw[j].y, sc);
+                d = e4m3x4_scaled_bf16(raw[j].z, sc);
+                e = e4m3x4_scaled_bf16(raw[j].w, sc);
+              } else {
+                a = s8x4_scaled_bf16(raw[j].x, sc);
+                b = s8x4_scaled_bf16(raw[j].y, sc);
+                d = s8x4_scaled_bf16(raw[j].z, sc);
+                e = s8x4_scaled_bf16(raw[j].w, sc);
+              }
+              sts128(rowa + (((2 * c) ^ (r & 7)) * 16), make_uint4(a.x, a.y, b.x, b.y));
+              sts128(rowa + (((2 * c + 1) ^ (r & 7)) * 16), make_uint4(d.x, d.y, e.x, e.y));
+            }
           }
           fence_proxy_async_smem();  // the tile is read next by the tensor cores
         }
@@ -1632,14 +1666,15 @@ int sm_count() {
 }
 
 // Persistent launch: one CTA per SM (or fewer when there are fewer items).
-template <int KIND, bool Q = false>
+template <int KIND, int QF = kQNone>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
+  constexpr bool Q = QF != kQNone;
   const int smem = smem_bytes<KIND, Q>();
   // the shared-memory opt-in and the resident-cluster count are per device
   const int dev = current_device();
   static bool configured[64] = {};
   if (dev < 0 || !configured[dev]) {
-    if (cudaFuncSetAttribute(moe_gemm_kernel<KIND, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(moe_gemm_kernel<KIND, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MLR_ERR_CUDA;
     if (dev >= 0) configured[dev] = true;
@@ -1666,17 +1701,17 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     if (resident == 0) {
       cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND, Q>, &cfg) != cudaSuccess || n <= 0)
+      if (cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<KIND, QF>, &cfg) != cudaSuccess || n <= 0)
         return MLR_ERR_CUDA;
       resident = n;
       if (dev >= 0) resident_of[dev] = n;
     }
     const int64_t pairs = max_items < resident ? max_items : resident;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
-    if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND, Q>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND, QF>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
   } else {
     const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-    moe_gemm_kernel<KIND, Q><<<grid, kLaunchThreads<KIND, Q>, smem, stream>>>(maps, p);
+    moe_gemm_kernel<KIND, QF><<<grid, kLaunchThreads<KIND, Q>, smem, stream>>>(maps, p);
     MLR_CHECK_LAUNCH();
   }
   note_launch();
@@ -1738,12 +1773,16 @@ bool make_map3_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The layer.  fp8: w_gate_up / w_down hold E4M3 codes with block scales
-// s_gu [E][ceil(2I/128)][ceil(H/128)] and s_d [E][ceil(H/128)][ceil(I/128)];
-// otherwise they are bf16 and the scales are unused.
+// The layer.  qf = kQFp8 / kQInt8: w_gate_up / w_down hold E4M3 / INT8 codes
+// with block scales s_gu [E][ceil(2I/128)][ceil(H/128)] and s_d
+// [E][ceil(H/128)][ceil(I/128)]; kQU4: two UINT4 codes per byte ([E][2I][H/2]
+// and [E][H][I/2]) with group scales and zero points s_gu, z_gu
+// [E][2I][ceil(H/128)] and s_d, z_d [E][H][ceil(I/128)]; kQNone: bf16, the
+// scales unused.
 int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
                 const int32_t* token_lora_mapping, const int32_t* lora_ranks, const float* scalings,
-                const void* w_gate_up, const void* w_down, const float* s_gu, const float* s_d, bool fp8,
+                const void* w_gate_up, const void* w_down, const float* s_gu, const float* s_d,
+                const uint8_t* z_gu, const uint8_t* z_d, int qf,
                 const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
                 const mlr_bf16* lora_b_down, int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L,
                 int32_t R, mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
@@ -1753,15 +1792,19 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     if (T < 0 || K < 1 || E < 1 || L < 0 || R < 0) return MLR_ERR_INVALID;
     return MLR_ERR_UNSUPPORTED;
   }
-  // FP8 codes are one byte: the TMA row strides (H and I bytes) must be 16-byte multiples
-  if (fp8 && (H % 16 != 0 || I % 16 != 0)) return MLR_ERR_UNSUPPORTED;
+  const bool quant = qf != kQNone;
+  // Codes are one byte (half a byte for UINT4): the TMA row strides (H and I
+  // codes) must be 16-byte multiples
+  const int cmul = qf == kQU4 ? 32 : 16;
+  if (quant && (H % cmul != 0 || I % cmul != 0)) return MLR_ERR_UNSUPPORTED;
   if (T == 0) return MLR_OK;
   const void* need[] = {x, topk_ids, topk_weights, token_lora_mapping, w_gate_up, w_down, y};
   for (const void* q : need)
     if (q == nullptr) return MLR_ERR_INVALID;
-  if (fp8 && (s_gu == nullptr || s_d == nullptr || (reinterpret_cast<uintptr_t>(s_gu) & 3) != 0 ||
-              (reinterpret_cast<uintptr_t>(s_d) & 3) != 0))
+  if (quant && (s_gu == nullptr || s_d == nullptr || (reinterpret_cast<uintptr_t>(s_gu) & 3) != 0 ||
+                (reinterpret_cast<uintptr_t>(s_d) & 3) != 0))
     return MLR_ERR_INVALID;
+  if (qf == kQU4 && (z_gu == nullptr || z_d == nullptr)) return MLR_ERR_INVALID;
   if (L > 0) {
     const void* lo[] = {lora_ranks, scalings, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down};
     for (const void* q : lo)
@@ -1802,17 +1845,20 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
             make_shrink2_maps(m_sgu, xs, cap, H, lora_a_gu, L, E, R, &abox_gu, &a3_gu, &aw_gu, &rm_sgu) &&
             make_shrink1_maps(m_sd, hbuf, cap, I, lora_a_down, L, E, R, &abox_d, &aw_d, &rm_sd) &&
             make_down_maps(m_dn, w_down, H, I, E, hbuf, cap, lora_b_down, L, R, zd, zcap, f.R16 / 8);
-  if (ok && I >= 128 && !fp8) {
+  if (ok && I >= 128 && !quant) {
     // W_gate_up as [(e, gate|up)][row][k]: a box {64, 128, 2} is a 128-row block of gate and of up
     ok = make_map3(&m_gu.m[kW3], w_gate_up, H, I, (uint64_t)E * 2, (uint64_t)H * 2, (uint64_t)I * H * 2, 64, 128, 2,
                    true);
     w3 = 1;
   }
-  if (ok && fp8) {
-    // codes: W_gate_up as [(e, gate|up)][I rows][H bytes], a box of 64 bytes x 128 rows of gate and
-    // of up; W_down as [e][H rows][I bytes], a box of 64 bytes x 128 rows.  Rows past I (or H) read 0.
-    ok = make_map3_u8(&m_gu.m[kW], w_gate_up, H, I, (uint64_t)E * 2, H, (uint64_t)I * H, 64, 128, 2) &&
-         make_map3_u8(&m_dn.m[kW], w_down, I, H, E, I, (uint64_t)H * I, 64, 128, 1) &&
+  if (ok && quant) {
+    // codes: W_gate_up as [(e, gate|up)][I rows][row bytes], a box of one K step's bytes (64, or 32
+    // for UINT4) x 128 rows of gate and of up; W_down as [e][H rows][row bytes], a box of one K
+    // step's bytes x 128 rows.  Rows past I (or H) read 0.
+    const uint64_t hb = qf == kQU4 ? (uint64_t)H / 2 : (uint64_t)H, ib = qf == kQU4 ? (uint64_t)I / 2 : (uint64_t)I;
+    const uint32_t kbox = qf == kQU4 ? 32 : 64;
+    ok = make_map3_u8(&m_gu.m[kW], w_gate_up, hb, I, (uint64_t)E * 2, hb, (uint64_t)I * hb, kbox, 128, 2) &&
+         make_map3_u8(&m_dn.m[kW], w_down, ib, H, E, ib, (uint64_t)H * ib, kbox, 128, 1) &&
          // the FP8 down GEMM runs on single CTAs: whole-tile row boxes over h, and
          // z boxes of zrows rows (a CTA loads a piece's z rows whole)
          make_row_maps(m_dn, hbuf, (uint64_t)ceil_div(I, 64) * cap, &rm_dn);
@@ -1928,9 +1974,11 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   {
     Params q = p;
     q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128); q.rmask = rm_gu; q.w3 = w3;
-    q.wscale = s_gu; q.wsr = (int)ceil_div(2 * I, 128); q.wsc = (int)ceil_div(H, 128);
-    rc = fp8 ? launch_gemm<kGateUp, true>(m_gu, q, f.max_base, stream)
-             : launch_gemm<kGateUp>(m_gu, q, f.max_base, stream);
+    q.wscale = s_gu; q.wzero = z_gu; q.wsr = (int)ceil_div(2 * I, 128); q.wsc = (int)ceil_div(H, 128);
+    rc = qf == kQFp8 ? launch_gemm<kGateUp, kQFp8>(m_gu, q, f.max_base, stream)
+       : qf == kQInt8 ? launch_gemm<kGateUp, kQInt8>(m_gu, q, f.max_base, stream)
+       : qf == kQU4 ? launch_gemm<kGateUp, kQU4>(m_gu, q, f.max_base, stream)
+                    : launch_gemm<kGateUp>(m_gu, q, f.max_base, stream);
     if (rc != MLR_OK) return rc;
   }
   prof_mark(prof, 3, stream);
@@ -1947,12 +1995,14 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   {
     Params q = p;
     // a pair covers 256 rows of H, a single CTA (FP8 weights) 128
-    q.n_tiles = counts; q.nblk = (int)ceil_div(H, fp8 ? 128 : 256); q.rmask = rm_dn;
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, quant ? 128 : 256); q.rmask = rm_dn;
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     q.dpair = det ? xs : nullptr;
-    q.wscale = s_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
-    rc = fp8 ? launch_gemm<kDown, true>(m_dn, q, f.max_base, stream)
-             : launch_gemm<kDown>(m_dn, q, f.max_base, stream);
+    q.wscale = s_d; q.wzero = z_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
+    rc = qf == kQFp8 ? launch_gemm<kDown, kQFp8>(m_dn, q, f.max_base, stream)
+       : qf == kQInt8 ? launch_gemm<kDown, kQInt8>(m_dn, q, f.max_base, stream)
+       : qf == kQU4 ? launch_gemm<kDown, kQU4>(m_dn, q, f.max_base, stream)
+                    : launch_gemm<kDown>(m_dn, q, f.max_base, stream);
     if (rc != MLR_OK) return rc;
   }
   prof_mark(prof, 5, stream);
@@ -1981,8 +2031,9 @@ extern "C" int fused_moe_lora_forward(const mlr_bf16* x, const int32_t* topk_ids
                                       void* workspace, size_t ws_bytes, int32_t* d_status,
                                       void* stream_) {
   return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up, w_down,
-                          nullptr, nullptr, false, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I,
-                          L, R, y, workspace, ws_bytes, d_status, static_cast<cudaStream_t>(stream_));
+                          nullptr, nullptr, nullptr, nullptr, mlr::kQNone, lora_a_gu, lora_b_gu, lora_a_down,
+                          lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes, d_status,
+                          static_cast<cudaStream_t>(stream_));
 }
 
 extern "C" int fused_moe_lora_forward_fp8(const mlr_bf16* x, const int32_t* topk_ids,
@@ -1996,9 +2047,42 @@ extern "C" int fused_moe_lora_forward_fp8(const mlr_bf16* x, const int32_t* topk
                                           mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
                                           void* stream_) {
   return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up_q,
-                          w_down_q, w_gate_up_scale, w_down_scale, true, lora_a_gu, lora_b_gu, lora_a_down,
-                          lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes, d_status,
-                          static_cast<cudaStream_t>(stream_));
+                          w_down_q, w_gate_up_scale, w_down_scale, nullptr, nullptr, mlr::kQFp8, lora_a_gu,
+                          lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes,
+                          d_status, static_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int fused_moe_lora_forward_int8(const mlr_bf16* x, const int32_t* topk_ids,
+                                           const float* topk_weights, const int32_t* token_lora_mapping,
+                                           const int32_t* lora_ranks, const float* scalings,
+                                           const int8_t* w_gate_up_q, const float* w_gate_up_scale,
+                                           const int8_t* w_down_q, const float* w_down_scale,
+                                           const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu,
+                                           const mlr_bf16* lora_a_down, const mlr_bf16* lora_b_down, int32_t T,
+                                           int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R,
+                                           mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                           void* stream_) {
+  return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up_q,
+                          w_down_q, w_gate_up_scale, w_down_scale, nullptr, nullptr, mlr::kQInt8, lora_a_gu,
+                          lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes,
+                          d_status, static_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int fused_moe_lora_forward_w4a16(const mlr_bf16* x, const int32_t* topk_ids,
+                                            const float* topk_weights, const int32_t* token_lora_mapping,
+                                            const int32_t* lora_ranks, const float* scalings,
+                                            const uint8_t* w_gate_up_q, const float* w_gate_up_scale,
+                                            const uint8_t* w_gate_up_zero, const uint8_t* w_down_q,
+                                            const float* w_down_scale, const uint8_t* w_down_zero,
+                                            const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu,
+                                            const mlr_bf16* lora_a_down, const mlr_bf16* lora_b_down, int32_t T,
+                                            int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R,
+                                            mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                            void* stream_) {
+  return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up_q,
+                          w_down_q, w_gate_up_scale, w_down_scale, w_gate_up_zero, w_down_zero, mlr::kQU4,
+                          lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I, L, R, y, workspace,
+                          ws_bytes, d_status, static_cast<cudaStream_t>(stream_));
 }
 
 // ------------------------------------------------------------------------

@@ -342,6 +342,35 @@ __device__ __forceinline__ uint2 e4m3x4_scaled_bf16(uint32_t w, float sc) {
   return o;
 }
 
+// Four INT8 codes (byte j of w is element j, two's complement) times `sc`,
+// rounded to bf16: element 2i in the low half of word i of the result.  The
+// int8 -> fp32 conversion is exact; the product is formed in fp32.
+__device__ __forceinline__ uint2 s8x4_scaled_bf16(uint32_t w, float sc) {
+  const float f0 = (float)((int32_t)(w << 24) >> 24) * sc;
+  const float f1 = (float)((int32_t)(w << 16) >> 24) * sc;
+  const float f2 = (float)((int32_t)(w << 8) >> 24) * sc;
+  const float f3 = (float)((int32_t)w >> 24) * sc;
+  uint2 o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(f1), "f"(f0));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(f3), "f"(f2));
+  return o;
+}
+
+// Eight UINT4 codes (nibble j of w, low nibble first, is element j) as
+// (code - zero) x sc, rounded to bf16: element 2i in the low half of word i.
+// code - zero is exact in fp32; the product is formed in fp32.
+__device__ __forceinline__ uint4 u4x8_scaled_bf16(uint32_t w, float zero, float sc) {
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = ((float)((w >> (4 * j)) & 15u) - zero) * sc;
+  uint4 o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(f[1]), "f"(f[0]));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(f[3]), "f"(f[2]));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(f[5]), "f"(f[4]));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(f[7]), "f"(f[6]));
+  return o;
+}
+
 // Vector fp32 reduction into global memory (16-byte aligned address).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),

@@ -271,6 +271,77 @@ def make_fp8_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> Fp8Expert
     return Fp8Experts(wq, ws, dq, ds)
 
 
+@dataclasses.dataclass
+class Int8Experts:
+    w_gate_up_q: torch.Tensor      # int8 [E, 2I, H]
+    w_gate_up_scale: torch.Tensor  # float32 [E, ceil(2I/128), ceil(H/128)]
+    w_down_q: torch.Tensor         # int8 [E, H, I]
+    w_down_scale: torch.Tensor     # float32 [E, ceil(H/128), ceil(I/128)]
+
+
+def make_int8_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> Int8Experts:
+    """Block-wise INT8 expert weights: codes round(N(0, 40^2)) clipped to
+    [-127, 127], one float32 scale per 128 x 128 block of U(0.75, 1.25) /
+    (40 sqrt(fan_in)), so code x scale has about the bf16 weights' spread."""
+    E, H, I = cfg.num_experts, cfg.hidden, cfg.intermediate
+    g = _gen(device, seed + 6)
+    nb = lambda n: (n + 127) // 128  # noqa: E731
+
+    def mat(rows, cols, fan_in):
+        z = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(40.0)
+        codes = z.round_().clamp_(-127, 127).to(torch.int8)
+        u = torch.rand((nb(rows), nb(cols)), generator=g, device=device, dtype=torch.float32)
+        return codes, (u * 0.5 + 0.75) / (40.0 * math.sqrt(fan_in))
+
+    wq = torch.empty(E, 2 * I, H, dtype=torch.int8, device=device)
+    ws = torch.empty(E, nb(2 * I), nb(H), dtype=torch.float32, device=device)
+    dq = torch.empty(E, H, I, dtype=torch.int8, device=device)
+    ds = torch.empty(E, nb(H), nb(I), dtype=torch.float32, device=device)
+    for e in range(E):
+        wq[e], ws[e] = mat(2 * I, H, H)
+        dq[e], ds[e] = mat(H, I, I)
+    return Int8Experts(wq, ws, dq, ds)
+
+
+@dataclasses.dataclass
+class W4A16Experts:
+    w_gate_up_q: torch.Tensor      # uint8 [E, 2I, H/2], two uint4 codes per byte (even column low)
+    w_gate_up_scale: torch.Tensor  # float32 [E, 2I, ceil(H/128)]
+    w_gate_up_zero: torch.Tensor   # uint8 [E, 2I, ceil(H/128)], 0..15
+    w_down_q: torch.Tensor         # uint8 [E, H, I/2]
+    w_down_scale: torch.Tensor     # float32 [E, H, ceil(I/128)]
+    w_down_zero: torch.Tensor      # uint8 [E, H, ceil(I/128)]
+
+
+def make_w4a16_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> W4A16Experts:
+    """4-bit expert weights: uniform codes 0..15, zero points uniform in 6..9,
+    one float32 scale per row and 128-column group of U(0.75, 1.25) /
+    sqrt(22.5 fan_in): code - zero has mean 0 and mean square 21.25 + 1.25 =
+    22.5, so (code - zero) x scale has about the bf16 weights' N(0, 1/fan_in)
+    spread."""
+    E, H, I = cfg.num_experts, cfg.hidden, cfg.intermediate
+    g = _gen(device, seed + 7)
+    nb = lambda n: (n + 127) // 128  # noqa: E731
+
+    def mat(rows, cols, fan_in):
+        codes = torch.randint(0, 16, (rows, cols), generator=g, device=device, dtype=torch.int32)
+        packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+        u = torch.rand((rows, nb(cols)), generator=g, device=device, dtype=torch.float32)
+        zero = torch.randint(6, 10, (rows, nb(cols)), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+        return packed, (u * 0.5 + 0.75) / math.sqrt(22.5 * fan_in), zero
+
+    wq = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+    ws = torch.empty(E, 2 * I, nb(H), dtype=torch.float32, device=device)
+    wz = torch.empty(E, 2 * I, nb(H), dtype=torch.uint8, device=device)
+    dq = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
+    ds = torch.empty(E, H, nb(I), dtype=torch.float32, device=device)
+    dz = torch.empty(E, H, nb(I), dtype=torch.uint8, device=device)
+    for e in range(E):
+        wq[e], ws[e], wz[e] = mat(2 * I, H, H)
+        dq[e], ds[e], dz[e] = mat(H, I, I)
+    return W4A16Experts(wq, ws, wz, dq, ds, dz)
+
+
 def make_x(cfg: LayerConfig, device="cpu", seed: int = 0) -> torch.Tensor:
     g = _gen(device, seed + 3)
     return torch.randn(cfg.num_tokens, cfg.hidden, generator=g, device=device,
