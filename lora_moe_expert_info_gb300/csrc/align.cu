@@ -40,19 +40,43 @@ int current_device_id() {
   return dev;
 }
 
+// Token of this thread's pair j = it * kThreads + tid of a chunk, advanced one
+// round (kThreads pairs) at a time without a division: t = tq, tr = its slot.
+struct TokenCursor {
+  int tq, tr, dq, dr, topk;
+  __device__ __forceinline__ TokenCursor(int64_t p0, int topk_) : topk(topk_) {
+    const int64_t p = p0 + threadIdx.x;  // < 2^31: align_plan bounds P
+    tq = (int)(p / topk);
+    tr = (int)(p - (int64_t)tq * topk);
+    dq = kThreads / topk;
+    dr = kThreads % topk;
+  }
+  __device__ __forceinline__ void next() {
+    tq += dq;
+    tr += dr;
+    if (tr >= topk) {
+      tr -= topk;
+      ++tq;
+    }
+  }
+};
+
 // Keys of this thread's pairs j = (bt + i) * kThreads + tid, i < kLoadBatch, of
 // the chunk starting at pair p0 with n pairs (-1 past the end or for an id out
-// of range, which also flags `bad`).  All loads are issued before any is used.
+// of range, which also flags `bad`).  All loads are issued before any is used;
+// cur holds the token of pair (bt * kThreads + tid) and is advanced past the batch.
 __device__ __forceinline__ void align_load_keys(const int32_t* __restrict__ topk_ids,
                                                 const int32_t* __restrict__ mapping, int64_t p0, int n, int bt,
-                                                int topk, int E, int C, int L, int (&key)[kLoadBatch], int& bad) {
+                                                TokenCursor& cur, int E, int C, int L, int (&key)[kLoadBatch],
+                                                int& bad) {
   int ev[kLoadBatch], lv[kLoadBatch];
 #pragma unroll
   for (int i = 0; i < kLoadBatch; ++i) {
     const int j = (bt + i) * kThreads + (int)threadIdx.x;
-    const int64_t p = p0 + (j < n ? j : 0);
-    ev[i] = __ldg(topk_ids + p);
-    lv[i] = __ldg(mapping + p / topk);
+    const bool in = j < n;
+    ev[i] = __ldg(topk_ids + p0 + (in ? j : 0));
+    lv[i] = __ldg(mapping + (in ? cur.tq : 0));
+    cur.next();
   }
 #pragma unroll
   for (int i = 0; i < kLoadBatch; ++i) {
@@ -80,10 +104,11 @@ align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
   int bad = 0;
   // keys in batches of kLoadBatch pairs: the batch's loads are issued together
   // (unconditionally, past-the-end lanes reading pair p0), then counted
+  TokenCursor cur(p0, topk);
 #pragma unroll
   for (int bt = 0; bt < kMaxItems; bt += kLoadBatch) {
     int key[kLoadBatch];
-    align_load_keys(topk_ids, mapping, p0, n, bt, topk, E, C, L, key, bad);
+    align_load_keys(topk_ids, mapping, p0, n, bt, cur, E, C, L, key, bad);
 #pragma unroll
     for (int i = 0; i < kLoadBatch; ++i)
       if (key[i] >= 0) atomicAdd(&hist[key[i]], 1u);
@@ -193,10 +218,11 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
   // rounds run on shared memory only.
   uint32_t ks[kMaxItems];
   int bad = 0;
+  TokenCursor cur(p0, topk);
 #pragma unroll
   for (int bt = 0; bt < kMaxItems; bt += kLoadBatch) {
     int key[kLoadBatch];
-    align_load_keys(topk_ids, mapping, p0, n, bt, topk, E, C, L, key, bad);
+    align_load_keys(topk_ids, mapping, p0, n, bt, cur, E, C, L, key, bad);
 #pragma unroll
     for (int i = 0; i < kLoadBatch; ++i) ks[bt + i] = key[i] >= 0 ? (uint32_t)key[i] : 0xFFFFFFFFu;
   }

@@ -80,13 +80,26 @@ batch_info_kernel(const int32_t* __restrict__ seg_indptr, const int32_t* __restr
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
     int bad = 0;
-    for (int i = threadIdx.x; i < bs; i += blockDim.x) {
-      const int a = seg_indptr[i], b = seg_indptr[i + 1];
-      if (b < a) bad |= MLR_STATUS_BAD_INDPTR;
-      if (max_len > 0 && b - a > max_len) bad |= MLR_STATUS_UNDERCOVERED;
-      const int l = weight_indices[i];
-      if (l < -1 || l >= num_loras) bad |= MLR_STATUS_INDEX;
-      else if (l >= 0) atomicOr(&s_bits[l >> 5], 1u << (l & 31));
+    // kVBatch segments per thread per round, their loads issued together
+    constexpr int kVBatch = 8;
+    for (int i0 = 0; i0 < bs; i0 += kVBatch * kThreads) {
+      int a[kVBatch], b[kVBatch], l[kVBatch];
+#pragma unroll
+      for (int q = 0; q < kVBatch; ++q) {
+        const int i = i0 + q * kThreads + (int)threadIdx.x;
+        const int ic = i < bs ? i : 0;
+        a[q] = __ldg(seg_indptr + ic);
+        b[q] = __ldg(seg_indptr + ic + 1);
+        l[q] = __ldg(weight_indices + ic);
+      }
+#pragma unroll
+      for (int q = 0; q < kVBatch; ++q) {
+        if (i0 + q * kThreads + (int)threadIdx.x >= bs) continue;
+        if (b[q] < a[q]) bad |= MLR_STATUS_BAD_INDPTR;
+        if (max_len > 0 && b[q] - a[q] > max_len) bad |= MLR_STATUS_UNDERCOVERED;
+        if (l[q] < -1 || l[q] >= num_loras) bad |= MLR_STATUS_INDEX;
+        else if (l[q] >= 0) atomicOr(&s_bits[l[q] >> 5], 1u << (l[q] & 31));
+      }
     }
     if (threadIdx.x == 0 && (seg_indptr[0] != 0 || seg_indptr[bs] != num_tokens))
       bad |= MLR_STATUS_BAD_INDPTR;

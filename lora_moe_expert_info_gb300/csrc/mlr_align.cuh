@@ -62,20 +62,6 @@ inline size_t align_block_smem(const AlignPlan& pl) {
   return (size_t)(2 * round_up((int64_t)(pl.NB + 1) * 4, 16) + 2 * round_up(pl.P * 2, 16));
 }
 
-// Bucket of pair p (e * (L+1) + lora + 1), or -1 with `bad` flagged for an
-// expert or adapter id out of range.
-static __device__ __forceinline__ int align_pair_key(const int32_t* __restrict__ topk_ids,
-                                                     const int32_t* __restrict__ mapping, int64_t p,
-                                                     int topk, int E, int C, int L, int& bad) {
-  const int e = __ldg(topk_ids + p);
-  const int l = __ldg(mapping + p / topk);
-  if (e < 0 || e >= E || l < -1 || l >= L) {
-    bad |= MLR_STATUS_INDEX;
-    return -1;
-  }
-  return e * C + (l + 1);
-}
-
 // Block-wide exclusive scan of s[0..n) in place; s[n] receives the total.
 // Ends with a barrier, so s is ready for every thread on return.
 static __device__ void align_block_scan(uint32_t* s, int n) {
