@@ -1897,7 +1897,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   // tiles of differing sizes); small batches keep the cheaper plain order
   const int by_span = f.al.P > 32 * (int64_t)E ? 1 : 0;
   const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
-  if (align_block_ok(f.al)) {
+  if (align_block_ok(f.al, scan_bytes)) {
     // one launch: the dense align and the tile plan (timed as the align stage)
     const size_t zs_off = align_block_smem(f.al), sm = zs_off + scan_bytes;
     if (sm > 48 * 1024 &&
@@ -2176,7 +2176,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
   const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
   int32_t* zeros_ids = reinterpret_cast<int32_t*>(ws + f.o_h);  // expert id 0 of every token
   if (cudaMemsetAsync(zeros_ids, 0, (size_t)T * 4, stream) != cudaSuccess) return MLR_ERR_CUDA;
-  if (align_block_ok(f.al)) {
+  if (align_block_ok(f.al, scan_bytes)) {
     const size_t zs_off = align_block_smem(f.al), sm = zs_off + scan_bytes;
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)

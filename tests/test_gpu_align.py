@@ -48,7 +48,7 @@ def _random(seed, T, K, E, L, p_none=0.1, distinct=True):
     (12, 30000, 2, 2, 1, 16), (13, 3, 4, 100, 399, 4096),
     # the limits of the single-block path: 16384 pairs, 8192 buckets (and one past each)
     (14, 2048, 8, 64, 7, 16), (15, 2049, 8, 64, 7, 16), (16, 100, 4, 128, 63, 16),
-    (17, 100, 4, 128, 64, 16),
+    (17, 100, 4, 128, 64, 16), (18, 4096, 8, 64, 7, 16),
 ])
 def test_random_cases(cuda_device, seed, T, K, E, L, bs):
     topk, mapping = _random(seed, T, K, E, L, distinct=(seed % 2 == 0))

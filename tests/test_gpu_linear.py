@@ -95,9 +95,9 @@ def test_mla_projection_full_size_sampled(cuda_device):
 
 def test_chunked_align_path(cuda_device):
     # more than 16,384 tokens: the align runs in chunks instead of one block
-    T = 20000
+    T = 36000
     c = Lin(cuda_device, T=T, D_in=128, offs=[0, 256], L=3, R=16, ranks=[16, 8, 16],
-            seg_lens=[5000, 7000, 3000, 5000], adapters=[2, -1, 0, 1], seed=4)
+            seg_lens=[9000, 12600, 5400, 9000], adapters=[2, -1, 0, 1], seed=4)
     y = c.gpu()
     toks = np.sort(np.random.default_rng(4).choice(T, 64, replace=False))
     toks = np.concatenate([[0, T - 1], toks])

@@ -7,8 +7,8 @@ The no-allocation entry point keeps its scratch in a fixed array inside the
 library.  These tests call it through the C ABI and check that its results
 equal, bit for bit, both the workspace-taking moe_lora_align and the CPU oracle
 on calls in a row (each later call reuses the shared scratch the one before it
-left behind, on the single-block path and on the four-launch chunked path with
-differently shaped count matrices), and that sizes beyond the fixed scratch are
+left behind, on the single-block path and on the chunked path with differently
+shaped count matrices), and that sizes beyond the fixed scratch are
 refused.  The file is named to be collected last and needs no state from other
 tests.
 """
@@ -87,14 +87,14 @@ def test_two_calls_in_a_row_match_workspace_align(cuda_device):
 
 
 def test_chunked_calls_in_a_row_with_other_shapes(cuda_device):
-    # Both calls take the four-launch chunked path (more than 16384 pairs); the
-    # second has fewer chunks and another bucket count, so its count matrix
-    # overlaps the stale one of the first call with a different layout.
-    t1, m1 = _inputs(3, 4096, 8, 128, 8, cuda_device)     # 32768 pairs, 128 x 9 buckets
-    assert 4096 * 8 > 16384
+    # Both calls take the chunked path (more than 16384 pairs); the second has
+    # fewer chunks and another bucket count, so its count matrix overlaps the
+    # stale one of the first call with a different layout.
+    t1, m1 = _inputs(3, 5000, 8, 128, 8, cuda_device)     # 40000 pairs, 128 x 9 buckets
+    assert 5000 * 8 > 16384
     _check_same_as_workspace_call(t1, m1, 128, 8, 16)
-    t2, m2 = _inputs(4, 3000, 6, 64, 4, cuda_device)      # 18000 pairs, 64 x 5 buckets
-    assert 3000 * 6 > 16384
+    t2, m2 = _inputs(4, 6000, 6, 64, 4, cuda_device)      # 36000 pairs, 64 x 5 buckets
+    assert 6000 * 6 > 16384
     _check_same_as_workspace_call(t2, m2, 64, 4, 32)
 
 
