@@ -201,9 +201,13 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
   extern __shared__ uint32_t smem[];
   const int C = L + 1, NB = E * C;
   const int nb4 = (int)round_up(NB + 1, 4);
-  uint32_t* off = smem;                                             // [NB + 1]
-  uint32_t* gb = smem + nb4;                                        // [NB + 1] (kBases)
-  uint16_t* stage = reinterpret_cast<uint16_t*>(smem + (kBases ? 2 : 1) * nb4);  // [chunk]
+  // kBases: gb [NB + 1], then off [NB + 1] and stage [chunk], which the final
+  // chunk-sorted list (order32 [chunk], one word per pair) later overwrites.
+  // Otherwise: off [NB + 1], stage [chunk].
+  uint32_t* gb = smem;                                              // (kBases)
+  uint32_t* off = smem + (kBases ? nb4 : 0);                        // [NB + 1]
+  uint16_t* stage = reinterpret_cast<uint16_t*>(off + nb4);         // [chunk]
+  uint32_t* order32 = off;                                          // (kBases) [chunk]
   for (int b = threadIdx.x; b < NB; b += blockDim.x) {
     off[b] = 0u;
     if (kBases) gb[b] = dense_start ? dense_start[b] : (btotal[b] + block_size - 1) / block_size * block_size;
@@ -265,6 +269,7 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
     const uint32_t* crow = cnt + (int64_t)blockIdx.x * NB;
     for (int b = threadIdx.x; b < NB; b += blockDim.x) gb[b] += crow[b];
   }
+  const int nvalid = (int)off[NB];  // valid pairs of the chunk (off is scanned)
 #pragma unroll
   for (int it = 0; it < kMaxItems; ++it)
     if (it < rounds && ks[it] != 0xFFFFFFFFu)
@@ -287,12 +292,39 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
       }
       const int round_start = m + 1;
       for (m = pos + 1; m < hi && (stage[m] >> 10) == (uint32_t)it; ++m) less += stage[m] < j;
-      const int64_t base = kBases ? (int64_t)gb[k] : (int64_t)(dense_start ? dense_start[k] : bstart[k]) + crow[k];
-      const int64_t dst = base + (round_start - lo) + less;
-      if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + j);
+      if (kBases) {
+        // the pair's place in the chunk's sorted list (written out below)
+        ks[it] = (ks[it] & 0xFFFF0000u) | (uint32_t)(round_start + less);
+      } else {
+        const int64_t base = (int64_t)(dense_start ? dense_start[k] : bstart[k]) + crow[k];
+        const int64_t dst = base + (round_start - lo) + less;
+        if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + j);
+      }
     }
   }
-  if (kBases || dense_start) return;
+  if (kBases) {
+    // The chunk's pairs in sorted order in shared memory (over off and stage,
+    // which are no longer read), then written out with consecutive threads on
+    // consecutive sorted places: the places of one bucket are consecutive in
+    // the output too, so the stores coalesce into runs.  gb[k] - off[k] is the
+    // output place of the chunk's sorted place 0 for bucket k (gb[k] >= off[k]:
+    // the global start of k counts at least this chunk's pairs of earlier buckets).
+    __syncthreads();  // every read of off and stage is done
+    for (int b = threadIdx.x; b < NB; b += blockDim.x) gb[b] -= off[b];
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it)
+      if (it < rounds && ks[it] != 0xFFFFFFFFu)
+        order32[ks[it] & 0xFFFFu] = (ks[it] & 0xFFFF0000u) | (uint32_t)(it * kThreads + threadIdx.x);
+    __syncthreads();
+    for (int q = threadIdx.x; q < nvalid; q += kThreads) {
+      const uint32_t v = order32[q];
+      const int64_t dst = (int64_t)gb[v >> 16] + q;
+      if (dst < capacity) sorted_ids[dst] = (int32_t)(p0 + (v & 0xFFFFu));
+    }
+    return;
+  }
+  if (dense_start) return;
 
   // Pad sentinels and per-block labels: one warp per bucket over the whole
   // grid, lanes writing consecutive entries.  Padded positions are below
@@ -353,9 +385,14 @@ AlignPlan align_plan(int32_t num_tokens, int32_t topk, int32_t num_experts, int3
 
 size_t align_smem_count(const AlignPlan& pl) { return (size_t)pl.NB * 4; }
 // Dynamic shared memory of the scatter: one (or, with the bucket bases, two)
-// bucket arrays of round_up(NB + 1, 4) words and the chunk's uint16 stage.
+// bucket arrays of round_up(NB + 1, 4) words and the chunk's uint16 stage (with
+// the bases, at least 4 bytes per pair of the chunk after the first array).
 size_t align_smem_scatter(const AlignPlan& pl, bool bases) {
-  return (size_t)((bases ? 2 : 1) * round_up(pl.NB + 1, 4) * 4 + round_up((int64_t)pl.chunk * 2, 16));
+  const int64_t nb = round_up(pl.NB + 1, 4) * 4, st = round_up((int64_t)pl.chunk * 2, 16);
+  if (!bases) return (size_t)(nb + st);
+  // gb, then off + stage, which the chunk-sorted list (4 bytes per pair) reuses
+  const int64_t tail = nb + st > (int64_t)pl.chunk * 4 ? nb + st : (int64_t)pl.chunk * 4;
+  return (size_t)(nb + tail);
 }
 bool align_bases_fit(const AlignPlan& pl) { return align_smem_scatter(pl, true) <= kSmemLimit; }
 

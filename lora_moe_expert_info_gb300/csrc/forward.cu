@@ -55,6 +55,7 @@ constexpr int kEpiWarp0 = 5;
 constexpr int kMaxThreads = 416;  // up to 13 warps (warps 1-3 idle)
 constexpr int kGatherThreads = 256;
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanRankCache = 1024;  // adapters whose ranks the plan keeps in shared memory
 constexpr int kShrinkRows = 128;  // max sorted rows per shrink tile
 constexpr int kGemvRows = 4;      // buckets with at most this many pairs take the CUDA-core shrink
 constexpr int kGemvThreads = 256;
@@ -998,6 +999,16 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
   __shared__ int big_n;
   __shared__ int4 big_q[kPlanBigQueue];
   if (threadIdx.x == 0) big_n = 0;
+  // the adapters' ranks, read once into shared memory when they fit: the
+  // per-expert loops below visit every bucket of an expert and would otherwise
+  // wait on a global load for each
+  __shared__ int32_t rank_cache[kPlanRankCache];
+  const int L = C - 1;
+  if (L <= kPlanRankCache) {
+    for (int l = threadIdx.x; l < L; l += kPlanThreads) rank_cache[l] = lora_ranks[l];
+    __syncthreads();
+    lora_ranks = rank_cache;
+  }
   // z region length of every bucket (LoRA buckets with rank > 0 and pairs only)
   for (int b = threadIdx.x; b < NB; b += kPlanThreads) {
     ustart_out[b] = us[b];
@@ -1260,29 +1271,36 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usor
     reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// acc[i] += A row . member row i (i < M) over k in [0, Kd), lane-strided in
-// 16-byte pieces with kBatch loads in flight; A is unpacked once per piece.
+// acc0[i] += A row 0 . member row i and acc1[i] += A row 1 . member row i
+// (i < M) over k in [0, Kd): the warp streams both rank rows at once, lanes
+// strided in 16-byte pieces with 2 x kBatch loads in flight (an 8 KB window of
+// A per warp); each A piece is unpacked once.  arow1 may repeat arow0.
 template <int M>
-__device__ __forceinline__ void gemv_dot(const uint16_t* __restrict__ arow, const uint16_t* xr, int Kp, int Kd,
-                                         int lane, float (&acc)[kGemvRows]) {
-  constexpr int kBatch = 8;  // a 4 KB rank row per warp
+__device__ __forceinline__ void gemv_dot2(const uint16_t* __restrict__ arow0, const uint16_t* __restrict__ arow1,
+                                          const uint16_t* xr, int Kp, int Kd, int lane, float (&acc0)[kGemvRows],
+                                          float (&acc1)[kGemvRows]) {
+  constexpr int kBatch = 8;
   for (int k0 = lane * 8; k0 < Kd; k0 += 32 * 8 * kBatch) {
-    uint4 av[kBatch];
+    uint4 av[2][kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int k = k0 + j * 256;
-      av[j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow + k)) : make_uint4(0, 0, 0, 0);
+      av[0][j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow0 + k)) : make_uint4(0, 0, 0, 0);
+      av[1][j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow1 + k)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int k = k0 + j * 256;
       if (k < Kd) {
-        const uint32_t aw[4] = {av[j].x, av[j].y, av[j].z, av[j].w};
-        float af[8];
+        float af[2][8];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          af[2 * w] = __uint_as_float(aw[w] << 16);
-          af[2 * w + 1] = __uint_as_float(aw[w] & 0xffff0000u);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t aw[4] = {av[h][j].x, av[h][j].y, av[h][j].z, av[h][j].w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            af[h][2 * w] = __uint_as_float(aw[w] << 16);
+            af[h][2 * w + 1] = __uint_as_float(aw[w] & 0xffff0000u);
+          }
         }
 #pragma unroll
         for (int i = 0; i < M; ++i) {
@@ -1290,8 +1308,11 @@ __device__ __forceinline__ void gemv_dot(const uint16_t* __restrict__ arow, cons
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            acc[i] = fmaf(af[2 * w], __uint_as_float(xw[w] << 16), acc[i]);
-            acc[i] = fmaf(af[2 * w + 1], __uint_as_float(xw[w] & 0xffff0000u), acc[i]);
+            const float x0 = __uint_as_float(xw[w] << 16), x1 = __uint_as_float(xw[w] & 0xffff0000u);
+            acc0[i] = fmaf(af[0][2 * w], x0, acc0[i]);
+            acc0[i] = fmaf(af[0][2 * w + 1], x1, acc0[i]);
+            acc1[i] = fmaf(af[1][2 * w], x0, acc1[i]);
+            acc1[i] = fmaf(af[1][2 * w + 1], x1, acc1[i]);
           }
         }
       }
@@ -1299,29 +1320,36 @@ __device__ __forceinline__ void gemv_dot(const uint16_t* __restrict__ arow, cons
   }
 }
 
+// CUDA-core shrink of buckets with at most kGemvRows pairs (NG rank blocks of
+// LoRA A per adapter: 2 gate|up, 1 down).  One block per bucket (grid-stride
+// over the listed buckets): the member rows are staged once in shared memory;
+// each warp streams two rank rows of A at a time against them; then the block
+// writes the bucket's whole z region with 16-byte stores (8 rank columns of
+// one row each): s_l * dot for member rows and ranks q < r, zeros elsewhere.
+// Dynamic shared memory: the member rows [kGemvRows][Kp] bf16, then the dots
+// [NG * R16][kGemvRows] fp32.
 template <int NG>
 __global__ void __launch_bounds__(kGemvThreads)
 shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restrict__ n_tiles,
                    const uint16_t* __restrict__ a, const uint16_t* __restrict__ rows, int Kd, int64_t cap,
                    int E, int R, int R16, const int32_t* __restrict__ lora_ranks,
                    const float* __restrict__ scalings, uint16_t* __restrict__ z, int64_t zcap) {
-  constexpr int kUnitRows = 2 * kGemvThreads / 32;  // rank rows per work unit (2 per warp)
-  extern __shared__ __align__(16) uint16_t xr[];  // [kGemvRows][Kp]
-  const int units = (NG * R + kUnitRows - 1) / kUnitRows;  // work units per bucket (upper bound)
-  const int nu = *n_tiles * units;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kGemvThreads / 32;
+  extern __shared__ __align__(16) uint8_t gemv_smem[];
   const int Kp = (Kd + 63) & ~63, kp8 = Kp / 8;
-  for (int unit = blockIdx.x; unit < nu; unit += gridDim.x) {
-    const int tile = unit / units, grp = unit - tile * units;
-    const int r = lora_ranks[tiles[tile].a.y];
-    if (grp * kUnitRows >= NG * r && grp > 0) continue;  // no rank rows left for this unit
+  uint16_t* xr = reinterpret_cast<uint16_t*>(gemv_smem);                      // [kGemvRows][Kp]
+  float* zv = reinterpret_cast<float*>(gemv_smem + (size_t)kGemvRows * Kp * 2);  // [NG * R16][kGemvRows]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = *n_tiles;
+  for (int tile = blockIdx.x; tile < nt; tile += gridDim.x) {
     const ShrinkRec t = tiles[tile];
     const int e = t.a.x, l = t.a.y, row0 = t.a.z, N = t.a.w;
     const int zrow0 = t.b.x, mlo = t.b.y, mhi = t.b.z;
     const int m = mhi - mlo;
+    const int r = lora_ranks[l];
     const int r16 = (r + 15) & ~15;
     const float sc = scalings[l];
-    __syncthreads();  // the previous unit's reads of xr are done
+    __syncthreads();  // the previous bucket's reads of xr and zv are done
     for (int idx = threadIdx.x; idx < m * kp8; idx += kGemvThreads) {
       const int i = idx / kp8, c = idx - i * kp8;  // 16-byte piece c of member row i
       const int64_t u = (int64_t)row0 + mlo + i;
@@ -1329,40 +1357,57 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
           *reinterpret_cast<const uint4*>(rows + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8);
     }
     __syncthreads();
-    const int task_end = min(NG * r, (grp + 1) * kUnitRows);
-    for (int task = grp * kUnitRows + warp; task < task_end; task += kGemvThreads / 32) {
-      const int g = task / r, q = task - g * r;
-      const uint16_t* arow = a + ((((int64_t)l * E + e) * NG + g) * R + q) * (int64_t)Kd;
-      float acc[kGemvRows];
+    const int nrows = NG * r;
+    for (int task = 2 * warp; task < nrows; task += 2 * kWarps) {
+      const int t1 = task + 1 < nrows ? task + 1 : task;
+      const int g0 = task / r, q0 = task - g0 * r, g1 = t1 / r, q1 = t1 - g1 * r;
+      const uint16_t* arow0 = a + ((((int64_t)l * E + e) * NG + g0) * R + q0) * (int64_t)Kd;
+      const uint16_t* arow1 = a + ((((int64_t)l * E + e) * NG + g1) * R + q1) * (int64_t)Kd;
+      float acc0[kGemvRows], acc1[kGemvRows];
 #pragma unroll
-      for (int i = 0; i < kGemvRows; ++i) acc[i] = 0.f;
+      for (int i = 0; i < kGemvRows; ++i) acc0[i] = acc1[i] = 0.f;
       static_assert(kGemvRows == 4, "one case per member count");
       switch (m) {  // uniform per CTA
-        case 1: gemv_dot<1>(arow, xr, Kp, Kd, lane, acc); break;
-        case 2: gemv_dot<2>(arow, xr, Kp, Kd, lane, acc); break;
-        case 3: gemv_dot<3>(arow, xr, Kp, Kd, lane, acc); break;
-        default: gemv_dot<4>(arow, xr, Kp, Kd, lane, acc); break;
+        case 1: gemv_dot2<1>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
+        case 2: gemv_dot2<2>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
+        case 3: gemv_dot2<3>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
+        default: gemv_dot2<4>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
       }
 #pragma unroll
       for (int i = 0; i < kGemvRows; ++i)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
-      if (lane < m) {
-        float v = acc[0];
+        for (int o = 16; o > 0; o >>= 1) {
+          acc0[i] += __shfl_xor_sync(0xffffffffu, acc0[i], o);
+          acc1[i] += __shfl_xor_sync(0xffffffffu, acc1[i], o);
+        }
+      if (lane < kGemvRows) {
+        float v0 = acc0[0], v1 = acc1[0];
 #pragma unroll
         for (int i = 1; i < kGemvRows; ++i)
-          if (lane == i) v = acc[i];
-        const int col = g * R16 + q;
-        z[((int64_t)(col >> 3) * zcap + zrow0 + mlo + lane) * 8 + (col & 7)] = f32_to_bf16_bits(sc * v);
+          if (lane == i) {
+            v0 = acc0[i];
+            v1 = acc1[i];
+          }
+        zv[(g0 * R16 + q0) * kGemvRows + lane] = sc * v0;
+        zv[(g1 * R16 + q1) * kGemvRows + lane] = sc * v1;
       }
     }
-    // the rest of the region (first unit): non-member columns for every rank,
-    // member columns past r
-    for (int idx = threadIdx.x; grp == 0 && idx < NG * r16 * N; idx += kGemvThreads) {
-      const int n = idx % N, rest = idx / N, q = rest % r16, g = rest / r16;
-      if (n >= mlo && n < mhi && q < r) continue;
-      const int col = g * R16 + q;
-      z[((int64_t)(col >> 3) * zcap + zrow0 + n) * 8 + (col & 7)] = 0;
+    __syncthreads();
+    // the bucket's z region: N rows x (NG * r16 / 8) chunks of 8 rank columns
+    const int cpg = r16 / 8, nchunk = NG * cpg;
+    for (int idx = threadIdx.x; idx < N * nchunk; idx += kGemvThreads) {
+      const int n = idx % N, c = idx / N, g = c / cpg, q8 = (c - g * cpg) * 8;
+      const bool member = n >= mlo && n < mhi;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int qa = q8 + 2 * j, qb = qa + 1;
+        const float va = (member && qa < r) ? zv[(g * R16 + qa) * kGemvRows + (n - mlo)] : 0.f;
+        const float vb = (member && qb < r) ? zv[(g * R16 + qb) * kGemvRows + (n - mlo)] : 0.f;
+        w[j] = (uint32_t)f32_to_bf16_bits(va) | ((uint32_t)f32_to_bf16_bits(vb) << 16);
+      }
+      const int col0 = g * R16 + q8;  // a multiple of 8: one chunk of z
+      *reinterpret_cast<uint4*>(z + ((int64_t)(col0 >> 3) * zcap + zrow0 + n) * 8) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -1725,7 +1770,7 @@ int launch_gemv(const ShrinkRec* tiles, const int32_t* n_tiles, int64_t max_tile
                 int Kd, const FwdLayout& f, int E, int R, const int32_t* lora_ranks, const float* scalings,
                 uint16_t* z, cudaStream_t stream) {
   if (max_tiles <= 0) return MLR_OK;
-  const int smem = kGemvRows * (int)round_up(Kd, 64) * 2;
+  const int smem = kGemvRows * (int)round_up(Kd, 64) * 2 + NG * f.R16 * kGemvRows * 4;
   const int dev = current_device();
   static int configured[64] = {};  // largest opt-in so far, per device
   if (smem > 48 * 1024 && (dev < 0 || smem > configured[dev])) {
@@ -1734,8 +1779,7 @@ int launch_gemv(const ShrinkRec* tiles, const int32_t* n_tiles, int64_t max_tile
       return MLR_ERR_CUDA;
     if (dev >= 0) configured[dev] = smem;
   }
-  const int64_t units = max_tiles * ((NG * R + 2 * kGemvThreads / 32 - 1) / (2 * kGemvThreads / 32));
-  const int64_t grid = units < 6 * (int64_t)sm_count() ? units : 6 * (int64_t)sm_count();
+  const int64_t grid = max_tiles < 8 * (int64_t)sm_count() ? max_tiles : 8 * (int64_t)sm_count();
   shrink_gemv_kernel<NG><<<(unsigned)grid, kGemvThreads, smem, stream>>>(
       tiles, n_tiles, static_cast<const uint16_t*>(a), rows, Kd, f.cap, E, R, f.R16, lora_ranks, scalings, z,
       f.zcap);

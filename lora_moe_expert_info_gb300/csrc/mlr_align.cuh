@@ -53,7 +53,9 @@ constexpr int kAlignBlockThreads = 1024;
 constexpr int kAlignBlockMaxItems = 16;
 constexpr int64_t kAlignBlockMaxPairs = kAlignBlockThreads * kAlignBlockMaxItems;
 constexpr int kAlignBlockMaxBuckets = 8192;
-constexpr size_t kAlignBlockSmemLimit = 227 * 1024;
+// dynamic shared memory of the one-block kernels, leaving room for their
+// static arrays (scan scratch, the plan's rank cache and queue) under 227 KB
+constexpr size_t kAlignBlockSmemLimit = 216 * 1024;
 
 // Dynamic shared memory of align_block: cnt[NB+1], start[NB+1] (uint32),
 // stage[P], order[P] (uint16).
