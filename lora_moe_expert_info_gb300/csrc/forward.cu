@@ -355,6 +355,12 @@ struct ExpandCursor {
   }
 };
 
+// Row-box height of a tile of nrows rows (0: several 64-row boxes).
+__device__ __forceinline__ int row_box_rows(const Params& p, int nrows) {
+  return nrows <= 64 ? 64 : (nrows <= 128 && (p.rmask & 1)) ? 128
+                          : (nrows <= 192 && (p.rmask & 4)) ? 192
+                          : (nrows <= 256 && (p.rmask & 2)) ? 256 : 0;
+}
 // Q (gate_up and down only): the expert weights are FP8 E4M3 with 128 x 128
 // block scales.  The producer loads the raw codes of a K step into the upper
 // half of the stage's weight area; warps 1-3 convert them in place into the
@@ -438,9 +444,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const bool main_step = s < nks;
         // the row tile of x_sorted / h: one 64/128/192/256-row box where the
         // map exists, else 64-row boxes
-        const int hb = it.nrows <= 64 ? 64 : (it.nrows <= 128 && (p.rmask & 1)) ? 128
-                                         : (it.nrows <= 192 && (p.rmask & 4)) ? 192
-                                         : (it.nrows <= 256 && (p.rmask & 2)) ? 256 : 0;
+        const int hb = row_box_rows(p, it.nrows);
         const int rbox = hb ? 1 : (int)ceil_div(it.nrows, 64);
         const int rbytes = hb ? hb * 128 : rbox * 8192;
         const CUtensorMap* rmap =
@@ -1271,30 +1275,28 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usor
     reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// acc0[i] += A row 0 . member row i and acc1[i] += A row 1 . member row i
-// (i < M) over k in [0, Kd): the warp streams both rank rows at once, lanes
-// strided in 16-byte pieces with 2 x kBatch loads in flight (an 8 KB window of
-// A per warp); each A piece is unpacked once.  arow1 may repeat arow0.
-template <int M>
-__device__ __forceinline__ void gemv_dot2(const uint16_t* __restrict__ arow0, const uint16_t* __restrict__ arow1,
-                                          const uint16_t* xr, int Kp, int Kd, int lane, float (&acc0)[kGemvRows],
-                                          float (&acc1)[kGemvRows]) {
-  constexpr int kBatch = 8;
-  for (int k0 = lane * 8; k0 < Kd; k0 += 32 * 8 * kBatch) {
-    uint4 av[2][kBatch];
+// acc[h][i] += A row h . member row i (h < NR, i < M) over k in [0, Kd): the
+// warp streams NR rank rows at once, lanes strided in 16-byte pieces with
+// NR x KB loads in flight; each A piece is unpacked once.  Rows may repeat.
+template <int M, int NR, int KB>
+__device__ __forceinline__ void gemv_dot(const uint16_t* const (&arow)[NR], const uint16_t* xr, int Kp, int Kd,
+                                         int lane, float (&acc)[NR][kGemvRows]) {
+  for (int k0 = lane * 8; k0 < Kd; k0 += 32 * 8 * KB) {
+    uint4 av[NR][KB];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
+    for (int j = 0; j < KB; ++j) {
       const int k = k0 + j * 256;
-      av[0][j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow0 + k)) : make_uint4(0, 0, 0, 0);
-      av[1][j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow1 + k)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int h = 0; h < NR; ++h)
+        av[h][j] = k < Kd ? __ldg(reinterpret_cast<const uint4*>(arow[h] + k)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
+    for (int j = 0; j < KB; ++j) {
       const int k = k0 + j * 256;
       if (k < Kd) {
-        float af[2][8];
+        float af[NR][8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NR; ++h) {
           const uint32_t aw[4] = {av[h][j].x, av[h][j].y, av[h][j].z, av[h][j].w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
@@ -1309,12 +1311,60 @@ __device__ __forceinline__ void gemv_dot2(const uint16_t* __restrict__ arow0, co
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const float x0 = __uint_as_float(xw[w] << 16), x1 = __uint_as_float(xw[w] & 0xffff0000u);
-            acc0[i] = fmaf(af[0][2 * w], x0, acc0[i]);
-            acc0[i] = fmaf(af[0][2 * w + 1], x1, acc0[i]);
-            acc1[i] = fmaf(af[1][2 * w], x0, acc1[i]);
-            acc1[i] = fmaf(af[1][2 * w + 1], x1, acc1[i]);
+#pragma unroll
+            for (int h = 0; h < NR; ++h) {
+              acc[h][i] = fmaf(af[h][2 * w], x0, acc[h][i]);
+              acc[h][i] = fmaf(af[h][2 * w + 1], x1, acc[h][i]);
+            }
           }
         }
+      }
+    }
+  }
+}
+
+// One warp's share of a bucket's rank rows, NR at a time: the dots with the m
+// member rows, scaled by sc, into zv[(g * R16 + q) * kGemvRows + member].
+template <int NG, int NR, int KB>
+__device__ __forceinline__ void gemv_rows(const uint16_t* __restrict__ a, const uint16_t* xr, int Kp, int Kd, int l,
+                                          int e, int E, int R, int R16, int r, int m, float sc, int warp, int lane,
+                                          float* zv) {
+  constexpr int kWarps = kGemvThreads / 32;
+  const int nrows = NG * r;
+  for (int task = NR * warp; task < nrows; task += NR * kWarps) {
+    const uint16_t* arow[NR];
+    int gq[NR];
+#pragma unroll
+    for (int h = 0; h < NR; ++h) {
+      const int t = task + h < nrows ? task + h : task;  // past the end: repeat the first row
+      const int g = t / r, q = t - g * r;
+      gq[h] = g * R16 + q;
+      arow[h] = a + ((((int64_t)l * E + e) * NG + g) * R + q) * (int64_t)Kd;
+    }
+    float acc[NR][kGemvRows];
+#pragma unroll
+    for (int h = 0; h < NR; ++h)
+#pragma unroll
+      for (int i = 0; i < kGemvRows; ++i) acc[h][i] = 0.f;
+    static_assert(kGemvRows == 4, "one case per member count");
+    switch (m) {  // uniform per CTA
+      case 1: gemv_dot<1, NR, KB>(arow, xr, Kp, Kd, lane, acc); break;
+      case 2: gemv_dot<2, NR, KB>(arow, xr, Kp, Kd, lane, acc); break;
+      case 3: gemv_dot<3, NR, KB>(arow, xr, Kp, Kd, lane, acc); break;
+      default: gemv_dot<4, NR, KB>(arow, xr, Kp, Kd, lane, acc); break;
+    }
+#pragma unroll
+    for (int h = 0; h < NR; ++h) {
+#pragma unroll
+      for (int i = 0; i < kGemvRows; ++i)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[h][i] += __shfl_xor_sync(0xffffffffu, acc[h][i], o);
+      if (lane < kGemvRows) {
+        float v = acc[h][0];
+#pragma unroll
+        for (int i = 1; i < kGemvRows; ++i)
+          if (lane == i) v = acc[h][i];
+        zv[gq[h] * kGemvRows + lane] = sc * v;
       }
     }
   }
@@ -1323,7 +1373,8 @@ __device__ __forceinline__ void gemv_dot2(const uint16_t* __restrict__ arow0, co
 // CUDA-core shrink of buckets with at most kGemvRows pairs (NG rank blocks of
 // LoRA A per adapter: 2 gate|up, 1 down).  One block per bucket (grid-stride
 // over the listed buckets): the member rows are staged once in shared memory;
-// each warp streams two rank rows of A at a time against them; then the block
+// each warp streams two (four, for short rows) rank rows of A at a time
+// against them; then the block
 // writes the bucket's whole z region with 16-byte stores (8 rank columns of
 // one row each): s_l * dot for member rows and ranks q < r, zeros elsewhere.
 // Dynamic shared memory: the member rows [kGemvRows][Kp] bf16, then the dots
@@ -1334,7 +1385,6 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
                    const uint16_t* __restrict__ a, const uint16_t* __restrict__ rows, int Kd, int64_t cap,
                    int E, int R, int R16, const int32_t* __restrict__ lora_ranks,
                    const float* __restrict__ scalings, uint16_t* __restrict__ z, int64_t zcap) {
-  constexpr int kWarps = kGemvThreads / 32;
   extern __shared__ __align__(16) uint8_t gemv_smem[];
   const int Kp = (Kd + 63) & ~63, kp8 = Kp / 8;
   uint16_t* xr = reinterpret_cast<uint16_t*>(gemv_smem);                      // [kGemvRows][Kp]
@@ -1357,41 +1407,10 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
           *reinterpret_cast<const uint4*>(rows + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8);
     }
     __syncthreads();
-    const int nrows = NG * r;
-    for (int task = 2 * warp; task < nrows; task += 2 * kWarps) {
-      const int t1 = task + 1 < nrows ? task + 1 : task;
-      const int g0 = task / r, q0 = task - g0 * r, g1 = t1 / r, q1 = t1 - g1 * r;
-      const uint16_t* arow0 = a + ((((int64_t)l * E + e) * NG + g0) * R + q0) * (int64_t)Kd;
-      const uint16_t* arow1 = a + ((((int64_t)l * E + e) * NG + g1) * R + q1) * (int64_t)Kd;
-      float acc0[kGemvRows], acc1[kGemvRows];
-#pragma unroll
-      for (int i = 0; i < kGemvRows; ++i) acc0[i] = acc1[i] = 0.f;
-      static_assert(kGemvRows == 4, "one case per member count");
-      switch (m) {  // uniform per CTA
-        case 1: gemv_dot2<1>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
-        case 2: gemv_dot2<2>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
-        case 3: gemv_dot2<3>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
-        default: gemv_dot2<4>(arow0, arow1, xr, Kp, Kd, lane, acc0, acc1); break;
-      }
-#pragma unroll
-      for (int i = 0; i < kGemvRows; ++i)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          acc0[i] += __shfl_xor_sync(0xffffffffu, acc0[i], o);
-          acc1[i] += __shfl_xor_sync(0xffffffffu, acc1[i], o);
-        }
-      if (lane < kGemvRows) {
-        float v0 = acc0[0], v1 = acc1[0];
-#pragma unroll
-        for (int i = 1; i < kGemvRows; ++i)
-          if (lane == i) {
-            v0 = acc0[i];
-            v1 = acc1[i];
-          }
-        zv[(g0 * R16 + q0) * kGemvRows + lane] = sc * v0;
-        zv[(g1 * R16 + q1) * kGemvRows + lane] = sc * v1;
-      }
-    }
+    // short rows (down shape, I <= 1024): four rank rows per warp at a time,
+    // else two; either way about 6-8 KB of A in flight per warp
+    if (Kd <= 1024) gemv_rows<NG, 4, 4>(a, xr, Kp, Kd, l, e, E, R, R16, r, m, sc, warp, lane, zv);
+    else gemv_rows<NG, 2, 8>(a, xr, Kp, Kd, l, e, E, R, R16, r, m, sc, warp, lane, zv);
     __syncthreads();
     // the bucket's z region: N rows x (NG * r16 / 8) chunks of 8 rank columns
     const int cpg = r16 / 8, nchunk = NG * cpg;
