@@ -81,6 +81,12 @@ def _load():
                                                  vp, i64, vp, ctypes.c_int]
             lib.oracle_e4m3_value.restype = ctypes.c_double
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint32]
+            lib.oracle_forward_fp8_w8a8.restype = ctypes.c_int
+            lib.oracle_forward_fp8_w8a8.argtypes = lib.oracle_forward_fp8.argtypes
+            lib.oracle_e4m3_round.restype = ctypes.c_double
+            lib.oracle_e4m3_round.argtypes = [ctypes.c_double]
+            lib.oracle_mx_group_exp.restype = ctypes.c_int
+            lib.oracle_mx_group_exp.argtypes = [ctypes.c_double]
             lib.oracle_lora_linear.restype = ctypes.c_int
             lib.oracle_lora_linear.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                                i64, i64, i64, i64, i64, i64, vp, vp, i64, vp, ctypes.c_int]
@@ -314,6 +320,48 @@ def forward_int8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scal
         c["x"][0], c["x"][1], c["topk_ids"].ctypes.data, c["topk_weights"].ctypes.data, c["mapping"].ctypes.data,
         c["lora_ranks"].ctypes.data, c["scalings"].ctypes.data, wq.ctypes.data, ws.ctypes.data,
         dq.ctypes.data, ds.ctypes.data, ops[0][0], ops[1][0], ops[2][0], ops[3][0], c["ldt"],
+        T, K, E, H, I, L, R, c["tok_ptr"], c["n_out"], y.ctypes.data, int(threads))
+    return int(st), y
+
+
+def e4m3_round(v: float) -> float:
+    """The nearest E4M3 value to v (ties to even); |v| <= 448."""
+    return float(_load().oracle_e4m3_round(float(v)))
+
+
+def mx_group_exp(amax: float) -> int:
+    """The power-of-two scale exponent of a 128-element group with largest magnitude amax."""
+    return int(_load().oracle_mx_group_exp(float(amax)))
+
+
+def forward_fp8_w8a8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                     w_gate_up_q, w_gate_up_exp, w_down_q, w_down_exp,
+                     lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens=None, threads: int = 0):
+    """The layer on FP8 tensor cores: W8A8 with power-of-two block scales.  Returns (status, y) float64.
+
+    w_gate_up_q [E,2I,H] and w_down_q [E,H,I] hold E4M3 codes (uint8 bytes);
+    w_gate_up_exp [E,ceil(2I/128),ceil(H/128)] and w_down_exp
+    [E,ceil(H/128),ceil(I/128)] the biased exponent e of each 128 x 128 block
+    (scale 2^(e-127)).  x and the intermediate are quantised per token and
+    128-channel group before the base GEMMs; the LoRA paths read them unquantised.
+    """
+    c = _quant_common(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                      lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, tokens)
+    wq = np.ascontiguousarray(np.asarray(w_gate_up_q).view(np.uint8))
+    dq = np.ascontiguousarray(np.asarray(w_down_q).view(np.uint8))
+    T, H, K, E, L, R = c["T"], c["H"], c["K"], c["E"], c["L"], c["R"]
+    I = wq.shape[1] // 2
+    assert wq.shape == (E, 2 * I, H) and dq.shape == (E, H, I)
+    we = np.ascontiguousarray(np.asarray(w_gate_up_exp, dtype=np.uint8))
+    de = np.ascontiguousarray(np.asarray(w_down_exp, dtype=np.uint8))
+    assert we.shape == (E, (2 * I + 127) // 128, (H + 127) // 128)
+    assert de.shape == (E, (H + 127) // 128, (I + 127) // 128)
+    y = np.zeros((c["n_out"], H), dtype=np.float64)
+    ops = c["ops"]
+    st = _load().oracle_forward_fp8_w8a8(
+        c["x"][0], c["x"][1], c["topk_ids"].ctypes.data, c["topk_weights"].ctypes.data, c["mapping"].ctypes.data,
+        c["lora_ranks"].ctypes.data, c["scalings"].ctypes.data, wq.ctypes.data, we.ctypes.data,
+        dq.ctypes.data, de.ctypes.data, ops[0][0], ops[1][0], ops[2][0], ops[3][0], c["ldt"],
         T, K, E, H, I, L, R, c["tok_ptr"], c["n_out"], y.ctypes.data, int(threads))
     return int(st), y
 

@@ -47,6 +47,17 @@
  *     code value x scale (the DeepSeek-V3 checkpoint layout, inverse scales
  *     [E, ceil(rows/128), ceil(cols/128)]).  Activations, LoRA A and B stay
  *     bf16; only the base weights are quantised.
+ *   - FP8 on FP8 tensor cores (W8A8, MX-style scaling): E4M3 expert weights
+ *     whose 128 x 128 block scales are powers of two, stored as biased 8-bit
+ *     exponents (UE8M0: scale = 2^(e - 127)); the activations that feed the
+ *     base GEMMs are quantised too, per token and group of 128 channels, with
+ *     a power-of-two scale 2^s, s the smallest integer with
+ *     max|group| x 2^-s <= 448 (clamped to [-127, 127]; 0 for an all-zero
+ *     group), each element rounded to the nearest E4M3 value (ties to even).
+ *     x is quantised from its bf16 value; the intermediate a = SiLU(g) * u is
+ *     first rounded to bf16 (the stored intermediate) and then quantised the
+ *     same way for the down GEMM.  The LoRA shrinks read the unquantised
+ *     (bf16) x and a.
  *
  * Parity pins (see tests/test_oracle_*.py): the worked mapping example of
  * [PR24160]; torch.repeat_interleave on random segments; brute-force sorted()
@@ -56,7 +67,10 @@
  * for FP8 experts, the E4M3 decoder against the format's defining values and
  * torch's float8_e4m3fn for all 256 codes, and the layer against the fp64
  * forward on weights dequantised with numpy (unit and power-of-two block
- * scales, ragged and gate/up-shared blocks).
+ * scales, ragged and gate/up-shared blocks); for the W8A8 layer, the E4M3
+ * rounding against torch's float8 cast on every tie, the group exponent
+ * against ceil(log2(amax / 448)), and the layer against a torch float64
+ * re-derivation with planted mistakes that must change it.
  */
 #include <math.h>
 #include <stdint.h>
@@ -245,13 +259,15 @@ double oracle_e4m3_value(uint32_t code) {
  *     byte j, element 2j+1 in the high nibble), with a scale and a zero point
  *     (0..15) per row and group of 128 columns:
  *     value = (code - zero[e][row][col / 128]) x scale[e][row][col / 128].
+ *   5 FP8 E4M3 codes with power-of-two block scales given as biased exponents:
+ *     value = code x 2^(ex[e][row / 128][col / 128] - 127).
  */
 typedef struct {
   const void* p;
   int dtype;
   const float* scale;
   int64_t rows, cols;
-  const uint8_t* zero;  /* dtype 4 only */
+  const uint8_t* zero;  /* dtype 4: zero points; dtype 5: block exponents */
 } WeightView;
 
 static double ld_w(const WeightView* v, int64_t e, int64_t row, int64_t col) {
@@ -263,6 +279,11 @@ static double ld_w(const WeightView* v, int64_t e, int64_t row, int64_t col) {
     if (v->dtype == 2) return oracle_e4m3_value(code) * sc;
     return (double)(code < 128 ? (int)code : (int)code - 256) * sc;
   }
+  if (v->dtype == 5) {
+    const int64_t rb = (v->rows + 127) / 128, cb = (v->cols + 127) / 128;
+    const int ex = (int)v->zero[(e * rb + row / 128) * cb + col / 128];
+    return ldexp(oracle_e4m3_value(((const uint8_t*)v->p)[idx]), ex - 127);
+  }
   if (v->dtype == 4) {
     const int64_t gpr = (v->cols + 127) / 128;  /* groups per row */
     const uint8_t byte = ((const uint8_t*)v->p)[(e * v->rows + row) * (v->cols / 2) + col / 2];
@@ -271,6 +292,68 @@ static double ld_w(const WeightView* v, int64_t e, int64_t row, int64_t col) {
     return (double)(code - (int)v->zero[g]) * (double)v->scale[g];
   }
   return ld(v->p, v->dtype, idx);
+}
+
+/*
+ * The nearest E4M3 value to v (ties to even), for |v| <= 448: normal values
+ * 2^e x 1.mmm (e >= -6) are spaced 2^(e-3); below 2^-6 the subnormals are
+ * spaced 2^-9.  rint rounds to nearest, ties to even.
+ */
+double oracle_e4m3_round(double v) {
+  const double a = fabs(v);
+  if (a == 0.0) return v;
+  int E;
+  frexp(a, &E);          /* a in [2^(E-1), 2^E) */
+  int e = E - 1;
+  if (e < -6) e = -6;
+  const double step = ldexp(1.0, e - 3);
+  const double q = rint(a / step) * step;
+  return v < 0.0 ? -q : q;
+}
+
+/*
+ * The power-of-two scale exponent of a group whose largest magnitude is amax:
+ * the smallest integer s with amax x 2^-s <= 448, clamped to [-127, 127];
+ * 0 for amax == 0.
+ */
+int oracle_mx_group_exp(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int E;
+  frexp(amax, &E);
+  int s = E - 9;  /* amax x 2^-s in [2^8, 2^9) */
+  while (ldexp(amax, -s) > 448.0) ++s;
+  while (ldexp(amax, -(s - 1)) <= 448.0) --s;
+  if (s < -127) s = -127;
+  if (s > 127) s = 127;
+  return s;
+}
+
+/* The nearest bf16 value to v (ties to even): 8 significant bits, spacing
+ * 2^-133 below 2^-126. */
+static double bf16_round(double v) {
+  const double a = fabs(v);
+  if (a == 0.0) return v;
+  int E;
+  frexp(a, &E);
+  int e = E - 1;
+  if (e < -126) e = -126;
+  const double step = ldexp(1.0, e - 7);
+  const double q = rint(a / step) * step;
+  return v < 0.0 ? -q : q;
+}
+
+/* q[0..n) = v quantised per group of 128 consecutive elements (the last group
+ * may be shorter) and dequantised: E4M3(v x 2^-s) x 2^s, s from the group's
+ * largest magnitude. */
+static void quant_groups(const double* v, double* q, int64_t n) {
+  for (int64_t g0 = 0; g0 < n; g0 += 128) {
+    const int64_t g1 = g0 + 128 < n ? g0 + 128 : n;
+    double amax = 0.0;
+    for (int64_t i = g0; i < g1; ++i)
+      if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    const int s = oracle_mx_group_exp(amax);
+    for (int64_t i = g0; i < g1; ++i) q[i] = ldexp(oracle_e4m3_round(ldexp(v[i], -s)), s);
+  }
 }
 
 /*
@@ -293,7 +376,7 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
                         const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
                         int w_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
                         int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
-                        int num_threads) {
+                        int num_threads, int act_q) {
   if (T < 0 || K < 1 || E < 1 || H < 1 || I < 1 || L < 0 || R < 0 || n_out < 0)
     return ORC_INVALID;
   for (int64_t l = 0; l < L; ++l)
@@ -319,7 +402,10 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
     double* zg = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
     double* zu = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
     double* zd = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1));
-    const int ok = xv && a && zg && zu && zd;
+    /* act_q: the quantised x and a that feed the base GEMMs */
+    double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+    double* aq = (double*)malloc(sizeof(double) * (size_t)I);
+    const int ok = xv && a && zg && zu && zd && xq && aq;
 #pragma omp for schedule(dynamic, 1)
     for (int64_t j = 0; j < n_out; ++j) {
       if (!ok) {
@@ -332,6 +418,8 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
         double* yrow = y + j * H;
         for (int64_t h = 0; h < H; ++h) yrow[h] = 0.0;
         for (int64_t h = 0; h < H; ++h) xv[h] = ld(x, x_dtype, t * H + h);
+        if (act_q) quant_groups(xv, xq, H);
+        const double* xb = act_q ? xq : xv;  /* the base GEMMs' input */
 
         const int32_t l = token_lora_mapping[t];
         const int used = (l >= 0) && (lora_ranks[l] > 0);
@@ -359,8 +447,8 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
           for (int64_t i = 0; i < I; ++i) {
             double g = 0.0, u = 0.0;
             for (int64_t h = 0; h < H; ++h) {
-              g += ld_w(wgu, e, i, h) * xv[h];
-              u += ld_w(wgu, e, I + i, h) * xv[h];
+              g += ld_w(wgu, e, i, h) * xb[h];
+              u += ld_w(wgu, e, I + i, h) * xb[h];
             }
             if (r > 0) {
               const int64_t bg = (((l * E + e) * 2 + 0) * I + i) * R;
@@ -375,6 +463,12 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
             }
             a[i] = silu(g) * u;
           }
+          /* act_q: a is stored as bf16, and the down GEMM reads it quantised */
+          if (act_q) {
+            for (int64_t i = 0; i < I; ++i) a[i] = bf16_round(a[i]);
+            quant_groups(a, aq, I);
+          }
+          const double* ab = act_q ? aq : a;
 
           /* LoRA shrink for down: zd = A_d a */
           for (int64_t q = 0; q < r; ++q) {
@@ -387,7 +481,7 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
           /* down projection with its LoRA delta, weighted into y */
           for (int64_t h = 0; h < H; ++h) {
             double d = 0.0;
-            for (int64_t i = 0; i < I; ++i) d += ld_w(wdn, e, h, i) * a[i];
+            for (int64_t i = 0; i < I; ++i) d += ld_w(wdn, e, h, i) * ab[i];
             if (r > 0) {
               const int64_t bd = ((l * E + e) * H + h) * R;
               double dd = 0.0;
@@ -399,7 +493,7 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
         }
       }
     }
-    free(xv); free(a); free(zg); free(zu); free(zd);
+    free(xv); free(a); free(zg); free(zu); free(zd); free(xq); free(aq);
   }
   return status;
 }
@@ -417,7 +511,7 @@ int oracle_forward(const void* x, int x_dtype, const int32_t* topk_ids,
   const WeightView wdn = {w_down, w_dtype, NULL, H, I, NULL};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, w_dtype, T, K, E, H, I, L, R,
-                      tokens, n_out, y, num_threads);
+                      tokens, n_out, y, num_threads, 0);
 }
 
 /*
@@ -443,7 +537,7 @@ int oracle_forward_fp8(const void* x, int x_dtype, const int32_t* topk_ids,
   const WeightView wdn = {w_down_q, 2, w_down_scale, H, I, NULL};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
-                      R, tokens, n_out, y, num_threads);
+                      R, tokens, n_out, y, num_threads, 0);
 }
 
 /*
@@ -468,7 +562,7 @@ int oracle_forward_int8(const void* x, int x_dtype, const int32_t* topk_ids,
   const WeightView wdn = {w_down_q, 3, w_down_scale, H, I, NULL};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
-                      R, tokens, n_out, y, num_threads);
+                      R, tokens, n_out, y, num_threads, 0);
 }
 
 /*
@@ -496,7 +590,36 @@ int oracle_forward_w4a16(const void* x, int x_dtype, const int32_t* topk_ids,
   const WeightView wdn = {w_down_q, 4, w_down_scale, H, I, w_down_zero};
   return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
                       &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
-                      R, tokens, n_out, y, num_threads);
+                      R, tokens, n_out, y, num_threads, 0);
+}
+
+/*
+ * The same layer on the FP8 tensor cores (W8A8 with power-of-two block
+ * scales; [PR22323] 功能与动机 and 实现拆解 item 1 name the FP8 method, the
+ * format is a reading): w_gate_up_q [E, 2I, H] and w_down_q [E, H, I] hold
+ * E4M3 codes; w_gate_up_exp [E, ceil(2I/128), ceil(H/128)] and w_down_exp
+ * [E, ceil(H/128), ceil(I/128)] the biased exponent e of each 128 x 128
+ * block (scale 2^(e - 127), e < 255).  x and the intermediate a are
+ * quantised per token and 128-channel group before the base GEMMs (see the
+ * readings above); the LoRA paths read them unquantised.
+ */
+int oracle_forward_fp8_w8a8(const void* x, int x_dtype, const int32_t* topk_ids,
+                            const float* topk_weights, const int32_t* token_lora_mapping,
+                            const int32_t* lora_ranks, const float* scalings,
+                            const uint8_t* w_gate_up_q, const uint8_t* w_gate_up_exp,
+                            const uint8_t* w_down_q, const uint8_t* w_down_exp, const void* lora_a_gu,
+                            const void* lora_b_gu, const void* lora_a_down, const void* lora_b_down,
+                            int lora_dtype, int64_t T, int64_t K, int64_t E, int64_t H, int64_t I,
+                            int64_t L, int64_t R, const int64_t* tokens, int64_t n_out, double* y,
+                            int num_threads) {
+  if (lora_dtype != 0 && lora_dtype != 1) return ORC_INVALID;
+  if (w_gate_up_q == NULL || w_gate_up_exp == NULL || w_down_q == NULL || w_down_exp == NULL)
+    return ORC_INVALID;
+  const WeightView wgu = {w_gate_up_q, 5, NULL, 2 * I, H, w_gate_up_exp};
+  const WeightView wdn = {w_down_q, 5, NULL, H, I, w_down_exp};
+  return forward_impl(x, x_dtype, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, &wgu,
+                      &wdn, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, lora_dtype, T, K, E, H, I, L,
+                      R, tokens, n_out, y, num_threads, 1);
 }
 
 /* ------------------------------------------------------------------------ */
