@@ -57,7 +57,10 @@
  *     x is quantised from its bf16 value; the intermediate a = SiLU(g) * u is
  *     first rounded to bf16 (the stored intermediate) and then quantised the
  *     same way for the down GEMM.  The LoRA shrinks read the unquantised
- *     (bf16) x and a.
+ *     (bf16) x and a.  Since a's quantisation (an integer decision) depends
+ *     on the LoRA delta, this layer takes it at the kernels' precision: the
+ *     scaled LoRA intermediates s_l * (A x) and s_l * (A_d a) are rounded to
+ *     bf16 before B multiplies them, as the GPU stores them.
  *
  * Parity pins (see tests/test_oracle_*.py): the worked mapping example of
  * [PR24160]; torch.repeat_interleave on random segments; brute-force sorted()
@@ -430,7 +433,8 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
           const int64_t e = topk_ids[t * K + k];
           const double w = (double)topk_weights[t * K + k];
 
-          /* LoRA shrink for gate and up: z = A x (first r rows only) */
+          /* LoRA shrink for gate and up: z = A x (first r rows only); act_q:
+           * s * z rounded to bf16 (s is then not applied again below) */
           for (int64_t q = 0; q < r; ++q) {
             const int64_t ag = (((l * E + e) * 2 + 0) * R + q) * H;
             const int64_t au = (((l * E + e) * 2 + 1) * R + q) * H;
@@ -439,9 +443,10 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
               sg += ld(lora_a_gu, w_dtype, ag + h) * xv[h];
               su += ld(lora_a_gu, w_dtype, au + h) * xv[h];
             }
-            zg[q] = sg;
-            zu[q] = su;
+            zg[q] = act_q ? bf16_round(s * sg) : sg;
+            zu[q] = act_q ? bf16_round(s * su) : su;
           }
+          const double sb = act_q ? 1.0 : s;  /* the scaling still to apply after B */
 
           /* gate and up projections, each with its own LoRA delta; SiLU(g) * u */
           for (int64_t i = 0; i < I; ++i) {
@@ -458,8 +463,8 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
                 dg += ld(lora_b_gu, w_dtype, bg + q) * zg[q];
                 du += ld(lora_b_gu, w_dtype, bu + q) * zu[q];
               }
-              g += s * dg;
-              u += s * du;
+              g += sb * dg;
+              u += sb * du;
             }
             a[i] = silu(g) * u;
           }
@@ -475,7 +480,7 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
             const int64_t ad = ((l * E + e) * R + q) * I;
             double sd = 0.0;
             for (int64_t i = 0; i < I; ++i) sd += ld(lora_a_down, w_dtype, ad + i) * a[i];
-            zd[q] = sd;
+            zd[q] = act_q ? bf16_round(s * sd) : sd;
           }
 
           /* down projection with its LoRA delta, weighted into y */
@@ -486,7 +491,7 @@ static int forward_impl(const void* x, int x_dtype, const int32_t* topk_ids,
               const int64_t bd = ((l * E + e) * H + h) * R;
               double dd = 0.0;
               for (int64_t q = 0; q < r; ++q) dd += ld(lora_b_down, w_dtype, bd + q) * zd[q];
-              d += s * dd;
+              d += sb * dd;
             }
             yrow[h] += w * d;
           }

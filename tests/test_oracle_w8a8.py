@@ -7,7 +7,10 @@ powers of two (biased 8-bit exponents, scale 2^(e-127)), and activations
 quantised per token and 128-channel group with a power-of-two scale 2^s, s
 the smallest integer with max|group| x 2^-s <= 448, each element rounded to
 the nearest E4M3 value (ties to even).  The intermediate a = SiLU(g) * u is
-rounded to bf16 first; the LoRA shrinks read the unquantised x and a.
+rounded to bf16 first; the LoRA shrinks read the unquantised x and a.  The
+decision on a's codes depends on the LoRA delta, so this layer takes it at
+the kernels' precision: the scaled LoRA intermediates s * (A x) and
+s * (A_d a) are rounded to bf16 before B multiplies them.
 
 Pinned against things other than the oracle's own loops:
   * the E4M3 rounding against torch's float8_e4m3fn cast, on every tie
@@ -20,8 +23,8 @@ Pinned against things other than the oracle's own loops:
     rounding) and broadcasts the block exponents with repeat; ragged shapes
     leave partial groups, partial blocks and a block shared by gate and up;
   * planted mistakes in that re-derivation (x or a not quantised, LoRA fed
-    the quantised operands, the exponent one too large, a not rounded) must
-    each change the layer.
+    the quantised operands, the exponent one too large, a or z not rounded)
+    must each change the layer.
 """
 import numpy as np
 import pytest
@@ -121,10 +124,11 @@ def _torch_layer(d, wq, we, dq, de, mistake=None):
         for k in range(topk.shape[1]):
             e = int(topk[t, k])
             g, u = Wgu[e, :I] @ xq, Wgu[e, I:] @ xq
+            zr = (lambda z: s * z) if mistake == "no_zround" else (lambda z: _to_bf16_direct((s * z).numpy()))
             if r > 0:
                 xl = xq if mistake == "lora_q" else xv
-                g = g + s * (Bgu[l, e, 0, :, :r] @ (Agu[l, e, 0, :r] @ xl))
-                u = u + s * (Bgu[l, e, 1, :, :r] @ (Agu[l, e, 1, :r] @ xl))
+                g = g + Bgu[l, e, 0, :, :r] @ zr(Agu[l, e, 0, :r] @ xl)
+                u = u + Bgu[l, e, 1, :, :r] @ zr(Agu[l, e, 1, :r] @ xl)
             a = F.silu(g) * u
             if mistake != "no_bf16":
                 a = _to_bf16_direct(a.numpy())
@@ -132,7 +136,7 @@ def _torch_layer(d, wq, we, dq, de, mistake=None):
             dd = Wd[e] @ aq
             if r > 0:
                 al = aq if mistake == "lora_q" else a
-                dd = dd + s * (Bd[l, e, :, :r] @ (Ad[l, e, :r] @ al))
+                dd = dd + Bd[l, e, :, :r] @ zr(Ad[l, e, :r] @ al)
             y[t] += float(w[t, k]) * dd
     return y.numpy()
 
@@ -162,7 +166,7 @@ def test_layer_matches_torch_rederivation(H, I):
     assert st == oracle.OK
     ref = _torch_layer(d, wq, we, dq, de)
     np.testing.assert_allclose(y, ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
-    for mistake in ("no_xq", "no_hq", "lora_q", "exp_off", "no_bf16"):
+    for mistake in ("no_xq", "no_hq", "lora_q", "exp_off", "no_bf16", "no_zround"):
         bad = _torch_layer(d, wq, we, dq, de, mistake)
         assert np.abs(bad - y).max() > 1e-6 * np.abs(y).max(), mistake
 
