@@ -309,7 +309,10 @@ def layer_work(cfg, batch, mapping, fp8=False, fmt=None):
     fmt (or fp8=True for "fp8"): the base expert weights' format.  "fp8" and
     "int8": one byte per weight plus a float32 scale per 128 x 128 block;
     "w4a16": half a byte per weight plus a float32 scale and a one-byte zero
-    point per row and 128-column group.  LoRA operands and activations stay bf16.
+    point per row and 128-column group; "w8a8": one byte per weight plus a
+    one-byte exponent per 128 x 128 block.  LoRA operands and the layer's
+    input and output stay bf16 (the quantised activation copies are
+    implementation traffic, not counted).
     """
     fmt = fmt or ("fp8" if fp8 else "bf16")
     import torch
@@ -332,6 +335,9 @@ def layer_work(cfg, batch, mapping, fp8=False, fmt=None):
     if fmt in ("fp8", "int8"):
         wgu = 2 * H * I + 4 * nb(2 * I) * nb(H)
         wdn = H * I + 4 * nb(H) * nb(I)
+    elif fmt == "w8a8":
+        wgu = 2 * H * I + nb(2 * I) * nb(H)
+        wdn = H * I + nb(H) * nb(I)
     elif fmt == "w4a16":
         wgu = H * I + 5 * 2 * I * nb(H)
         wdn = H * I // 2 + 5 * H * nb(I)
@@ -370,7 +376,7 @@ def make_inputs(cfg_name, device, seed, fmt="bf16"):
     w = workloads.make_weights(cfg, b.lora_ranks, device=device, seed=seed)
     x = workloads.make_x(cfg, device=device, seed=seed)
     make = {"fp8": workloads.make_fp8_experts, "int8": workloads.make_int8_experts,
-            "w4a16": workloads.make_w4a16_experts}.get(fmt)
+            "w4a16": workloads.make_w4a16_experts, "w8a8": workloads.make_fp8_w8a8_experts}.get(fmt)
     q = make(cfg, device=device, seed=seed) if make else None
     return cfg, b, w, x, q
 
@@ -378,7 +384,16 @@ def make_inputs(cfg_name, device, seed, fmt="bf16"):
 QUANT_KEYS = {"fp8": ("w_gate_up_q", "w_gate_up_scale", "w_down_q", "w_down_scale"),
               "int8": ("w_gate_up_q", "w_gate_up_scale", "w_down_q", "w_down_scale"),
               "w4a16": ("w_gate_up_q", "w_gate_up_scale", "w_gate_up_zero", "w_down_q", "w_down_scale",
-                        "w_down_zero")}
+                        "w_down_zero"),
+              "w8a8": ("w_gate_up_q", "w_gate_up_exp", "w_down_q", "w_down_exp")}
+# The FP8 tensor cores' dense peak: the measured bf16 peak times the nominal
+# FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s).
+FP8_OVER_BF16 = 2.0
+
+
+def peak_kind_of(fmt):
+    """The tensor peak a format's base GEMMs run against."""
+    return "fp8_tflops" if fmt == "w8a8" else PEAK_KIND
 
 
 def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None, seed=0, q=None, fmt="bf16"):
@@ -394,7 +409,8 @@ def oracle_sample_rate(cfg, b, w, x, mapping_np, target_s=10.0, max_tokens=None,
         fwd = oracle.forward
         host = [bits(w.w_gate_up), bits(w.w_down)] + lora
     else:
-        fwd = {"fp8": oracle.forward_fp8, "int8": oracle.forward_int8, "w4a16": oracle.forward_w4a16}[fmt]
+        fwd = {"fp8": oracle.forward_fp8, "int8": oracle.forward_int8, "w4a16": oracle.forward_w4a16,
+               "w8a8": oracle.forward_fp8_w8a8}[fmt]
         host = [getattr(q, k).cpu().numpy() for k in QUANT_KEYS[fmt]] + lora
     xb = bits(x)
     ids = b.topk_ids.cpu().numpy()
@@ -480,11 +496,13 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
     enabled = torch.empty(L, dtype=torch.int32, device=dev)
     mapping = torch.empty(T, dtype=torch.int32, device=dev)
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(mlr.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R), dtype=torch.uint8, device=dev)
+    wsb = (mlr.fused_moe_lora_workspace_bytes_fp8_w8a8 if fmt == "w8a8" else mlr.fused_moe_lora_workspace_bytes)
+    ws = torch.empty(wsb(T, K, E, H, I, L, R), dtype=torch.uint8, device=dev)
     lk = {k: getattr(w, k) for k in ("lora_a_gu", "lora_b_gu", "lora_a_down", "lora_b_down")}
     if q is not None:
         forward = {"fp8": mlr.fused_moe_lora_forward_fp8, "int8": mlr.fused_moe_lora_forward_int8,
-                   "w4a16": mlr.fused_moe_lora_forward_w4a16}[fmt]
+                   "w4a16": mlr.fused_moe_lora_forward_w4a16,
+                   "w8a8": mlr.fused_moe_lora_forward_fp8_w8a8}[fmt]
         wk = dict({k: getattr(q, k) for k in QUANT_KEYS[fmt]}, **lk)
     else:
         forward = mlr.fused_moe_lora_forward
@@ -587,16 +605,18 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
                          f"OpenMP over tokens"}
 
     peaks, peak_src = load_peaks()
+    peaks["fp8_tflops"] = peaks[PEAK_KIND] * FP8_OVER_BF16
+    pk = peak_kind_of(fmt)
     ms_step = ms_max / args.steps
-    rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, PEAK_KIND)
+    rf = roofline_entry(st_work[dom][0], st_work[dom][1], dom_ms, peaks, pk)
     rf["kernel"] = STAGE_KERNELS.get(dom, dom)
     rf["stage"] = dom
-    rf["peak_source"] = peak_label(peak_src)
+    rf["peak_source"] = peak_label(peak_src, pk)
     rf["traffic"] = recorded_traffic(dom, cfg.name + ("" if fmt == "bf16" else "_" + fmt))
     rf["algorithmic_bytes"] = int(st_work[dom][1])
     rf["algorithmic_flops"] = int(st_work[dom][0])
     rf["launch_ms"] = round(dom_ms, 4)
-    layer = layer_fractions(flops, byts, ms_step, peaks)
+    layer = layer_fractions(flops, byts, ms_step, peaks, pk)
     entry = {"value": round(weak_scaling_rate(T, world, ms_step), 1), "unit": "tokens/s",
              "ms_per_step": round(ms_step, 4),
              "config": {"workload": cfg.name, "tokens": T, "hidden": H, "intermediate": I, "experts": E,
@@ -615,22 +635,24 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
     return entry
 
 
-def layer_fractions(flops, byts, ms_step, peaks):
+def layer_fractions(flops, byts, ms_step, peaks, peak_kind=PEAK_KIND):
     """The layer's roofline entry with both fractions: HBM (bytes) and the
-    dense bf16 tensor peak (FLOPs), the latter being the prefill bar."""
-    layer = roofline_entry(flops, byts, ms_step, peaks, PEAK_KIND)
+    dense tensor peak of the base GEMMs' type (FLOPs), the latter being the
+    prefill bar."""
+    layer = roofline_entry(flops, byts, ms_step, peaks, peak_kind)
     s = ms_step * 1e-3
     layer["hbm_frac"] = round(byts / s / 1e9 / peaks["hbm_gbs"], 4)
-    layer["tensor_frac"] = round(flops / s / 1e12 / peaks[PEAK_KIND], 4)
+    layer["tensor_frac"] = round(flops / s / 1e12 / peaks[peak_kind], 4)
     layer["roofline_ms"] = round(1e3 * max(byts / (peaks["hbm_gbs"] * 1e9),
-                                           flops / (peaks[PEAK_KIND] * 1e12)), 4)
+                                           flops / (peaks[peak_kind] * 1e12)), 4)
     layer["algorithmic_bytes"] = int(byts)
     layer["algorithmic_flops"] = int(flops)
     return layer
 
 
-def peak_label(src):
-    return f"{src} {PEAK_KIND} (MEASURED_PEAKS.json)" if src == "measured" else f"fallback {PEAK_KIND}"
+def peak_label(src, kind=PEAK_KIND):
+    base = f"{src} {PEAK_KIND} (MEASURED_PEAKS.json)" if src == "measured" else f"fallback {PEAK_KIND}"
+    return base if kind == PEAK_KIND else f"{base} x {FP8_OVER_BF16:g} (nominal FP8 / bf16 ratio)"
 
 
 def metadata_bytes(bs, L, T, P, npad, block_size):
@@ -784,7 +806,8 @@ def run_ours(args, rank, world, dist):
         return None
     line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8" if args.weights == "w8a8" else "bf16",
             "data": "synthetic",
             "config": dict(head["config"],
                            parallelism=f"dp{world} (replicas)" if world > 1 else "single GPU"),
@@ -805,7 +828,9 @@ LINEAR_CONFIGS = {
 }
 WEIGHT_LABEL = {"bf16": "bf16", "fp8": "fp8 e4m3, fp32 scale per 128x128 block (bf16 LoRA)",
                 "int8": "int8, fp32 scale per 128x128 block (bf16 LoRA)",
-                "w4a16": "uint4 two per byte, fp32 scale and uint8 zero point per row and 128 columns (bf16 LoRA)"}
+                "w4a16": "uint4 two per byte, fp32 scale and uint8 zero point per row and 128 columns (bf16 LoRA)",
+                "w8a8": "fp8 e4m3 weights and activations on the FP8 tensor cores, power-of-two scales per "
+                        "128x128 weight block and per token and 128 channels (bf16 LoRA)"}
 LINEAR_METRIC = "MLA fused-projection LoRA tokens/s and % of roofline (bf16, 1×GB300)"
 
 
@@ -1033,8 +1058,9 @@ def main(argv=None):
     ap.add_argument("--extras", default=DEFAULT_EXTRAS,
                     help="comma-separated workloads measured after the headline and reported under "
                          "'workloads' ('' for none)")
-    ap.add_argument("--weights", choices=["bf16", "fp8", "int8", "w4a16"], default="bf16",
-                    help="base expert weights of the MoE workloads: bf16, or FP8 E4M3 with 128x128 block scales")
+    ap.add_argument("--weights", choices=["bf16", "fp8", "int8", "w4a16", "w8a8"], default="bf16",
+                    help="base expert weights of the MoE workloads: bf16; FP8 E4M3, INT8 or UINT4 codes "
+                         "dequantised on chip; or w8a8: FP8 weights and activations on the FP8 tensor cores")
     ap.add_argument("--combine", choices=["atomic", "deterministic"], default="deterministic",
                     help="top-k combine of the MoE forward (the other one is timed beside it)")
     ap.add_argument("--seed", type=int, default=0)

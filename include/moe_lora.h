@@ -275,6 +275,45 @@ int fused_moe_lora_forward_w4a16(const mlr_bf16* x, const int32_t* topk_ids, con
                                  int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
                                  size_t ws_bytes, int32_t* d_status, void* stream);
 
+/* Scratch bytes fused_moe_lora_forward_fp8_w8a8 needs for these sizes (0 on bad
+ * sizes): fused_moe_lora_workspace_bytes plus the quantised activations. */
+size_t fused_moe_lora_workspace_bytes_fp8_w8a8(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                              int32_t hidden, int32_t intermediate, int32_t num_loras,
+                                              int32_t max_rank);
+
+/*
+ * fused_moe_lora_forward_fp8_w8a8 -- the layer on the FP8 tensor cores (sglang
+ * PR #22323 page, 功能与动机 and 实现拆解 item 1 name the FP8 method; the
+ * format is a reading): both base GEMMs multiply E4M3 weights by E4M3
+ * activations with power-of-two block scales, accumulating in fp32.
+ *
+ *   w_gate_up_q   uint8 [E, 2I, H]  E4M3 codes;  w_down_q uint8 [E, H, I]
+ *   w_gate_up_exp uint8 [E, ceil(2I/128), ceil(H/128)]  biased exponent e of
+ *                 each 128 x 128 block: weight = code value x 2^(e - 127)
+ *   w_down_exp    uint8 [E, ceil(H/128), ceil(I/128)]
+ * Exponent bytes must be below 255.  The activations that feed the base GEMMs
+ * are quantised on the way, per token (pair) and group of 128 channels: scale
+ * 2^s with s the smallest integer such that max|group| x 2^-s <= 448
+ * (clamped to [-127, 127]; 0 for an all-zero group), each value rounded to
+ * the nearest E4M3 value, ties to even.  x is quantised from its bf16 value,
+ * the gate_up output SiLU(g) * u after its rounding to bf16.  The LoRA
+ * shrinks read the unquantised bf16 x and gate_up output; LoRA stacks, y and
+ * every other argument are those of fused_moe_lora_forward, except the
+ * workspace size (fused_moe_lora_workspace_bytes_fp8_w8a8).  Additional
+ * limits: hidden and intermediate multiples of 16; both exponent arrays
+ * non-null (else MLR_ERR_INVALID).
+ */
+int fused_moe_lora_forward_fp8_w8a8(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
+                                    const int32_t* token_lora_mapping, const int32_t* lora_ranks,
+                                    const float* scalings, const uint8_t* w_gate_up_q,
+                                    const uint8_t* w_gate_up_exp, const uint8_t* w_down_q,
+                                    const uint8_t* w_down_exp, const mlr_bf16* lora_a_gu,
+                                    const mlr_bf16* lora_b_gu, const mlr_bf16* lora_a_down,
+                                    const mlr_bf16* lora_b_down, int32_t num_tokens, int32_t topk,
+                                    int32_t num_experts, int32_t hidden, int32_t intermediate,
+                                    int32_t num_loras, int32_t max_rank, mlr_bf16* y, void* workspace,
+                                    size_t ws_bytes, int32_t* d_status, void* stream);
+
 /* Scratch bytes lora_linear_forward needs for these sizes (0 on bad sizes). */
 size_t lora_linear_workspace_bytes(int32_t num_tokens, int32_t in_features, int32_t out_features,
                                    int32_t num_loras, int32_t max_rank, int32_t num_slices);

@@ -28,8 +28,8 @@ from . import _build
 
 __all__ = ["moe_lora_batch_info", "moe_lora_align", "moe_lora_align_capacity",
            "moe_lora_align_workspace_bytes", "fused_moe_lora_forward", "fused_moe_lora_forward_fp8",
-           "fused_moe_lora_forward_int8", "fused_moe_lora_forward_w4a16",
-           "fused_moe_lora_workspace_bytes", "lora_linear_forward", "lora_tp_qkv_b_rows", "tp_take_rows",
+           "fused_moe_lora_forward_int8", "fused_moe_lora_forward_w4a16", "fused_moe_lora_forward_fp8_w8a8",
+           "fused_moe_lora_workspace_bytes", "fused_moe_lora_workspace_bytes_fp8_w8a8", "lora_linear_forward", "lora_tp_qkv_b_rows", "tp_take_rows",
            "set_wait_limit_ns", "wait_limit_ns", "set_deterministic", "deterministic", "library", "library_path", "MoeLoraError", "STATUS_BITS"]
 
 MLR_OK = 0
@@ -112,6 +112,10 @@ def library() -> ctypes.CDLL:
                 lib.fused_moe_lora_forward_int8.argtypes = [vp] * 14 + [i32] * 7 + [vp, vp, sz, vp, vp]
                 lib.fused_moe_lora_forward_w4a16.restype = ctypes.c_int
                 lib.fused_moe_lora_forward_w4a16.argtypes = [vp] * 16 + [i32] * 7 + [vp, vp, sz, vp, vp]
+                lib.fused_moe_lora_workspace_bytes_fp8_w8a8.restype = sz
+                lib.fused_moe_lora_workspace_bytes_fp8_w8a8.argtypes = [i32] * 7
+                lib.fused_moe_lora_forward_fp8_w8a8.restype = ctypes.c_int
+                lib.fused_moe_lora_forward_fp8_w8a8.argtypes = [vp] * 14 + [i32] * 7 + [vp, vp, sz, vp, vp]
             if hasattr(lib, "lora_linear_forward"):
                 lib.lora_linear_workspace_bytes.restype = sz
                 lib.lora_linear_workspace_bytes.argtypes = [i32] * 6
@@ -439,7 +443,7 @@ def fused_moe_lora_forward_fp8(x, topk_ids, topk_weights, token_lora_mapping, lo
 
 def _quant_forward(fn_name, x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, quant,
                    lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, y, workspace, stream, check, status,
-                   I_of, code_shapes, side_shapes):
+                   I_of, code_shapes, side_shapes, ws_fn="fused_moe_lora_workspace_bytes"):
     """Shared marshalling of the quantised-expert forwards: `quant` is the list of
     (tensor, name, dtype) of the code / scale / zero arrays in C argument order;
     code_shapes(E, I, H) and side_shapes(E, I, H) give their expected shapes."""
@@ -475,7 +479,7 @@ def _quant_forward(fn_name, x, topk_ids, topk_weights, token_lora_mapping, lora_
     if y is None:
         y = torch.empty(T, H, dtype=bf, device=dev)
     _req(y, "y", bf, dev)
-    wsb = int(lib.fused_moe_lora_workspace_bytes(T, K, E, H, I, L, R))
+    wsb = int(getattr(lib, ws_fn)(T, K, E, H, I, L, R))
     if wsb == 0 and T > 0:
         raise ValueError(f"{fn_name}: unsupported sizes")
     if workspace is None:
@@ -534,6 +538,32 @@ def fused_moe_lora_forward_w4a16(x, topk_ids, topk_weights, token_lora_mapping, 
                           lambda E, I, H: [(E, 2 * I, H // 2), (E, 2 * I, cb(H)), (E, 2 * I, cb(H)),
                                            (E, H, I // 2), (E, H, cb(I)), (E, H, cb(I))],
                           lambda E, I, H: [])
+
+
+def fused_moe_lora_workspace_bytes_fp8_w8a8(T, K, E, H, I, L, R) -> int:
+    return int(library().fused_moe_lora_workspace_bytes_fp8_w8a8(T, K, E, H, I, L, R))
+
+
+@_on_stream
+def fused_moe_lora_forward_fp8_w8a8(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings,
+                                    w_gate_up_q, w_gate_up_exp, w_down_q, w_down_exp,
+                                    lora_a_gu, lora_b_gu, lora_a_down, lora_b_down,
+                                    y: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None, stream=None,
+                                    check: bool = True, status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The layer on the FP8 tensor cores: w_gate_up_q [E,2I,H] and w_down_q
+    [E,H,I] E4M3 codes (uint8), w_gate_up_exp [E,ceil(2I/128),ceil(H/128)] and
+    w_down_exp [E,ceil(H/128),ceil(I/128)] uint8 biased block exponents (scale
+    2^(e-127)); the activations of the base GEMMs are quantised per token and
+    128-channel group on the way (see the C header)."""
+    cb = lambda n: (n + 127) // 128  # noqa: E731
+    quant = [(w_gate_up_q, "w_gate_up_q", torch.uint8), (w_gate_up_exp, "w_gate_up_exp", torch.uint8),
+             (w_down_q, "w_down_q", torch.uint8), (w_down_exp, "w_down_exp", torch.uint8)]
+    return _quant_forward("fused_moe_lora_forward_fp8_w8a8", x, topk_ids, topk_weights, token_lora_mapping,
+                          lora_ranks, scalings, quant, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, y,
+                          workspace, stream, check, status, lambda w: w.shape[1] // 2,
+                          lambda E, I, H: [(E, 2 * I, H), (E, cb(2 * I), cb(H)), (E, H, I), (E, cb(H), cb(I))],
+                          lambda E, I, H: [], ws_fn="fused_moe_lora_workspace_bytes_fp8_w8a8")
 
 
 @_on_stream

@@ -65,8 +65,12 @@ constexpr uint64_t kCopyGraceNs = 1000000;  // after an abort: time for issued T
 enum Kind : int { kShrinkGU = 0, kGateUp = 1, kShrinkD = 2, kDown = 3 };
 // Base expert weight formats: bf16, or codes that converter warps dequantise
 // on chip -- FP8 E4M3 and INT8 with 128 x 128 block scales, UINT4 (two per
-// byte) with a scale and zero point per row and 128-column group.
-enum QFmt : int { kQNone = 0, kQFp8 = 1, kQInt8 = 2, kQU4 = 3 };
+// byte) with a scale and zero point per row and 128-column group -- or FP8
+// E4M3 with power-of-two block scales fed to the FP8 tensor cores as they are
+// (kQMx: block-scaled MMAs on E4M3 weights and E4M3-quantised activations).
+enum QFmt : int { kQNone = 0, kQFp8 = 1, kQInt8 = 2, kQU4 = 3, kQMx = 4 };
+// Formats that go through the converter warps.
+template <int QF> constexpr bool kConvOf = QF == kQFp8 || QF == kQInt8 || QF == kQU4;
 // Raw code bytes of one weight row per 64-wide K step.
 template <int QF> constexpr int kRawRowBytes = QF == kQU4 ? 32 : 64;
 
@@ -78,7 +82,7 @@ template <int KIND> constexpr int kThreadsOf = (kEpiWarp0 + kEpiWarps<KIND>) * 3
 // FP8-weight kernels add three converter warps after the epilogue (16 warps,
 // 512 threads): with warps 1-3 they are the six converter warps.
 constexpr int kCvWarps = 6;
-template <int KIND, bool Q> constexpr int kLaunchThreads = kThreadsOf<KIND> + (Q ? 96 : 0);
+template <int KIND, int QF> constexpr int kLaunchThreads = kThreadsOf<KIND> + (kConvOf<QF> ? 96 : 0);
 
 template <int KIND> struct Cfg;
 // The shrinks stage two 64-wide K chunks per ring slot (LoRA A in [0, 32 KB),
@@ -94,14 +98,34 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 6, kStageByte
 // each CTA loads half of every row tile, so the row bytes per SM drop by half.
 // The FP8-weight down GEMM runs on single CTAs: a pair would need a
 // cluster-scope release from the peer's converters at every K step.
-template <int KIND, bool Q = false> constexpr bool kPairOf = KIND == kDown && !Q;
+template <int KIND, int QF = kQNone> constexpr bool kPairOf = KIND == kDown && QF == kQNone;
 
 // Ring of a GEMM: the FP8 down GEMM on a single CTA stages its 128 weight rows
 // [0, 16 KB) and all of the tile's rows [16 KB, 48 KB).
-template <int KIND, bool Q> struct CfgOf : Cfg<KIND> {};
-template <> struct CfgOf<kDown, true> {
+template <int KIND, int QF> struct CfgOf : Cfg<KIND> {};
+template <> struct CfgOf<kDown, kQFp8> {
   static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256;
 };
+template <> struct CfgOf<kDown, kQInt8> : CfgOf<kDown, kQFp8> {};
+template <> struct CfgOf<kDown, kQU4> : CfgOf<kDown, kQFp8> {};
+// Block-scaled FP8 (kQMx): a K step is 128 E4M3 codes (128 bytes per row, the
+// bf16 kernels' 64 elements), so the stages keep their byte layout.  Tiles
+// are at most kMxTileRows rows, which leaves TMEM columns for the scale
+// factors after the accumulators: per stage kMxSfCols columns from column
+// kAccBufs * kAccCols (A scales of gate [0, 4) and up [4, 8) or of W_down
+// [0, 4), B scales [8, 16)).  down runs on single CTAs with the FP8 down
+// ring (the block-scaled MMA reads its scales from this CTA's TMEM).
+constexpr int kMxTileRows = 224;
+constexpr int kMxSfCols = 16;
+template <> struct CfgOf<kGateUp, kQMx> {
+  static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 2 * kMxTileRows;
+};
+template <> struct CfgOf<kDown, kQMx> {
+  static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = kMxTileRows;
+};
+template <int KIND, int QF> constexpr int kSfCol0 = CfgOf<KIND, QF>::kAccBufs * CfgOf<KIND, QF>::kAccCols;
+static_assert(kSfCol0<kGateUp, kQMx> + 3 * kMxSfCols <= 512 && kSfCol0<kDown, kQMx> + 4 * kMxSfCols <= 512,
+              "scale factors fit TMEM");
 
 // Tensor maps of one GEMM kind, by slot.
 //   all:     kW = weight rows (base GEMMs) / LoRA A in 64-row boxes (shrinks),
@@ -181,6 +205,14 @@ struct Params {
   const float* wscale;  // FP8 / INT8: [E][wsr][wsc] block scales (weight = code x scale);
                         // UINT4: [E][rows][wsc] group scales
   const uint8_t* wzero;   // UINT4: [E][rows][wsc] group zero points
+  // block-scaled FP8: weight block exponents [E][wsr][wsc] (scale 2^(e-127)),
+  // the B operand's per-row exponents [K/128][cap] (x for gate_up, h for
+  // down), and gate_up's outputs: h as E4M3 codes [I/128][cap][128] and its
+  // exponents [I/128][cap]
+  const uint8_t* wexp;
+  const uint8_t* sfx;
+  uint8_t* h8;
+  uint8_t* sh;
   int64_t P;
   uint64_t wait_ns;  // give-up limit of the pipeline waits
   const float* topk_weights;
@@ -214,11 +246,16 @@ struct __align__(16) Ctl {
   float w[2][kTileRows];
 };
 
-template <int KIND, bool Q = false>
+// Block-scaled FP8 gate_up: after Ctl, the column maxima of h that the lane
+// quarters of an epilogue half exchange, [half][chunk parity][quarter][32].
+template <int KIND, int QF> constexpr int kAmaxBytes = (KIND == kGateUp && QF == kQMx) ? 2 * 2 * 4 * 32 * 4 : 0;
+
+template <int KIND, int QF = kQNone>
 constexpr int smem_bytes() {
-  using CF = CfgOf<KIND, Q>;
+  using CF = CfgOf<KIND, QF>;
   static_assert(CF::kStages <= 8, "ring barriers");
-  return CF::kStages * CF::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) + 1024;
+  return CF::kStages * CF::kStageBytes + (kEpiWarps<KIND> / 4) * kEpiBytes + (int)sizeof(Ctl) +
+         kAmaxBytes<KIND, QF> + 1024;
 }
 
 // SiLU(v) = v * sigmoid(v), with sigmoid(v) = (1 + tanh(v / 2)) / 2: one
@@ -355,6 +392,46 @@ struct ExpandCursor {
   }
 };
 
+// Block-scaled FP8: the scale factors of one main step (K block kb), as the
+// four TMEM words of a lane: A scales of this lane's weight row (gate and up
+// rows for gate_up), B scales of tile rows 32 i + lane.  Every byte of a word
+// holds the same exponent, so the four K = 32 MMAs of the step (scale ids
+// 0..3) read the same value.  Loaded before the stage is free so that the
+// loads overlap the wait.
+struct SfWords {
+  uint32_t a0, a1, b[8];
+};
+template <int KIND>
+__device__ __forceinline__ void sf_load(const Params& p, const Item& it, int kb, int quarter, int lane, SfWords& v) {
+  const int r = it.mb * 128 + quarter * 32 + lane;  // row of the gate (up) block, or of W_down
+  uint32_t e0 = 127u, e1 = 127u;                    // rows past I / H read zero codes
+  if (KIND == kGateUp) {
+    if (r < p.I) {
+      e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
+      e1 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + (p.I + r) / 128) * p.wsc + kb);
+    }
+  } else if (r < p.H) {
+    e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
+  }
+  v.a0 = e0 * 0x01010101u;
+  v.a1 = e1 * 0x01010101u;
+  const uint8_t* sx = p.sfx + (int64_t)kb * p.cap + it.row0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = 32 * i + lane;
+    v.b[i] = (n < it.nrows ? (uint32_t)__ldg(sx + n) : 127u) * 0x01010101u;
+  }
+}
+// The words into this warp's lane quarter of the stage's scale-factor columns:
+// A scales in columns [0, 4) (gate / W_down) and [4, 8) (up) -- the MMA reads
+// row m's at column m / 32 of lane m --, B scales of rows 32 i + lane in
+// column 8 + i of every quarter.
+__device__ __forceinline__ void sf_store(uint32_t taddr, const SfWords& v) {
+  const uint32_t w[16] = {v.a0, v.a0, v.a0, v.a0, v.a1, v.a1, v.a1, v.a1,
+                          v.b[0], v.b[1], v.b[2], v.b[3], v.b[4], v.b[5], v.b[6], v.b[7]};
+  tmem_st16_wait(taddr, w);
+}
+
 // Row-box height of a tile of nrows rows (0: several 64-row boxes).
 __device__ __forceinline__ int row_box_rows(const Params& p, int nrows) {
   return nrows <= 64 ? 64 : (nrows <= 128 && (p.rmask & 1)) ? 128
@@ -367,17 +444,19 @@ __device__ __forceinline__ int row_box_rows(const Params& p, int nrows) {
 // bf16 tile the MMAs read (code x scale, 128-byte swizzle), so the MMAs, the
 // LoRA expand and the epilogue are those of the bf16 kernel.
 template <int KIND, int QF = kQNone>
-__global__ void __launch_bounds__(QF != kQNone ? 512 : kMaxThreads, 1)
+__global__ void __launch_bounds__(kConvOf<QF> ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
-  constexpr bool Q = QF != kQNone;
-  static_assert(!Q || KIND == kGateUp || KIND == kDown, "quantised weights: the base GEMMs only");
-  using CF = CfgOf<KIND, Q>;
+  constexpr bool Q = kConvOf<QF>;   // converter warps dequantise the weights
+  constexpr bool MX = QF == kQMx;    // block-scaled FP8 MMAs
+  static_assert(QF == kQNone || KIND == kGateUp || KIND == kDown, "quantised weights: the base GEMMs only");
+  using CF = CfgOf<KIND, QF>;
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
   constexpr bool kShrink = (KIND == kShrinkGU || KIND == kShrinkD);
   constexpr int kGates = (KIND == kGateUp) ? 2 : 1;
+  constexpr int kUOff = MX ? kMxTileRows : 256;  // gate_up: TMEM column of the up accumulator
 
-  constexpr bool kPair = kPairOf<KIND, Q>;
+  constexpr bool kPair = kPairOf<KIND, QF>;
   const int n_items = *p.n_tiles * p.nblk;
   // work unit: a CTA, or for pairs a cluster (both CTAs take the same items and
   // leave together)
@@ -392,14 +471,18 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int kHalves = kEpiWarps<KIND> / 4;  // epilogue warps per TMEM lane quarter
   Ctl& c = *reinterpret_cast<Ctl*>(epi + kHalves * kEpiBytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, 64);  // 64-wide K chunks
+  // K steps of 128 bytes per row: 64 bf16 elements, or 128 E4M3 codes for the
+  // block-scaled GEMMs
+  const int nk = (int)ceil_div(KIND == kShrinkGU || KIND == kGateUp ? p.H : p.I, MX ? 128 : 64);
   const int nks = kShrink ? (nk + 1) / 2 : nk;  // main steps (a shrink step covers two chunks)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // FP8: the producer's arrival plus one per converter warp (on a pair,
       // both CTAs' converter warps arrive on the leader's barrier)
-      mbar_init(&c.full[s], Q ? 1 + (kPair ? 2 : 1) * kCvWarps : 1);
+      // block-scaled FP8: the producer's arrival plus one per scale-factor
+      // warp of lane quarters 1-3 (the producer warp writes quarter 0)
+      mbar_init(&c.full[s], Q ? 1 + (kPair ? 2 : 1) * kCvWarps : (MX ? 4 : 1));
       mbar_init(&c.empty[s], 1);
       if (Q) mbar_init(&c.raw_full[s], 1);
     }
@@ -439,9 +522,18 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       for (int s = 0; s < nsteps; ++s, ++gs) {
         const int st = gs % S, round = gs / S;
         uint8_t* sbuf = smem + st * SB;
+        const bool main_step = s < nks;
+        SfWords sfw;
+        if (MX && main_step) sf_load<KIND>(p, it, s, 0, lane, sfw);
         const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort, p.wait_ns);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-        const bool main_step = s < nks;
+        if (MX && main_step) {
+          // lane quarter 0 of the stage's scale factors, before the stage's
+          // full barrier can complete
+          sf_store(tmem + kSfCol0<KIND, QF> + st * kMxSfCols, sfw);
+          tc_fence_before();
+          __syncwarp();
+        }
         // the row tile of x_sorted / h: one 64/128/192/256-row box where the
         // map exists, else 64-row boxes
         const int hb = row_box_rows(p, it.nrows);
@@ -517,7 +609,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               tma_load_3d(sbuf + 32768, &maps.m[xh == 64 ? kX2x64 : kX2x128], &c.full[st], 0, it.row0, c0);
             } else if (KIND == kGateUp) {
               const int i0 = it.mb * 128;
-              if (Q) {
+              if (MX) {
+                // E4M3 codes of the gate and up blocks, 128 bytes of K per row
+                // (the code matrices are mapped as 2-byte elements: the same
+                // bytes and swizzle, 64 elements per K step)
+                mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
+                tma_load_3d(sbuf, &maps.m[kW3], &c.full[st], kb * 64, i0, it.e * 2);
+              } else if (Q) {
                 // raw codes of the gate and up blocks: [gate|up][128 rows][row bytes]
                 mbar_arrive_expect_tx(&c.raw_full[st], 256 * kRawRowBytes<QF>);
                 tma_load_3d(sbuf + 16384, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, i0, it.e * 2);
@@ -536,10 +634,17 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             } else if (!kPair) {
               // kDown with FP8 weights, on a single CTA: raw codes of 128 weight rows
               // on their own barrier, then all of the tile's rows
-              static_assert(KIND != kDown || kPair || Q, "bf16 down runs on CTA pairs");
-              mbar_arrive_expect_tx(&c.raw_full[st], 128 * kRawRowBytes<QF>);
-              tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, it.mb * 128, it.e);
-              mbar_arrive_expect_tx(&c.full[st], rbytes);
+              static_assert(KIND != kDown || kPair || QF != kQNone, "bf16 down runs on CTA pairs");
+              if (MX) {
+                // E4M3 codes of 128 W_down rows, 128 bytes of K per row
+                // (mapped as 64 2-byte elements)
+                mbar_arrive_expect_tx(&c.full[st], 16384 + rbytes);
+                tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
+              } else {
+                mbar_arrive_expect_tx(&c.raw_full[st], 128 * kRawRowBytes<QF>);
+                tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, it.mb * 128, it.e);
+                mbar_arrive_expect_tx(&c.full[st], rbytes);
+              }
               for (int q = 0; q < rbox; ++q)
                 tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else {  // kDown, on a CTA pair: this CTA's 128 weight rows and half of the tile's rows
@@ -586,6 +691,28 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
           }
         }
+      }
+    }
+  } else if (MX && warp < 4) {
+    // ====== block-scaled FP8: scale factors of lane quarters 1-3 (warps 1-3) ======
+    // Each main step's A and B scales go into the stage's TMEM columns once
+    // the stage is free (the MMAs that read the previous ones have completed),
+    // then the warp arrives on the stage's full barrier.
+    int gs = 0;
+    bool ok = true;
+    for (int item = unit; item < n_items && ok; item += n_units) {
+      const Item it = load_item<KIND>(p, item);
+      const int nsteps = nks + it.nexp;
+      for (int s = 0; s < nsteps; ++s, ++gs) {
+        const int st = gs % S, round = gs / S;
+        SfWords sfw;
+        if (s < nks) sf_load<KIND>(p, it, s, warp, lane, sfw);
+        const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort, p.wait_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        if (s < nks) sf_store(tmem + ((uint32_t)(warp * 32) << 16) + kSfCol0<KIND, QF> + st * kMxSfCols, sfw);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.full[st]);
       }
     }
   } else if (Q && (warp < 4 || warp >= kThreadsOf<KIND> / 32)) {
@@ -712,7 +839,22 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (!mbar_wait(&c.full[st], round & 1, abort, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sb = smem_u32(smem + st * SB);
-          if (s < nks) {
+          if (s < nks && MX) {
+            // four K = 32 block-scaled MMAs; scale ids 0..3 pick the (equal) bytes
+            const uint32_t sf = tmem + kSfCol0<KIND, QF> + st * kMxSfCols;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t a = (s > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t idm = idesc_mx_e4m3(128, it.nrows, kk, kk);
+              if (KIND == kGateUp) {
+                const uint64_t bx = sdesc_sw128(sb + 32768 + kk * 32);
+                mma_mx(acc, sdesc_sw128(sb + kk * 32), bx, idm, sf, sf + 8, a);
+                mma_mx(acc + kUOff, sdesc_sw128(sb + 16384 + kk * 32), bx, idm, sf + 4, sf + 8, a);
+              } else {
+                mma_mx(acc, sdesc_sw128(sb + kk * 32), sdesc_sw128(sb + 16384 + kk * 32), idm, sf, sf + 8, a);
+              }
+            }
+          } else if (s < nks) {
             const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, it.nrows);
             if (KIND == kGateUp) {
 #pragma unroll
@@ -742,7 +884,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             cur.next(pc.z, kGates);
             const int nch = min(8, (pc.z - kg * 64) / 8);
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
-            const uint32_t d = acc + (KIND == kGateUp ? g * 256 : 0) + (pc.x & 0xffff);
+            const uint32_t d = acc + (KIND == kGateUp ? g * kUOff : 0) + (pc.x & 0xffff);
             const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, pc.x >> 16);
             for (int k16 = 0; k16 < nch / 2; ++k16)
               mma_issue<kPair>(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
@@ -807,13 +949,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (ncol == 32) {
             float gv[32], uv[32];
             tmem_ld32(tl + c0, gv);
-            tmem_ld32(tl + 256 + c0, uv);
+            tmem_ld32(tl + kUOff + c0, uv);
 #pragma unroll
             for (int j = 0; j < 32; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           } else {
             float gv[16], uv[16];
             tmem_ld16(tl + c0, gv);
-            tmem_ld16(tl + 256 + c0, uv);
+            tmem_ld16(tl + kUOff + c0, uv);
 #pragma unroll
             for (int j = 0; j < 16; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
           }
@@ -828,6 +970,62 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (n < ncol && chunk_ok && col >= it.lo && col < it.hi) {
               const uint4 v = i < p.I ? *reinterpret_cast<const uint4*>(ws + n * 32 + (q & 3) * 8) : make_uint4(0, 0, 0, 0);
               *reinterpret_cast<uint4*>(p.h + ((int64_t)(i >> 6) * p.cap + it.row0 + col) * 64 + (i & 63)) = v;
+            }
+          }
+          if (MX) {
+            // h as E4M3 codes for the block-scaled down GEMM, per column (pair)
+            // and the tile's 128 rows of I (one quantisation group): lane j
+            // takes column c0 + j, whose 32 rows of this warp are 64 contiguous
+            // bytes of the staging area; the half's four lane quarters combine
+            // their column maxima through shared memory; each warp writes its
+            // 32 codes of the column, quarter 0 also the column's exponent.
+            const uint16_t* colp = ws + lane * 32;
+            // load order rotated by lane pair so that a warp's loads spread
+            // over the banks; selects (not indexing) put the pieces in place
+            const int rot = (lane >> 1) & 3;
+            uint4 ld[4], cv[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) ld[m] = *reinterpret_cast<const uint4*>(colp + ((m + rot) & 3) * 8);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = (k - rot) & 3;  // ld[r] holds piece k
+              cv[k] = r == 0 ? ld[0] : r == 1 ? ld[1] : r == 2 ? ld[2] : ld[3];
+            }
+            uint32_t cm = 0;
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              if (iw + mm * 8 >= p.I) cv[mm] = make_uint4(0, 0, 0, 0);  // rows past I (I % 16 == 0)
+              const uint32_t wv[4] = {cv[mm].x, cv[mm].y, cv[mm].z, cv[mm].w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) cm = max(cm, max(wv[k] & 0x7fffu, (wv[k] >> 16) & 0x7fffu));
+            }
+            static_assert(!MX || KIND != kGateUp || kAmaxBytes<KIND, QF> == 2048, "column-maxima buffer");
+            uint32_t* am = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + sizeof(Ctl)) +
+                           (eh * 2 + ((c0 >> 6) & 1)) * 128;
+            am[quarter * 32 + lane] = cm;
+            named_bar_sync(5 + eh, 128);
+            const uint32_t gm = max(max(am[lane], am[32 + lane]), max(am[64 + lane], am[96 + lane]));
+            const int sxp = mx_group_exp_bf16(gm);
+            const float sc = exp2_neg(sxp);
+            uint32_t qw[8];
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              const uint32_t wv[4] = {cv[mm].x, cv[mm].y, cv[mm].z, cv[mm].w};
+#pragma unroll
+              for (int k = 0; k < 4; k += 2) {
+                const uint32_t lo = f32x2_to_e4m3x2(__uint_as_float(wv[k] << 16) * sc,
+                                                    __uint_as_float(wv[k] & 0xffff0000u) * sc);
+                const uint32_t hi = f32x2_to_e4m3x2(__uint_as_float(wv[k + 1] << 16) * sc,
+                                                    __uint_as_float(wv[k + 1] & 0xffff0000u) * sc);
+                qw[mm * 2 + k / 2] = lo | (hi << 16);
+              }
+            }
+            const int col = c0 + lane;
+            if (lane < ncol && col >= it.lo && col < it.hi) {
+              uint4* dst = reinterpret_cast<uint4*>(p.h8 + ((int64_t)it.mb * p.cap + it.row0 + col) * 128 + quarter * 32);
+              dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+              dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+              if (quarter == 0) p.sh[(int64_t)it.mb * p.cap + it.row0 + col] = (uint8_t)(sxp + 127);
             }
           }
           __syncwarp();
@@ -980,10 +1178,12 @@ __device__ int block_offsets(int mine, int* total) {
 __device__ __forceinline__ int floor16(int v) { return v & ~15; }
 __device__ __forceinline__ int ceil16(int v) { return (v + 15) & ~15; }
 // Rows per base tile of an expert spanning `span` rows (a multiple of 16):
-// ceil(span / 256) tiles of equal size, rounded up to 16 (the count of tiles is
-// then ceil(span / tile_rows), every tile non-empty and at most 256 rows).
-__device__ __forceinline__ int tile_rows(int span) {
-  const int nt = (span + kTileRows - 1) / kTileRows;
+// ceil(span / max_rows) tiles of equal size, rounded up to 16 (the count of
+// tiles is then ceil(span / tile_rows), every tile non-empty and at most
+// max_rows rows; max_rows is 256, or kMxTileRows for the block-scaled FP8
+// GEMMs, a multiple of 16 either way).
+__device__ __forceinline__ int tile_rows(int span, int max_rows) {
+  const int nt = (span + max_rows - 1) / max_rows;
   return ceil16((span + nt - 1) / nt);
 }
 
@@ -996,7 +1196,8 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
                            int E, int C, int R, uint32_t* __restrict__ ustart_out,
                            TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                            ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                           int32_t* __restrict__ counts, int32_t* status, int gemv_rows, int by_span) {
+                           int32_t* __restrict__ counts, int32_t* status, int gemv_rows, int by_span,
+                           int max_rows) {
   const int NB = E * C;
   int bad = 0;
   // experts with many tiles, planned by the whole block at the end
@@ -1068,7 +1269,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
       if (ue1 == ue0) continue;
       const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
-      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      const int ts = tile_rows(span, max_rows), nt = (span + ts - 1) / ts;
       my_t += nt;
       for (int b = e * C + 1; b < (e + 1) * C; ++b) {
         if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
@@ -1097,7 +1298,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       for (int e = e0; e < e1; ++e) {
         const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
         if (ue1 == ue0) continue;
-        const int span = ceil16(ue1) - floor16(ue0), ts = tile_rows(span);
+        const int span = ceil16(ue1) - floor16(ue0), ts = tile_rows(span, max_rows);
         atomicAdd(&cls_base[span_class(span)], (span + ts - 1) / ts);
       }
       __syncthreads();
@@ -1116,7 +1317,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       if (ue1 == ue0) continue;
       // nt tiles of equal size (a multiple of 16) over [floor16(first row), ceil16(end))
       const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
-      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      const int ts = tile_rows(span, max_rows), nt = (span + ts - 1) / ts;
       int toff = toff_seq;
       toff_seq += nt;
       if (by_span) {
@@ -1185,7 +1386,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       const int e = bq.x;
       const int ue0 = (int)us[e * C], ue1 = (int)us[(e + 1) * C];
       const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
-      const int ts = tile_rows(span), nt = (span + ts - 1) / ts;
+      const int ts = tile_rows(span, max_rows), nt = (span + ts - 1) / ts;
       for (int k = threadIdx.x; k < nt; k += kPlanThreads) {
         int pk = bq.z;
         for (int b = e * C + 1; b < (e + 1) * C; ++b) {
@@ -1208,7 +1409,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
             int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
             ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status,
-            int gemv_rows, int by_span) {
+            int gemv_rows, int by_span, int max_rows) {
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -1217,7 +1418,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
   __syncthreads();
   align_block_scan(us, NB);
   plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts,
-             status, gemv_rows, by_span);
+             status, gemv_rows, by_span, max_rows);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
@@ -1230,7 +1431,8 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
                   int32_t* __restrict__ usorted, uint32_t* __restrict__ ustart,
                   TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                   ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
-                  int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows, int by_span) {
+                  int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows, int by_span,
+                  int max_rows) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
@@ -1238,7 +1440,7 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
   align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, nullptr, nullptr, nullptr, nullptr, nullptr, P,
               status, usorted);
   plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
-             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows, by_span);
+             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows, by_span, max_rows);
 }
 
 // Dense x_sorted: row u < n = ustart[NB] (the valid pairs) is x[usorted[u] / K]
@@ -1268,6 +1470,65 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usor
       for (int j = 0; j < kBatch; ++j) {
         const int c = c0 + 32 * j;
         if (c < pieces16) *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
+      }
+    }
+  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < yacc_n4; i += (int64_t)gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Block-scaled FP8: gather_x_kernel's work (x_sorted in bf16 for the LoRA
+// shrink, y_acc zeroed) plus x quantised per row and 128-column group for the
+// base GEMM: x8 [H/128][cap][128] E4M3 codes (zeros past H) and sx
+// [H/128][cap] biased exponents (rows [n, cap): zero codes, exponent 127).
+// Half a warp takes one group, eight values per lane.
+__global__ void __launch_bounds__(kGatherThreads)
+gather_x_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usorted,
+                   const uint32_t* __restrict__ n_valid, int K, int H, int64_t cap, uint16_t* __restrict__ xs,
+                   uint8_t* __restrict__ x8, uint8_t* __restrict__ sx, float* __restrict__ yacc, int64_t yacc_n4) {
+  const int64_t n = *n_valid;
+  const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+  const int64_t wpb = kGatherThreads / 32;
+  const int ng = (H + 127) / 128;                 // groups per row
+  const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces of an x_sorted row
+  const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
+  constexpr int kPairs = 4;  // pairs of groups in flight per warp
+  for (int64_t u = w0; u < cap; u += ws) {
+    const bool real = u < n;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(usorted[u] / K) * H : 0));
+    for (int g0 = 0; g0 < ng; g0 += 2 * kPairs) {
+      uint4 v[kPairs];
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const int g = g0 + 2 * j + half, c = g * 16 + hl;  // c: 16-byte piece of the row
+        v[j] = (real && g < ng && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        if (g0 + 2 * j >= ng) break;  // the same for both halves
+        const int g = g0 + 2 * j + half, c = g * 16 + hl;
+        if (g < ng && c < pieces16)
+          *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
+        const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m = max(m, max(wv[k] & 0x7fffu, (wv[k] >> 16) & 0x7fffu));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));  // within the half
+        const int s = mx_group_exp_bf16(m);
+        const float sc = exp2_neg(s);
+        uint32_t q[2];
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          const uint32_t lo = f32x2_to_e4m3x2(__uint_as_float(wv[k] << 16) * sc, __uint_as_float(wv[k] & 0xffff0000u) * sc);
+          const uint32_t hi =
+              f32x2_to_e4m3x2(__uint_as_float(wv[k + 1] << 16) * sc, __uint_as_float(wv[k + 1] & 0xffff0000u) * sc);
+          q[k / 2] = lo | (hi << 16);
+        }
+        if (g < ng) {
+          *reinterpret_cast<uint2*>(x8 + ((int64_t)g * cap + u) * 128 + hl * 8) = make_uint2(q[0], q[1]);
+          if (hl == 0) sx[(int64_t)g * cap + u] = (uint8_t)(s + 127);
+        }
       }
     }
   }
@@ -1663,10 +1924,12 @@ struct FwdLayout {
   int R16, C, mtiles_gu, mtiles_d;
   int64_t cap, zcap, max_base, max_shrink, max_pieces, max_gemv;
   int64_t o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted,
-      o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, total;
+      o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, o_x8, o_sx, o_h8, o_sh, total;
 };
 
-FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R) {
+// act_q (block-scaled FP8): also the quantised x and h with their exponents.
+FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R,
+                     bool act_q = false) {
   FwdLayout f{};
   f.ok = false;
   if (T < 0 || K < 1 || E < 1 || H < 128 || I < 64 || L < 0 || R < 0) return f;
@@ -1684,7 +1947,7 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.cap = round_up(P, 16) + kTileRows;
   // z regions: each non-empty LoRA bucket adds < 32 rows of 16-row alignment
   f.zcap = round_up(P + 32 * nb_nonempty, 16) + kTileRows;
-  f.max_base = P / kTileRows + 2 * (int64_t)E + 1;
+  f.max_base = P / kMxTileRows + 2 * (int64_t)E + 1;  // tiles of at most 256 (or kMxTileRows) rows
   f.max_shrink = (P + 32 * nb_nonempty) / kShrinkRows + nb_nonempty + 1;
   f.max_pieces = nb_nonempty + f.max_base;
   f.max_gemv = nb_nonempty;
@@ -1704,6 +1967,12 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.o_zd = take(f.zcap * f.R16 * 2);
   f.o_yacc = take((int64_t)T * H * 4);
   f.o_xs = take(f.cap * round_up(H, 64) * 2);
+  if (act_q) {
+    f.o_x8 = take(f.cap * round_up(H, 128));
+    f.o_sx = take(ceil_div(H, 128) * f.cap);
+    f.o_h8 = take(f.cap * round_up(I, 128));
+    f.o_sh = take(ceil_div(I, 128) * f.cap);
+  }
   f.total = o;
   f.ok = true;
   return f;
@@ -1732,8 +2001,8 @@ int sm_count() {
 // Persistent launch: one CTA per SM (or fewer when there are fewer items).
 template <int KIND, int QF = kQNone>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
-  constexpr bool Q = QF != kQNone;
-  const int smem = smem_bytes<KIND, Q>();
+  static_assert(smem_bytes<KIND, QF>() <= 227 * 1024, "shared memory per CTA");
+  const int smem = smem_bytes<KIND, QF>();
   // the shared-memory opt-in and the resident-cluster count are per device
   const int dev = current_device();
   static bool configured[64] = {};
@@ -1746,7 +2015,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   const int64_t max_items = max_tiles * p.nblk;
   if (max_items <= 0) return MLR_OK;
   if (max_items > INT32_MAX) return MLR_ERR_UNSUPPORTED;
-  if (kPairOf<KIND, Q>) {
+  if (kPairOf<KIND, QF>) {
     // clusters of two CTAs, as many as can be resident at once (a persistent
     // grid with one pair more than fits would run that pair after the others)
     cudaLaunchAttribute attr[1];
@@ -1755,7 +2024,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kLaunchThreads<KIND, Q>);
+    cfg.blockDim = dim3(kLaunchThreads<KIND, QF>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1775,7 +2044,7 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND, QF>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
   } else {
     const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-    moe_gemm_kernel<KIND, QF><<<grid, kLaunchThreads<KIND, Q>, smem, stream>>>(maps, p);
+    moe_gemm_kernel<KIND, QF><<<grid, kLaunchThreads<KIND, QF>, smem, stream>>>(maps, p);
     MLR_CHECK_LAUNCH();
   }
   note_launch();
@@ -1818,6 +2087,14 @@ extern "C" size_t fused_moe_lora_workspace_bytes(int32_t num_tokens, int32_t top
   return f.ok ? (size_t)f.total : 0;
 }
 
+extern "C" size_t fused_moe_lora_workspace_bytes_fp8_w8a8(int32_t num_tokens, int32_t topk, int32_t num_experts,
+                                                         int32_t hidden, int32_t intermediate, int32_t num_loras,
+                                                         int32_t max_rank) {
+  const mlr::FwdLayout f =
+      mlr::fwd_layout(num_tokens, topk, num_experts, hidden, intermediate, num_loras, max_rank, true);
+  return f.ok ? (size_t)f.total : 0;
+}
+
 namespace mlr {
 namespace {
 
@@ -1840,7 +2117,10 @@ bool make_map3_u8(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, ui
 // with block scales s_gu [E][ceil(2I/128)][ceil(H/128)] and s_d
 // [E][ceil(H/128)][ceil(I/128)]; kQU4: two UINT4 codes per byte ([E][2I][H/2]
 // and [E][H][I/2]) with group scales and zero points s_gu, z_gu
-// [E][2I][ceil(H/128)] and s_d, z_d [E][H][ceil(I/128)]; kQNone: bf16, the
+// [E][2I][ceil(H/128)] and s_d, z_d [E][H][ceil(I/128)]; kQMx: E4M3 codes
+// with power-of-two block scales given as biased exponents in z_gu
+// [E][ceil(2I/128)][ceil(H/128)] and z_d [E][ceil(H/128)][ceil(I/128)], the
+// activations quantised on the way (s_gu, s_d unused); kQNone: bf16, the
 // scales unused.
 int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_weights,
                 const int32_t* token_lora_mapping, const int32_t* lora_ranks, const float* scalings,
@@ -1850,7 +2130,8 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
                 const mlr_bf16* lora_b_down, int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int32_t L,
                 int32_t R, mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
                 cudaStream_t stream) {
-  const FwdLayout f = fwd_layout(T, K, E, H, I, L, R);
+  const bool mx = qf == kQMx;
+  const FwdLayout f = fwd_layout(T, K, E, H, I, L, R, mx);
   if (!f.ok) {
     if (T < 0 || K < 1 || E < 1 || L < 0 || R < 0) return MLR_ERR_INVALID;
     return MLR_ERR_UNSUPPORTED;
@@ -1864,10 +2145,10 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   const void* need[] = {x, topk_ids, topk_weights, token_lora_mapping, w_gate_up, w_down, y};
   for (const void* q : need)
     if (q == nullptr) return MLR_ERR_INVALID;
-  if (quant && (s_gu == nullptr || s_d == nullptr || (reinterpret_cast<uintptr_t>(s_gu) & 3) != 0 ||
+  if (quant && !mx && (s_gu == nullptr || s_d == nullptr || (reinterpret_cast<uintptr_t>(s_gu) & 3) != 0 ||
                 (reinterpret_cast<uintptr_t>(s_d) & 3) != 0))
     return MLR_ERR_INVALID;
-  if (qf == kQU4 && (z_gu == nullptr || z_d == nullptr)) return MLR_ERR_INVALID;
+  if ((qf == kQU4 || mx) && (z_gu == nullptr || z_d == nullptr)) return MLR_ERR_INVALID;
   if (L > 0) {
     const void* lo[] = {lora_ranks, scalings, lora_a_gu, lora_b_gu, lora_a_down, lora_b_down};
     for (const void* q : lo)
@@ -1893,6 +2174,10 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   uint16_t* zd = reinterpret_cast<uint16_t*>(ws + f.o_zd);
   float* yacc = reinterpret_cast<float*>(ws + f.o_yacc);
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + f.o_xs);
+  uint8_t* x8 = mx ? reinterpret_cast<uint8_t*>(ws + f.o_x8) : nullptr;
+  uint8_t* sx = mx ? reinterpret_cast<uint8_t*>(ws + f.o_sx) : nullptr;
+  uint8_t* h8 = mx ? reinterpret_cast<uint8_t*>(ws + f.o_h8) : nullptr;
+  uint8_t* sh = mx ? reinterpret_cast<uint8_t*>(ws + f.o_sh) : nullptr;
   const uint32_t* btotal = reinterpret_cast<const uint32_t*>(aws + f.al.btotal_off);
 
   // tensor maps
@@ -1914,7 +2199,21 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
                    true);
     w3 = 1;
   }
-  if (ok && quant) {
+  if (ok && mx) {
+    // E4M3 codes mapped as 2-byte elements: 128 bytes = 64 elements per K step
+    // with the bf16 kernels' 128-byte swizzle.  W_gate_up as [(e, gate|up)][I
+    // rows][H/2] (a box is a 128-row block of gate and of up), W_down as [E*H
+    // rows][I/2], the quantised x and h as [K/128 chunk][cap rows][64]; the
+    // single-CTA down GEMM takes whole-tile row boxes over h.  Codes past H
+    // (or I) and rows past I (or H) read 0.
+    const uint64_t hk8 = (uint64_t)ceil_div(H, 128), ik8 = (uint64_t)ceil_div(I, 128);
+    ok = make_map3(&m_gu.m[kW3], w_gate_up, (uint64_t)H / 2, I, (uint64_t)E * 2, (uint64_t)H, (uint64_t)I * H, 64,
+                   128, 2, true) &&
+         make_map(&m_gu.m[kRows], x8, 64, hk8 * cap, 64, 64, true) && make_row_maps(m_gu, x8, hk8 * cap, &rm_gu) &&
+         make_map(&m_dn.m[kW], w_down, (uint64_t)I / 2, (uint64_t)E * H, 64, 128, true) &&
+         make_map(&m_dn.m[kRows], h8, 64, ik8 * cap, 64, 64, true) && make_row_maps(m_dn, h8, ik8 * cap, &rm_dn);
+    w3 = 1;
+  } else if (ok && quant) {
     // codes: W_gate_up as [(e, gate|up)][I rows][row bytes], a box of one K step's bytes (64, or 32
     // for UINT4) x 128 rows of gate and of up; W_down as [e][H rows][row bytes], a box of one K
     // step's bytes x 128 rows.  Rows past I (or H) read 0.
@@ -1925,6 +2224,8 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
          // the FP8 down GEMM runs on single CTAs: whole-tile row boxes over h, and
          // z boxes of zrows rows (a CTA loads a piece's z rows whole)
          make_row_maps(m_dn, hbuf, (uint64_t)ceil_div(I, 64) * cap, &rm_dn);
+  }
+  if (ok && quant) {
     const int nc[3] = {8, 4, 2};
     const int zslot[3] = {kZ8, kZ4, kZ2};
     for (int j = 0; ok && L > 0 && j < 3; ++j) {
@@ -1959,6 +2260,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   // largest experts first when experts average more than 32 rows (several
   // tiles of differing sizes); small batches keep the cheaper plain order
   const int by_span = f.al.P > 32 * (int64_t)E ? 1 : 0;
+  const int max_rows = mx ? kMxTileRows : kTileRows;  // rows per base tile
   const size_t scan_bytes = (size_t)round_up(((int64_t)f.al.NB + 1) * 4, 16);
   if (align_block_ok(f.al, scan_bytes)) {
     // one launch: the dense align and the tile plan (timed as the align stage)
@@ -1970,7 +2272,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, by_span);
+                                                       gemv_rows, by_span, max_rows);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
@@ -1985,7 +2287,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
                                                   shrink_tiles, gemv_tiles, counts, d_status, gemv_rows,
-                                                  by_span);
+                                                  by_span, max_rows);
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, topk_ids, token_lora_mapping, K, E, L, aws, ustart, usorted, stream)) !=
@@ -1996,8 +2298,12 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   {
     const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
-    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, yacc,
-                                                         det ? 0 : (int64_t)T * H / 4);
+    if (mx)
+      gather_x_mx_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, x8, sx,
+                                                              yacc, det ? 0 : (int64_t)T * H / 4);
+    else
+      gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, yacc,
+                                                           det ? 0 : (int64_t)T * H / 4);
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -2038,7 +2344,9 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     Params q = p;
     q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128); q.rmask = rm_gu; q.w3 = w3;
     q.wscale = s_gu; q.wzero = z_gu; q.wsr = (int)ceil_div(2 * I, 128); q.wsc = (int)ceil_div(H, 128);
+    q.wexp = z_gu; q.sfx = sx; q.h8 = h8; q.sh = sh;
     rc = qf == kQFp8 ? launch_gemm<kGateUp, kQFp8>(m_gu, q, f.max_base, stream)
+       : qf == kQMx ? launch_gemm<kGateUp, kQMx>(m_gu, q, f.max_base, stream)
        : qf == kQInt8 ? launch_gemm<kGateUp, kQInt8>(m_gu, q, f.max_base, stream)
        : qf == kQU4 ? launch_gemm<kGateUp, kQU4>(m_gu, q, f.max_base, stream)
                     : launch_gemm<kGateUp>(m_gu, q, f.max_base, stream);
@@ -2062,7 +2370,9 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     q.dpair = det ? xs : nullptr;
     q.wscale = s_d; q.wzero = z_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
+    q.wexp = z_d; q.sfx = sh;
     rc = qf == kQFp8 ? launch_gemm<kDown, kQFp8>(m_dn, q, f.max_base, stream)
+       : qf == kQMx ? launch_gemm<kDown, kQMx>(m_dn, q, f.max_base, stream)
        : qf == kQInt8 ? launch_gemm<kDown, kQInt8>(m_dn, q, f.max_base, stream)
        : qf == kQU4 ? launch_gemm<kDown, kQU4>(m_dn, q, f.max_base, stream)
                     : launch_gemm<kDown>(m_dn, q, f.max_base, stream);
@@ -2146,6 +2456,22 @@ extern "C" int fused_moe_lora_forward_w4a16(const mlr_bf16* x, const int32_t* to
                           w_down_q, w_gate_up_scale, w_down_scale, w_gate_up_zero, w_down_zero, mlr::kQU4,
                           lora_a_gu, lora_b_gu, lora_a_down, lora_b_down, T, K, E, H, I, L, R, y, workspace,
                           ws_bytes, d_status, static_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int fused_moe_lora_forward_fp8_w8a8(const mlr_bf16* x, const int32_t* topk_ids,
+                                               const float* topk_weights, const int32_t* token_lora_mapping,
+                                               const int32_t* lora_ranks, const float* scalings,
+                                               const uint8_t* w_gate_up_q, const uint8_t* w_gate_up_exp,
+                                               const uint8_t* w_down_q, const uint8_t* w_down_exp,
+                                               const mlr_bf16* lora_a_gu, const mlr_bf16* lora_b_gu,
+                                               const mlr_bf16* lora_a_down, const mlr_bf16* lora_b_down, int32_t T,
+                                               int32_t K, int32_t E, int32_t H, int32_t I, int32_t L, int32_t R,
+                                               mlr_bf16* y, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                               void* stream_) {
+  return mlr::moe_forward(x, topk_ids, topk_weights, token_lora_mapping, lora_ranks, scalings, w_gate_up_q,
+                          w_down_q, nullptr, nullptr, w_gate_up_exp, w_down_exp, mlr::kQMx, lora_a_gu, lora_b_gu,
+                          lora_a_down, lora_b_down, T, K, E, H, I, L, R, y, workspace, ws_bytes, d_status,
+                          static_cast<cudaStream_t>(stream_));
 }
 
 // ------------------------------------------------------------------------
@@ -2247,7 +2573,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(zeros_ids, token_lora_mapping, (int)f.al.P, 1, 1, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, 0);
+                                                       gemv_rows, 0, kTileRows);
     MLR_CHECK_LAUNCH();
     note_launch();
   } else {
@@ -2258,7 +2584,8 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, 1, f.C, R, ustart, base_tiles, pieces,
-                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows, 0);
+                                                  shrink_tiles, gemv_tiles, counts, d_status, gemv_rows, 0,
+                                                  kTileRows);
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, zeros_ids, token_lora_mapping, 1, 1, L, aws, ustart, usorted, stream)) !=

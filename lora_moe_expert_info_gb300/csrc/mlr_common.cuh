@@ -415,6 +415,61 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ---- block-scaled FP8 MMAs (tcgen05.mma kind::mxf8f6f4) ----
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: E4M3 A and B,
+// both K-major, fp32 D, UE8M0 scale factors (bit 23); a_id / b_id pick the
+// byte of each scale-factor cell that this K = 32 MMA reads.
+__device__ __forceinline__ uint32_t idesc_mx_e4m3(uint32_t M, uint32_t N, uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (a_id << 29);
+}
+// D[tmem] (+)= (A x 2^sfa) * (B x 2^sfb)^T, E4M3 operands in shared memory, one
+// UE8M0 scale per row of A and of B for this K = 32 step, read from TMEM:
+// the scale of A row m at lane m, column sfa + m / 32; the scale of B row n at
+// lane n % 32 of every lane quarter, column sfb + n / 32 (measured on GB300).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// Registers -> TMEM: this warp's 32 lanes, 16 consecutive 32-bit columns each;
+// returns once the stores are complete.
+__device__ __forceinline__ void tmem_st16_wait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// Two fp32 values rounded to E4M3 (nearest, ties to even; the callers keep
+// |v| <= 448): v0 in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float v0, float v1) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(v1), "f"(v0));
+  return d;
+}
+// The power-of-two scale exponent s of a group of activations from the bf16
+// bit pattern of its largest magnitude: the smallest integer with
+// amax x 2^-s <= 448 = 1.75 x 2^8, clamped below at -127; 0 for amax == 0.
+// amax = 1.m x 2^E (7 mantissa bits m7): s = E - 8 if 1.m <= 1.75 (m7 <= 96),
+// else E - 7.
+__device__ __forceinline__ int mx_group_exp_bf16(uint32_t amax_bits) {
+  if (amax_bits == 0) return 0;
+  const int ef = (int)((amax_bits >> 7) & 0xffu);
+  if (ef == 0) return -127;  // below 2^-126
+  const int s = ef - 127 - ((amax_bits & 0x7fu) <= 96u ? 8 : 7);
+  return s < -127 ? -127 : s;
+}
+// 2^-s as a float, for s in [-127, 120].
+__device__ __forceinline__ float exp2_neg(int s) { return __int_as_float((127 - s) << 23); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   __nv_bfloat16_raw raw = static_cast<__nv_bfloat16_raw>(__float2bfloat16_rn(f));
   return raw.x;

@@ -272,6 +272,44 @@ def make_fp8_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> Fp8Expert
 
 
 @dataclasses.dataclass
+class Fp8W8A8Experts:
+    w_gate_up_q: torch.Tensor    # uint8 [E, 2I, H], FP8 E4M3 codes
+    w_gate_up_exp: torch.Tensor  # uint8 [E, ceil(2I/128), ceil(H/128)], biased block exponents
+    w_down_q: torch.Tensor       # uint8 [E, H, I]
+    w_down_exp: torch.Tensor     # uint8 [E, ceil(H/128), ceil(I/128)]
+
+
+def make_fp8_w8a8_experts(cfg: LayerConfig, device="cpu", seed: int = 0) -> Fp8W8A8Experts:
+    """FP8 E4M3 expert weights with power-of-two block scales.
+
+    Codes are N(0, 32^2) samples cast to E4M3 (torch's float8_e4m3fn); each
+    128 x 128 block's exponent is e0 or e0 + 1 at random, with 2^(e0 - 127)
+    the largest power of two at or below 1 / (32 sqrt(fan_in)), so code x
+    2^(e - 127) has about the bf16 weights' N(0, 1/fan_in) spread within a
+    factor of two.
+    """
+    E, H, I = cfg.num_experts, cfg.hidden, cfg.intermediate
+    g = _gen(device, seed + 8)
+    nb = lambda n: (n + 127) // 128  # noqa: E731
+
+    def mat(rows, cols, fan_in):
+        z = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(32.0)
+        codes = z.to(torch.float8_e4m3fn).view(torch.uint8)
+        e0 = 127 + math.floor(math.log2(1.0 / (32.0 * math.sqrt(fan_in))))
+        ex = torch.randint(0, 2, (nb(rows), nb(cols)), generator=g, device=device, dtype=torch.int32) + e0
+        return codes, ex.to(torch.uint8)
+
+    wq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
+    we = torch.empty(E, nb(2 * I), nb(H), dtype=torch.uint8, device=device)
+    dq = torch.empty(E, H, I, dtype=torch.uint8, device=device)
+    de = torch.empty(E, nb(H), nb(I), dtype=torch.uint8, device=device)
+    for e in range(E):
+        wq[e], we[e] = mat(2 * I, H, H)
+        dq[e], de[e] = mat(H, I, I)
+    return Fp8W8A8Experts(wq, we, dq, de)
+
+
+@dataclasses.dataclass
 class Int8Experts:
     w_gate_up_q: torch.Tensor      # int8 [E, 2I, H]
     w_gate_up_scale: torch.Tensor  # float32 [E, ceil(2I/128), ceil(H/128)]
