@@ -112,17 +112,18 @@ template <> struct CfgOf<kDown, kQU4> : CfgOf<kDown, kQFp8> {};
 // bf16 kernels' 64 elements), so the stages keep their byte layout.  Tiles
 // are at most kMxTileRows rows, which leaves TMEM columns for the scale
 // factors after the accumulators: per stage kMxSfCols columns from column
-// kAccBufs * kAccCols (A scales of gate [0, 4) and up [4, 8) or of W_down
-// [0, 4), B scales [8, 16)).  down runs on single CTAs with the FP8 down
-// ring (the block-scaled MMA reads its scales from this CTA's TMEM).
+// kAccBufs * kAccCols (A scales of the first [0, 4) and second [4, 8) weight
+// block, B scales [8, 16)).  Both GEMMs run on single CTAs (the block-scaled
+// MMA reads its scales from this CTA's TMEM) with two 128-row weight blocks
+// per item sharing the row tile: gate and up for gate_up, two consecutive
+// 128-row blocks of W_down for down (which halves the row-tile bytes per MMA
+// against one block, the bound of a single-CTA GEMM here).
 constexpr int kMxTileRows = 224;
 constexpr int kMxSfCols = 16;
 template <> struct CfgOf<kGateUp, kQMx> {
   static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 2 * kMxTileRows;
 };
-template <> struct CfgOf<kDown, kQMx> {
-  static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = kMxTileRows;
-};
+template <> struct CfgOf<kDown, kQMx> : CfgOf<kGateUp, kQMx> {};
 template <int KIND, int QF> constexpr int kSfCol0 = CfgOf<KIND, QF>::kAccBufs * CfgOf<KIND, QF>::kAccCols;
 static_assert(kSfCol0<kGateUp, kQMx> + 3 * kMxSfCols <= 512 && kSfCol0<kDown, kQMx> + 4 * kMxSfCols <= 512,
               "scale factors fit TMEM");
@@ -213,6 +214,7 @@ struct Params {
   const uint8_t* sfx;
   uint8_t* h8;
   uint8_t* sh;
+  int blocks2;  // down: an item covers two 128-row blocks of W_down (block-scaled FP8)
   int64_t P;
   uint64_t wait_ns;  // give-up limit of the pipeline waits
   const float* topk_weights;
@@ -291,7 +293,8 @@ __device__ __forceinline__ void item_base(Item& it, const TileRec* rec, const Pa
   it.pg = p.pieces + h.w;
   it.pc = rec->pc;
   it.lo = f.x; it.hi = f.y; it.np = f.z;
-  it.nexp = KIND == kGateUp ? (f.w & 0xffff) : (f.w >> 16);
+  // expand steps: per piece and 64 ranks, one per gate / up (or W_down block)
+  it.nexp = (KIND == kGateUp || p.blocks2) ? (f.w & 0xffff) : (f.w >> 16);
   it.zrow0 = it.mlo = it.mhi = 0;
   it.r = it.r8 = it.r16 = 0;
   it.po = it.a3 = it.aw = 0;
@@ -403,15 +406,17 @@ struct SfWords {
 };
 template <int KIND>
 __device__ __forceinline__ void sf_load(const Params& p, const Item& it, int kb, int quarter, int lane, SfWords& v) {
-  const int r = it.mb * 128 + quarter * 32 + lane;  // row of the gate (up) block, or of W_down
-  uint32_t e0 = 127u, e1 = 127u;                    // rows past I / H read zero codes
+  uint32_t e0 = 127u, e1 = 127u;  // rows past I / H read zero codes
   if (KIND == kGateUp) {
+    const int r = it.mb * 128 + quarter * 32 + lane;  // row of the gate (and the up) block
     if (r < p.I) {
       e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
       e1 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + (p.I + r) / 128) * p.wsc + kb);
     }
-  } else if (r < p.H) {
-    e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
+  } else {
+    const int r = it.mb * 256 + quarter * 32 + lane;  // row of the first W_down block (second: + 128)
+    if (r < p.H) e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
+    if (r + 128 < p.H) e1 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + (r + 128) / 128) * p.wsc + kb);
   }
   v.a0 = e0 * 0x01010101u;
   v.a1 = e1 * 0x01010101u;
@@ -453,8 +458,11 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int S = CF::kStages;
   constexpr int SB = CF::kStageBytes;
   constexpr bool kShrink = (KIND == kShrinkGU || KIND == kShrinkD);
-  constexpr int kGates = (KIND == kGateUp) ? 2 : 1;
-  constexpr int kUOff = MX ? kMxTileRows : 256;  // gate_up: TMEM column of the up accumulator
+  // two weight blocks per item sharing the row tile: gate_up, and the
+  // block-scaled down GEMM
+  constexpr bool kTwoBlk = KIND == kGateUp || (KIND == kDown && MX);
+  constexpr int kGates = kTwoBlk ? 2 : 1;
+  constexpr int kUOff = MX ? kMxTileRows : 256;  // TMEM column of the second block's accumulator
 
   constexpr bool kPair = kPairOf<KIND, QF>;
   const int n_items = *p.n_tiles * p.nblk;
@@ -480,9 +488,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     for (int s = 0; s < S; ++s) {
       // FP8: the producer's arrival plus one per converter warp (on a pair,
       // both CTAs' converter warps arrive on the leader's barrier)
-      // block-scaled FP8: the producer's arrival plus one per scale-factor
-      // warp of lane quarters 1-3 (the producer warp writes quarter 0)
-      mbar_init(&c.full[s], Q ? 1 + (kPair ? 2 : 1) * kCvWarps : (MX ? 4 : 1));
+      // block-scaled FP8: the producer's expect_tx arrival plus one per
+      // scale-factor warp (the producer warp writes lane quarter 0 after
+      // issuing the step's copies, warps 1-3 quarters 1-3)
+      mbar_init(&c.full[s], Q ? 1 + (kPair ? 2 : 1) * kCvWarps : (MX ? 5 : 1));
       mbar_init(&c.empty[s], 1);
       if (Q) mbar_init(&c.raw_full[s], 1);
     }
@@ -527,13 +536,6 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         if (MX && main_step) sf_load<KIND>(p, it, s, 0, lane, sfw);
         const bool w_ok = mbar_wait(&c.empty[st], (round & 1) ^ 1, abort, p.wait_ns);
         if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
-        if (MX && main_step) {
-          // lane quarter 0 of the stage's scale factors, before the stage's
-          // full barrier can complete
-          sf_store(tmem + kSfCol0<KIND, QF> + st * kMxSfCols, sfw);
-          tc_fence_before();
-          __syncwarp();
-        }
         // the row tile of x_sorted / h: one 64/128/192/256-row box where the
         // map exists, else 64-row boxes
         const int hb = row_box_rows(p, it.nrows);
@@ -636,17 +638,18 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               // on their own barrier, then all of the tile's rows
               static_assert(KIND != kDown || kPair || QF != kQNone, "bf16 down runs on CTA pairs");
               if (MX) {
-                // E4M3 codes of 128 W_down rows, 128 bytes of K per row
-                // (mapped as 64 2-byte elements)
-                mbar_arrive_expect_tx(&c.full[st], 16384 + rbytes);
-                tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 128);
+                // E4M3 codes of two 128-row W_down blocks (one 256-row box),
+                // 128 bytes of K per row (mapped as 64 2-byte elements)
+                mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
+                tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * p.H + it.mb * 256);
               } else {
                 mbar_arrive_expect_tx(&c.raw_full[st], 128 * kRawRowBytes<QF>);
                 tma_load_3d(sbuf + 8192, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, it.mb * 128, it.e);
                 mbar_arrive_expect_tx(&c.full[st], rbytes);
               }
               for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 16384 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+                tma_load_2d(sbuf + (MX ? 32768 : 16384) + q * 8192, rmap, &c.full[st], 0,
+                            kb * p.cap + it.row0 + q * 64);
             } else {  // kDown, on a CTA pair: this CTA's 128 weight rows and half of the tile's rows
               const int hh = pair_row_box(it.nrows);
               if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (16384 + hh * 128));
@@ -669,7 +672,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zh * 16));
             else if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
             const uint32_t fb = kPair ? cluster_addr(&c.full[st], 0) : 0u;
-            const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128;
+            const int m0 = kPair ? it.mb * 256 + (int)rank * 128
+                                 : (KIND == kDown && MX) ? it.mb * 256 + g * 128 : it.mb * 128;
             const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
                                              : (pl * p.E + it.e) * p.H + m0;
             // z columns of this step: gate_up's gate / up half, or (down with a
@@ -690,6 +694,16 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               ch += nc;
             }
           }
+        }
+        if (MX) {
+          // lane quarter 0 of the stage's scale factors, after the copies are
+          // issued (the full barrier waits for this arrival too)
+          if (main_step) {
+            sf_store(tmem + kSfCol0<KIND, QF> + st * kMxSfCols, sfw);
+            tc_fence_before();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.full[st]);
         }
       }
     }
@@ -846,7 +860,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t a = (s > 0 || kk > 0) ? 1u : 0u;
               const uint32_t idm = idesc_mx_e4m3(128, it.nrows, kk, kk);
-              if (KIND == kGateUp) {
+              if (kTwoBlk) {
                 const uint64_t bx = sdesc_sw128(sb + 32768 + kk * 32);
                 mma_mx(acc, sdesc_sw128(sb + kk * 32), bx, idm, sf, sf + 8, a);
                 mma_mx(acc + kUOff, sdesc_sw128(sb + 16384 + kk * 32), bx, idm, sf + 4, sf + 8, a);
@@ -884,7 +898,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             cur.next(pc.z, kGates);
             const int nch = min(8, (pc.z - kg * 64) / 8);
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
-            const uint32_t d = acc + (KIND == kGateUp ? g * kUOff : 0) + (pc.x & 0xffff);
+            const uint32_t d = acc + (kTwoBlk ? g * kUOff : 0) + (pc.x & 0xffff);
             const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, pc.x >> 16);
             for (int k16 = 0; k16 < nch / 2; ++k16)
               mma_issue<kPair>(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
@@ -1036,7 +1050,11 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         // lane then holds 4 consecutive rows of one token: one 16-byte vector
         // reduction into y_acc.  Only the warp synchronises.
         static_assert(KIND != kDown || kEpiWarps<KIND> * 2048 <= kHalves * kEpiBytes, "per-warp staging");
-        const int hq = (kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128) + quarter * 32;
+        // two W_down blocks per item (block-scaled FP8): epilogue half eh
+        // takes block eh, all columns; otherwise the halves split the columns
+        const int hq = (kPair ? it.mb * 256 + (int)rank * 128 : kTwoBlk ? it.mb * 256 + eh * 128 : it.mb * 128) +
+                       quarter * 32;
+        const uint32_t tlb = tl + (kTwoBlk ? eh * kUOff : 0);
         const int* tk = c.tok[il & 1];
         const float* wk = c.w[il & 1];
         float* wb = reinterpret_cast<float*>(epi) + (warp - kEpiWarp0) * 512;  // [16 columns][32 rows]
@@ -1047,14 +1065,15 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const uint64_t ypol = l2_evict_last_policy();
         const bool ykeep = p.ykeep != 0;
         const bool hv = hq + q4 < p.H;   // H is a multiple of 8: all 4 rows or none
-        for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
+        const int cstep = kTwoBlk ? 32 : 32 * kHalves;
+        for (int c0 = kTwoBlk ? 0 : 32 * eh; c0 < it.nrows; c0 += cstep) {  // this half's chunks
           const int nc = min(32, it.nrows - c0);  // 32 or 16
           float v[32];
           if (nc == 32) {
-            tmem_ld32(tl + c0, v);
+            tmem_ld32(tlb + c0, v);
           } else {
             float v16[16];
-            tmem_ld16(tl + c0, v16);
+            tmem_ld16(tlb + c0, v16);
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = v16[j];
           }
@@ -2210,7 +2229,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     ok = make_map3(&m_gu.m[kW3], w_gate_up, (uint64_t)H / 2, I, (uint64_t)E * 2, (uint64_t)H, (uint64_t)I * H, 64,
                    128, 2, true) &&
          make_map(&m_gu.m[kRows], x8, 64, hk8 * cap, 64, 64, true) && make_row_maps(m_gu, x8, hk8 * cap, &rm_gu) &&
-         make_map(&m_dn.m[kW], w_down, (uint64_t)I / 2, (uint64_t)E * H, 64, 128, true) &&
+         make_map(&m_dn.m[kW], w_down, (uint64_t)I / 2, (uint64_t)E * H, 64, 256, true) &&
          make_map(&m_dn.m[kRows], h8, 64, ik8 * cap, 64, 64, true) && make_row_maps(m_dn, h8, ik8 * cap, &rm_dn);
     w3 = 1;
   } else if (ok && quant) {
@@ -2365,8 +2384,10 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   prof_mark(prof, 4, stream);
   {
     Params q = p;
-    // a pair covers 256 rows of H, a single CTA (FP8 weights) 128
-    q.n_tiles = counts; q.nblk = (int)ceil_div(H, quant ? 128 : 256); q.rmask = rm_dn;
+    // a CTA pair covers 256 rows of H (bf16), a single CTA 128 (weights
+    // dequantised on chip) or two blocks of 128 (block-scaled FP8)
+    q.n_tiles = counts; q.nblk = (int)ceil_div(H, quant && !mx ? 128 : 256); q.rmask = rm_dn;
+    q.blocks2 = mx ? 1 : 0;
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     q.dpair = det ? xs : nullptr;
     q.wscale = s_d; q.wzero = z_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
