@@ -40,6 +40,19 @@ int current_device_id() {
   return dev;
 }
 
+// SMs of the current device (148 when it cannot be read, e.g. without a GPU).
+int device_sm_count() {
+  static int n[64] = {};
+  const int dev = current_device_id();
+  if (dev < 0) return 148;
+  if (n[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
 // Token of this thread's pair j = it * kThreads + tid of a chunk, advanced one
 // round (kThreads pairs) at a time without a division: t = tq, tr = its slot.
 struct TokenCursor {
@@ -368,8 +381,12 @@ AlignPlan align_plan(int32_t num_tokens, int32_t topk, int32_t num_experts, int3
   const int64_t NB = (int64_t)num_experts * (num_loras + 1);
   if (pl.P >= INT32_MAX || NB > kMaxAlignBuckets) return pl;
   pl.NB = (int)NB;
-  int64_t chunk = round_up(ceil_div(pl.P, 148), kThreads);
-  chunk = chunk < kThreads ? kThreads : (chunk > kMaxChunk ? kMaxChunk : chunk);
+  // chunks: a whole number of waves of the scatter (one 1024-thread block per
+  // SM), each chunk at most kMaxChunk pairs
+  const int64_t sms = device_sm_count();
+  int64_t chunk = round_up(ceil_div(pl.P, sms), kThreads);
+  for (int64_t waves = 2; chunk > kMaxChunk; ++waves) chunk = round_up(ceil_div(pl.P, sms * waves), kThreads);
+  chunk = chunk < kThreads ? kThreads : chunk;
   pl.chunk = (int)chunk;
   pl.G = (int)ceil_div(pl.P, chunk);
   const int64_t buckets = pl.P < NB ? pl.P : NB;
