@@ -271,6 +271,12 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 __device__ __forceinline__ float silu_f(float v) { return v * fmaf(0.5f, tanh_approx(0.5f * v), 0.5f); }
+// SiLU to about 1e-6 relative: sigmoid(v) = 1 / (1 + e^-v) with the fast
+// exponential and reciprocal (for v << 0, e^-v = inf gives 0, the limit).  The
+// block-scaled FP8 layer quantises h to E4M3 right after its bf16 rounding;
+// the tanh form's sigmoid loses relative precision for v << 0 (about 0.5% near
+// v = -6), enough to move codes across E4M3 rounding boundaries.
+__device__ __forceinline__ float silu_acc(float v) { return v * __fdividef(1.f, 1.f + __expf(-v)); }
 
 // One work item: tile rows, weight block, adapter (shrinks: with its rank).
 struct Item {
@@ -965,13 +971,13 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             tmem_ld32(tl + c0, gv);
             tmem_ld32(tl + kUOff + c0, uv);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+            for (int j = 0; j < 32; ++j) ws[j * 32 + lane] = f32_to_bf16_bits((MX ? silu_acc(gv[j]) : silu_f(gv[j])) * uv[j]);
           } else {
             float gv[16], uv[16];
             tmem_ld16(tl + c0, gv);
             tmem_ld16(tl + kUOff + c0, uv);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ws[j * 32 + lane] = f32_to_bf16_bits(silu_f(gv[j]) * uv[j]);
+            for (int j = 0; j < 16; ++j) ws[j * 32 + lane] = f32_to_bf16_bits((MX ? silu_acc(gv[j]) : silu_f(gv[j])) * uv[j]);
           }
           __syncwarp();
           // h is chunk-major: [I/64][cap][64]; rows past I are stored as zeros.

@@ -14,6 +14,7 @@ prefills on sampled tokens.
 """
 import numpy as np
 import pytest
+import torch
 
 import lora_moe_expert_info_gb300 as mlr
 import oracle
@@ -98,3 +99,41 @@ def test_repeatable(cuda_device):
     c = workload_case("qwen_moe_prefill", cuda_device)
     q = quant_of(c)
     assert (gpu(c, q) == gpu(c, q)).all()
+
+
+def test_empty_batch(cuda_device):
+    # T = 0: nothing to do, an empty y
+    c = custom_case(cuda_device, T=8, K=2, E=4, H=128, I=128, L=2, R=16, ranks=[16, 8], seg_lens=[8],
+                    adapters=[0])
+    q = quant_of(c)
+    lo = [getattr(c.w, k) for k in LORA]
+    y = mlr.fused_moe_lora_forward_fp8_w8a8(c.x[:0], c.b.topk_ids[:0], c.b.topk_weights[:0],
+                                            torch.zeros(0, dtype=torch.int32, device=cuda_device),
+                                            c.b.lora_ranks, c.scal, q.w_gate_up_q, q.w_gate_up_exp, q.w_down_q,
+                                            q.w_down_exp, *lo)
+    assert tuple(y.shape) == (0, 128)
+
+
+def test_no_adapter_slots(cuda_device):
+    # L = 0: the base layer only, nothing of the LoRA path runs
+    c = custom_case(cuda_device, T=70, K=2, E=6, H=192, I=256, L=0, R=0, ranks=[], seg_lens=[70],
+                    adapters=[-1])
+    q = quant_of(c, seed=3)
+    assert within(gpu(c, q), ref(c, q)) <= 0
+
+
+def test_all_ranks_zero_equals_base(cuda_device):
+    c = custom_case(cuda_device, T=64, K=2, E=4, H=128, I=128, L=3, R=16, ranks=[0, 0, 0],
+                    seg_lens=[30, 34], adapters=[0, 2], lora_std="fan_in")
+    q = quant_of(c, seed=4)
+    y, y0 = gpu(c, q), gpu(c, q, mapping=np.full_like(c.mapping, -1))
+    assert within(y, ref(c, q)) <= 0
+    assert np.array_equal(y, y0)
+
+
+def test_hidden_not_multiple_of_16_refused(cuda_device):
+    c = custom_case(cuda_device, T=20, K=2, E=4, H=136, I=64, L=2, R=16, ranks=[16, 8], seg_lens=[20],
+                    adapters=[0])
+    q = quant_of(c)
+    with pytest.raises(mlr.MoeLoraError):
+        gpu(c, q)
