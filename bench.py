@@ -126,6 +126,23 @@ def stage_index(lib, name):
         i += 1
 
 
+def capture_steps(step, n, stream):
+    """A CUDA graph of n steps, captured on a side stream: replaying it runs the
+    same launches (same kernels, same arguments) without the host's per-launch
+    cost.  One warm replay uploads it."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(n):
+            step()
+    stream.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
 def timed_region(lib, args, step, stream, dist, local, dom):
     """The timed steps: barrier and synchronise on both sides, CUDA events on the
     launching stream, clocks sampled throughout.  Only the two events that bound
@@ -157,6 +174,26 @@ def timed_region(lib, args, step, stream, dist, local, dom):
     lib.moe_lora_profile_stages(all_stages(lib))
     n_launch = lib.moe_lora_launch_count() - n_launch0
     return e0.elapsed_time(e1), live[dom], n_launch, clk
+
+
+def graph_region(args, step, stream, dist):
+    """The same steps as one CUDA graph replay (captured after the eager timed
+    region, no profiling events inside): ms over all steps, barriers and
+    synchronisation on both sides, CUDA events on the stream."""
+    import torch
+    g = capture_steps(step, args.steps, stream)
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1)
 
 
 def pipelined_e2e(n_steps, upload, compute, download, stream):
@@ -531,6 +568,7 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
     dom = max((s for s in STAGE_KERNELS if s in stages), key=lambda s: stages[s])
     ms_total, dom_ms, n_launch, clk = timed_region(lib, args, step, stream, dist, local, dom)
     ms_max = reduce_max(ms_total, dist, dev)
+    graph_ms = reduce_max(graph_region(args, step, stream, dist), dist, dev) / args.steps if args.graph else None
     # the other top-k combine, timed the same way (events around the steps)
     mode = mlr.deterministic()
     mlr.set_deterministic(not mode)
@@ -625,6 +663,9 @@ def measure_moe(name, args, rank, world, dist, lib, with_e2e, with_cpu):
                         "l2": f"no flush: each step streams {byts / 1e9:.2f} GB of algorithmic bytes "
                               f"(> 129 MB L2)"},
              "roofline": rf, "layer_roofline": layer,
+             "graph": None if graph_ms is None else {
+                 "ms_per_step": round(graph_ms, 4), "value": round(weak_scaling_rate(T, world, graph_ms), 1),
+                 "note": "the same steps as one CUDA graph replay (captured after the timed region)"},
              "stages_ms": {k: round(v, 4) for k, v in stages.items()},
              "combine": combine,
              "gpu_launches": int(n_launch), "clocks": clk.summary()}
@@ -811,7 +852,7 @@ def run_ours(args, rank, world, dist):
             "data": "synthetic",
             "config": dict(head["config"],
                            parallelism=f"dp{world} (replicas)" if world > 1 else "single GPU"),
-            "roofline": head["roofline"], "layer_roofline": head["layer_roofline"],
+            "roofline": head["roofline"], "layer_roofline": head["layer_roofline"], "graph": head["graph"],
             "stages_ms": head["stages_ms"], "combine": head["combine"], "cpu_baseline": head.get("cpu_baseline"),
             "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
     if extras:
@@ -1067,6 +1108,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="skip the extra measurement of the steps as one CUDA graph replay")
     args = ap.parse_args(argv)
     if args.config in LINEAR_CONFIGS and args.weights != "bf16":
         ap.error("--weights applies to the MoE workloads only")
