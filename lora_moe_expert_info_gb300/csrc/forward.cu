@@ -1254,12 +1254,14 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
   if (threadIdx.x == 0) ustart_out[NB] = us[NB];
   __syncthreads();
   align_block_scan(zs, NB);  // zs[b]: first z row of bucket b's region
-  auto rank16 = [&](int b) -> int {  // rank rounded to 16 of a LoRA bucket, or 0
-    const int cl = b % C;
+  // rank rounded to 16 of adapter class cl (adapter cl - 1), 0 for class 0 (no
+  // adapter); the per-expert loops walk the classes without a division
+  auto rank16c = [&](int cl) -> int {
     if (cl == 0) return 0;
     const int r = lora_ranks[cl - 1];
     return (r > 0 && r <= R) ? (r + 15) & ~15 : 0;
   };
+  auto rank16 = [&](int b) -> int { return rank16c(b % C); };  // of bucket b
   // tile k of expert e (tiles of ts rows from r0 over span rows) at slot
   // `slot`, its pieces at pieces[poff ..]; returns the number of pieces
   auto write_tile = [&](int e, int k, int slot, int poff, int r0, int span, int ts) -> int {
@@ -1268,13 +1270,13 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
     const int N = min(ts, r0 + span - row0);
     TileRec& rec = base_tiles[slot];
     int np = 0, nexp_gu = 0, nexp_d = 0;
-    for (int b = e * C + 1; b < (e + 1) * C; ++b) {
-      const int r16 = rank16(b);
+    for (int b = e * C + 1, cl = 1; cl < C; ++b, ++cl) {
+      const int r16 = rank16c(cl);
       if (r16 == 0 || us[b + 1] == us[b]) continue;
       const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
       const int a0 = max(z0, row0), a1 = min(z1, row0 + N);
       if (a1 <= a0) continue;
-      const int4 pc = make_int4((a0 - row0) | ((a1 - a0) << 16), b % C - 1, r16, (int)zs[b] + (a0 - z0));
+      const int4 pc = make_int4((a0 - row0) | ((a1 - a0) << 16), cl - 1, r16, (int)zs[b] + (a0 - z0));
       pieces[poff + np] = pc;
       if (np < kInlinePieces) rec.pc[np] = pc;
       ++np;
@@ -1296,8 +1298,12 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       const int r0 = floor16(ue0), span = ceil16(ue1) - r0;
       const int ts = tile_rows(span, max_rows), nt = (span + ts - 1) / ts;
       my_t += nt;
-      for (int b = e * C + 1; b < (e + 1) * C; ++b) {
-        if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+      for (int b = e * C + 1, cl = 1; cl < C; ++b, ++cl) {
+        if (rank16c(cl) == 0 || us[b + 1] == us[b]) continue;
+        if (nt == 1) {  // one tile: every bucket meets it
+          ++my_p;
+          continue;
+        }
         const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
         my_p += (z1 - 1 - r0) / ts - (z0 - r0) / ts + 1;  // tiles it meets
       }
@@ -1354,8 +1360,8 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
         const int q = atomicAdd(&big_n, 1);
         if (q < kPlanBigQueue) {
           big_q[q] = make_int4(e, toff, poff, 0);
-          for (int b = e * C + 1; b < (e + 1) * C; ++b) {
-            if (rank16(b) == 0 || us[b + 1] == us[b]) continue;
+          for (int b = e * C + 1, cl = 1; cl < C; ++b, ++cl) {
+            if (rank16c(cl) == 0 || us[b + 1] == us[b]) continue;
             const int z0 = floor16((int)us[b]), z1 = ceil16((int)us[b + 1]);
             poff += (z1 - 1 - r0) / ts - (z0 - r0) / ts + 1;  // tiles it meets
           }
