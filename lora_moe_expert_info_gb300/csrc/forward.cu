@@ -214,7 +214,6 @@ struct Params {
   const uint8_t* sfx;
   uint8_t* h8;
   uint8_t* sh;
-  int blocks2;  // down: an item covers two 128-row blocks of W_down (block-scaled FP8)
   int64_t P;
   uint64_t wait_ns;  // give-up limit of the pipeline waits
   const float* topk_weights;
@@ -299,8 +298,8 @@ __device__ __forceinline__ void item_base(Item& it, const TileRec* rec, const Pa
   it.pg = p.pieces + h.w;
   it.pc = rec->pc;
   it.lo = f.x; it.hi = f.y; it.np = f.z;
-  // expand steps: per piece and 64 ranks, one per gate / up (or W_down block)
-  it.nexp = (KIND == kGateUp || p.blocks2) ? (f.w & 0xffff) : (f.w >> 16);
+  // expand steps: per piece and 64 ranks, one per gate / up for gate_up, one for down
+  it.nexp = KIND == kGateUp ? (f.w & 0xffff) : (f.w >> 16);
   it.zrow0 = it.mlo = it.mhi = 0;
   it.r = it.r8 = it.r16 = 0;
   it.po = it.a3 = it.aw = 0;
@@ -467,7 +466,11 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   // two weight blocks per item sharing the row tile: gate_up, and the
   // block-scaled down GEMM
   constexpr bool kTwoBlk = KIND == kGateUp || (KIND == kDown && MX);
-  constexpr int kGates = kTwoBlk ? 2 : 1;
+  // expand units per piece and 64 ranks: gate and up for gate_up; the
+  // block-scaled down GEMM expands both of its W_down blocks in one step (they
+  // share the piece's z rows, loaded once)
+  constexpr int kGates = KIND == kGateUp ? 2 : 1;
+  constexpr bool kExp2 = KIND == kDown && MX;
   constexpr int kUOff = MX ? kMxTileRows : 256;  // TMEM column of the second block's accumulator
 
   constexpr bool kPair = kPairOf<KIND, QF>;
@@ -675,28 +678,34 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             // pairs: this CTA's 128 rows of LoRA B and half of the piece's z rows
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
             const int zoff = kPair ? (int)rank * ((pc.x >> 16) >> 1) : 0;
-            if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (2048 + zh * 16));
+            // kExp2: LoRA B of both W_down blocks at [0, 16 KB) and [16 KB, 32 KB),
+            // the z rows once at [32 KB, 64 KB); else B at [0, 16 KB), z after it
+            constexpr int kNb = kExp2 ? 2 : 1;
+            const int zbase = kExp2 ? 32768 : 16384;
+            if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (kNb * 2048 + zh * 16));
             else if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
             const uint32_t fb = kPair ? cluster_addr(&c.full[st], 0) : 0u;
-            const int m0 = kPair ? it.mb * 256 + (int)rank * 128
-                                 : (KIND == kDown && MX) ? it.mb * 256 + g * 128 : it.mb * 128;
-            const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
-                                             : (pl * p.E + it.e) * p.H + m0;
             // z columns of this step: gate_up's gate / up half, or (down with a
             // split B) the rank slice of the output block's part
             const int zslice = (KIND == kDown && it.mb >= p.zslice_blk) ? p.R16 : 0;
             const int zc0 = ((KIND == kGateUp ? g * p.R16 : zslice) + kg * 64) >> 3;
+            for (int gb = 0; gb < kNb; ++gb) {
+              const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : kExp2 ? it.mb * 256 + gb * 128 : it.mb * 128;
+              const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
+                                               : (pl * p.E + it.e) * p.H + m0;
+              for (int ch = 0; ch < nch;) {
+                const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
+                const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
+                if (kPair) tma_load_3d_pair(sbuf + ch * 2048, &maps.m[bs], fb, 0, brow, kg * 8 + ch);
+                else tma_load_3d(sbuf + gb * 16384 + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
+                ch += nc;
+              }
+            }
             for (int ch = 0; ch < nch;) {
               const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
-              const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
               const int zs = zh == 64 ? (nc == 8 ? kZ8s : (nc == 4 ? kZ4s : kZ2s)) : (nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2));
-              if (kPair) {
-                tma_load_3d_pair(sbuf + ch * 2048, &maps.m[bs], fb, 0, brow, kg * 8 + ch);
-                tma_load_3d_pair(sbuf + 16384 + ch * zh * 16, &maps.m[zs], fb, 0, zrow + zoff, zc0 + ch);
-              } else {
-                tma_load_3d(sbuf + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
-                tma_load_3d(sbuf + 16384 + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
-              }
+              if (kPair) tma_load_3d_pair(sbuf + zbase + ch * zh * 16, &maps.m[zs], fb, 0, zrow + zoff, zc0 + ch);
+              else tma_load_3d(sbuf + zbase + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
               ch += nc;
             }
           }
@@ -904,11 +913,16 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             cur.next(pc.z, kGates);
             const int nch = min(8, (pc.z - kg * 64) / 8);
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
-            const uint32_t d = acc + (kTwoBlk ? g * kUOff : 0) + (pc.x & 0xffff);
             const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, pc.x >> 16);
-            for (int k16 = 0; k16 < nch / 2; ++k16)
-              mma_issue<kPair>(d, sdesc_noswz(sb + k16 * 2 * 2048, 2048, 128),
-                       sdesc_noswz(sb + 16384 + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
+            const uint32_t zb = sb + (kExp2 ? 32768 : 16384);
+#pragma unroll
+            for (int gb = 0; gb < (kExp2 ? 2 : 1); ++gb) {
+              // gate_up: the gate or up accumulator; kExp2: W_down block gb's
+              const uint32_t d = acc + (KIND == kGateUp ? g * kUOff : kExp2 ? gb * kUOff : 0) + (pc.x & 0xffff);
+              for (int k16 = 0; k16 < nch / 2; ++k16)
+                mma_issue<kPair>(d, sdesc_noswz(sb + gb * 16384 + k16 * 2 * 2048, 2048, 128),
+                                 sdesc_noswz(zb + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
+            }
           }
           mma_commit_to<kPair>(&c.empty[st]);
         }
@@ -2399,7 +2413,6 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     // a CTA pair covers 256 rows of H (bf16), a single CTA 128 (weights
     // dequantised on chip) or two blocks of 128 (block-scaled FP8)
     q.n_tiles = counts; q.nblk = (int)ceil_div(H, quant && !mx ? 128 : 256); q.rmask = rm_dn;
-    q.blocks2 = mx ? 1 : 0;
     q.ykeep = (int64_t)T * H * 4 <= ((int64_t)64 << 20) ? 1 : 0;  // half of the 129 MB L2
     q.dpair = det ? xs : nullptr;
     q.wscale = s_d; q.wzero = z_d; q.wsr = (int)ceil_div(H, 128); q.wsc = (int)ceil_div(I, 128);
