@@ -144,6 +144,10 @@ static_assert(kSfCol0<kGateUp, kQMx> + 3 * kMxSfCols <= 512 && kSfCol0<kDown, kQ
 //            kZ8s/kZ4s/kZ2s the same with 64-row boxes (pieces of <= 64 rows)
 //            kW3 (gate_up) = W_gate_up viewed as [(e,gate|up)][row][k]: one
 //            box holds a 128-row block of gate and of up
+//            kBJ8/kBJ4/kBJ2 (gate_up) = LoRA B viewed as [(l,e,gate|up)][rank
+//            chunk][row][8]: one box holds the rank chunks of a gate and of an
+//            up block; kZJ4/kZJ2 (zrows-row boxes) and kZJ8s/kZJ4s/kZJ2s
+//            (64-row boxes) the z rows of a piece's gate and up columns
 // Each TMA box costs the SM's copy engine a roughly fixed time whatever its
 // size (measured on GB300 from L2: 8 KB and 32 KB boxes take about the same
 // time), so every operand of a K step is fetched with as few boxes as possible.
@@ -151,7 +155,8 @@ enum MapSlot {
   kW = 0, kRows = 1, kA32 = 2, kA16 = 3, kA8 = 4, kA3x16 = 5, kA3x32 = 6, kA3x64 = 7,
   kB8 = 2, kB4 = 3, kB2 = 4, kZ8 = 5, kZ4 = 6, kZ2 = 7,
   kX2x64 = 9, kX2x128 = 10, kAW16 = 11, kAW32 = 12, kAW64 = 13,  // shrinks: two-chunk boxes
-  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14, kNumMaps = 15,
+  kRows128 = 8, kRows256 = 9, kW3 = 10, kZ8s = 11, kZ4s = 12, kZ2s = 13, kRows192 = 14,
+  kBJ8 = 15, kBJ4 = 16, kBJ2 = 17, kZJ4 = 18, kZJ2 = 19, kZJ8s = 20, kZJ4s = 21, kZJ2s = 22, kNumMaps = 23,
   kRh32 = 9, kRh96 = 14  // pair kinds: half-tile row boxes of 32 / 96 rows (64 / 128 use kRows / kRows128)
 };
 struct Maps {
@@ -172,10 +177,19 @@ struct Maps {
 // column range [j0, j0 + nj) of one bucket, whose z rows start at zrow.  All
 // pieces are at pieces[poff..]; the first kInlinePieces are also stored in the
 // record so that one warp-wide load brings a whole typical tile.
+// gate_up expand: the gate and the up half of a piece share one step when
+// both fit a 64 KB stage -- LoRA B of both gates at [0, 32 KB), their z rows
+// at [32 KB, 64 KB): pieces of at most 32 ranks (z boxes of up to 256 rows),
+// or of 64 ranks over at most 64 columns (z boxes of 64 rows).  The plan
+// counts the steps with the same rule.
+__host__ __device__ __forceinline__ bool gu_joint_piece(int r16, int nj) {
+  return r16 <= 32 || (r16 == 64 && nj <= 64);
+}
+
 struct TileRec {
   int4 head;  // {e, row0, N, poff}
   int4 info;  // {lo, hi, np, nexp_gu | nexp_d << 16}: expand steps of gate_up (2 per
-              // 64 ranks of a piece) and of down (1 per 64 ranks)
+              // 64 ranks of a piece, or 1 for a joint piece) and of down (1 per 64 ranks)
   int4 pc[kInlinePieces];
 };
 static_assert(sizeof(TileRec) == 32 * 16, "one int4 per lane");
@@ -202,6 +216,7 @@ struct Params {
   int ykeep;      // down: 1 if y_acc fits in half of L2 (its reductions are then marked evict-last)
   int zslice_blk; // down: 256-row blocks from this index on read the second rank slice of z (split B)
   int w3;         // gate_up: 1 if the gate+up weight map exists
+  int gu_joint;   // gate_up: 1 if the joint gate+up LoRA B and z maps exist (joint expand steps)
   int wsr, wsc;   // FP8 weights: 128-row and 128-column scale blocks per expert matrix
   const float* wscale;  // FP8 / INT8: [E][wsr][wsc] block scales (weight = code x scale);
                         // UINT4: [E][rows][wsc] group scales
@@ -386,10 +401,15 @@ __device__ __forceinline__ int shrink_a_stride(const Item& it) {
 }
 
 // Walks the expand steps of a base item in order: per bucket, per gate (2 for
-// gate_up), per 64 ranks.  Producer and MMA warp walk the same sequence.
+// gate_up), per 64 ranks; a joint gate_up step covers both gates of a piece.
+// Producer and MMA warp walk the same sequence.
 struct ExpandCursor {
   int b = 0, g = 0, kg = 0;
-  __device__ __forceinline__ void next(int r16, int ngates) {  // r16 of piece b
+  __device__ __forceinline__ void next(int r16, int ngates, bool joint) {  // r16 of piece b
+    if (joint) {
+      ++b;
+      return;
+    }
     if (++kg == (r16 + 63) >> 6) {
       kg = 0;
       if (++g == ngates) {
@@ -472,6 +492,8 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int kGates = KIND == kGateUp ? 2 : 1;
   constexpr bool kExp2 = KIND == kDown && MX;
   constexpr int kUOff = MX ? kMxTileRows : 256;  // TMEM column of the second block's accumulator
+  static_assert(KIND != kGateUp || (SB >= 64 * 1024 && !kPairOf<KIND, QF>), "a joint expand step fills 64 KB");
+  static_assert(sizeof(Maps) + sizeof(Params) <= 4096, "kernel parameters");
 
   constexpr bool kPair = kPairOf<KIND, QF>;
   const int n_items = *p.n_tiles * p.nblk;
@@ -673,40 +695,52 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int4 pc = it.piece(cur.b);  // {j0 | nj << 16, l, r16, zrow}
             const int pl = pc.y, pr16 = pc.z, zrow = pc.w;
             const int g = cur.g, kg = cur.kg;
-            cur.next(pr16, kGates);
+            const bool joint = KIND == kGateUp && p.gu_joint && gu_joint_piece(pr16, pc.x >> 16);
+            cur.next(pr16, kGates, joint);
             const int nch = min(8, (pr16 - kg * 64) / 8);  // rank chunks of 8 (even)
             // pairs: this CTA's 128 rows of LoRA B and half of the piece's z rows
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
             const int zoff = kPair ? (int)rank * ((pc.x >> 16) >> 1) : 0;
-            // kExp2: LoRA B of both W_down blocks at [0, 16 KB) and [16 KB, 32 KB),
-            // the z rows once at [32 KB, 64 KB); else B at [0, 16 KB), z after it
-            constexpr int kNb = kExp2 ? 2 : 1;
-            const int zbase = kExp2 ? 32768 : 16384;
-            if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (kNb * 2048 + zh * 16));
-            else if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
-            const uint32_t fb = kPair ? cluster_addr(&c.full[st], 0) : 0u;
-            // z columns of this step: gate_up's gate / up half, or (down with a
-            // split B) the rank slice of the output block's part
-            const int zslice = (KIND == kDown && it.mb >= p.zslice_blk) ? p.R16 : 0;
-            const int zc0 = ((KIND == kGateUp ? g * p.R16 : zslice) + kg * 64) >> 3;
-            for (int gb = 0; gb < kNb; ++gb) {
-              const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : kExp2 ? it.mb * 256 + gb * 128 : it.mb * 128;
-              const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
-                                               : (pl * p.E + it.e) * p.H + m0;
+            if (joint) {
+              // gate and up in one step: LoRA B as [gate|up][chunk][128 rows][8]
+              // at [0, 32 KB), z as [gate|up][chunk][zh rows][8] at [32 KB, 64 KB);
+              // 8 chunks come with 64-row z boxes only (gu_joint_piece)
+              mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
+              const int bs = nch == 8 ? kBJ8 : (nch == 4 ? kBJ4 : kBJ2);
+              const int zs = zh == 64 ? (nch == 8 ? kZJ8s : (nch == 4 ? kZJ4s : kZJ2s)) : (nch == 4 ? kZJ4 : kZJ2);
+              tma_load_4d(sbuf, &maps.m[bs], &c.full[st], 0, it.mb * 128, 0, (pl * p.E + it.e) * 2);
+              tma_load_4d(sbuf + 32768, &maps.m[zs], &c.full[st], 0, zrow, 0, 0);
+            } else {
+              // kExp2: LoRA B of both W_down blocks at [0, 16 KB) and [16 KB, 32 KB),
+              // the z rows once at [32 KB, 64 KB); else B at [0, 16 KB), z after it
+              constexpr int kNb = kExp2 ? 2 : 1;
+              const int zbase = kExp2 ? 32768 : 16384;
+              if (!kPair) mbar_arrive_expect_tx(&c.full[st], nch * (kNb * 2048 + zh * 16));
+              else if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
+              const uint32_t fb = kPair ? cluster_addr(&c.full[st], 0) : 0u;
+              // z columns of this step: gate_up's gate / up half, or (down with a
+              // split B) the rank slice of the output block's part
+              const int zslice = (KIND == kDown && it.mb >= p.zslice_blk) ? p.R16 : 0;
+              const int zc0 = ((KIND == kGateUp ? g * p.R16 : zslice) + kg * 64) >> 3;
+              for (int gb = 0; gb < kNb; ++gb) {
+                const int m0 = kPair ? it.mb * 256 + (int)rank * 128 : kExp2 ? it.mb * 256 + gb * 128 : it.mb * 128;
+                const int brow = KIND == kGateUp ? ((pl * p.E + it.e) * 2 + g) * p.I + m0
+                                                 : (pl * p.E + it.e) * p.H + m0;
+                for (int ch = 0; ch < nch;) {
+                  const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
+                  const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
+                  if (kPair) tma_load_3d_pair(sbuf + ch * 2048, &maps.m[bs], fb, 0, brow, kg * 8 + ch);
+                  else tma_load_3d(sbuf + gb * 16384 + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
+                  ch += nc;
+                }
+              }
               for (int ch = 0; ch < nch;) {
                 const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
-                const int bs = nc == 8 ? kB8 : (nc == 4 ? kB4 : kB2);
-                if (kPair) tma_load_3d_pair(sbuf + ch * 2048, &maps.m[bs], fb, 0, brow, kg * 8 + ch);
-                else tma_load_3d(sbuf + gb * 16384 + ch * 2048, &maps.m[bs], &c.full[st], 0, brow, kg * 8 + ch);
+                const int zs = zh == 64 ? (nc == 8 ? kZ8s : (nc == 4 ? kZ4s : kZ2s)) : (nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2));
+                if (kPair) tma_load_3d_pair(sbuf + zbase + ch * zh * 16, &maps.m[zs], fb, 0, zrow + zoff, zc0 + ch);
+                else tma_load_3d(sbuf + zbase + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
                 ch += nc;
               }
-            }
-            for (int ch = 0; ch < nch;) {
-              const int nc = (nch - ch >= 8 && (p.bmask & 1)) ? 8 : ((nch - ch >= 4 && (p.bmask & 2)) ? 4 : 2);
-              const int zs = zh == 64 ? (nc == 8 ? kZ8s : (nc == 4 ? kZ4s : kZ2s)) : (nc == 8 ? kZ8 : (nc == 4 ? kZ4 : kZ2));
-              if (kPair) tma_load_3d_pair(sbuf + zbase + ch * zh * 16, &maps.m[zs], fb, 0, zrow + zoff, zc0 + ch);
-              else tma_load_3d(sbuf + zbase + ch * zh * 16, &maps.m[zs], &c.full[st], 0, zrow, zc0 + ch);
-              ch += nc;
             }
           }
         }
@@ -910,18 +944,31 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           } else {
             const int4 pc = it.piece(cur.b);
             const int g = cur.g, kg = cur.kg;
-            cur.next(pc.z, kGates);
+            const bool joint = KIND == kGateUp && p.gu_joint && gu_joint_piece(pc.z, pc.x >> 16);
+            cur.next(pc.z, kGates, joint);
             const int nch = min(8, (pc.z - kg * 64) / 8);
             const int zh = kPair ? pair_z_rows(pc.x >> 16) : z_box_rows(p, pc.x >> 16);
             const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, pc.x >> 16);
-            const uint32_t zb = sb + (kExp2 ? 32768 : 16384);
+            if (joint) {
+              // gate and up: LoRA B of gate gg at gg * nch chunks, its z rows at
+              // 32 KB + gg * nch chunks of zh rows
+              for (int gg = 0; gg < 2; ++gg) {
+                const uint32_t d = acc + gg * kUOff + (pc.x & 0xffff);
+                const uint32_t bb = sb + gg * nch * 2048, zb = sb + 32768 + gg * nch * zh * 16;
+                for (int k16 = 0; k16 < nch / 2; ++k16)
+                  mma_issue<kPair>(d, sdesc_noswz(bb + k16 * 2 * 2048, 2048, 128),
+                                   sdesc_noswz(zb + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
+              }
+            } else {
+              const uint32_t zb = sb + (kExp2 ? 32768 : 16384);
 #pragma unroll
-            for (int gb = 0; gb < (kExp2 ? 2 : 1); ++gb) {
-              // gate_up: the gate or up accumulator; kExp2: W_down block gb's
-              const uint32_t d = acc + (KIND == kGateUp ? g * kUOff : kExp2 ? gb * kUOff : 0) + (pc.x & 0xffff);
-              for (int k16 = 0; k16 < nch / 2; ++k16)
-                mma_issue<kPair>(d, sdesc_noswz(sb + gb * 16384 + k16 * 2 * 2048, 2048, 128),
-                                 sdesc_noswz(zb + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
+              for (int gb = 0; gb < (kExp2 ? 2 : 1); ++gb) {
+                // gate_up: the gate or up accumulator; kExp2: W_down block gb's
+                const uint32_t d = acc + (KIND == kGateUp ? g * kUOff : kExp2 ? gb * kUOff : 0) + (pc.x & 0xffff);
+                for (int k16 = 0; k16 < nch / 2; ++k16)
+                  mma_issue<kPair>(d, sdesc_noswz(sb + gb * 16384 + k16 * 2 * 2048, 2048, 128),
+                                   sdesc_noswz(zb + k16 * 2 * zh * 16, zh * 16, 128), idesc, 1u);
+              }
             }
           }
           mma_commit_to<kPair>(&c.empty[st]);
@@ -1236,7 +1283,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
                            TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                            ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
                            int32_t* __restrict__ counts, int32_t* status, int gemv_rows, int by_span,
-                           int max_rows) {
+                           int max_rows, int gu_joint) {
   const int NB = E * C;
   int bad = 0;
   // experts with many tiles, planned by the whole block at the end
@@ -1294,7 +1341,7 @@ __device__ void plan_block(const uint32_t* us, uint32_t* zs, const int32_t* __re
       pieces[poff + np] = pc;
       if (np < kInlinePieces) rec.pc[np] = pc;
       ++np;
-      nexp_gu += 2 * ((r16 + 63) >> 6);
+      nexp_gu += (gu_joint && gu_joint_piece(r16, a1 - a0)) ? 1 : 2 * ((r16 + 63) >> 6);
       nexp_d += (r16 + 63) >> 6;
     }
     rec.head = make_int4(e, row0, N, poff);
@@ -1454,7 +1501,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
             int R, uint32_t* __restrict__ ustart, TileRec* __restrict__ base_tiles,
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
             ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status,
-            int gemv_rows, int by_span, int max_rows) {
+            int gemv_rows, int by_span, int max_rows, int gu_joint) {
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -1463,7 +1510,7 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
   __syncthreads();
   align_block_scan(us, NB);
   plan_block(us, zs, lora_ranks, E, C, R, ustart, base_tiles, pieces, shrink_tiles, gemv_tiles, counts,
-             status, gemv_rows, by_span, max_rows);
+             status, gemv_rows, by_span, max_rows, gu_joint);
 }
 
 // Small batches: the single-block align followed by the tile plan, in one
@@ -1477,7 +1524,7 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
                   TileRec* __restrict__ base_tiles, int4* __restrict__ pieces,
                   ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
                   int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows, int by_span,
-                  int max_rows) {
+                  int max_rows, int gu_joint) {
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
@@ -1485,7 +1532,8 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
   align_block(topk_ids, mapping, P, topk, E, L, kBlock, sm, nullptr, nullptr, nullptr, nullptr, nullptr, P,
               status, usorted);
   plan_block(sm.cnt, reinterpret_cast<uint32_t*>(ap_smem + zs_offset), lora_ranks, E, C, R, ustart,
-             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows, by_span, max_rows);
+             base_tiles, pieces, shrink_tiles, gemv_tiles, counts, status, gemv_rows, by_span, max_rows,
+             gu_joint);
 }
 
 // Dense x_sorted: row u < n = ustart[NB] (the valid pairs) is x[usorted[u] / K]
@@ -1844,7 +1892,7 @@ bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint6
 
 // 4-D bf16 view {d0..d3} with byte strides s1..s3, 128-byte swizzle.
 bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&d)[4], const uint64_t (&st)[3],
-               const uint32_t (&b)[4]) {
+               const uint32_t (&b)[4], bool swizzle128 = true) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {d[0], d[1], d[2], d[3]};
@@ -1852,8 +1900,8 @@ bool make_map4(CUtensorMap* m, const void* base, const uint64_t (&d)[4], const u
   cuuint32_t box[4] = {b[0], b[1], b[2], b[3]};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Row-operand maps with 128-, 256- and 192-row boxes over a chunk-major buffer
@@ -2291,6 +2339,26 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
            make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
     }
   }
+  // joint gate+up expand steps: LoRA B as [(l, e, gate|up)][chunk][I rows][8]
+  // (a box holds 128 rows of a gate and of an up block: I >= 128) and z as
+  // [gate|up][chunk][zcap][8] (its two column halves)
+  int gu_joint = 0;
+  if (ok && L > 0 && I >= 128 && zrows >= 64) {
+    const uint32_t nc[3] = {8, 4, 2};
+    const int bslot[3] = {kBJ8, kBJ4, kBJ2}, zslot[3] = {-1, kZJ4, kZJ2}, zsslot[3] = {kZJ8s, kZJ4s, kZJ2s};
+    const uint64_t rc16 = (uint64_t)f.R16 / 8;
+    for (int j = 0; ok && j < 3; ++j) {
+      if (nc[j] > (uint32_t)(R / 8)) continue;
+      const uint64_t bd[4] = {8, (uint64_t)I, (uint64_t)R / 8, (uint64_t)L * E * 2};
+      const uint64_t bst[3] = {(uint64_t)R * 2, 16, (uint64_t)I * R * 2};
+      const uint64_t zd4[4] = {8, zcap, rc16, 2};
+      const uint64_t zst[3] = {16, zcap * 16, rc16 * zcap * 16};
+      ok = make_map4(&m_gu.m[bslot[j]], lora_b_gu, bd, bst, {8, 128, nc[j], 2}, false) &&
+           make_map4(&m_gu.m[zsslot[j]], zgu, zd4, zst, {8, 64, nc[j], 2}, false) &&
+           (zslot[j] < 0 || make_map4(&m_gu.m[zslot[j]], zgu, zd4, zst, {8, zrows, nc[j], 2}, false));
+    }
+    gu_joint = ok ? 1 : 0;
+  }
   if (!ok) return MLR_ERR_CUDA;
 
   // deterministic combine: the down GEMM writes each pair's weighted row into
@@ -2317,7 +2385,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, by_span, max_rows);
+                                                       gemv_rows, by_span, max_rows, gu_joint);
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
@@ -2332,7 +2400,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
                                                   shrink_tiles, gemv_tiles, counts, d_status, gemv_rows,
-                                                  by_span, max_rows);
+                                                  by_span, max_rows, gu_joint);
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, topk_ids, token_lora_mapping, K, E, L, aws, ustart, usorted, stream)) !=
@@ -2361,6 +2429,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   p.zrows = (int)zrows;
   p.zshort = zrows >= 64 ? 1 : 0;  // zcap >= 256, so the 64-row maps always exist
   p.bmask = bmask;
+  p.gu_joint = gu_joint;
   p.P = (int64_t)T * K;
   p.wait_ns = wait_limit_ns();
   p.topk_weights = topk_weights;
@@ -2619,7 +2688,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
     align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(zeros_ids, token_lora_mapping, (int)f.al.P, 1, 1, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, 0, kTileRows);
+                                                       gemv_rows, 0, kTileRows, 0);
     MLR_CHECK_LAUNCH();
     note_launch();
   } else {
@@ -2631,7 +2700,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
       return MLR_ERR_CUDA;
     plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, 1, f.C, R, ustart, base_tiles, pieces,
                                                   shrink_tiles, gemv_tiles, counts, d_status, gemv_rows, 0,
-                                                  kTileRows);
+                                                  kTileRows, 0);
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, zeros_ids, token_lora_mapping, 1, 1, L, aws, ustart, usorted, stream)) !=

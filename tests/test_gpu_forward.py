@@ -250,6 +250,24 @@ def test_many_tiles_per_expert(cuda_device):
     assert within(y, r) <= 0 and within(y0, r0) <= 0
 
 
+def joint_expand_case(dev, seed=6):
+    # gate_up LoRA expand: pieces of ranks 16 and 32 and a 64-rank bucket of
+    # about 30 rows take joint gate+up steps, the 48-rank piece and a 64-rank
+    # bucket of about 80 rows one step per gate; I = 192 ends in a half-filled
+    # 128-row block (zero-filled LoRA B rows)
+    return custom_case(dev, T=400, K=1, E=2, H=128, I=192, L=5, R=64, ranks=[16, 32, 48, 64, 64],
+                       seg_lens=[60, 60, 60, 60, 160], adapters=[0, 1, 2, 3, 4], lora_std="fan_in", seed=seed)
+
+
+def test_gate_up_joint_and_split_expand_steps(cuda_device):
+    c = joint_expand_case(cuda_device)
+    none = np.full_like(c.mapping, -1)
+    y, y0 = c.gpu(), c.gpu(mapping=none)
+    r, r0 = c.ref(), c.ref(mapping=none)
+    assert np.abs(r - r0).max() > 0.5
+    assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
 def test_chunked_align_path(cuda_device):
     # 33,600 pairs: past the single-block align (16,384 pairs), so the chunked
     # align and the separate plan launch run

@@ -19,7 +19,7 @@ import torch
 import lora_moe_expert_info_gb300 as mlr
 import oracle
 from lora_moe_expert_info_gb300 import workloads
-from test_gpu_forward import bits, custom_case, within, workload_case
+from test_gpu_forward import bits, custom_case, joint_expand_case, within, workload_case
 from test_gpu_quant import LORA, _common, _ref_common
 
 pytestmark = pytest.mark.gpu
@@ -76,6 +76,15 @@ def test_lora_delta(cuda_device):
     r, r0 = ref(c, q), ref(c, q, mapping=none)
     assert np.abs(r - r0).max() > 0.5
     assert within(y, r) <= 0 and within(y0, r0) <= 0
+
+
+def test_gate_up_joint_and_split_expand_steps(cuda_device):
+    c = joint_expand_case(cuda_device)
+    q = quant_of(c, seed=5)
+    none = np.full_like(c.mapping, -1)
+    y, r = gpu(c, q), ref(c, q)
+    assert np.abs(r - ref(c, q, mapping=none)).max() > 0.5
+    assert within(y, r) <= 0
 
 
 def test_decode_all_tokens(cuda_device):
