@@ -420,12 +420,11 @@ struct ExpandCursor {
   }
 };
 
-// Block-scaled FP8: the scale factors of one main step (K block kb), as the
-// four TMEM words of a lane: A scales of this lane's weight row (gate and up
-// rows for gate_up), B scales of tile rows 32 i + lane.  Every byte of a word
-// holds the same exponent, so the four K = 32 MMAs of the step (scale ids
-// 0..3) read the same value.  Loaded before the stage is free so that the
-// loads overlap the wait.
+// Block-scaled FP8: the scale exponents of one main step (K block kb) that a
+// lane writes: A exponents of this lane's weight row (gate and up rows for
+// gate_up, the rows of both W_down blocks for down), B exponents of tile rows
+// 32 i + lane.  Loaded before the stage is free; nothing consumes the loaded
+// bytes until sf_store, after the wait, so the loads overlap the wait.
 struct SfWords {
   uint32_t a0, a1, b[8];
 };
@@ -443,22 +442,26 @@ __device__ __forceinline__ void sf_load(const Params& p, const Item& it, int kb,
     if (r < p.H) e0 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + r / 128) * p.wsc + kb);
     if (r + 128 < p.H) e1 = __ldg(p.wexp + ((int64_t)it.e * p.wsr + (r + 128) / 128) * p.wsc + kb);
   }
-  v.a0 = e0 * 0x01010101u;
-  v.a1 = e1 * 0x01010101u;
+  v.a0 = e0;
+  v.a1 = e1;
   const uint8_t* sx = p.sfx + (int64_t)kb * p.cap + it.row0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int n = 32 * i + lane;
-    v.b[i] = (n < it.nrows ? (uint32_t)__ldg(sx + n) : 127u) * 0x01010101u;
+    v.b[i] = n < it.nrows ? (uint32_t)__ldg(sx + n) : 127u;
   }
 }
 // The words into this warp's lane quarter of the stage's scale-factor columns:
 // A scales in columns [0, 4) (gate / W_down) and [4, 8) (up) -- the MMA reads
 // row m's at column m / 32 of lane m --, B scales of rows 32 i + lane in
-// column 8 + i of every quarter.
+// column 8 + i of every quarter.  Every byte of a word holds the same
+// exponent, so the four K = 32 MMAs of the step (scale ids 0..3) read the
+// same value.
 __device__ __forceinline__ void sf_store(uint32_t taddr, const SfWords& v) {
-  const uint32_t w[16] = {v.a0, v.a0, v.a0, v.a0, v.a1, v.a1, v.a1, v.a1,
-                          v.b[0], v.b[1], v.b[2], v.b[3], v.b[4], v.b[5], v.b[6], v.b[7]};
+  const uint32_t a0 = v.a0 * 0x01010101u, a1 = v.a1 * 0x01010101u;
+  uint32_t w[16] = {a0, a0, a0, a0, a1, a1, a1, a1};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[8 + i] = v.b[i] * 0x01010101u;
   tmem_st16_wait(taddr, w);
 }
 
@@ -1061,25 +1064,22 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             // their column maxima through shared memory; each warp writes its
             // 32 codes of the column, quarter 0 also the column's exponent.
             const uint16_t* colp = ws + lane * 32;
-            // load order rotated by lane pair so that a warp's loads spread
-            // over the banks; selects (not indexing) put the pieces in place
+            // the column's four pieces of 8 rows, loaded in an order rotated by
+            // lane pair so that a warp's loads spread over the banks: ld[r]
+            // holds piece (r + rot) & 3, whose codes go to that piece's 8 bytes
+            // of the output (the maximum needs no order)
             const int rot = (lane >> 1) & 3;
-            uint4 ld[4], cv[4];
+            uint4 ld[4];
+            uint32_t cm2 = 0;  // maxima of |h| bits, two 16-bit halves
 #pragma unroll
-            for (int m = 0; m < 4; ++m) ld[m] = *reinterpret_cast<const uint4*>(colp + ((m + rot) & 3) * 8);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = (k - rot) & 3;  // ld[r] holds piece k
-              cv[k] = r == 0 ? ld[0] : r == 1 ? ld[1] : r == 2 ? ld[2] : ld[3];
+            for (int r = 0; r < 4; ++r) {
+              const int k = (r + rot) & 3;
+              ld[r] = *reinterpret_cast<const uint4*>(colp + k * 8);
+              if (iw + k * 8 >= p.I) ld[r] = make_uint4(0, 0, 0, 0);  // rows past I (I % 16 == 0)
+              cm2 = __vmaxu2(cm2, __vmaxu2(ld[r].x & 0x7fff7fffu, ld[r].y & 0x7fff7fffu));
+              cm2 = __vmaxu2(cm2, __vmaxu2(ld[r].z & 0x7fff7fffu, ld[r].w & 0x7fff7fffu));
             }
-            uint32_t cm = 0;
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-              if (iw + mm * 8 >= p.I) cv[mm] = make_uint4(0, 0, 0, 0);  // rows past I (I % 16 == 0)
-              const uint32_t wv[4] = {cv[mm].x, cv[mm].y, cv[mm].z, cv[mm].w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) cm = max(cm, max(wv[k] & 0x7fffu, (wv[k] >> 16) & 0x7fffu));
-            }
+            const uint32_t cm = max(cm2 & 0xffffu, cm2 >> 16);
             static_assert(!MX || KIND != kGateUp || kAmaxBytes<KIND, QF> == 2048, "column-maxima buffer");
             uint32_t* am = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&c) + sizeof(Ctl)) +
                            (eh * 2 + ((c0 >> 6) & 1)) * 128;
@@ -1088,26 +1088,24 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const uint32_t gm = max(max(am[lane], am[32 + lane]), max(am[64 + lane], am[96 + lane]));
             const int sxp = mx_group_exp_bf16(gm);
             const float sc = exp2_neg(sxp);
-            uint32_t qw[8];
+            const int col = c0 + lane;
+            const bool st_ok = lane < ncol && col >= it.lo && col < it.hi;
+            uint8_t* dst = p.h8 + ((int64_t)it.mb * p.cap + it.row0 + col) * 128 + quarter * 32;
 #pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-              const uint32_t wv[4] = {cv[mm].x, cv[mm].y, cv[mm].z, cv[mm].w};
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t wv[4] = {ld[r].x, ld[r].y, ld[r].z, ld[r].w};
+              uint32_t q2[2];
 #pragma unroll
               for (int k = 0; k < 4; k += 2) {
                 const uint32_t lo = f32x2_to_e4m3x2(__uint_as_float(wv[k] << 16) * sc,
                                                     __uint_as_float(wv[k] & 0xffff0000u) * sc);
                 const uint32_t hi = f32x2_to_e4m3x2(__uint_as_float(wv[k + 1] << 16) * sc,
                                                     __uint_as_float(wv[k + 1] & 0xffff0000u) * sc);
-                qw[mm * 2 + k / 2] = lo | (hi << 16);
+                q2[k / 2] = lo | (hi << 16);
               }
+              if (st_ok) *reinterpret_cast<uint2*>(dst + ((r + rot) & 3) * 8) = make_uint2(q2[0], q2[1]);
             }
-            const int col = c0 + lane;
-            if (lane < ncol && col >= it.lo && col < it.hi) {
-              uint4* dst = reinterpret_cast<uint4*>(p.h8 + ((int64_t)it.mb * p.cap + it.row0 + col) * 128 + quarter * 32);
-              dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-              dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-              if (quarter == 0) p.sh[(int64_t)it.mb * p.cap + it.row0 + col] = (uint8_t)(sxp + 127);
-            }
+            if (st_ok && quarter == 0) p.sh[(int64_t)it.mb * p.cap + it.row0 + col] = (uint8_t)(sxp + 127);
           }
           __syncwarp();
         }
