@@ -88,7 +88,10 @@ template <int KIND> struct Cfg;
 // The shrinks stage two 64-wide K chunks per ring slot (LoRA A in [0, 32 KB),
 // the x / h rows in [32 KB, 64 KB)): twice the bytes per TMA box.
 template <> struct Cfg<kShrinkGU> { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
-template <> struct Cfg<kGateUp>   { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512; };
+// gate_up (bf16) runs on CTA pairs: a stage holds this CTA's 128-row blocks of
+// gate [0, 16 KB) and up [16 KB, 32 KB) and its half of the tile's rows
+// [32 KB, 48 KB); the accumulators are gate [0, 256) and up [256, 512).
+template <> struct Cfg<kGateUp>   { static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 1, kAccCols = 512; };
 template <> struct Cfg<kShrinkD>  { static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 2, kAccCols = 256; };
 // down runs on CTA pairs: a stage holds this CTA's 128 weight rows [0, 16 KB)
 // and its half of the tile's rows [16 KB, 32 KB).
@@ -96,13 +99,23 @@ template <> struct Cfg<kDown>     { static constexpr int kStages = 6, kStageByte
 
 // GEMM kinds that run on CTA pairs (cluster of two, M = 256 tensor-core MMAs):
 // each CTA loads half of every row tile, so the row bytes per SM drop by half.
-// The FP8-weight down GEMM runs on single CTAs: a pair would need a
-// cluster-scope release from the peer's converters at every K step.
-template <int KIND, int QF = kQNone> constexpr bool kPairOf = KIND == kDown && QF == kQNone;
+// The bf16 gate_up pair covers 256 rows of I (each CTA its own 128 rows of
+// gate and of up, so SiLU(g) * u stays within a CTA) and the bf16 down pair
+// 256 rows of H.  The quantised GEMMs run on single CTAs: the converters
+// would need a cluster-scope release at every K step, and so would the
+// block-scaled MMAs' scale factors (each CTA of a pair reads its own).
+template <int KIND, int QF = kQNone> constexpr bool kPairOf = (KIND == kDown || KIND == kGateUp) && QF == kQNone;
 
 // Ring of a GEMM: the FP8 down GEMM on a single CTA stages its 128 weight rows
-// [0, 16 KB) and all of the tile's rows [16 KB, 48 KB).
+// [0, 16 KB) and all of the tile's rows [16 KB, 48 KB); the gate_up GEMMs with
+// weights dequantised on chip (single CTAs) their gate and up blocks [0, 32 KB)
+// and all of the tile's rows [32 KB, 64 KB).
 template <int KIND, int QF> struct CfgOf : Cfg<KIND> {};
+template <> struct CfgOf<kGateUp, kQFp8> {
+  static constexpr int kStages = 3, kStageBytes = 64 * 1024, kAccBufs = 1, kAccCols = 512;
+};
+template <> struct CfgOf<kGateUp, kQInt8> : CfgOf<kGateUp, kQFp8> {};
+template <> struct CfgOf<kGateUp, kQU4> : CfgOf<kGateUp, kQFp8> {};
 template <> struct CfgOf<kDown, kQFp8> {
   static constexpr int kStages = 4, kStageBytes = 48 * 1024, kAccBufs = 2, kAccCols = 256;
 };
@@ -495,7 +508,9 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int kGates = KIND == kGateUp ? 2 : 1;
   constexpr bool kExp2 = KIND == kDown && MX;
   constexpr int kUOff = MX ? kMxTileRows : 256;  // TMEM column of the second block's accumulator
-  static_assert(KIND != kGateUp || (SB >= 64 * 1024 && !kPairOf<KIND, QF>), "a joint expand step fills 64 KB");
+  // a joint gate_up expand step: LoRA B [0, 32 KB), z rows from 32 KB (at most
+  // 32 KB on a single CTA, 16 KB for this CTA's half on a pair)
+  static_assert(KIND != kGateUp || SB >= (kPairOf<KIND, QF> ? 48 : 64) * 1024, "joint expand step");
   static_assert(sizeof(Maps) + sizeof(Params) <= 4096, "kernel parameters");
 
   constexpr bool kPair = kPairOf<KIND, QF>;
@@ -657,16 +672,24 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 tma_load_3d(sbuf + 16384, &maps.m[kW], &c.raw_full[st], kb * kRawRowBytes<QF>, i0, it.e * 2);
                 mbar_arrive_expect_tx(&c.full[st], rbytes);
               } else {
-                mbar_arrive_expect_tx(&c.full[st], 32768 + rbytes);
+                // on the pair: this CTA's 128 rows of the gate and up blocks
+                // (rows i0 + 128 rank of the pair's 256) and half of the tile's rows
+                const int hh = pair_row_box(it.nrows);
+                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * (32768 + hh * 128));
+                const uint32_t fb = cluster_addr(&c.full[st], 0);
+                const int ip = it.mb * 256 + (int)rank * 128;
                 if (p.w3) {
-                  tma_load_3d(sbuf, &maps.m[kW3], &c.full[st], kb * 64, i0, it.e * 2);
+                  tma_load_3d_pair(sbuf, &maps.m[kW3], fb, kb * 64, ip, it.e * 2);
                 } else {
-                  tma_load_2d(sbuf, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + i0);
-                  tma_load_2d(sbuf + 16384, &maps.m[kW], &c.full[st], kb * 64, it.e * 2 * p.I + p.I + i0);
+                  tma_load_2d_pair(sbuf, &maps.m[kW], fb, kb * 64, it.e * 2 * p.I + ip);
+                  tma_load_2d_pair(sbuf + 16384, &maps.m[kW], fb, kb * 64, it.e * 2 * p.I + p.I + ip);
                 }
+                tma_load_2d_pair(sbuf + 32768, &maps.m[pair_row_slot(hh)], fb, 0,
+                                 kb * p.cap + it.row0 + (int)rank * (it.nrows >> 1));
               }
-              for (int q = 0; q < rbox; ++q)
-                tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
+              if (!kPair)
+                for (int q = 0; q < rbox; ++q)
+                  tma_load_2d(sbuf + 32768 + q * 8192, rmap, &c.full[st], 0, kb * p.cap + it.row0 + q * 64);
             } else if (!kPair) {
               // kDown with FP8 weights, on a single CTA: raw codes of 128 weight rows
               // on their own barrier, then all of the tile's rows
@@ -706,13 +729,22 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int zoff = kPair ? (int)rank * ((pc.x >> 16) >> 1) : 0;
             if (joint) {
               // gate and up in one step: LoRA B as [gate|up][chunk][128 rows][8]
-              // at [0, 32 KB), z as [gate|up][chunk][zh rows][8] at [32 KB, 64 KB);
+              // at [0, 32 KB), z as [gate|up][chunk][zh rows][8] from 32 KB (on a
+              // pair: this CTA's 128 rows of B and half of the piece's z rows);
               // 8 chunks come with 64-row z boxes only (gu_joint_piece)
-              mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
               const int bs = nch == 8 ? kBJ8 : (nch == 4 ? kBJ4 : kBJ2);
               const int zs = zh == 64 ? (nch == 8 ? kZJ8s : (nch == 4 ? kZJ4s : kZJ2s)) : (nch == 4 ? kZJ4 : kZJ2);
-              tma_load_4d(sbuf, &maps.m[bs], &c.full[st], 0, it.mb * 128, 0, (pl * p.E + it.e) * 2);
-              tma_load_4d(sbuf + 32768, &maps.m[zs], &c.full[st], 0, zrow, 0, 0);
+              const int bc = (pl * p.E + it.e) * 2;
+              if (kPair) {
+                if (rank == 0) mbar_arrive_expect_tx(&c.full[st], 2 * 2 * nch * (2048 + zh * 16));
+                const uint32_t fb = cluster_addr(&c.full[st], 0);
+                tma_load_4d_pair(sbuf, &maps.m[bs], fb, 0, it.mb * 256 + (int)rank * 128, 0, bc);
+                tma_load_4d_pair(sbuf + 32768, &maps.m[zs], fb, 0, zrow + zoff, 0, 0);
+              } else {
+                mbar_arrive_expect_tx(&c.full[st], 2 * nch * (2048 + zh * 16));
+                tma_load_4d(sbuf, &maps.m[bs], &c.full[st], 0, it.mb * 128, 0, bc);
+                tma_load_4d(sbuf + 32768, &maps.m[zs], &c.full[st], 0, zrow, 0, 0);
+              }
             } else {
               // kExp2: LoRA B of both W_down blocks at [0, 16 KB) and [16 KB, 32 KB),
               // the z rows once at [32 KB, 64 KB); else B at [0, 16 KB), z after it
@@ -1026,7 +1058,7 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         // Only the warp synchronises.
         static_assert(KIND != kGateUp || kEpiWarps<KIND> * 2048 <= kHalves * kEpiBytes, "per-warp staging");
         uint16_t* ws = reinterpret_cast<uint16_t*>(epi) + (warp - kEpiWarp0) * 1024;  // [32 columns][32 rows]
-        const int iw = it.mb * 128 + quarter * 32;  // first row of h of this warp
+        const int iw = (kPair ? it.mb * 256 + (int)rank * 128 : it.mb * 128) + quarter * 32;  // first row of h of this warp
         const bool chunk_ok = iw < (int)round_up(p.I, 64);
         for (int c0 = 32 * eh; c0 < it.nrows; c0 += 32 * kHalves) {  // this half's chunks
           const int ncol = min(32, it.nrows - c0);  // 32 or 16
@@ -2280,7 +2312,9 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   const uint64_t hk = (uint64_t)ceil_div(H, 64);
   const uint32_t zrows = (uint32_t)(f.zcap < 256 ? f.zcap : 256);
   bool ok = make_map(&m_gu.m[kW], w_gate_up, H, (uint64_t)E * 2 * I, 64, 128, true) &&
-            make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) && make_row_maps(m_gu, xs, hk * cap, &rm_gu) &&
+            make_map(&m_gu.m[kRows], xs, 64, hk * cap, 64, 64, true) &&
+            // bf16 gate_up runs on CTA pairs (half-tile row boxes); the others take whole tiles
+            (qf == kQNone ? make_pair_row_maps(m_gu, xs, hk * cap) : make_row_maps(m_gu, xs, hk * cap, &rm_gu)) &&
             make_shrink2_maps(m_sgu, xs, cap, H, lora_a_gu, L, E, R, &abox_gu, &a3_gu, &aw_gu, &rm_sgu) &&
             make_shrink1_maps(m_sd, hbuf, cap, I, lora_a_down, L, E, R, &abox_d, &aw_d, &rm_sd) &&
             make_down_maps(m_dn, w_down, H, I, E, hbuf, cap, lora_b_down, L, R, zd, zcap, f.R16 / 8);
@@ -2324,6 +2358,9 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
       ok = make_map3(&m_dn.m[zslot[j]], zd, 8, zcap, (uint64_t)f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]);
     }
   }
+  // z rows per box of the gate_up expand: a CTA of a pair loads half of a
+  // piece's rows (at most 128), a single CTA all of them
+  const uint32_t zr_gu = qf == kQNone ? 128u : zrows;
   if (ok && L > 0) {
     // gate_up expand: LoRA B stacks as [rank chunk][row][8] (each row's ranks are
     // contiguous) and chunk-major z [column/8][zcap][8]
@@ -2333,7 +2370,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
       if (nc[j] > R / 8) continue;  // a box may not span more rank chunks than exist
       ok = make_map3(&m_gu.m[bslot[j]], lora_b_gu, 8, (uint64_t)L * E * 2 * I, (uint64_t)R / 8, (uint64_t)R * 2, 16,
                      8, 128, nc[j]) &&
-           make_map3(&m_gu.m[zslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, zrows, nc[j]) &&
+           make_map3(&m_gu.m[zslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, zr_gu, nc[j]) &&
            make_map3(&m_gu.m[zsslot[j]], zgu, 8, zcap, (uint64_t)2 * f.R16 / 8, 16, zcap * 16, 8, 64, nc[j]);
     }
   }
@@ -2353,7 +2390,7 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
       const uint64_t zst[3] = {16, zcap * 16, rc16 * zcap * 16};
       ok = make_map4(&m_gu.m[bslot[j]], lora_b_gu, bd, bst, {8, 128, nc[j], 2}, false) &&
            make_map4(&m_gu.m[zsslot[j]], zgu, zd4, zst, {8, 64, nc[j], 2}, false) &&
-           (zslot[j] < 0 || make_map4(&m_gu.m[zslot[j]], zgu, zd4, zst, {8, zrows, nc[j], 2}, false));
+           (zslot[j] < 0 || make_map4(&m_gu.m[zslot[j]], zgu, zd4, zst, {8, zr_gu, nc[j], 2}, false));
     }
     gu_joint = ok ? 1 : 0;
   }
@@ -2454,7 +2491,8 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   prof_mark(prof, 2, stream);
   {
     Params q = p;
-    q.n_tiles = counts; q.nblk = (int)ceil_div(I, 128); q.rmask = rm_gu; q.w3 = w3;
+    // a CTA pair covers 256 rows of I (bf16), a single CTA 128
+    q.n_tiles = counts; q.nblk = (int)ceil_div(I, qf == kQNone ? 256 : 128); q.rmask = rm_gu; q.w3 = w3;
     q.wscale = s_gu; q.wzero = z_gu; q.wsr = (int)ceil_div(2 * I, 128); q.wsc = (int)ceil_div(H, 128);
     q.wexp = z_gu; q.sfx = sx; q.h8 = h8; q.sh = sh;
     rc = qf == kQFp8 ? launch_gemm<kGateUp, kQFp8>(m_gu, q, f.max_base, stream)
