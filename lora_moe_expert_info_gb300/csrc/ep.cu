@@ -178,15 +178,24 @@ __global__ void ep_combine_kernel(const uint16_t* __restrict__ rows, const int32
   const int64_t t = i / g8;
   const int c = (int)(i - t * g8) * 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int k = 0; k < K; ++k) {
-    const int q = __ldg(pair_pos + t * K + k);
-    if (q < 0) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(rows + (int64_t)q * H + c));
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  // up to 8 pairs' rows in flight before any is added; the sum runs in increasing k
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint4 v[8];
+    int q[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[2 * j] += __uint_as_float(wv[j] << 16);
-      acc[2 * j + 1] += __uint_as_float(wv[j] & 0xffff0000u);
+    for (int j = 0; j < 8; ++j) {
+      q[j] = k0 + j < K ? __ldg(pair_pos + t * K + k0 + j) : -1;
+      v[j] = q[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(rows + (int64_t)q[j] * H + c)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (q[j] < 0) continue;
+      const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[2 * u] += __uint_as_float(wv[u] << 16);
+        acc[2 * u + 1] += __uint_as_float(wv[u] & 0xffff0000u);
+      }
     }
   }
   uint4 o;

@@ -1818,7 +1818,9 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
 // Deterministic top-k combine: y[t] = sum over k, in increasing k, of the
 // pair rows dpair[t*K + k] (bf16 w * d written by the down GEMM), in fp32.
 // Pairs the align dropped (expert or adapter id out of range) never received
-// a row and add nothing.  One thread per 8 consecutive columns of a token.
+// a row and add nothing.  One thread per 8 consecutive columns of a token; the
+// rows of up to 8 pairs are loaded before any is added, so that a thread keeps
+// 8 loads in flight (the sum still runs in increasing k).
 __global__ void combine_kernel(const uint16_t* __restrict__ dpair, const int32_t* __restrict__ topk_ids,
                                const int32_t* __restrict__ mapping, int64_t T, int K, int H, int E, int L,
                                uint16_t* __restrict__ y) {
@@ -1830,16 +1832,26 @@ __global__ void combine_kernel(const uint16_t* __restrict__ dpair, const int32_t
   const int l = __ldg(mapping + t);
   const bool lora_ok = l >= -1 && l < L;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int k = 0; k < K; ++k) {
-    const int64_t pr = t * K + k;
-    const int e = __ldg(topk_ids + pr);
-    if (!lora_ok || e < 0 || e >= E) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(dpair + pr * H + c));
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint4 v[8];
+    uint32_t ok = 0;  // bit j: pair k0 + j has a row
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[2 * q] += __uint_as_float(wv[q] << 16);
-      acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
+    for (int j = 0; j < 8; ++j) {
+      const int64_t pr = t * K + k0 + j;
+      const int e = k0 + j < K ? __ldg(topk_ids + pr) : -1;
+      const bool has = lora_ok && e >= 0 && e < E;
+      ok |= has ? 1u << j : 0u;
+      v[j] = has ? __ldg(reinterpret_cast<const uint4*>(dpair + pr * H + c)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!((ok >> j) & 1)) continue;
+      const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(wv[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
+      }
     }
   }
   uint4 o;
