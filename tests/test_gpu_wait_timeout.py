@@ -5,8 +5,8 @@ filling or draining, the FP8 converters' raw tiles) gives up after a limit that
 the host sets (moe_lora_set_wait_limit_ns, 2 s by default) and reports
 MLR_STATUS_TIMEOUT instead of spinning.  These tests set the limit to 1 ns, so
 that the first wait of every GEMM launch that is not already satisfied gives up:
-the single-CTA gate_up and shrinks, the CTA-pair down GEMM and the FP8
-converter warps.  The call must still return normally with the timeout bit set,
+the single-CTA shrinks, the CTA-pair gate_up and down GEMMs, the FP8 converter
+warps and the block-scaled W8A8 GEMMs (their scale-factor warps included).  The call must still return normally with the timeout bit set,
 and after the limit is put back the next call on the same context must match
 the oracle, which shows that every role left, freed its TMEM and kept the
 context usable.  No fault, trap or endless wait is involved: the waits are
@@ -108,6 +108,27 @@ def test_fp8_converter_waits_give_up_then_recover(cuda_device, short_waits):
                                   q.w_gate_up_q.cpu().numpy(), q.w_gate_up_scale.cpu().numpy(),
                                   q.w_down_q.cpu().numpy(), q.w_down_scale.cpu().numpy(),
                                   *[bits(getattr(w, k)) for k in WKEYS[2:]])
+    assert st == 0 and within(y, yref) <= 0
+
+
+def test_w8a8_waits_give_up_then_recover(cuda_device, short_waits):
+    cfg, b, w, x, mp = _tiny(cuda_device)
+    q = workloads.make_fp8_w8a8_experts(cfg, device=cuda_device, seed=0)
+    args = dict(x=x, topk_ids=b.topk_ids, topk_weights=b.topk_weights, token_lora_mapping=mp,
+                lora_ranks=b.lora_ranks, scalings=b.scalings, w_gate_up_q=q.w_gate_up_q,
+                w_gate_up_exp=q.w_gate_up_exp, w_down_q=q.w_down_q, w_down_exp=q.w_down_exp,
+                **{k: getattr(w, k) for k in WKEYS[2:]})
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    mlr.fused_moe_lora_forward_fp8_w8a8(**args, check=False, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & TIMEOUT
+    mlr.set_wait_limit_ns(DEFAULT_NS)
+    y = mlr.fused_moe_lora_forward_fp8_w8a8(**args).float().cpu().numpy()
+    st, yref = oracle.forward_fp8_w8a8(bits(x), b.topk_ids.cpu().numpy(), b.topk_weights.cpu().numpy(),
+                                       mp.cpu().numpy(), b.lora_ranks.cpu().numpy(), b.scalings.cpu().numpy(),
+                                       q.w_gate_up_q.cpu().numpy(), q.w_gate_up_exp.cpu().numpy(),
+                                       q.w_down_q.cpu().numpy(), q.w_down_exp.cpu().numpy(),
+                                       *[bits(getattr(w, k)) for k in WKEYS[2:]])
     assert st == 0 and within(y, yref) <= 0
 
 
