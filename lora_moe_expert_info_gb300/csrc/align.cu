@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(kThreads, 2)  // two blocks per SM: 32 registe
 align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ mapping,
                    int64_t P, int topk, int E, int L, int chunk, uint32_t* __restrict__ cnt,
                    int32_t* d_status) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   extern __shared__ uint32_t hist[];
   const int C = L + 1, NB = E * C;
   for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0u;
@@ -139,6 +141,8 @@ align_count_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
 // then each thread rewrites its segment.
 __global__ void __launch_bounds__(kColThreads)
 align_colscan_kernel(uint32_t* __restrict__ cnt, int G, int NB, uint32_t* __restrict__ btotal) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   __shared__ uint32_t part[kColWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int b = blockIdx.x * 32 + lane;
@@ -178,6 +182,8 @@ __global__ void __launch_bounds__(kThreads)
 align_bucketscan_kernel(const uint32_t* __restrict__ btotal, int NB, int block_size,
                         uint32_t* __restrict__ bstart, int32_t* __restrict__ num_post_pad,
                         int64_t capacity, int32_t* d_status) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   extern __shared__ uint32_t sb[];
   for (int b = threadIdx.x; b < NB; b += blockDim.x)
     sb[b] = (btotal[b] + block_size - 1) / block_size * block_size;
@@ -209,6 +215,8 @@ align_scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __rest
                      int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
                      int32_t* __restrict__ num_post_pad, int64_t capacity, int32_t* d_status,
                      const uint32_t* __restrict__ dense_start) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   // dense_start != nullptr: the dense order (no padding, no labels) for the
   // forward; sorted_ids then receives pair ids at dense_start[b] + rank.
   extern __shared__ uint32_t smem[];
@@ -362,6 +370,8 @@ align_block_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restri
                    int32_t* __restrict__ block_expert, int32_t* __restrict__ block_lora,
                    int32_t* __restrict__ num_post_pad, uint32_t* __restrict__ bstart,
                    int64_t capacity, int32_t* d_status) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char align_smem[];
   const AlignBlockSmem sm = align_block_carve(align_smem, E * (L + 1), P);
   align_block(topk_ids, mapping, P, topk, E, L, block_size, sm, sorted_ids, block_expert, block_lora,
@@ -427,10 +437,10 @@ int launch_scatter(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* 
       return MLR_ERR_CUDA;
     if (dev >= 0) configured[dev] = sm;
   }
-  align_scatter_kernel<kBases><<<pl.G, kThreads, sm, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk,
+  if (launch_pdl(align_scatter_kernel<kBases>, dim3(pl.G), dim3(kThreads), sm, stream, topk_ids, mapping, pl.P, topk, E, L, pl.chunk,
                                                                block_size, cnt, btotal, bstart, sorted_ids,
                                                                block_expert, block_lora, num_post_pad, capacity,
-                                                               d_status, dense_start);
+                                                               d_status, dense_start) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;
@@ -450,9 +460,9 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
         cudaFuncSetAttribute(align_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    align_block_kernel<<<1, kAlignBlockThreads, sm, stream>>>(
+    if (launch_pdl(align_block_kernel, dim3(1), dim3(kAlignBlockThreads), sm, stream, 
         topk_ids, mapping, (int)pl.P, topk, E, L, block_size, sorted_ids, block_expert, block_lora,
-        num_post_pad, bstart, capacity, d_status);
+        num_post_pad, bstart, capacity, d_status) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
     return MLR_OK;
@@ -464,12 +474,12 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
       return MLR_ERR_CUDA;
   }
   if (pl.G > 0) {
-    align_count_kernel<<<pl.G, kThreads, sm_count, stream>>>(topk_ids, mapping, pl.P, topk, E, L,
-                                                             pl.chunk, cnt, d_status);
+    if (launch_pdl(align_count_kernel, dim3(pl.G), dim3(kThreads), sm_count, stream, topk_ids, mapping, pl.P, topk, E, L,
+                                                             pl.chunk, cnt, d_status) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
   }
-  align_colscan_kernel<<<(int)ceil_div(pl.NB, 32), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
+  if (launch_pdl(align_colscan_kernel, dim3((int)ceil_div(pl.NB, 32)), dim3(kColThreads), 0, stream, cnt, pl.G, pl.NB, btotal) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   if (pl.G > 0 && align_bases_fit(pl))  // the scatter scans the bucket totals itself
@@ -480,8 +490,8 @@ int align_launch(const AlignPlan& pl, const int32_t* topk_ids, const int32_t* ma
       cudaFuncSetAttribute(align_bucketscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan) !=
           cudaSuccess)
     return MLR_ERR_CUDA;
-  align_bucketscan_kernel<<<1, kThreads, sm_scan, stream>>>(btotal, pl.NB, block_size, bstart, num_post_pad,
-                                                            capacity, d_status);
+  if (launch_pdl(align_bucketscan_kernel, dim3(1), dim3(kThreads), sm_scan, stream, btotal, pl.NB, block_size, bstart, num_post_pad,
+                                                            capacity, d_status) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   if (pl.G > 0)
@@ -501,12 +511,12 @@ int align_dense_count(const AlignPlan& pl, const int32_t* topk_ids, const int32_
           cudaSuccess)
     return MLR_ERR_CUDA;
   if (pl.G > 0) {
-    align_count_kernel<<<pl.G, kThreads, sm_count, stream>>>(topk_ids, mapping, pl.P, topk, E, L, pl.chunk, cnt,
-                                                             d_status);
+    if (launch_pdl(align_count_kernel, dim3(pl.G), dim3(kThreads), sm_count, stream, topk_ids, mapping, pl.P, topk, E, L, pl.chunk, cnt,
+                                                             d_status) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
   }
-  align_colscan_kernel<<<(int)ceil_div(pl.NB, 32), kColThreads, 0, stream>>>(cnt, pl.G, pl.NB, btotal);
+  if (launch_pdl(align_colscan_kernel, dim3((int)ceil_div(pl.NB, 32)), dim3(kColThreads), 0, stream, cnt, pl.G, pl.NB, btotal) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;

@@ -67,6 +67,8 @@ batch_info_kernel(const int32_t* __restrict__ seg_indptr, const int32_t* __restr
                   const int32_t* __restrict__ lora_ranks, int bs, int num_loras, int num_tokens,
                   int max_len, int32_t* __restrict__ mapping, int32_t* __restrict__ enabled,
                   int32_t* d_status, int vec_ok) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   __shared__ int32_t s_ptr[kStaged + 1];
   __shared__ int32_t s_wi[kStaged];
   __shared__ uint32_t s_bits[kMaxLoras / 32];
@@ -172,9 +174,9 @@ extern "C" int moe_lora_batch_info(const int32_t* seg_indptr, const int32_t* wei
   if (max_len > 0 && (int64_t)bs * (int64_t)max_len < (int64_t)num_tokens) return MLR_ERR_UNDERCOVERED;
   const int ntile = (int)ceil_div(num_tokens, kTile);
   const int vec_ok = (reinterpret_cast<uintptr_t>(token_lora_mapping) % 16) == 0;
-  batch_info_kernel<<<ntile + 1, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  if (launch_pdl(batch_info_kernel, dim3(ntile + 1), dim3(kThreads), 0, static_cast<cudaStream_t>(stream), 
       seg_indptr, weight_indices, lora_ranks, bs, num_loras, num_tokens, max_len,
-      token_lora_mapping, adapter_enabled, d_status, vec_ok);
+      token_lora_mapping, adapter_enabled, d_status, vec_ok) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;

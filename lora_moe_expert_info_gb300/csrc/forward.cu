@@ -492,6 +492,8 @@ __device__ __forceinline__ int row_box_rows(const Params& p, int nrows) {
 template <int KIND, int QF = kQNone>
 __global__ void __launch_bounds__(kConvOf<QF> ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   constexpr bool Q = kConvOf<QF>;   // converter warps dequantise the weights
   constexpr bool MX = QF == kQMx;    // block-scaled FP8 MMAs
   static_assert(QF == kQNone || KIND == kGateUp || KIND == kDown, "quantised weights: the base GEMMs only");
@@ -1532,6 +1534,8 @@ plan_kernel(const uint32_t* __restrict__ btotal, const int32_t* __restrict__ lor
             int4* __restrict__ pieces, ShrinkRec* __restrict__ shrink_tiles,
             ShrinkRec* __restrict__ gemv_tiles, int32_t* __restrict__ counts, int32_t* status,
             int gemv_rows, int by_span, int max_rows, int gu_joint) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char plan_smem[];
   const int NB = E * C;
   uint32_t* us = reinterpret_cast<uint32_t*>(plan_smem);
@@ -1555,6 +1559,8 @@ align_plan_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restric
                   ShrinkRec* __restrict__ shrink_tiles, ShrinkRec* __restrict__ gemv_tiles,
                   int32_t* __restrict__ counts, int32_t* status, int zs_offset, int gemv_rows, int by_span,
                   int max_rows, int gu_joint) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   static_assert(kPlanThreads == kAlignBlockThreads, "one block runs both");
   extern __shared__ __align__(16) unsigned char ap_smem[];
   const int C = L + 1, NB = E * C;
@@ -1573,6 +1579,8 @@ __global__ void __launch_bounds__(kGatherThreads)
 gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usorted,
                 const uint32_t* __restrict__ n_valid, int K, int H, int64_t cap, uint16_t* __restrict__ xs,
                 float* __restrict__ yacc, int64_t yacc_n4) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   const int64_t n = *n_valid;
   const int lane = threadIdx.x & 31;
   const int64_t wpb = kGatherThreads / 32;
@@ -1609,6 +1617,8 @@ __global__ void __launch_bounds__(kGatherThreads)
 gather_x_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usorted,
                    const uint32_t* __restrict__ n_valid, int K, int H, int64_t cap, uint16_t* __restrict__ xs,
                    uint8_t* __restrict__ x8, uint8_t* __restrict__ sx, float* __restrict__ yacc, int64_t yacc_n4) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   const int64_t n = *n_valid;
   const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
   const int64_t wpb = kGatherThreads / 32;
@@ -1769,6 +1779,8 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
                    const uint16_t* __restrict__ a, const uint16_t* __restrict__ rows, int Kd, int64_t cap,
                    int E, int R, int R16, const int32_t* __restrict__ lora_ranks,
                    const float* __restrict__ scalings, uint16_t* __restrict__ z, int64_t zcap) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t gemv_smem[];
   const int Kp = (Kd + 63) & ~63, kp8 = Kp / 8;
   uint16_t* xr = reinterpret_cast<uint16_t*>(gemv_smem);                      // [kGemvRows][Kp]
@@ -1824,6 +1836,8 @@ shrink_gemv_kernel(const ShrinkRec* __restrict__ tiles, const int32_t* __restric
 __global__ void combine_kernel(const uint16_t* __restrict__ dpair, const int32_t* __restrict__ topk_ids,
                                const int32_t* __restrict__ mapping, int64_t T, int K, int H, int E, int L,
                                uint16_t* __restrict__ y) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   const int g8 = H / 8;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * g8) return;
@@ -1863,6 +1877,8 @@ __global__ void combine_kernel(const uint16_t* __restrict__ dpair, const int32_t
 }
 
 __global__ void convert_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, int64_t n) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 4 <= n) {
     const float4 v = *reinterpret_cast<const float4*>(yacc + i);
@@ -2153,17 +2169,20 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
   if (kPairOf<KIND, QF>) {
     // clusters of two CTAs, as many as can be resident at once (a persistent
     // grid with one pair more than fits would run that pair after the others)
-    cudaLaunchAttribute attr[1];
+    // (and programmatic stream serialization, see pdl_wait)
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kLaunchThreads<KIND, QF>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
     static int resident_of[64] = {};
     int resident = dev >= 0 ? resident_of[dev] : 0;
     if (resident == 0) {
@@ -2176,10 +2195,11 @@ int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream
     }
     const int64_t pairs = max_items < resident ? max_items : resident;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, moe_gemm_kernel<KIND, QF>, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
   } else {
     const int grid = (int)(max_items < sm_count() ? max_items : sm_count());
-    moe_gemm_kernel<KIND, QF><<<grid, kLaunchThreads<KIND, QF>, smem, stream>>>(maps, p);
+    if (launch_pdl(moe_gemm_kernel<KIND, QF>, dim3(grid), dim3(kLaunchThreads<KIND, QF>), smem, stream, maps, p) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
   }
   note_launch();
@@ -2203,9 +2223,9 @@ int launch_gemv(const ShrinkRec* tiles, const int32_t* n_tiles, int64_t max_tile
     if (dev >= 0) configured[dev] = smem;
   }
   const int64_t grid = max_tiles < 8 * (int64_t)sm_count() ? max_tiles : 8 * (int64_t)sm_count();
-  shrink_gemv_kernel<NG><<<(unsigned)grid, kGemvThreads, smem, stream>>>(
+  if (launch_pdl(shrink_gemv_kernel<NG>, dim3((unsigned)grid), dim3(kGemvThreads), smem, stream, 
       tiles, n_tiles, static_cast<const uint16_t*>(a), rows, Kd, f.cap, E, R, f.R16, lora_ranks, scalings, z,
-      f.zcap);
+      f.zcap) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   return MLR_OK;
@@ -2429,10 +2449,10 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
         cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
+    if (launch_pdl(align_plan_kernel, dim3(1), dim3(kPlanThreads), sm, stream, topk_ids, token_lora_mapping, (int)f.al.P, K, E, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, by_span, max_rows, gu_joint);
+                                                       gemv_rows, by_span, max_rows, gu_joint) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
     prof_mark(prof, 0, stream);
@@ -2445,9 +2465,9 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), sm, stream, btotal, lora_ranks, E, f.C, R, ustart, base_tiles, pieces,
                                                   shrink_tiles, gemv_tiles, counts, d_status, gemv_rows,
-                                                  by_span, max_rows, gu_joint);
+                                                  by_span, max_rows, gu_joint) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, topk_ids, token_lora_mapping, K, E, L, aws, ustart, usorted, stream)) !=
@@ -2458,12 +2478,12 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   {
     const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
-    if (mx)
-      gather_x_mx_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, x8, sx,
-                                                              yacc, det ? 0 : (int64_t)T * H / 4);
-    else
-      gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, K, H, f.cap, xs, yacc,
-                                                           det ? 0 : (int64_t)T * H / 4);
+    const cudaError_t e =
+        mx ? launch_pdl(gather_x_mx_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted, ustart + f.al.NB, K,
+                        H, f.cap, xs, x8, sx, yacc, det ? 0 : (int64_t)T * H / 4)
+           : launch_pdl(gather_x_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted, ustart + f.al.NB, K, H,
+                        f.cap, xs, yacc, det ? 0 : (int64_t)T * H / 4);
+    if (e != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -2543,11 +2563,13 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * H;
-  if (det)
-    combine_kernel<<<(unsigned)ceil_div(n / 8, 256), 256, 0, stream>>>(xs, topk_ids, token_lora_mapping, T, K, H, E,
-                                                                        L, y);
-  else
-    convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
+  {
+    const cudaError_t e =
+        det ? launch_pdl(combine_kernel, dim3((unsigned)ceil_div(n / 8, 256)), dim3(256), 0, stream, xs, topk_ids,
+                         token_lora_mapping, T, K, H, E, L, y)
+            : launch_pdl(convert_kernel, dim3((unsigned)ceil_div(ceil_div(n, 4), 256)), dim3(256), 0, stream, yacc, y, n);
+    if (e != cudaSuccess) return MLR_ERR_CUDA;
+  }
   MLR_CHECK_LAUNCH();
   note_launch();
   prof_mark(prof, 6, stream);
@@ -2733,10 +2755,10 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(align_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    align_plan_kernel<<<1, kPlanThreads, sm, stream>>>(zeros_ids, token_lora_mapping, (int)f.al.P, 1, 1, L, R,
+    if (launch_pdl(align_plan_kernel, dim3(1), dim3(kPlanThreads), sm, stream, zeros_ids, token_lora_mapping, (int)f.al.P, 1, 1, L, R,
                                                        lora_ranks, usorted, ustart, base_tiles, pieces,
                                                        shrink_tiles, gemv_tiles, counts, d_status, (int)zs_off,
-                                                       gemv_rows, 0, kTileRows, 0);
+                                                       gemv_rows, 0, kTileRows, 0) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
   } else {
@@ -2746,9 +2768,9 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
       return MLR_ERR_CUDA;
-    plan_kernel<<<1, kPlanThreads, sm, stream>>>(btotal, lora_ranks, 1, f.C, R, ustart, base_tiles, pieces,
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), sm, stream, btotal, lora_ranks, 1, f.C, R, ustart, base_tiles, pieces,
                                                   shrink_tiles, gemv_tiles, counts, d_status, gemv_rows, 0,
-                                                  kTileRows, 0);
+                                                  kTileRows, 0) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
     if ((rc = align_dense_scatter(f.al, zeros_ids, token_lora_mapping, 1, 1, L, aws, ustart, usorted, stream)) !=
@@ -2759,8 +2781,8 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
   {
     const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
-    gather_x_kernel<<<grid, kGatherThreads, 0, stream>>>(x, usorted, ustart + f.al.NB, 1, D_in, f.cap, xs, yacc,
-                                                         (int64_t)T * D_out / 4);
+    if (launch_pdl(gather_x_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted, ustart + f.al.NB, 1, D_in, f.cap, xs, yacc,
+                                                         (int64_t)T * D_out / 4) != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
   }
@@ -2817,7 +2839,7 @@ extern "C" int lora_linear_forward(const mlr_bf16* x, const mlr_bf16* w, const i
   }
   prof_mark(prof, 5, stream);
   const int64_t n = (int64_t)T * D_out;
-  convert_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(yacc, y, n);
+  if (launch_pdl(convert_kernel, dim3((unsigned)ceil_div(ceil_div(n, 4), 256)), dim3(256), 0, stream, yacc, y, n) != cudaSuccess) return MLR_ERR_CUDA;
   MLR_CHECK_LAUNCH();
   note_launch();
   prof_mark(prof, 6, stream);

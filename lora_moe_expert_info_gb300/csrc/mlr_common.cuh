@@ -25,6 +25,17 @@ namespace mlr {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;  // largest settable limit: 60 s
 
+// Programmatic dependent launch.  The library's kernels are launched with
+// programmatic stream serialization (launch_pdl): a kernel may then be
+// scheduled while its predecessor on the stream is still finishing.  Each
+// kernel calls pdl_wait() before its first access to global memory -- it
+// returns once the predecessor grid has completed and its writes are visible
+// (at once for a kernel launched the ordinary way) -- and pdl_trigger() right
+// after, so that its own successor may be scheduled as soon as every block of
+// this grid has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
@@ -481,6 +492,24 @@ __device__ __forceinline__ float exp2_neg(int s) { return __int_as_float((127 - 
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   __nv_bfloat16_raw raw = static_cast<__nv_bfloat16_raw>(__float2bfloat16_rn(f));
   return raw.x;
+}
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization (see pdl_wait); returns the launch's error.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace mlr
