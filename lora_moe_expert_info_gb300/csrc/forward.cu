@@ -492,8 +492,6 @@ __device__ __forceinline__ int row_box_rows(const Params& p, int nrows) {
 template <int KIND, int QF = kQNone>
 __global__ void __launch_bounds__(kConvOf<QF> ? 512 : kMaxThreads, 1)
 moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
-  pdl_wait();  // the predecessor on the stream has completed
-  pdl_trigger();
   constexpr bool Q = kConvOf<QF>;   // converter warps dequantise the weights
   constexpr bool MX = QF == kQMx;    // block-scaled FP8 MMAs
   static_assert(QF == kQNone || KIND == kGateUp || KIND == kDown, "quantised weights: the base GEMMs only");
@@ -516,12 +514,10 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   static_assert(sizeof(Maps) + sizeof(Params) <= 4096, "kernel parameters");
 
   constexpr bool kPair = kPairOf<KIND, QF>;
-  const int n_items = *p.n_tiles * p.nblk;
   // work unit: a CTA, or for pairs a cluster (both CTAs take the same items and
   // leave together)
   const int unit = kPair ? (int)cluster_id_x() : (int)blockIdx.x;
   const int n_units = kPair ? (int)num_clusters_x() : (int)gridDim.x;
-  if (unit >= n_items) return;
   const uint32_t rank = kPair ? cluster_rank() : 0u;
 
   extern __shared__ uint8_t smem_raw[];
@@ -568,6 +564,12 @@ moe_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   if (kPair) cluster_sync_all();  // the peer's copies and commits may target this CTA's barriers from here on
   else __syncthreads();
   tc_fence_after();
+  // The setup above touches no global memory, so it overlaps the predecessor's
+  // last blocks; the plan's outputs are read only after this wait.  A unit
+  // without items runs no role's loop and goes straight to the teardown.
+  pdl_wait();
+  pdl_trigger();
+  const int n_items = *p.n_tiles * p.nblk;
   const uint32_t tmem = c.tmem;
   volatile int* abort = &c.abort;
 
