@@ -126,11 +126,13 @@ template <> struct CfgOf<kDown, kQU4> : CfgOf<kDown, kQFp8> {};
 // are at most kMxTileRows rows, which leaves TMEM columns for the scale
 // factors after the accumulators: per stage kMxSfCols columns from column
 // kAccBufs * kAccCols (A scales of the first [0, 4) and second [4, 8) weight
-// block, B scales [8, 16)).  Both GEMMs run on single CTAs (the block-scaled
-// MMA reads its scales from this CTA's TMEM) with two 128-row weight blocks
-// per item sharing the row tile: gate and up for gate_up, two consecutive
-// 128-row blocks of W_down for down (which halves the row-tile bytes per MMA
-// against one block, the bound of a single-CTA GEMM here).
+// block, B scales [8, 16)).  Both GEMMs run on single CTAs with two 128-row
+// weight blocks per item sharing the row tile: gate and up for gate_up, two
+// consecutive 128-row blocks of W_down for down (which halves the row-tile
+// bytes per MMA against one block).  On a CTA pair each CTA's rows read the
+// scales in its own TMEM, so the peer's scale-factor writes would have to be
+// signalled to the leader at every K step; that per-step signal cost more than
+// the pair saved (measured on the down GEMM).
 constexpr int kMxTileRows = 224;
 constexpr int kMxSfCols = 16;
 template <> struct CfgOf<kGateUp, kQMx> {
@@ -2151,7 +2153,8 @@ int sm_count() {
   return n[dev];
 }
 
-// Persistent launch: one CTA per SM (or fewer when there are fewer items).
+// Persistent launch: one CTA per SM, or for the pair kinds as many clusters of
+// two as are resident at once (fewer when there are fewer items).
 template <int KIND, int QF = kQNone>
 int launch_gemm(const Maps& maps, const Params& p, int64_t max_tiles, cudaStream_t stream) {
   static_assert(smem_bytes<KIND, QF>() <= 227 * 1024, "shared memory per CTA");
