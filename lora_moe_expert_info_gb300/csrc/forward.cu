@@ -1612,40 +1612,149 @@ gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usor
     reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Block-scaled FP8: gather_x_kernel's work (x_sorted in bf16 for the LoRA
-// shrink, y_acc zeroed) plus x quantised per row and 128-column group for the
-// base GEMM: x8 [H/128][cap][128] E4M3 codes (zeros past H) and sx
-// [H/128][cap] biased exponents (rows [n, cap): zero codes, exponent 127).
-// Half a warp takes one group, eight values per lane.
+// Position of each placed pair in the dense order: pos[usorted[u]] = u for
+// u < n.  Pairs the align leaves out (ids out of range, which it reports)
+// are not written; the token-major gathers skip them by the align's own rule.
 __global__ void __launch_bounds__(kGatherThreads)
-gather_x_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ usorted,
-                   const uint32_t* __restrict__ n_valid, int K, int H, int64_t cap, uint16_t* __restrict__ xs,
-                   uint8_t* __restrict__ x8, uint8_t* __restrict__ sx, float* __restrict__ yacc, int64_t yacc_n4) {
+dense_pos_kernel(const int32_t* __restrict__ usorted, const uint32_t* __restrict__ n_valid,
+                 int32_t* __restrict__ pos) {
   pdl_wait();  // the predecessor on the stream has completed
   pdl_trigger();
   const int64_t n = *n_valid;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (int64_t)gridDim.x * blockDim.x)
+    pos[usorted[u]] = (int32_t)u;
+}
+
+// Tasks of the gathers.  Token-major (pos given): task t < T nkc (nkc =
+// ceil(K / 32)) is token t / nkc with its pairs k in [32 (t % nkc), + 32),
+// whose row of x is read once and written to the dense rows of those pairs
+// that the align places (expert in [0, E), adapter in [-1, L)); task T nkc + i
+// is the padding row n + i, written as zeros.  Row-major (pos null): task u <
+// cap is dense row u, the row of x of pair usorted[u] for u < n, else zeros.
+// Lane j returns the task's j-th destination row, or -1; tok is the token
+// whose row is read, or -1.
+__device__ __forceinline__ int64_t gather_tasks(int T, int K, int64_t n, int64_t cap, const int32_t* pos) {
+  return pos ? (int64_t)T * ((K + 31) >> 5) + (cap - n) : cap;
+}
+__device__ __forceinline__ int gather_task_row(int64_t task, int T, int K, int E, int L, int64_t n,
+                                               const int32_t* __restrict__ topk_ids,
+                                               const int32_t* __restrict__ mapping,
+                                               const int32_t* __restrict__ usorted,
+                                               const int32_t* __restrict__ pos, int lane, int64_t& tok) {
+  if (pos == nullptr) {
+    tok = task < n ? usorted[task] / K : -1;
+    return lane == 0 ? (int)task : -1;
+  }
+  const int nkc = (K + 31) >> 5;
+  int u = -1;
+  if (task < (int64_t)T * nkc) {
+    tok = task / nkc;
+    const int k = (int)(task - tok * nkc) * 32 + lane;
+    if (k < K) {
+      const int64_t pr = tok * K + k;
+      const int e = __ldg(topk_ids + pr), l = __ldg(mapping + tok);
+      if (e >= 0 && e < E && l >= -1 && l < L) {
+        const int v = pos[pr];
+        if (v >= 0 && v < n) u = v;  // (a stale entry after a reported index error stays in range)
+      }
+    }
+  } else {
+    tok = -1;
+    if (lane == 0) u = (int)(n + (task - (int64_t)T * nkc));
+  }
+  return u;
+}
+
+// gather_x_kernel's result (x_sorted [H/64][cap][64], zeros past H and in
+// rows [n, cap); y_acc zeroed), token-major: each token's row read once for
+// its K pairs.
+__global__ void __launch_bounds__(kGatherThreads)
+gather_x_tok_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
+                    const int32_t* __restrict__ mapping, const int32_t* __restrict__ usorted,
+                    const int32_t* __restrict__ pos,
+                    const uint32_t* __restrict__ n_valid, int T, int K, int E, int L, int H, int64_t cap,
+                    uint16_t* __restrict__ xs, float* __restrict__ yacc, int64_t yacc_n4) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
+  const int64_t n = *n_valid;
+  const int64_t n_tasks = gather_tasks(T, K, n, cap, pos);
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = kGatherThreads / 32;
+  const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces per padded row
+  const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
+  constexpr int kBatch = 8;  // 16-byte loads in flight per lane (4 KB per warp)
+  for (int64_t task = w0; task < n_tasks; task += ws) {
+    int64_t tok;
+    const int myu = gather_task_row(task, T, K, E, L, n, topk_ids, mapping, usorted, pos, lane, tok);
+    const uint32_t dests = __ballot_sync(0xffffffffu, myu >= 0);
+    if (dests == 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (tok >= 0 ? tok * H : 0));
+    // every lane runs every batch (the shuffles below need the whole warp)
+    for (int c0 = 0; c0 < pieces16; c0 += 32 * kBatch) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c = c0 + lane + 32 * j;
+        v[j] = (tok >= 0 && c < pieces16 && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+      for (uint32_t m = dests; m; m &= m - 1) {
+        const int64_t u = __shfl_sync(0xffffffffu, myu, __ffs(m) - 1);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int c = c0 + lane + 32 * j;
+          if (c < pieces16) *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
+        }
+      }
+    }
+  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < yacc_n4; i += (int64_t)gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Block-scaled FP8: gather_x_tok_kernel's work (x_sorted in bf16 for the LoRA
+// shrink, y_acc zeroed) plus x quantised per row and 128-column group for the
+// base GEMM: x8 [H/128][cap][128] E4M3 codes (zeros past H) and sx
+// [H/128][cap] biased exponents (rows [n, cap): zero codes, exponent 127).
+// Token-major (TOK: a token's groups are quantised once and written to the
+// rows of its K pairs) or row-major, like gather_x_tok_kernel and
+// gather_x_kernel.  Half a warp takes one group, eight values per lane.
+template <bool TOK>
+__global__ void __launch_bounds__(kGatherThreads)
+gather_x_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
+                   const int32_t* __restrict__ mapping, const int32_t* __restrict__ usorted,
+                   const int32_t* __restrict__ pos,
+                   const uint32_t* __restrict__ n_valid, int T, int K, int E, int L, int H, int64_t cap,
+                   uint16_t* __restrict__ xs, uint8_t* __restrict__ x8, uint8_t* __restrict__ sx,
+                   float* __restrict__ yacc, int64_t yacc_n4) {
+  pdl_wait();  // the predecessor on the stream has completed
+  pdl_trigger();
+  const int64_t n = *n_valid;
+  const int64_t n_tasks = gather_tasks(T, K, n, cap, pos);
   const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
   const int64_t wpb = kGatherThreads / 32;
   const int ng = (H + 127) / 128;                 // groups per row
   const int pieces16 = (int)round_up(H, 64) / 8;  // 16-byte pieces of an x_sorted row
   const int64_t w0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5), ws = (int64_t)gridDim.x * wpb;
   constexpr int kPairs = 4;  // pairs of groups in flight per warp
-  for (int64_t u = w0; u < cap; u += ws) {
-    const bool real = u < n;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (real ? (int64_t)(usorted[u] / K) * H : 0));
+  for (int64_t task = w0; task < n_tasks; task += ws) {
+    int64_t tok;
+    // TOK: lane j's destination row; else the one row is the task's
+    const int myu = TOK ? gather_task_row(task, T, K, E, L, n, topk_ids, mapping, usorted, pos, lane, tok) : 0;
+    if (!TOK) tok = task < n ? usorted[task] / K : -1;
+    const uint32_t dests = TOK ? __ballot_sync(0xffffffffu, myu >= 0) : 1u;
+    if (dests == 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (tok >= 0 ? tok * H : 0));
     for (int g0 = 0; g0 < ng; g0 += 2 * kPairs) {
       uint4 v[kPairs];
 #pragma unroll
       for (int j = 0; j < kPairs; ++j) {
         const int g = g0 + 2 * j + half, c = g * 16 + hl;  // c: 16-byte piece of the row
-        v[j] = (real && g < ng && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        v[j] = (tok >= 0 && g < ng && c * 8 < H) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int j = 0; j < kPairs; ++j) {
         if (g0 + 2 * j >= ng) break;  // the same for both halves
         const int g = g0 + 2 * j + half, c = g * 16 + hl;
-        if (g < ng && c < pieces16)
-          *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
         const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         uint32_t m = 0;
 #pragma unroll
@@ -1662,9 +1771,14 @@ gather_x_mx_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ u
               f32x2_to_e4m3x2(__uint_as_float(wv[k + 1] << 16) * sc, __uint_as_float(wv[k + 1] & 0xffff0000u) * sc);
           q[k / 2] = lo | (hi << 16);
         }
-        if (g < ng) {
-          *reinterpret_cast<uint2*>(x8 + ((int64_t)g * cap + u) * 128 + hl * 8) = make_uint2(q[0], q[1]);
-          if (hl == 0) sx[(int64_t)g * cap + u] = (uint8_t)(s + 127);
+        for (uint32_t dm = dests; dm; dm &= dm - 1) {
+          const int64_t u = TOK ? (int64_t)__shfl_sync(0xffffffffu, myu, __ffs(dm) - 1) : task;
+          if (g < ng && c < pieces16)
+            *reinterpret_cast<uint4*>(xs + ((int64_t)(c >> 3) * cap + u) * 64 + (c & 7) * 8) = v[j];
+          if (g < ng) {
+            *reinterpret_cast<uint2*>(x8 + ((int64_t)g * cap + u) * 128 + hl * 8) = make_uint2(q[0], q[1]);
+            if (hl == 0) sx[(int64_t)g * cap + u] = (uint8_t)(s + 127);
+          }
         }
       }
     }
@@ -2078,7 +2192,7 @@ struct FwdLayout {
   AlignPlan al;
   int R16, C, mtiles_gu, mtiles_d;
   int64_t cap, zcap, max_base, max_shrink, max_pieces, max_gemv;
-  int64_t o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted,
+  int64_t o_align, o_base, o_shrink, o_gemv, o_pieces, o_ustart, o_usorted, o_pos,
       o_counts, o_zgu, o_h, o_zd, o_yacc, o_xs, o_x8, o_sx, o_h8, o_sh, total;
 };
 
@@ -2116,6 +2230,7 @@ FwdLayout fwd_layout(int32_t T, int32_t K, int32_t E, int32_t H, int32_t I, int3
   f.o_pieces = take(f.max_pieces * 16);
   f.o_ustart = take(((int64_t)f.al.NB + 1) * 4);
   f.o_usorted = take(f.cap * 4);
+  f.o_pos = take(P * 4);  // dense row of each pair, for the token-major gathers
   f.o_counts = take(16);
   f.o_zgu = take(f.zcap * 2 * f.R16 * 2);
   f.o_h = take(f.cap * round_up(I, 64) * 2);
@@ -2481,13 +2596,36 @@ int moe_forward(const mlr_bf16* x, const int32_t* topk_ids, const float* topk_we
     prof_mark(prof, 0, stream);
   }
   {
-    const int64_t blocks = ceil_div(f.cap, kGatherThreads / 32);
+    // Row by row of x_sorted, each reading its token's row of x: the K rows
+    // of a token read it at scattered times, from L2 while x_sorted's writes
+    // leave it there.  Where they stream more than twice the 129 MB L2, the
+    // dense row of each pair is found first and x_sorted is written token by
+    // token (each row of x read once for its K pairs).
+    const bool tok_major = (int64_t)f.al.P * round_up(H, 64) * 2 > ((int64_t)256 << 20);
+    int32_t* pos = tok_major ? reinterpret_cast<int32_t*>(ws + f.o_pos) : nullptr;
+    if (tok_major) {
+      const int64_t pblocks = ceil_div(f.al.P, kGatherThreads);
+      if (launch_pdl(dense_pos_kernel, dim3((unsigned)(pblocks < 4 * sm_count() ? pblocks : 4 * sm_count())),
+                     dim3(kGatherThreads), 0, stream, usorted, ustart + f.al.NB, pos) != cudaSuccess)
+        return MLR_ERR_CUDA;
+      MLR_CHECK_LAUNCH();
+      note_launch();
+    }
+    // (the kernels stride over their tasks; the padding rows number cap - n >= cap - P)
+    const int64_t tasks = tok_major ? (int64_t)T * ceil_div(K, 32) + (f.cap - f.al.P) : f.cap;
+    const int64_t blocks = ceil_div(tasks > 0 ? tasks : 1, kGatherThreads / 32);
     const int grid = (int)(blocks < 16 * sm_count() ? blocks : 16 * sm_count());
     const cudaError_t e =
-        mx ? launch_pdl(gather_x_mx_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted, ustart + f.al.NB, K,
-                        H, f.cap, xs, x8, sx, yacc, det ? 0 : (int64_t)T * H / 4)
-           : launch_pdl(gather_x_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted, ustart + f.al.NB, K, H,
-                        f.cap, xs, yacc, det ? 0 : (int64_t)T * H / 4);
+        mx ? launch_pdl(tok_major ? gather_x_mx_kernel<true> : gather_x_mx_kernel<false>, dim3(grid),
+                        dim3(kGatherThreads), 0, stream, x, topk_ids, token_lora_mapping, (const int32_t*)usorted,
+                        (const int32_t*)pos, ustart + f.al.NB, T, K, E, L, H, f.cap, xs, x8, sx, yacc,
+                        det ? 0 : (int64_t)T * H / 4)
+           : tok_major
+               ? launch_pdl(gather_x_tok_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, topk_ids,
+                            token_lora_mapping, (const int32_t*)usorted, (const int32_t*)pos, ustart + f.al.NB, T, K,
+                            E, L, H, f.cap, xs, yacc, det ? 0 : (int64_t)T * H / 4)
+               : launch_pdl(gather_x_kernel, dim3(grid), dim3(kGatherThreads), 0, stream, x, usorted,
+                            ustart + f.al.NB, K, H, f.cap, xs, yacc, det ? 0 : (int64_t)T * H / 4);
     if (e != cudaSuccess) return MLR_ERR_CUDA;
     MLR_CHECK_LAUNCH();
     note_launch();
